@@ -1,0 +1,27 @@
+"""GB300-native Engram hot path: n-gram hash -> table gather/dequant -> wkv projection -> gate.
+
+The compute lives in ``libengram.so`` (hand-written sm_103a CUDA behind a C ABI declared in
+``include/engram.h``); this package is its thin Python binding.
+"""
+from .binding import (  # noqa: F401
+    ERR_PIPE_TIMEOUT,
+    ERR_RAW_ID,
+    ERR_ROW_ID,
+    TABLE_FORMATS,
+    EngramDims,
+    EngramError,
+    ForwardPlan,
+    HashTables,
+    LayerWeights,
+    engram_forward,
+    engram_gate,
+    engram_gather_dequant,
+    engram_hash,
+    engram_layout,
+    engram_project,
+    forward_workspace_bytes,
+    hash_multipliers,
+    lib,
+    make_dims,
+    set_gemm_tile,
+)

@@ -1,0 +1,312 @@
+"""ctypes binding of libengram: argument marshalling only.
+
+Every stage runs in the CUDA library; these wrappers check tensor dtypes and
+devices, pass raw pointers, sizes and the current CUDA stream, and turn a
+non-zero return code into ``EngramError``.  There is no fallback: if the
+library is missing, ``lib()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libengram.so")
+
+TABLE_BF16, TABLE_FP8_E8M0, TABLE_Q2K = 0, 1, 2
+TABLE_FORMATS = {"bf16": TABLE_BF16, "fp8": TABLE_FP8_E8M0, "q2k": TABLE_Q2K}
+ERR_RAW_ID, ERR_ROW_ID, ERR_PIPE_TIMEOUT = 1, 2, 4
+INT64_MAX = (1 << 63) - 1
+
+
+class EngramError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} failed ({code}): {msg}")
+        self.code = code
+
+
+class EngramDims(C.Structure):
+    _fields_ = [("layers", C.c_int32), ("max_ngram", C.c_int32), ("n_heads", C.c_int32),
+                ("head_dim", C.c_int32), ("hidden", C.c_int32), ("hc", C.c_int32),
+                ("raw_vocab", C.c_int32), ("compressed_vocab", C.c_int32), ("pad_id", C.c_int32),
+                ("eps", C.c_float), ("clamp", C.c_float)]
+
+    @property
+    def cols(self) -> int:
+        return (self.max_ngram - 1) * self.n_heads
+
+
+class _LayerWeights(C.Structure):
+    _fields_ = [("table_format", C.c_int32), ("table", C.c_void_p), ("table_scales", C.c_void_p),
+                ("table_rows", C.c_int64), ("wkv", C.c_void_p), ("q_weight", C.c_void_p),
+                ("k_weight", C.c_void_p)]
+
+
+class _HashTables(C.Structure):
+    _fields_ = [("token_map", C.c_void_p), ("multipliers", C.c_void_p), ("primes", C.c_void_p),
+                ("offsets", C.c_void_p)]
+
+
+class _Tokens(C.Structure):
+    _fields_ = [("input_ids", C.c_void_p), ("T", C.c_int64), ("cu_seqlens", C.c_void_p),
+                ("num_seqs", C.c_int32), ("sequence_ids", C.c_void_p), ("token_mask", C.c_void_p),
+                ("lookback_ids", C.c_void_p)]
+
+
+_lib = None
+P, I32, I64, SZ = C.c_void_p, C.c_int32, C.c_int64, C.c_size_t
+
+
+def lib() -> C.CDLL:
+    """The loaded CUDA library.  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libengram.so not built ({LIB_PATH}); run "
+                               "`python -m engram_gram_hash_02_gb300.build`")
+        L = C.CDLL(LIB_PATH)
+        L.engram_last_error.restype = C.c_char_p
+        L.engram_version.restype = C.c_char_p
+        L.engram_layout.argtypes = [I64, I32, I32, I32, P, P, P]
+        L.engram_hash.argtypes = [P, P, I64, P, I32, P, P, P, P, P, P, P, P, P, P]
+        L.engram_gather_dequant.argtypes = [I32, P, I64, I64, I32, I32, P, P, I64, P, P, P]
+        L.engram_project.argtypes = [P, P, P, I64, I32, I32, P, SZ, P, P]
+        L.engram_gate.argtypes = [P, P, P, P, P, P, I64, P]
+        L.engram_forward_workspace_bytes.argtypes = [P, I64]
+        L.engram_forward_workspace_bytes.restype = SZ
+        L.engram_forward.argtypes = [P, P, P, P, P, P, SZ, P, P, P]
+        L.engram_set_gemm_tile.argtypes = [I32]
+        L.engram_set_gemm_tile.restype = None
+        _lib = L
+    return _lib
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        raise EngramError(fn, rc, lib().engram_last_error().decode())
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _dev(t: torch.Tensor, dtype, name: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype} (got {t.dtype})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _opt(t, dtype, name):
+    return None if t is None else _dev(t, dtype, name)
+
+
+def _stream(stream) -> int | None:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _u16(t: torch.Tensor, name: str) -> torch.Tensor:
+    """bf16 tensors cross the C boundary as their bit patterns."""
+    return _dev(t, torch.bfloat16, name)
+
+
+# ---------------------------------------------------------------------------------------------
+# host-side setup
+# ---------------------------------------------------------------------------------------------
+
+def engram_layout(vocab_size: int, layers: int, max_ngram: int, n_heads: int):
+    """Prime bucket sizes, offsets and rows per layer (computed by the library on the host)."""
+    cols = (max_ngram - 1) * n_heads
+    primes = np.zeros((layers, cols), dtype=np.int64)
+    offsets = np.zeros((layers, cols), dtype=np.int64)
+    rows = np.zeros(layers, dtype=np.int64)
+    _check("engram_layout", lib().engram_layout(vocab_size, layers, max_ngram, n_heads,
+                                                 primes.ctypes.data, offsets.ctypes.data, rows.ctypes.data))
+    return primes, offsets, rows
+
+
+def hash_multipliers(layer_ids, max_ngram: int, compressed_vocab: int) -> np.ndarray:
+    """Odd multiplier per (layer, window slot): 2x+1 with x drawn by numpy's default_rng
+    seeded 10007*layer_id in [0, max(1, (INT64_MAX // V) // 2)), as the vLLM page's
+    compute_hash_multipliers defines them (host setup, once per model)."""
+    bound = max(1, (INT64_MAX // int(compressed_vocab)) // 2)
+    out = np.empty((len(layer_ids), max_ngram), dtype=np.int64)
+    for i, layer_id in enumerate(layer_ids):
+        x = np.random.default_rng(10007 * int(layer_id)).integers(0, bound, size=(max_ngram,), dtype=np.int64)
+        out[i] = x * 2 + 1
+    return out
+
+
+def make_dims(layers, max_ngram, n_heads, head_dim, hidden, hc, raw_vocab, compressed_vocab,
+              pad_id, eps=1e-6, clamp=1e-6) -> EngramDims:
+    return EngramDims(layers, max_ngram, n_heads, head_dim, hidden, hc, raw_vocab,
+                      compressed_vocab, pad_id, eps, clamp)
+
+
+# ---------------------------------------------------------------------------------------------
+# stages
+# ---------------------------------------------------------------------------------------------
+
+def engram_hash(dims: EngramDims, input_ids, token_map, multipliers, primes, offsets, cu_seqlens=None,
+                sequence_ids=None, token_mask=None, lookback_ids=None, out=None, err=None, stream=None):
+    _dev(input_ids, torch.int32, "input_ids")
+    T = input_ids.numel()
+    _dev(token_map, torch.int32, "token_map")
+    _dev(multipliers, torch.int64, "multipliers")
+    _dev(primes, torch.int64, "primes")
+    _dev(offsets, torch.int64, "offsets")
+    _opt(cu_seqlens, torch.int32, "cu_seqlens")
+    _opt(sequence_ids, torch.int32, "sequence_ids")
+    _opt(token_mask, torch.uint8, "token_mask")
+    _opt(lookback_ids, torch.int32, "lookback_ids")
+    _opt(err, torch.int32, "err")
+    if out is None:
+        out = torch.empty((T, dims.layers, dims.cols), dtype=torch.int32, device=input_ids.device)
+    _dev(out, torch.int32, "out")
+    S = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    _check("engram_hash", lib().engram_hash(
+        C.byref(dims), _ptr(input_ids), T, _ptr(cu_seqlens), S, _ptr(sequence_ids), _ptr(token_mask),
+        _ptr(lookback_ids), _ptr(token_map), _ptr(multipliers), _ptr(primes), _ptr(offsets), _ptr(out),
+        _ptr(err), _stream(stream)))
+    return out
+
+
+def engram_gather_dequant(fmt: str, ids, table, scales, num_rows: int, head_dim: int, out=None, err=None,
+                          stream=None):
+    """ids: int32 [T, C] (a strided view [T, L, C][:, l] is fine: rows must have unit column stride)."""
+    if not (isinstance(ids, torch.Tensor) and ids.is_cuda and ids.dtype == torch.int32 and ids.dim() == 2
+            and ids.stride(1) == 1):
+        raise ValueError("ids must be a CUDA int32 [T, C] tensor with unit column stride")
+    T, Cc = ids.shape
+    code = TABLE_FORMATS[fmt]
+    if not (table.is_cuda and table.is_contiguous()):
+        raise ValueError("table must be a contiguous CUDA tensor")
+    if scales is not None:
+        _dev(scales, torch.uint8, "scales")
+    if out is None:
+        out = torch.empty((T, Cc * head_dim), dtype=torch.bfloat16, device=ids.device)
+    _u16(out, "out")
+    _opt(err, torch.int32, "err")
+    _check("engram_gather_dequant", lib().engram_gather_dequant(
+        code, _ptr(ids), ids.stride(0), T, Cc, head_dim, _ptr(table), _ptr(scales), int(num_rows), _ptr(out),
+        _ptr(err), _stream(stream)))
+    return out
+
+
+def engram_project(A, wkv, out=None, err=None, stream=None):
+    _u16(A, "A")
+    _u16(wkv, "wkv")
+    T, K = A.shape
+    N, K2 = wkv.shape
+    if K != K2:
+        raise ValueError(f"A is [T, {K}] but wkv is [{N}, {K2}]")
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.bfloat16, device=A.device)
+    _u16(out, "out")
+    _opt(err, torch.int32, "err")
+    _check("engram_project", lib().engram_project(_ptr(A), _ptr(wkv), _ptr(out), T, K, N, None, 0, _ptr(err),
+                                                   _stream(stream)))
+    return out
+
+
+def engram_gate(dims: EngramDims, streams, kv, q_weight, k_weight, token_mask=None, stream=None):
+    """Updates ``streams`` (fp32 [T, hc, H]) in place and returns it."""
+    _dev(streams, torch.float32, "streams")
+    _u16(kv, "kv")
+    _u16(q_weight, "q_weight")
+    _u16(k_weight, "k_weight")
+    _opt(token_mask, torch.uint8, "token_mask")
+    T = streams.shape[0]
+    _check("engram_gate", lib().engram_gate(C.byref(dims), _ptr(streams), _ptr(kv), _ptr(q_weight),
+                                             _ptr(k_weight), _ptr(token_mask), T, _stream(stream)))
+    return streams
+
+
+def set_gemm_tile(bn: int = 0):
+    lib().engram_set_gemm_tile(int(bn))
+
+
+# ---------------------------------------------------------------------------------------------
+# whole path
+# ---------------------------------------------------------------------------------------------
+
+@dataclass
+class LayerWeights:
+    fmt: str
+    table: torch.Tensor
+    scales: torch.Tensor | None
+    num_rows: int
+    wkv: torch.Tensor
+    q_weight: torch.Tensor
+    k_weight: torch.Tensor
+
+
+@dataclass
+class HashTables:
+    token_map: torch.Tensor
+    multipliers: torch.Tensor
+    primes: torch.Tensor
+    offsets: torch.Tensor
+
+
+def forward_workspace_bytes(dims: EngramDims, T: int) -> int:
+    return int(lib().engram_forward_workspace_bytes(C.byref(dims), T))
+
+
+class ForwardPlan:
+    """Marshalled arguments of engram_forward for fixed tensors, so a hot loop pays one
+    ctypes call per step."""
+
+    def __init__(self, dims: EngramDims, tables: HashTables, layers: list, input_ids, streams: list,
+                 cu_seqlens=None, sequence_ids=None, token_mask=None, lookback_ids=None, workspace=None,
+                 out_ids=None, err=None):
+        self.dims = dims
+        T = input_ids.numel()
+        _dev(input_ids, torch.int32, "input_ids")
+        for name, t, dt in (("cu_seqlens", cu_seqlens, torch.int32), ("sequence_ids", sequence_ids, torch.int32),
+                            ("token_mask", token_mask, torch.uint8), ("lookback_ids", lookback_ids, torch.int32),
+                            ("out_ids", out_ids, torch.int32), ("err", err, torch.int32)):
+            _opt(t, dt, name)
+        self._tables = _HashTables(_ptr(tables.token_map), _ptr(tables.multipliers), _ptr(tables.primes),
+                                   _ptr(tables.offsets))
+        arr = (_LayerWeights * len(layers))()
+        for i, w in enumerate(layers):
+            arr[i] = _LayerWeights(TABLE_FORMATS[w.fmt], _ptr(w.table), _ptr(w.scales), int(w.num_rows),
+                                   _ptr(w.wkv), _ptr(w.q_weight), _ptr(w.k_weight))
+            _dev(streams[i], torch.float32, f"streams[{i}]")
+        self._layers = arr
+        S = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+        self._tokens = _Tokens(_ptr(input_ids), T, _ptr(cu_seqlens), S, _ptr(sequence_ids), _ptr(token_mask),
+                               _ptr(lookback_ids))
+        self._streams = (C.c_void_p * len(streams))(*[s.data_ptr() for s in streams])
+        need = forward_workspace_bytes(dims, T)
+        if workspace is None:
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=input_ids.device)
+        self.workspace = workspace
+        self._ws_bytes = workspace.numel() * workspace.element_size()
+        self._out_ids = out_ids
+        self._err = err
+        self._keep = (tables, layers, input_ids, streams, cu_seqlens, sequence_ids, token_mask, lookback_ids)
+
+    def run(self, stream=None):
+        _check("engram_forward", lib().engram_forward(
+            C.byref(self.dims), C.byref(self._tables), self._layers, C.byref(self._tokens), self._streams,
+            _ptr(self.workspace), self._ws_bytes, _ptr(self._out_ids), _ptr(self._err), _stream(stream)))
+
+
+def engram_forward(dims: EngramDims, tables: HashTables, layers: list, input_ids, streams: list, **kw):
+    """Hash once, then per layer gather -> project -> gate (streams updated in place)."""
+    stream = kw.pop("stream", None)
+    plan = ForwardPlan(dims, tables, layers, input_ids, streams, **kw)
+    plan.run(stream)
+    return plan

@@ -1,0 +1,261 @@
+// The extern "C" boundary of libengram: argument checks, error reporting, and the forward
+// pass that chains hash -> (gather -> project -> gate) per layer on one stream.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <mutex>
+#include <string>
+
+#include "internal.cuh"
+
+namespace engram {
+
+static thread_local std::string g_last_error;
+
+void set_error(const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+}
+
+int fail_cuda(cudaError_t e, const char* what) {
+  set_error("%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+  return ENGRAM_ECUDA;
+}
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+void set_gemm_bn_override(int bn);
+
+static int check_dims(const EngramDims* d, bool need_hash, bool need_gate) {
+  ENGRAM_CHECK_ARG(d != nullptr, "dims is NULL");
+  if (need_hash) {
+    ENGRAM_CHECK_ARG(d->layers >= 1, "layers must be >= 1 (got %d)", d->layers);
+    ENGRAM_CHECK_ARG(d->max_ngram >= 2 && d->max_ngram <= 8, "max_ngram must be in [2, 8] (got %d)", d->max_ngram);
+    ENGRAM_CHECK_ARG(d->n_heads >= 1, "n_heads must be >= 1 (got %d)", d->n_heads);
+    ENGRAM_CHECK_ARG((int64_t)d->layers * (d->max_ngram - 1) * d->n_heads <= 256,
+                     "layers * n_hash_cols must be <= 256");
+    ENGRAM_CHECK_ARG(d->raw_vocab >= 1, "raw_vocab must be >= 1");
+    ENGRAM_CHECK_ARG(d->compressed_vocab >= 1, "compressed_vocab must be >= 1");
+    ENGRAM_CHECK_ARG(d->pad_id >= 0 && d->pad_id < d->compressed_vocab, "pad_id %d outside [0, %d)", d->pad_id,
+                     d->compressed_vocab);
+  }
+  if (need_gate) {
+    ENGRAM_CHECK_ARG(d->hidden >= 8 && d->hidden <= 8192 && d->hidden % 8 == 0,
+                     "hidden must be a multiple of 8 in [8, 8192] (got %d)", d->hidden);
+    ENGRAM_CHECK_ARG(d->hc >= 1 && d->hc <= 8, "hc must be in [1, 8] (got %d)", d->hc);
+    ENGRAM_CHECK_ARG(d->eps >= 0.f, "eps must be >= 0");
+    ENGRAM_CHECK_ARG(d->clamp >= 0.f, "clamp must be >= 0");
+  }
+  return ENGRAM_OK;
+}
+
+static int check_gather(int32_t fmt, const int32_t* ids, int64_t ids_stride_t, int64_t T, int32_t C,
+                        int32_t D, const void* table, const uint8_t* scales, int64_t num_rows,
+                        const uint16_t* out) {
+  ENGRAM_CHECK_ARG(T >= 0, "T must be >= 0");
+  ENGRAM_CHECK_ARG(C >= 1, "C must be >= 1");
+  ENGRAM_CHECK_ARG(ids_stride_t >= C, "ids_stride_t (%lld) must be >= C (%d)", (long long)ids_stride_t, C);
+  ENGRAM_CHECK_ARG(num_rows >= 0, "num_rows must be >= 0");
+  ENGRAM_CHECK_ARG(ids != nullptr && table != nullptr && out != nullptr, "ids, table and out must be non-NULL");
+  ENGRAM_CHECK_ARG(aligned(out, 16), "out must be 16-byte aligned");
+  switch (fmt) {
+    case ENGRAM_TABLE_FP8_E8M0:
+      ENGRAM_CHECK_ARG(D >= 32 && D % 32 == 0, "FP8 head_dim must be a multiple of 32 (got %d)", D);
+      ENGRAM_CHECK_ARG(scales != nullptr, "FP8 table needs scales");
+      ENGRAM_CHECK_ARG(aligned(table, 16), "FP8 table must be 16-byte aligned");
+      break;
+    case ENGRAM_TABLE_Q2K:
+      ENGRAM_CHECK_ARG(D == 256, "Q2_K rows are 256 wide (got head_dim %d)", D);
+      ENGRAM_CHECK_ARG(aligned(table, 4), "Q2_K table must be 4-byte aligned");
+      break;
+    case ENGRAM_TABLE_BF16:
+      ENGRAM_CHECK_ARG(D >= 8 && D % 8 == 0, "bf16 head_dim must be a multiple of 8 (got %d)", D);
+      ENGRAM_CHECK_ARG(aligned(table, 16), "bf16 table must be 16-byte aligned");
+      break;
+    default:
+      ENGRAM_CHECK_ARG(false, "unknown table format %d", fmt);
+  }
+  return ENGRAM_OK;
+}
+
+static int check_project(const uint16_t* A, const uint16_t* wkv, const uint16_t* kv, int64_t T, int32_t K,
+                         int32_t N) {
+  ENGRAM_CHECK_ARG(T >= 0 && T < (int64_t)1 << 31, "T must be in [0, 2^31)");
+  ENGRAM_CHECK_ARG(K >= 8 && K % 8 == 0, "K must be a positive multiple of 8 (got %d)", K);
+  ENGRAM_CHECK_ARG(N >= 16 && N % 16 == 0, "N must be a positive multiple of 16 (got %d)", N);
+  ENGRAM_CHECK_ARG(A != nullptr && wkv != nullptr && kv != nullptr, "A, wkv and kv must be non-NULL");
+  ENGRAM_CHECK_ARG(aligned(A, 16) && aligned(wkv, 16) && aligned(kv, 16), "A, wkv and kv must be 16-byte aligned");
+  return ENGRAM_OK;
+}
+
+static int check_gate(const EngramDims* d, const float* streams, const uint16_t* kv, const uint16_t* qw,
+                      const uint16_t* kw, int64_t T) {
+  int rc = check_dims(d, false, true);
+  if (rc) return rc;
+  ENGRAM_CHECK_ARG(T >= 0 && T < (int64_t)1 << 31, "T must be in [0, 2^31)");
+  ENGRAM_CHECK_ARG(streams && kv && qw && kw, "streams, kv, q_weight and k_weight must be non-NULL");
+  ENGRAM_CHECK_ARG(aligned(streams, 16) && aligned(kv, 16) && aligned(qw, 16) && aligned(kw, 16),
+                   "streams, kv, q_weight and k_weight must be 16-byte aligned");
+  return ENGRAM_OK;
+}
+
+static size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace engram
+
+using namespace engram;
+
+extern "C" {
+
+const char* engram_last_error(void) { return g_last_error.c_str(); }
+const char* engram_version(void) { return "libengram 0.1 (sm_103a)"; }
+
+void engram_set_gemm_tile(int32_t bn) {
+  set_gemm_bn_override((bn >= 16 && bn <= 256 && bn % 16 == 0) ? bn : 0);
+}
+
+int engram_hash(const EngramDims* dims, const int32_t* input_ids, int64_t T, const int32_t* cu_seqlens,
+                int32_t S, const int32_t* sequence_ids, const uint8_t* token_mask, const int32_t* lookback_ids,
+                const int32_t* token_map, const int64_t* multipliers, const int64_t* primes,
+                const int64_t* offsets, int32_t* out_ids, int32_t* err_flag, engram_stream_t stream) {
+  int rc = check_dims(dims, true, false);
+  if (rc) return rc;
+  ENGRAM_CHECK_ARG(T >= 0 && T < (int64_t)1 << 34, "T must be in [0, 2^34)");
+  if (T == 0) return ENGRAM_OK;
+  ENGRAM_CHECK_ARG(input_ids && token_map && multipliers && primes && offsets && out_ids,
+                   "input_ids, token_map, multipliers, primes, offsets and out_ids must be non-NULL");
+  if (cu_seqlens != nullptr) {
+    ENGRAM_CHECK_ARG(S >= 1, "cu_seqlens given with S = %d", S);
+  } else {
+    S = 1;
+  }
+  HashParams p{};
+  p.input_ids = input_ids;
+  p.cu_seqlens = cu_seqlens;
+  p.sequence_ids = sequence_ids;
+  p.token_mask = token_mask;
+  p.lookback_ids = lookback_ids;
+  p.token_map = token_map;
+  p.multipliers = multipliers;
+  p.primes = primes;
+  p.offsets = offsets;
+  p.out = out_ids;
+  p.err = err_flag;
+  p.T = T;
+  p.S = S;
+  p.layers = dims->layers;
+  p.max_ngram = dims->max_ngram;
+  p.n_heads = dims->n_heads;
+  p.cols = (dims->max_ngram - 1) * dims->n_heads;
+  p.raw_vocab = dims->raw_vocab;
+  p.pad_id = dims->pad_id;
+  cudaError_t e = launch_hash(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ENGRAM_OK : fail_cuda(e, "engram_hash: launch");
+}
+
+int engram_gather_dequant(int32_t fmt, const int32_t* ids, int64_t ids_stride_t, int64_t T, int32_t C,
+                          int32_t head_dim, const void* table, const uint8_t* scales, int64_t num_rows,
+                          uint16_t* out, int32_t* err_flag, engram_stream_t stream) {
+  if (T == 0) return ENGRAM_OK;
+  int rc = check_gather(fmt, ids, ids_stride_t, T, C, head_dim, table, scales, num_rows, out);
+  if (rc) return rc;
+  GatherParams p{fmt, ids, ids_stride_t, T, C, head_dim, table, scales, num_rows, out, err_flag};
+  cudaError_t e = launch_gather(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ENGRAM_OK : fail_cuda(e, "engram_gather_dequant: launch");
+}
+
+int engram_project(const uint16_t* A, const uint16_t* wkv, uint16_t* kv, int64_t T, int32_t K, int32_t N,
+                   void* workspace, size_t ws_bytes, int32_t* err_flag, engram_stream_t stream) {
+  (void)workspace;
+  (void)ws_bytes;
+  if (T == 0) return ENGRAM_OK;
+  int rc = check_project(A, wkv, kv, T, K, N);
+  if (rc) return rc;
+  GemmParams p{A, wkv, kv, T, K, N, err_flag};
+  return launch_gemm(p, static_cast<cudaStream_t>(stream));
+}
+
+int engram_gate(const EngramDims* dims, float* streams, const uint16_t* kv, const uint16_t* q_weight,
+                const uint16_t* k_weight, const uint8_t* token_mask, int64_t T, engram_stream_t stream) {
+  if (T == 0) return check_dims(dims, false, true);
+  int rc = check_gate(dims, streams, kv, q_weight, k_weight, T);
+  if (rc) return rc;
+  GateParams p{streams, kv, q_weight, k_weight, token_mask, T, dims->hidden, dims->hc, dims->eps, dims->clamp};
+  cudaError_t e = launch_gate(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ENGRAM_OK : fail_cuda(e, "engram_gate: launch");
+}
+
+size_t engram_forward_workspace_bytes(const EngramDims* d, int64_t T) {
+  if (d == nullptr || T < 0) return 0;
+  const int64_t C = (int64_t)(d->max_ngram - 1) * d->n_heads;
+  const int64_t K = C * d->head_dim;
+  const int64_t N = (int64_t)d->hidden * (d->hc + 1);
+  return round256((size_t)(T * d->layers * C * 4)) + round256((size_t)(T * K * 2)) + round256((size_t)(T * N * 2));
+}
+
+int engram_forward(const EngramDims* dims, const EngramHashTables* tables, const EngramLayerWeights* layers,
+                   const EngramTokens* tok, float* const* streams, void* workspace, size_t ws_bytes,
+                   int32_t* out_ids, int32_t* err_flag, engram_stream_t stream) {
+  int rc = check_dims(dims, true, true);
+  if (rc) return rc;
+  ENGRAM_CHECK_ARG(tables && layers && tok && streams, "tables, layers, tokens and streams must be non-NULL");
+  const int64_t T = tok->T;
+  ENGRAM_CHECK_ARG(T >= 0 && T < (int64_t)1 << 31, "T must be in [0, 2^31)");
+  if (T == 0) return ENGRAM_OK;
+  const int L = dims->layers;
+  const int C = (dims->max_ngram - 1) * dims->n_heads;
+  const int64_t K = (int64_t)C * dims->head_dim;
+  const int64_t N = (int64_t)dims->hidden * (dims->hc + 1);
+  ENGRAM_CHECK_ARG(K <= 0x7fffffff && N <= 0x7fffffff, "K or N too large");
+  const size_t need = engram_forward_workspace_bytes(dims, T);
+  ENGRAM_CHECK_ARG(workspace != nullptr && ws_bytes >= need, "workspace needs %zu bytes (got %zu)", need, ws_bytes);
+  ENGRAM_CHECK_ARG(aligned(workspace, 256), "workspace must be 256-byte aligned");
+  // validate every layer before launching anything
+  for (int l = 0; l < L; ++l) {
+    const EngramLayerWeights& w = layers[l];
+    rc = check_gather(w.table_format, reinterpret_cast<const int32_t*>(16), (int64_t)L * C, T, C, dims->head_dim,
+                      w.table, w.table_scales, w.table_rows, reinterpret_cast<const uint16_t*>(workspace));
+    if (rc) return rc;
+    rc = check_project(reinterpret_cast<const uint16_t*>(workspace), w.wkv, reinterpret_cast<const uint16_t*>(workspace),
+                       T, (int32_t)K, (int32_t)N);
+    if (rc) return rc;
+    rc = check_gate(dims, streams[l], reinterpret_cast<const uint16_t*>(workspace), w.q_weight, w.k_weight, T);
+    if (rc) return rc;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* ids = out_ids != nullptr ? out_ids : reinterpret_cast<int32_t*>(ws);
+  uint16_t* A = reinterpret_cast<uint16_t*>(ws + round256((size_t)(T * L * C * 4)));
+  uint16_t* kv = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(A) + round256((size_t)(T * K * 2)));
+
+  rc = engram_hash(dims, tok->input_ids, T, tok->cu_seqlens, tok->num_seqs, tok->sequence_ids, tok->token_mask,
+                   tok->lookback_ids, tables->token_map, tables->multipliers, tables->primes, tables->offsets, ids,
+                   err_flag, stream);
+  if (rc) return rc;
+  for (int l = 0; l < L; ++l) {
+    const EngramLayerWeights& w = layers[l];
+    rc = engram_gather_dequant(w.table_format, ids + (int64_t)l * C, (int64_t)L * C, T, C, dims->head_dim, w.table,
+                               w.table_scales, w.table_rows, A, err_flag, stream);
+    if (rc) return rc;
+    rc = engram_project(A, w.wkv, kv, T, (int32_t)K, (int32_t)N, nullptr, 0, err_flag, stream);
+    if (rc) return rc;
+    rc = engram_gate(dims, streams[l], kv, w.q_weight, w.k_weight, tok->token_mask, T, stream);
+    if (rc) return rc;
+  }
+  return ENGRAM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,239 @@
+// Stage 2: gather table rows by id and dequantise to bf16 rows of the projection operand.
+//
+// FP8-E4M3 rows with one E8M0 scale per 32 values follow the vLLM "deepseek_v41.common.engram"
+// page (ParallelEngramEmbedding, _engram_lookup_kernel: value * 2^(byte-127) in fp32, then
+// bf16; rows outside the table read as zeros). The 84-byte Q2_K row follows the Atlas
+// "engram_v41" page (stage 2, ENGRAM_ROW_BYTES), read as the public GGML Q2_K super-block.
+//
+// HBM-bound random row reads. FP8: one thread per 16-byte chunk of a row (16 threads per
+// 256-wide row, so a row is one coalesced 256-byte read), four chunks per thread in flight,
+// scales applied in registers, 32 bytes of bf16 written per chunk. Q2_K: one warp per row;
+// lanes 0..20 read the 84 bytes as 21 words (one coalesced read), shuffles hand each lane
+// the quants, scale nibbles and d/dmin of its 8 outputs.
+#include <cuda_fp8.h>
+
+#include "internal.cuh"
+
+namespace engram {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kChunksPerThread = 4;
+constexpr int kQ2kRowsPerWarp = 4;
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// two e4m3 bytes (low 16 bits of x) -> two floats, exactly
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t x) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(x & 0xFFFFu), __NV_E4M3);
+  return __half22float2(*reinterpret_cast<__half2*>(&h));
+}
+
+__device__ __forceinline__ uint32_t dequant_pair(uint32_t bytes2, float scale) {
+  float2 f = e4m3x2_to_float2(bytes2);
+  return pack_bf16x2(f.x * scale, f.y * scale);
+}
+
+__device__ __forceinline__ void flag(int32_t* err, int32_t bit) {
+  if (err != nullptr) atomicOr(err, bit);
+}
+
+// ---- FP8-E4M3 + E8M0 ------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads)
+gather_fp8_kernel(const GatherParams p) {
+  const int chunks_per_row = p.D >> 4;                 // 16 values per chunk
+  const int64_t total = p.T * p.C * chunks_per_row;
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  const uint8_t* __restrict__ weight = static_cast<const uint8_t*>(p.table);
+  const int sblocks = p.D >> 5;                        // scales per row
+
+  for (int64_t base = (int64_t)blockIdx.x * kThreads + threadIdx.x; base < total;
+       base += stride * kChunksPerThread) {
+    uint4 v[kChunksPerThread];
+    uint32_t sb[kChunksPerThread];
+    bool ok[kChunksPerThread];
+#pragma unroll
+    for (int u = 0; u < kChunksPerThread; ++u) {
+      const int64_t i = base + u * stride;
+      ok[u] = false;
+      v[u] = make_uint4(0, 0, 0, 0);
+      sb[u] = 0;
+      if (i < total) {
+        const int64_t r = i / chunks_per_row;
+        const int j = (int)(i - r * chunks_per_row);
+        const int64_t t = r / p.C;
+        const int col = (int)(r - t * p.C);
+        const int64_t id = __ldg(p.ids + t * p.ids_stride_t + col);
+        if (id >= 0 && id < p.num_rows) {
+          ok[u] = true;
+          v[u] = ld_stream_v4(weight + id * p.D + (j << 4));
+          sb[u] = __ldg(p.scales + id * sblocks + (j >> 1));
+        } else if (j == 0) {
+          flag(p.err, ENGRAM_ERR_ROW_ID);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kChunksPerThread; ++u) {
+      const int64_t i = base + u * stride;
+      if (i >= total) continue;
+      uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+      if (ok[u]) {
+        const float scale = __uint_as_float(sb[u] << 23);  // E8M0 byte is the fp32 exponent field
+        lo.x = dequant_pair(v[u].x, scale);
+        lo.y = dequant_pair(v[u].x >> 16, scale);
+        lo.z = dequant_pair(v[u].y, scale);
+        lo.w = dequant_pair(v[u].y >> 16, scale);
+        hi.x = dequant_pair(v[u].z, scale);
+        hi.y = dequant_pair(v[u].z >> 16, scale);
+        hi.z = dequant_pair(v[u].w, scale);
+        hi.w = dequant_pair(v[u].w >> 16, scale);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(p.out + (i << 4));   // chunk i -> 16 bf16 at 16*i
+      dst[0] = lo;
+      dst[1] = hi;
+    }
+  }
+}
+
+// ---- bf16 rows: copy ----------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads)
+gather_bf16_kernel(const GatherParams p) {
+  const int chunks_per_row = p.D >> 3;                 // 8 values per chunk
+  const int64_t total = p.T * p.C * chunks_per_row;
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  const uint16_t* __restrict__ table = static_cast<const uint16_t*>(p.table);
+  for (int64_t base = (int64_t)blockIdx.x * kThreads + threadIdx.x; base < total;
+       base += stride * kChunksPerThread) {
+    uint4 v[kChunksPerThread];
+#pragma unroll
+    for (int u = 0; u < kChunksPerThread; ++u) {
+      const int64_t i = base + u * stride;
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (i < total) {
+        const int64_t r = i / chunks_per_row;
+        const int j = (int)(i - r * chunks_per_row);
+        const int64_t t = r / p.C;
+        const int col = (int)(r - t * p.C);
+        const int64_t id = __ldg(p.ids + t * p.ids_stride_t + col);
+        if (id >= 0 && id < p.num_rows) {
+          v[u] = ld_stream_v4(table + id * p.D + (j << 3));
+        } else if (j == 0) {
+          flag(p.err, ENGRAM_ERR_ROW_ID);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kChunksPerThread; ++u) {
+      const int64_t i = base + u * stride;
+      if (i < total) reinterpret_cast<uint4*>(p.out)[i] = v[u];
+    }
+  }
+}
+
+// ---- Q2_K: one 84-byte super-block per 256-wide row ---------------------------------------
+// Element e: sub-block b = e/16 (scale = low nibble, min = high nibble of byte b),
+// quant = (qs[32*(e/128) + e%32] >> 2*((e%128)/32)) & 3, then d*scale*q - dmin*min.
+// Lane L writes elements 8L..8L+7: half = L/16, bit pair j = (L/4)%4, l0 = 8*(L%4), b = L/2.
+__global__ void __launch_bounds__(kThreads)
+gather_q2k_kernel(const GatherParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+  const int64_t rows = p.T * p.C;
+  const uint32_t* __restrict__ table = static_cast<const uint32_t*>(p.table);
+
+  const int half = lane >> 4;
+  const int jshift = 2 * ((lane >> 2) & 3);
+  const int qword = 4 + 8 * half + 2 * (lane & 3);      // word index of qs[32*half + l0]
+  const int sword = lane >> 3;                          // word holding scales[b], b = lane/2
+  const int sshift = 8 * ((lane >> 1) & 3);
+
+  for (int64_t r0 = warp * kQ2kRowsPerWarp; r0 < rows; r0 += nwarps * kQ2kRowsPerWarp) {
+    uint32_t word[kQ2kRowsPerWarp];
+    bool ok[kQ2kRowsPerWarp];
+#pragma unroll
+    for (int u = 0; u < kQ2kRowsPerWarp; ++u) {
+      const int64_t r = r0 + u;
+      ok[u] = false;
+      word[u] = 0;
+      if (r < rows) {
+        const int64_t t = r / p.C;
+        const int col = (int)(r - t * p.C);
+        const int64_t id = __ldg(p.ids + t * p.ids_stride_t + col);
+        ok[u] = id >= 0 && id < p.num_rows;
+        if (ok[u] && lane < 21) word[u] = __ldg(table + id * 21 + lane);
+        if (!ok[u] && lane == 0) flag(p.err, ENGRAM_ERR_ROW_ID);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kQ2kRowsPerWarp; ++u) {
+      const int64_t r = r0 + u;
+      const uint32_t q0 = __shfl_sync(0xffffffffu, word[u], qword);
+      const uint32_t q1 = __shfl_sync(0xffffffffu, word[u], qword + 1);
+      const uint32_t sw = __shfl_sync(0xffffffffu, word[u], sword);
+      const uint32_t dw = __shfl_sync(0xffffffffu, word[u], 20);
+      if (r >= rows) continue;
+      uint4 o = make_uint4(0, 0, 0, 0);
+      if (ok[u]) {
+        const uint32_t sc = (sw >> sshift) & 0xFFu;
+        const float d = __half2float(__ushort_as_half((unsigned short)(dw & 0xFFFFu)));
+        const float dmin = __half2float(__ushort_as_half((unsigned short)(dw >> 16)));
+        const float dl = d * (float)(sc & 15u);       // exact
+        const float nml = -(dmin * (float)(sc >> 4)); // exact
+        float y[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t byte = ((i < 4 ? q0 : q1) >> (8 * (i & 3))) & 0xFFu;
+          const float q = (float)((byte >> jshift) & 3u);
+          y[i] = fmaf(dl, q, nml);                    // dl*q exact: one rounding of the difference
+        }
+        o.x = pack_bf16x2(y[0], y[1]);
+        o.y = pack_bf16x2(y[2], y[3]);
+        o.z = pack_bf16x2(y[4], y[5]);
+        o.w = pack_bf16x2(y[6], y[7]);
+      }
+      reinterpret_cast<uint4*>(p.out + r * 256)[lane] = o;
+    }
+  }
+}
+
+unsigned grid_for(int64_t work_items, int64_t per_block) {
+  int64_t b = (work_items + per_block - 1) / per_block;
+  if (b < 1) b = 1;
+  const int64_t cap = (int64_t)num_sms() * 64;
+  return (unsigned)(b < cap ? b : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream) {
+  const int64_t rows = p.T * p.C;
+  switch (p.fmt) {
+    case ENGRAM_TABLE_FP8_E8M0:
+      gather_fp8_kernel<<<grid_for(rows * (p.D / 16), kThreads * kChunksPerThread), kThreads, 0, stream>>>(p);
+      break;
+    case ENGRAM_TABLE_BF16:
+      gather_bf16_kernel<<<grid_for(rows * (p.D / 8), kThreads * kChunksPerThread), kThreads, 0, stream>>>(p);
+      break;
+    case ENGRAM_TABLE_Q2K:
+      gather_q2k_kernel<<<grid_for(rows, (kThreads / 32) * kQ2kRowsPerWarp), kThreads, 0, stream>>>(p);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace engram

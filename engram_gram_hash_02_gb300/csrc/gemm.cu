@@ -1,0 +1,423 @@
+// Stage 3: the wkv projection kv[T, N] = A[T, K] * wkv[N, K]^T on tcgen05 tensor cores.
+//
+// The projection of the vLLM "deepseek_v41.common.engram" page (Engram.__init__: wkv maps
+// n_hash_cols*head_dim -> dim*(hc+1); Engram.forward) and of the Atlas "engram_v41" page
+// (stage 3: dense bf16 GEMM). bf16 operands, fp32 accumulation in tensor memory, bf16 out.
+//
+// One CTA computes a tile of up to 256 rows (two 128-row accumulators) x BN columns:
+//   warp 0      TMA producer: 128B-swizzled K-major tiles of A (128 rows x 64) and of wkv
+//               (BN rows x 64) into a ring of shared-memory stages, mbarrier complete_tx.
+//   warp 1      allocates tensor memory; one lane issues tcgen05.mma (M=128, N=BN, K=16,
+//               kind::f16) per 16-wide k step and releases a stage with tcgen05.commit.
+//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator (each warp its 32-lane quarter),
+//               bf16 round, 16-byte stores to kv.
+// Both tiles of a 256-row block share each wkv tile, so wkv is read from memory once per
+// column block. BN is picked per shape so the number of tiles fills the SMs in few waves.
+//
+// Every mbarrier wait is bounded (2 s of %globaltimer); on expiry the CTA raises an abort
+// flag, reports ENGRAM_ERR_PIPE_TIMEOUT, drains its in-flight copies and MMAs (again
+// bounded), frees its tensor memory and exits.
+#include <cuda.h>
+
+#include <mutex>
+
+#include "internal.cuh"
+
+namespace engram {
+namespace {
+
+constexpr int kBK = 64;                    // k elements per stage (128 bytes = one swizzle row)
+constexpr int kUmmaK = 16;                 // k per tcgen05.mma for 16-bit operands
+constexpr int kThreads = 192;
+constexpr int kMaxStages = 8;
+constexpr int kATileBytes = 128 * kBK * 2;  // 16 KB
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr int kSmemBudget = 232448;        // 227 KB opt-in maximum per CTA
+
+struct Ctl {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t acc_full;
+  uint32_t tmem_base;
+  int32_t abort_flag;
+};
+
+struct GemmArgs {
+  int32_t M, K, N;
+  int32_t BN, msub, stages, num_kb;
+  int32_t m_tiles, n_tiles, group_m;
+  int32_t stage_bytes;
+  uint32_t idesc;
+  uint32_t tmem_cols, acc_stride;
+  int32_t* err;
+};
+
+// ---- PTX wrappers ------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false if this CTA aborted (here or in another role).
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int32_t* abort_flag,
+                                       int32_t* err, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > limit_ns) {
+        *abort_flag = 1;
+        if (err != nullptr) atomicOr(err, ENGRAM_ERR_PIPE_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// 32 lanes x 16 columns of 32-bit accumulator: thread i gets lane (quarter*32 + i)
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand stored as 128-byte rows with the 128B
+// swizzle (what TMA writes with CU_TENSOR_MAP_SWIZZLE_128B); 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address
+  d |= (uint64_t)1 << 16;                      // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;            // stride byte offset: next 8-row group
+  d |= (uint64_t)1 << 46;                      // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;                      // 128-byte swizzle
+  return d;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo_f32), __uint_as_float(hi_f32));
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                uint16_t* __restrict__ D, const GemmArgs a) {
+  // a timeout anywhere in this launch (or an earlier one sharing the flag word) voids the
+  // result: later CTAs do no work instead of each waiting out its own time limit
+  if (a.err != nullptr && (*reinterpret_cast<volatile int32_t*>(a.err) & ENGRAM_ERR_PIPE_TIMEOUT)) return;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t tiles = (raw_base + 1023u) & ~1023u;          // swizzled tiles need 1 KB alignment
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem_raw + (tiles - raw_base) + a.stages * a.stage_bytes);
+  volatile int32_t* abort_flag = &ctl->abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // grouped raster: consecutive CTAs sweep group_m row blocks of one column block
+  const int tile = blockIdx.x;
+  const int per_group = a.group_m * a.n_tiles;
+  const int first_m = (tile / per_group) * a.group_m;
+  const int gsize = min(a.m_tiles - first_m, a.group_m);
+  const int in_group = tile % per_group;
+  const int m_blk = first_m + in_group % gsize;
+  const int n_blk = in_group / gsize;
+  const int m0 = m_blk * 128 * a.msub;
+  const int n0 = n_blk * a.BN;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+    }
+    mbar_init(smem_u32(&ctl->acc_full), 1);
+    ctl->abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&ctl->tmem_base)),
+                 "r"(a.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int issued = 0;
+      bool ok = true;
+      for (int kb = 0; kb < a.num_kb; ++kb) {
+        const int s = kb % a.stages;
+        const uint32_t ph = (uint32_t)(kb / a.stages) & 1u;
+        if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, a.err, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        const uint32_t full = smem_u32(&ctl->full[s]);
+        const uint32_t st = tiles + (uint32_t)(s * a.stage_bytes);
+        mbar_expect_tx(full, (uint32_t)a.stage_bytes);
+        tma_load_2d(st, &tmA, full, kb * kBK, m0);
+        if (a.msub == 2) tma_load_2d(st + kATileBytes, &tmA, full, kb * kBK, m0 + 128);
+        tma_load_2d(st + a.msub * kATileBytes, &tmB, full, kb * kBK, n0);
+        issued = kb + 1;
+      }
+      if (!ok) {
+        // drain: the copies still in flight must land before shared memory goes away
+        const int first = issued > a.stages ? issued - a.stages : 0;
+        for (int kb = first; kb < issued; ++kb) {
+          const int s = kb % a.stages;
+          const uint32_t ph = (uint32_t)(kb / a.stages) & 1u;
+          volatile int32_t never = 0;
+          mbar_wait(smem_u32(&ctl->full[s]), ph, &never, nullptr, kWaitLimitNs / 4);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      for (int kb = 0; kb < a.num_kb; ++kb) {
+        const int s = kb % a.stages;
+        const uint32_t ph = (uint32_t)(kb / a.stages) & 1u;
+        if (!mbar_wait(smem_u32(&ctl->full[s]), ph, abort_flag, a.err, kWaitLimitNs)) break;
+        tc_fence_after();
+        const uint32_t st = tiles + (uint32_t)(s * a.stage_bytes);
+        const uint32_t b_addr = st + (uint32_t)(a.msub * kATileBytes);
+#pragma unroll
+        for (int k = 0; k < kBK / kUmmaK; ++k) {
+          const uint64_t bdesc = smem_desc_sw128(b_addr + k * kUmmaK * 2);
+          for (int ms = 0; ms < a.msub; ++ms) {
+            const uint64_t adesc = smem_desc_sw128(st + ms * kATileBytes + k * kUmmaK * 2);
+            tc_mma(tmem + ms * a.acc_stride, adesc, bdesc, a.idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+        }
+        tc_commit(smem_u32(&ctl->empty[s]));   // stage free once these MMAs have read it
+      }
+      tc_commit(smem_u32(&ctl->acc_full));     // accumulators final (or drained, on abort)
+    }
+  } else {
+    // ---------------- epilogue: TMEM -> registers -> bf16 -> global ----------------
+    const int q = warp & 3;                    // TMEM lane quarter this warp may access
+    const bool ok = mbar_wait(smem_u32(&ctl->acc_full), 0, abort_flag, a.err, kWaitLimitNs);
+    tc_fence_after();
+    if (ok && *abort_flag == 0) {
+      for (int ms = 0; ms < a.msub; ++ms) {
+        const int64_t row = (int64_t)m0 + ms * 128 + q * 32 + lane;
+        const bool row_ok = row < a.M;
+        uint16_t* drow = D + row * (int64_t)a.N;
+        for (int c = 0; c < a.BN; c += 16) {
+          uint32_t r[16];
+          tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ms * a.acc_stride + c), r);
+          tmem_ld_wait();
+          const int col = n0 + c;
+          if (row_ok && col < a.N) {
+            uint4 lo, hi;
+            lo.x = pack_bf16x2(r[0], r[1]);   lo.y = pack_bf16x2(r[2], r[3]);
+            lo.z = pack_bf16x2(r[4], r[5]);   lo.w = pack_bf16x2(r[6], r[7]);
+            hi.x = pack_bf16x2(r[8], r[9]);   hi.y = pack_bf16x2(r[10], r[11]);
+            hi.z = pack_bf16x2(r[12], r[13]); hi.w = pack_bf16x2(r[14], r[15]);
+            uint4* dst = reinterpret_cast<uint4*>(drow + col);
+            dst[0] = lo;
+            dst[1] = hi;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    if (*abort_flag) {
+      // make sure no MMA is still writing the accumulators we are about to free
+      volatile int32_t never = 0;
+      mbar_wait(smem_u32(&ctl->acc_full), 0, &never, nullptr, kWaitLimitNs / 4);
+    }
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols)
+                 : "memory");
+  }
+}
+
+// ---- host side ------------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 map over a row-major [rows, K] matrix; box = 64 k x box_rows rows, 128B swizzle
+bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int g_bn_override = 0;  // engram_set_gemm_tile
+
+int pick_bn(int64_t m_tiles, int N, int sms) {
+  if (g_bn_override > 0) return g_bn_override;
+  int best = 256;
+  double best_cost = 1e300;
+  for (int bn = 256; bn >= 64; bn -= 16) {
+    const int64_t tiles = m_tiles * ((N + bn - 1) / bn);
+    const int64_t waves = (tiles + sms - 1) / sms;
+    // a wave costs about its tile width plus a fixed share for the A operand and setup
+    const double cost = (double)waves * (bn + 48);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+uint32_t pow2_at_least(uint32_t x) {
+  uint32_t p = 32;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+}  // namespace
+
+void set_gemm_bn_override(int bn) { g_bn_override = bn; }
+
+int launch_gemm(const GemmParams& p, cudaStream_t stream) {
+  const int sms = num_sms();
+  GemmArgs a{};
+  a.M = (int32_t)p.M;
+  a.K = p.K;
+  a.N = p.N;
+  a.msub = p.M > 128 ? 2 : 1;
+  a.m_tiles = (int32_t)((p.M + 128 * a.msub - 1) / (128 * a.msub));
+  a.BN = pick_bn(a.m_tiles, p.N, sms);
+  a.n_tiles = (p.N + a.BN - 1) / a.BN;
+  a.group_m = 16;
+  a.num_kb = (p.K + kBK - 1) / kBK;
+  a.stage_bytes = a.msub * kATileBytes + a.BN * kBK * 2;
+  const int ctl_bytes = (int)sizeof(Ctl);
+  a.stages = (kSmemBudget - 1024 - ctl_bytes) / a.stage_bytes;
+  if (a.stages > kMaxStages) a.stages = kMaxStages;
+  if (a.stages < 2) {
+    set_error("engram_project: tile of %d columns does not fit shared memory", a.BN);
+    return ENGRAM_EINVAL;
+  }
+  a.acc_stride = pow2_at_least((uint32_t)a.BN);
+  a.tmem_cols = a.acc_stride * a.msub;
+  a.idesc = (1u << 4)                         // accumulate in f32
+            | (1u << 7) | (1u << 10)          // A and B are bf16
+            | ((uint32_t)(a.BN >> 3) << 17)   // N
+            | ((uint32_t)(128 >> 4) << 24);   // M = 128; A and B K-major (bits 15, 16 = 0)
+  a.err = p.err;
+
+  CUtensorMap mA, mB;
+  if (!make_map(&mA, p.A, p.M, p.K, 128) || !make_map(&mB, p.B, p.N, p.K, (uint32_t)a.BN)) {
+    set_error("engram_project: cuTensorMapEncodeTiled failed (driver entry point missing or bad layout)");
+    return ENGRAM_ECUDA;
+  }
+  const int smem = 1024 + a.stages * a.stage_bytes + ctl_bytes;
+  static bool configured[64] = {false};     // the attribute is per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(wkv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+    if (e != cudaSuccess) return fail_cuda(e, "engram_project: cudaFuncSetAttribute");
+    if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
+  const int64_t grid = (int64_t)a.m_tiles * a.n_tiles;
+  if (grid > 0x7fffffff) {
+    set_error("engram_project: too many tiles");
+    return ENGRAM_EINVAL;
+  }
+  wkv_gemm_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(mA, mB, p.D, a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_cuda(e, "engram_project: launch");
+  return ENGRAM_OK;
+}
+
+}  // namespace engram

@@ -1,0 +1,86 @@
+// Internal declarations shared by the CUDA translation units of libengram.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/engram.h"
+
+namespace engram {
+
+// ---- host-side error reporting -------------------------------------------------------
+void set_error(const char* fmt, ...);
+int fail_cuda(cudaError_t e, const char* what);
+
+#define ENGRAM_CHECK_ARG(cond, ...)            \
+  do {                                          \
+    if (!(cond)) {                              \
+      ::engram::set_error(__VA_ARGS__);         \
+      return ENGRAM_EINVAL;                     \
+    }                                           \
+  } while (0)
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int num_sms();  // of the current device, cached per device
+
+// ---- launchers (validated arguments only) ---------------------------------------------
+struct HashParams {
+  const int32_t* input_ids;
+  const int32_t* cu_seqlens;
+  const int32_t* sequence_ids;
+  const uint8_t* token_mask;
+  const int32_t* lookback_ids;
+  const int32_t* token_map;
+  const int64_t* multipliers;
+  const int64_t* primes;
+  const int64_t* offsets;
+  int32_t* out;
+  int32_t* err;
+  int64_t T;
+  int32_t S;
+  int32_t layers, max_ngram, n_heads, cols;
+  int32_t raw_vocab, pad_id;
+};
+cudaError_t launch_hash(const HashParams& p, cudaStream_t stream);
+
+struct GatherParams {
+  int32_t fmt;
+  const int32_t* ids;
+  int64_t ids_stride_t;
+  int64_t T;
+  int32_t C, D;
+  const void* table;
+  const uint8_t* scales;
+  int64_t num_rows;
+  uint16_t* out;
+  int32_t* err;
+};
+cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
+
+struct GemmParams {
+  const uint16_t* A;
+  const uint16_t* B;
+  uint16_t* D;
+  int64_t M;
+  int32_t K, N;
+  int32_t* err;
+};
+// returns ENGRAM_OK or an error code (sets the message)
+int launch_gemm(const GemmParams& p, cudaStream_t stream);
+
+struct GateParams {
+  float* streams;
+  const uint16_t* kv;
+  const uint16_t* q_weight;
+  const uint16_t* k_weight;
+  const uint8_t* token_mask;
+  int64_t T;
+  int32_t H, hc;
+  float eps, clamp;
+};
+cudaError_t launch_gate(const GateParams& p, cudaStream_t stream);
+
+}  // namespace engram

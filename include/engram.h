@@ -1,0 +1,229 @@
+/*
+ * libengram: the DeepSeek-V4.1 Engram residual-memory hot path on one GB300.
+ *
+ *   hash -> gather + dequant -> wkv projection -> gate (in place)
+ *
+ * Sources of the operation (pages, by title and section):
+ *   [Atlas] "spark_model::layers::engram_v41" rustdoc: module overview, stages 1-4,
+ *           constant ENGRAM_ROW_BYTES.
+ *   [NeMo]  "nemo_automodel.components.models.deepseek_v41.engram": DeepseekV41Engram.forward,
+ *           DeepseekV41NgramHash.forward, _engram_gate_core.
+ *   [vLLM]  "vllm.models.deepseek_v41.common.engram": Engram, EngramLayout, NgramHashState,
+ *           ParallelEngramEmbedding.lookup / _engram_lookup_kernel, compute_hash_multipliers,
+ *           find_next_prime, _is_prime.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named "device" are device memory owned by the caller; the library keeps no
+ *     reference after the call returns and (except where stated) allocates nothing.
+ *   - bf16 tensors are passed as uint16_t bit patterns.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Work is enqueued on it and
+ *     the call returns without synchronising.
+ *   - Return value: ENGRAM_OK (0), or a negative code; engram_last_error() then returns a
+ *     thread-local message. Arguments are checked on the host before any launch; a failed
+ *     check launches nothing.
+ *   - Data-dependent faults found on the device (an id outside its range) never trap: the
+ *     kernel substitutes the documented value and ORs a bit into the caller's `err_flag`
+ *     word (device int32, may be NULL to skip reporting). The caller reads it when it likes.
+ *   - T == 0 is a no-op that returns ENGRAM_OK.
+ */
+#ifndef ENGRAM_H_
+#define ENGRAM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ENGRAM_OK 0
+#define ENGRAM_EINVAL (-1) /* bad argument (shape, pointer, alignment, format) */
+#define ENGRAM_ECUDA (-2)  /* a CUDA call or launch failed */
+
+/* bits of the device err_flag word */
+#define ENGRAM_ERR_RAW_ID 1        /* raw input id outside [0, raw_vocab): used pad_id */
+#define ENGRAM_ERR_ROW_ID 2        /* row id outside [0, num_rows): wrote a zero row */
+#define ENGRAM_ERR_PIPE_TIMEOUT 4  /* a GEMM pipeline wait ran past its time limit */
+
+typedef void* engram_stream_t; /* a cudaStream_t */
+
+/* Table row formats. */
+enum EngramTableFmt {
+  ENGRAM_TABLE_BF16 = 0,    /* bf16 [rows, head_dim] */
+  ENGRAM_TABLE_FP8_E8M0 = 1,/* e4m3 [rows, head_dim] + one E8M0 byte per 32 values [rows, head_dim/32] */
+  ENGRAM_TABLE_Q2K = 2      /* one 84-byte Q2_K super-block per 256-wide row [rows, 84] */
+};
+
+/*
+ * Model dimensions ([vLLM] EngramLayout fields; [NeMo] DeepseekV41Engram attributes).
+ *   layers           engram layers sharing one hash call (len(engram_layer_ids))
+ *   max_ngram        n-gram sizes 2..max_ngram are hashed; lookback depth is max_ngram-1
+ *   n_heads          hash heads per n-gram size; C = (max_ngram-1)*n_heads columns
+ *   head_dim         D, width of one table row
+ *   hidden           H
+ *   hc               hc_mult, number of highway streams
+ *   raw_vocab        entries of token_map
+ *   compressed_vocab V; every compressed id and pad_id lies in [0, V)
+ *   pad_id           compressed id that fills unavailable window slots
+ *   eps              rms_norm_eps of the two branch norms
+ *   clamp            lower clamp of |score| before the signed square root (1e-6)
+ */
+typedef struct EngramDims {
+  int32_t layers, max_ngram, n_heads, head_dim, hidden, hc;
+  int32_t raw_vocab, compressed_vocab, pad_id;
+  float eps, clamp;
+} EngramDims;
+
+const char* engram_last_error(void);
+const char* engram_version(void);
+
+/*
+ * Host-side layout ([vLLM] EngramLayout.__init__, find_next_prime, _is_prime).
+ * For each layer and each n-gram size the search restarts above vocab_size-1 and takes
+ * n_heads successive primes never handed out before in the model. Columns are n-gram size
+ * major, head minor. offsets are the exclusive running sum of a layer's primes.
+ *   primes_out  host int64 [layers, C]     offsets_out host int64 [layers, C]
+ *   rows_out    host int64 [layers]        (table rows a layer needs = sum of its primes)
+ * Host memory only, no GPU needed. vocab_size + all primes must stay below 2^32.
+ */
+int engram_layout(int64_t vocab_size, int32_t layers, int32_t max_ngram, int32_t n_heads,
+                  int64_t* primes_out, int64_t* offsets_out, int64_t* rows_out);
+
+/*
+ * Stage 1: n-gram hash ids ([NeMo] DeepseekV41NgramHash.forward; [vLLM] NgramHashState.forward;
+ * [Atlas] stage 1).
+ * For token t, layer l, n-gram size n and head h (column c = (n-2)*n_heads + h):
+ *     mix = XOR_{k<n} ( w_k(t) * multipliers[l][k] )        (int64, each product < 2^63)
+ *     out = offsets[l][c] + mix mod primes[l][c]
+ * where w_k(t) is the compressed id k positions back, or pad_id once the walk back from t
+ * meets: a dead position (token_mask 0 or sequence_ids 0; a dead t pads its whole window), a
+ * change of sequence_ids between neighbours, the start of t's sequence (cu_seqlens), or, in
+ * the lookback row, an entry < 0. lookback_ids[s][i] is the compressed id at position
+ * cu_seqlens[s] - (max_ngram-1) + i and belongs to the document of the chunk's first token.
+ *   input_ids     device int32 [T] raw tokenizer ids; ids outside [0, raw_vocab) hash as pad_id
+ *                 and set ENGRAM_ERR_RAW_ID
+ *   cu_seqlens    device int32 [S+1], 0 = cu[0] <= ... <= cu[S] = T; NULL = one sequence [0, T)
+ *   sequence_ids  device int32 [T] document ids, 0 = padding; NULL = none
+ *   token_mask    device uint8 [T], 0 = image/padding; NULL = all valid
+ *   lookback_ids  device int32 [S, max_ngram-1] compressed ids, < 0 = unavailable; NULL = none
+ *   token_map     device int32 [raw_vocab] raw -> compressed id
+ *   multipliers   device int64 [layers, max_ngram], odd, multiplier * (V-1) < 2^63
+ *   primes        device int64 [layers, C]      offsets device int64 [layers, C]
+ *   out_ids       device int32 [T, layers, C]   (offsets + primes must fit int32)
+ * Requires 2 <= max_ngram <= 8, layers * C <= 256.
+ */
+int engram_hash(const EngramDims* dims, const int32_t* input_ids, int64_t T,
+                const int32_t* cu_seqlens, int32_t S, const int32_t* sequence_ids,
+                const uint8_t* token_mask, const int32_t* lookback_ids,
+                const int32_t* token_map, const int64_t* multipliers, const int64_t* primes,
+                const int64_t* offsets, int32_t* out_ids, int32_t* err_flag,
+                engram_stream_t stream);
+
+/*
+ * Stage 2: gather rows by id and dequantise to bf16 ([vLLM] _engram_lookup_kernel;
+ * [Atlas] stage 2, ENGRAM_ROW_BYTES).
+ *   FP8_E8M0: y = bf16_rne( float(e4m3 v) * float(bits = scale_byte << 23) ), one scale per 32.
+ *   Q2K:      element e of the 84-byte block (16 B sub-block scale|min<<4, 64 B 2-bit quants,
+ *             fp16 d, fp16 dmin): q = (qs[32*(e/128) + e%32] >> 2*((e%128)/32)) & 3,
+ *             y = bf16_rne( d*(sc&15)*q - dmin*(sc>>4) ) with sc = scales[e/16].
+ *   BF16:     copy.
+ * Ids outside [0, num_rows) give a zero row and set ENGRAM_ERR_ROW_ID.
+ *   ids          device int32, row t at ids + t*ids_stride_t, C contiguous entries
+ *   table        device, format `fmt`, 16-byte aligned (4-byte for Q2K)
+ *   scales       device uint8 [num_rows, head_dim/32] for FP8_E8M0, else ignored
+ *   out          device bf16 [T, C*head_dim] row-major (row t = C rows of head_dim), 16-byte aligned
+ * head_dim: multiple of 32 (FP8), 256 (Q2K), 8 (BF16).
+ */
+int engram_gather_dequant(int32_t fmt, const int32_t* ids, int64_t ids_stride_t, int64_t T,
+                          int32_t C, int32_t head_dim, const void* table, const uint8_t* scales,
+                          int64_t num_rows, uint16_t* out, int32_t* err_flag,
+                          engram_stream_t stream);
+
+/*
+ * Stage 3: wkv projection kv = A * wkv^T ([vLLM] Engram.__init__ (wkv) and Engram.forward;
+ * [Atlas] stage 3). bf16 operands, fp32 accumulation on tcgen05 tensor cores, bf16 output.
+ *   A    device bf16 [T, K] row-major       wkv device bf16 [N, K] row-major (nn.Linear layout)
+ *   kv   device bf16 [T, N] row-major; columns [j*H, (j+1)*H) are stream j's key, [hc*H, N)
+ *        the shared value
+ * K % 8 == 0, N % 16 == 0, all three 16-byte aligned. workspace/ws_bytes are unused (pass
+ * NULL/0). ENGRAM_ERR_PIPE_TIMEOUT in err_flag means the result is invalid; while that bit is
+ * set in the word passed, later calls with the same word skip the work.
+ */
+int engram_project(const uint16_t* A, const uint16_t* wkv, uint16_t* kv, int64_t T, int32_t K,
+                   int32_t N, void* workspace, size_t ws_bytes, int32_t* err_flag,
+                   engram_stream_t stream);
+
+/* Tuning knob for engram_project: force the tile width (columns per CTA, a multiple of 16 in
+ * [16, 256]); 0 restores the automatic choice. Process-wide; not thread-safe against calls. */
+void engram_set_gemm_tile(int32_t bn);
+
+/*
+ * Stage 4: gate, in place on the fp32 highway ([NeMo] _engram_gate_core; [vLLM]
+ * Engram.forward; [Atlas] stage 4). For each token t with token_mask[t] != 0 and stream j:
+ *   s   = <h_j * rsqrt(mean(h_j^2)+eps) * q_weight[j], key_j * rsqrt(mean(key_j^2)+eps) * k_weight[j]> / sqrt(H)
+ *   g   = sigmoid( sign(s) * sqrt(max(|s|, clamp)) )
+ *   h_j = h_j + g * value
+ * Masked tokens are not read or written.
+ *   streams   device fp32 [T, hc, H] (in/out), 16-byte aligned
+ *   kv        device bf16 [T, (hc+1)*H] (output of engram_project)
+ *   q_weight, k_weight device bf16 [hc, H]
+ *   token_mask device uint8 [T] or NULL
+ * H % 8 == 0, 8 <= H <= 8192, 1 <= hc <= 8.
+ */
+int engram_gate(const EngramDims* dims, float* streams, const uint16_t* kv,
+                const uint16_t* q_weight, const uint16_t* k_weight, const uint8_t* token_mask,
+                int64_t T, engram_stream_t stream);
+
+/* Per-layer resident weights ([Atlas] EngramLayerWeights; [vLLM] Engram parameters). */
+typedef struct EngramLayerWeights {
+  int32_t table_format;        /* EngramTableFmt */
+  const void* table;           /* device, see engram_gather_dequant */
+  const uint8_t* table_scales; /* device, FP8_E8M0 only */
+  int64_t table_rows;
+  const uint16_t* wkv;         /* device bf16 [(hc+1)*H, C*head_dim] */
+  const uint16_t* q_weight;    /* device bf16 [hc, H] */
+  const uint16_t* k_weight;    /* device bf16 [hc, H] */
+} EngramLayerWeights;
+
+/* Hash tables ([Atlas] EngramHashTables). All device memory. */
+typedef struct EngramHashTables {
+  const int32_t* token_map;   /* [raw_vocab] */
+  const int64_t* multipliers; /* [layers, max_ngram] */
+  const int64_t* primes;      /* [layers, C] */
+  const int64_t* offsets;     /* [layers, C] */
+} EngramHashTables;
+
+/* One call's tokens. All device memory; see engram_hash. */
+typedef struct EngramTokens {
+  const int32_t* input_ids;
+  int64_t T;
+  const int32_t* cu_seqlens;
+  int32_t num_seqs;
+  const int32_t* sequence_ids;
+  const uint8_t* token_mask;
+  const int32_t* lookback_ids;
+} EngramTokens;
+
+/* Bytes of device workspace engram_forward needs for T tokens (256-byte aligned pieces:
+ * hash ids [T, layers, C] int32, rows [T, C*head_dim] bf16, kv [T, (hc+1)*H] bf16). */
+size_t engram_forward_workspace_bytes(const EngramDims* dims, int64_t T);
+
+/*
+ * The whole path: one hash launch for all layers, then per layer gather -> project -> gate.
+ *   layers     host array [dims->layers] of per-layer weights
+ *   streams    host array [dims->layers] of device fp32 [T, hc, H] highways, updated in place
+ *   workspace  device, >= engram_forward_workspace_bytes(dims, T), 256-byte aligned
+ *   out_ids    device int32 [T, layers, C] or NULL: if given, the hash writes the ids there
+ *              (and the workspace's id region goes unused)
+ * Launches 1 + 3*layers kernels on `stream`.
+ */
+int engram_forward(const EngramDims* dims, const EngramHashTables* tables,
+                   const EngramLayerWeights* layers, const EngramTokens* tokens,
+                   float* const* streams, void* workspace, size_t ws_bytes, int32_t* out_ids,
+                   int32_t* err_flag, engram_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ENGRAM_H_ */

@@ -1,0 +1,543 @@
+"""Benchmark of the Engram hot path (hash -> gather/dequant -> wkv projection -> gate).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step is one pass of the whole path over one batch of the workload (default: the decode
+step, 256 sequences x 1 new token, FP8+E8M0 table of ~25M rows, hidden 4096, hc 4).  Inputs
+are resident in HBM; the L2 is flushed (512 MB write) before every timed step; each step is
+timed with CUDA events on the launching stream, per kernel as well.  Under torchrun every
+rank runs its own replica (the path needs no exchange): weak scaling, max time over ranks.
+
+--impl reference times the CPU oracle (oracle/) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from engram_synth import get_workload  # noqa: E402
+from engram_synth.case import make_case, to_device  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+
+# DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by kernel and
+# workload, with the sha256 of the kernel's source at capture time (stale -> traffic null).
+NCU_TRAFFIC: dict = {}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def src_sha(name: str) -> str:
+    with open(os.path.join(ROOT, "engram_gram_hash_02_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for r in csv.reader(io.StringIO(out)):
+            if len(r) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(r[0].strip().split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(r[2]), float(r[3]), [x.strip() for x in r[6:10]], r[5].strip()))
+            except Exception:
+                continue
+        inside = [x for x in rows if self.t0 - 1 <= x[0] <= self.t1 + 1] or rows
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for x in inside for i, v in enumerate(x[3]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median([x[1] for x in inside])), "sm_max_mhz": max(x[2] for x in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ------------------------------------------------------------------------------------------------
+# the CUDA path
+# ------------------------------------------------------------------------------------------------
+
+class Path:
+    """Device-resident workload plus pre-marshalled C-ABI calls for each stage."""
+
+    def __init__(self, w, device, table_rows=None):
+        import ctypes as C
+
+        import engram_gram_hash_02_gb300 as E
+        from engram_gram_hash_02_gb300 import binding as B
+        self.E, self.C, self.B = E, C, B
+        self.w, self.device = w, device
+        if table_rows:
+            # profiling only: primes near table_rows / cols, so the table holds about table_rows
+            # rows and every hashed id stays inside it
+            from dataclasses import replace
+            w = replace(w, vocab_size=max(1024, int(table_rows) // w.cols))
+            self.w = w
+        primes, offsets, rows, mult = self._layout(E, w)
+        self.case = case = make_case(w, rows, device)
+        b = case.batch
+        self.pad = int(b["token_map"][w.pad_token_id])
+        self.dims = E.make_dims(w.layers, w.max_ngram, w.n_heads, w.head_dim, w.hidden, w.hc, w.raw_vocab,
+                                w.compressed_vocab, self.pad, w.eps, w.clamp)
+        d = device
+        self.input_ids = to_device(b["input_ids"], d)
+        self.cu = to_device(b["cu_seqlens"], d)
+        self.sid = to_device(b["sequence_ids"], d)
+        self.mask = to_device(b["token_mask"], d)
+        self.lookback = to_device(b["lookback_ids"], d)
+        self.tables = E.HashTables(to_device(b["token_map"], d), to_device(mult, d), to_device(primes, d),
+                                   to_device(offsets, d))
+        self.layers = [E.LayerWeights(t["fmt"], t["table"], t["scales"], t["num_rows"], case.wkv[l],
+                                      case.q_weight[l], case.k_weight[l]) for l, t in enumerate(case.tables)]
+        self.streams = [s.clone() for s in case.streams]
+        T, L, Cc, K, N = w.tokens, w.layers, w.cols, w.K, w.N
+        self.ids = torch.empty((T, L, Cc), dtype=torch.int32, device=d)
+        self.A = torch.empty((T, K), dtype=torch.bfloat16, device=d)
+        self.kv = torch.empty((T, N), dtype=torch.bfloat16, device=d)
+        self.err = torch.zeros(1, dtype=torch.int32, device=d)
+        self.table_rows = rows
+
+    @staticmethod
+    def _layout(E, w):
+        primes, offsets, rows = E.engram_layout(w.vocab_size, w.layers, w.max_ngram, w.n_heads)
+        mult = E.hash_multipliers(w.layer_ids, w.max_ngram, w.compressed_vocab)
+        return primes, offsets, rows, mult
+
+    def stage_calls(self, stream):
+        """One closure per kernel launch of a step, in order, with arguments marshalled once."""
+        lib, B, w, C = self.E.lib(), self.B, self.w, self.C
+        p = B._ptr
+        s = stream.cuda_stream
+        T, L, Cc, K, N = w.tokens, w.layers, w.cols, w.K, w.N
+        dims = self.dims
+        S = self.cu.numel() - 1
+        hash_args = (C.byref(dims), p(self.input_ids), T, p(self.cu), S, p(self.sid), p(self.mask),
+                     p(self.lookback), p(self.tables.token_map), p(self.tables.multipliers),
+                     p(self.tables.primes), p(self.tables.offsets), p(self.ids), p(self.err), s)
+        calls = [("hash", lambda: lib.engram_hash(*hash_args))]
+        for l, lw in enumerate(self.layers):
+            g_args = (B.TABLE_FORMATS[lw.fmt], self.ids.data_ptr() + 4 * l * Cc, L * Cc, T, Cc, w.head_dim,
+                      p(lw.table), p(lw.scales), int(lw.num_rows), p(self.A), p(self.err), s)
+            pr_args = (p(self.A), p(lw.wkv), p(self.kv), T, K, N, None, 0, p(self.err), s)
+            ga_args = (C.byref(dims), p(self.streams[l]), p(self.kv), p(lw.q_weight), p(lw.k_weight),
+                       p(self.mask), T, s)
+            calls.append((f"gather{l}", lambda a=g_args: lib.engram_gather_dequant(*a)))
+            calls.append((f"project{l}", lambda a=pr_args: lib.engram_project(*a)))
+            calls.append((f"gate{l}", lambda a=ga_args: lib.engram_gate(*a)))
+        return calls
+
+
+def stage_model(w, name, peaks_d):
+    """Algorithmic bytes / flops of one launch of a stage at workload w."""
+    T, L, Cc, D, K, N, H, hc = w.tokens, w.layers, w.cols, w.head_dim, w.K, w.N, w.hidden, w.hc
+    row = {"fp8": D + D // 32, "q2k": 84, "bf16": 2 * D}[w.table_format]
+    if name == "hash":
+        return {"bytes": 8 * T + 4 * T * L * Cc, "flops": 0, "bound": "alu"}
+    if name.startswith("gather"):
+        return {"bytes": T * Cc * (row + 4) + 2 * T * K, "flops": 0, "bound": "hbm"}
+    if name.startswith("project"):
+        by = 2 * N * K + 2 * T * K + 2 * T * N
+        fl = 2 * T * N * K
+        t_hbm = by / (peaks_d["hbm_gbs"] * 1e9)
+        t_tc = fl / (peaks_d["bf16_tflops"] * 1e12)
+        return {"bytes": by, "flops": fl, "bound": "hbm" if t_hbm >= t_tc else "tensor"}
+    if name.startswith("gate"):
+        return {"bytes": 8 * hc * H * T + 2 * N * T + 4 * hc * H, "flops": 8 * hc * H * T, "bound": "hbm"}
+    raise ValueError(name)
+
+
+def kernel_src(name):
+    for pre, src in (("hash", "hash.cu"), ("gather", "gather.cu"), ("project", "gemm.cu"), ("gate", "gate.cu")):
+        if name.startswith(pre):
+            return src
+    return None
+
+
+def run_ours(args, rank, world, device):
+    w = get_workload(args.workload)
+    path = Path(w, device)
+    stream = torch.cuda.current_stream()
+    calls = path.stage_calls(stream)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def step(evs=None):
+        for i, (name, fn) in enumerate(calls):
+            if evs is not None:
+                evs[i].record(stream)
+            rc = fn()
+            if rc != 0:
+                raise RuntimeError(f"{name} failed: {path.E.lib().engram_last_error().decode()}")
+        if evs is not None:
+            evs[len(calls)].record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if path.err.item() != 0:
+        raise RuntimeError(f"device error flag {path.err.item()} during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("t0")
+    wall0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.fill_(float(k))
+        step(ev[k])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if sampler:
+        sampler.mark("t1")
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    if path.err.item() != 0:
+        raise RuntimeError(f"device error flag {path.err.item()} in the timed region")
+
+    per_step = np.array([e[0].elapsed_time(e[-1]) for e in ev])               # ms
+    per_kernel = {name: float(np.mean([e[i].elapsed_time(e[i + 1]) for e in ev]))
+                  for i, (name, _) in enumerate(calls)}
+    ms = float(per_step.mean())
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens = w.tokens * w.layers
+    value = world * tokens / (ms / 1e3)
+
+    # ---- end to end through the public API with host buffers -------------------------------
+    e2e = run_e2e(args, path, stream, device) if not args.no_e2e else None
+    if world > 1 and e2e is not None:
+        t = torch.tensor([e2e["ms"]], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e["ms"] = float(t.item())
+
+    if rank != 0:
+        return None
+    pk, pk_kind = peaks()
+    dom = max(per_kernel, key=per_kernel.get)
+    model = stage_model(w, dom, pk)
+    t_s = per_kernel[dom] / 1e3
+    if model["bound"] == "tensor":
+        achieved, peak, unit = model["flops"] / t_s / 1e12, pk["bf16_tflops"], "TFLOP/s"
+    elif model["bound"] == "hbm":
+        achieved, peak, unit = model["bytes"] / t_s / 1e9, pk["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = model["bytes"] / t_s / 1e9, None, "GB/s"
+    key = f"{dom}@{w.name}"
+    traffic = None
+    rec = NCU_TRAFFIC.get(key)
+    if rec and rec.get("src_sha") == src_sha(kernel_src(dom)):
+        traffic = rec["bytes"]
+    stages = {}
+    for name, t in per_kernel.items():
+        m = stage_model(w, name, pk)
+        stages[name] = {"us": round(t * 1e3, 2), "GB/s": round(m["bytes"] / (t / 1e3) / 1e9, 1)}
+        if m["flops"] and name.startswith("project"):
+            stages[name]["TFLOP/s"] = round(m["flops"] / (t / 1e3) / 1e12, 1)
+    line = {
+        "metric": "engram_tokens_per_s_per_layer",
+        "value": round(value, 1),
+        "unit": "tokens/s per layer",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; tables, weights and ids drawn on device)",
+        "config": {"workload": w.name, "tokens": w.tokens, "layers": w.layers, "hash_cols": w.cols,
+                   "head_dim": w.head_dim, "table": w.table_format, "table_rows": int(sum(path.table_rows)),
+                   "hidden": w.hidden, "hc": w.hc, "K": w.K, "N": w.N,
+                   "l2": "flushed before every timed step (512 MB write)", "parallelism": f"replicas{world}"},
+        "gpu_launches": args.steps * len(calls),
+        "stages": stages,
+        "roofline": {"kernel": dom, "bound": model["bound"], "achieved": round(achieved, 1),
+                     "peak": peak, "unit": unit, "frac": None if peak is None else round(achieved / peak, 4),
+                     "peak_source": f"{pk_kind} ({'hbm_gbs' if unit == 'GB/s' else 'bf16_tflops'}, burst)",
+                     "algorithmic_bytes": model["bytes"], "algorithmic_flops": model["flops"],
+                     "traffic": traffic},
+        "clocks": clocks,
+        "wall_s_timed": round(wall, 4),
+    }
+    if e2e is not None:
+        line["e2e"] = {"value": round(world * tokens / (e2e["ms"] / 1e3), 1), "unit": "tokens/s per layer",
+                       "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                       "ms_per_step": round(e2e["ms"], 5)}
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, path.case, args.cpu_tokens)
+    return line
+
+
+def run_only(args, device):
+    """Run one stage alone (for short profiler captures); prints its mean time."""
+    path = Path(get_workload(args.workload), device, args.table_rows)
+    w = path.w
+    stream = torch.cuda.current_stream()
+    calls = [(n, f) for n, f in path.stage_calls(stream) if n.startswith(args.only)]
+    if args.only != "hash":                     # later stages read the hash output
+        path.stage_calls(stream)[0][1]()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        for _, f in calls:
+            f()
+    a.record(stream)
+    for _ in range(args.steps):
+        for _, f in calls:
+            f()
+    b.record(stream)
+    b.synchronize()
+    err = int(path.err.item())
+    print(json.dumps({"profile_stage": args.only, "workload": w.name, "table_rows": args.table_rows,
+                      "us_per_launch": round(a.elapsed_time(b) * 1e3 / max(1, args.steps * len(calls)), 2),
+                      "err": err}))
+    if err:
+        raise SystemExit(f"device error flag {err}")
+
+
+def run_e2e(args, path, stream, device):
+    """engram_forward with per-step host->device copies of the inputs (pinned) and a
+    device->host read of the updated streams, all inside the timed region."""
+    E, w = path.E, path.w
+    host = {}
+    for name in ("input_ids", "cu", "sid", "mask", "lookback"):
+        t = getattr(path, name)
+        if t is not None:
+            host[name] = t.cpu().pin_memory()
+    h_streams = [s.cpu().pin_memory() for s in path.case.streams]
+    out_streams = [torch.empty_like(s).pin_memory() for s in h_streams]
+    plan = E.ForwardPlan(path.dims, path.tables, path.layers, path.input_ids, path.streams,
+                         cu_seqlens=path.cu, sequence_ids=path.sid, token_mask=path.mask,
+                         lookback_ids=path.lookback, out_ids=path.ids, err=path.err)
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + sum(
+        s.numel() * s.element_size() for s in h_streams)
+    d2h = sum(s.numel() * s.element_size() for s in h_streams)
+
+    def step():
+        for name, t in host.items():
+            getattr(path, name).copy_(t, non_blocking=True)
+        for l, s in enumerate(h_streams):
+            path.streams[l].copy_(s, non_blocking=True)
+        plan.run(stream)
+        for l, s in enumerate(out_streams):
+            s.copy_(path.streams[l], non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    n = args.steps
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        step()
+    b.record(stream)
+    b.synchronize()
+    return {"ms": a.elapsed_time(b) / n, "h2d": int(h2d), "d2h": int(d2h)}
+
+
+# ------------------------------------------------------------------------------------------------
+# the CPU oracle (baseline line and reference arm)
+# ------------------------------------------------------------------------------------------------
+
+class OracleRunner:
+    """The oracle on host copies of the workload: rows of the table are fetched once for the
+    tokens in the sample, so each timed step runs the oracle's full path on them."""
+
+    def __init__(self, w, case, n_tokens):
+        from oracle import engram_oracle as O
+        self.O, self.w = O, w
+        b = case.batch
+        self.b = b
+        self.pad = int(b["token_map"][w.pad_token_id])
+        self.primes, self.offsets, _ = O.layout(w.vocab_size, w.layers, w.max_ngram, w.n_heads)
+        self.mult = O.hash_multipliers(w.layer_ids, w.max_ngram, w.compressed_vocab)
+        win, _ = O.windows(b["input_ids"], b["token_map"], self.pad, w.max_ngram, b["cu_seqlens"],
+                           b["sequence_ids"], b["token_mask"], b["lookback_ids"])
+        ids = O.hash_ids(win, self.mult, self.primes, self.offsets, w.compressed_vocab)
+        T = w.tokens
+        n = min(n_tokens, T)
+        self.sel = np.linspace(0, T - 1, n).round().astype(np.int64)
+        self.layers = []
+        for l, tab in enumerate(case.tables):
+            need = np.unique(ids[self.sel, l, :].reshape(-1))
+            idx = torch.from_numpy(need).to(tab["table"].device)
+            t = tab["table"].index_select(0, idx).cpu()
+            t_np = t.view(torch.int16).numpy().view(np.uint16) if tab["fmt"] == "bf16" else t.numpy()
+            s_np = tab["scales"].index_select(0, idx).cpu().numpy() if tab["scales"] is not None else None
+            self.layers.append({"fmt": tab["fmt"], "need": need, "table": t_np, "scales": s_np,
+                                "wkv": case.wkv[l].cpu().view(torch.int16).numpy().view(np.uint16),
+                                "q": case.q_weight[l].cpu().view(torch.int16).numpy().view(np.uint16),
+                                "k": case.k_weight[l].cpu().view(torch.int16).numpy().view(np.uint16),
+                                "h": case.streams[l].index_select(0, torch.from_numpy(self.sel).to(
+                                    case.streams[l].device)).cpu().numpy()})
+
+    def step(self):
+        O, w, b = self.O, self.w, self.b
+        win, _ = O.windows(b["input_ids"], b["token_map"], self.pad, w.max_ngram, b["cu_seqlens"],
+                           b["sequence_ids"], b["token_mask"], b["lookback_ids"])
+        ids = O.hash_ids(win, self.mult, self.primes, self.offsets, w.compressed_vocab)
+        mask = b["token_mask"]
+        for l, lay in enumerate(self.layers):
+            sub = np.searchsorted(lay["need"], ids[self.sel, l, :])
+            a_bits, _ = O.gather(lay["fmt"], lay["table"], lay["scales"], sub, len(lay["need"]), w.head_dim)
+            kv = O.project(a_bits, lay["wkv"])
+            O.gate(lay["h"], kv, lay["q"], lay["k"], w.eps, w.clamp, None if mask is None else mask[self.sel])
+
+
+def cpu_baseline(w, case, n_tokens):
+    r = OracleRunner(w, case, n_tokens)
+    r.step()                                  # warm (page in the fp64 weights once)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        r.step()
+        reps += 1
+        if time.perf_counter() - t0 > 10.0 or reps >= 20:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": round(len(r.sel) * w.layers / dt, 2), "unit": "tokens/s per layer",
+            "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{len(r.sel)} of {w.tokens} tokens per pass (hash over all {w.tokens}), {reps} passes, "
+                      f"numpy fp64, BLAS threads = host cores"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    w = get_workload(args.workload)
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    import engram_gram_hash_02_gb300 as E
+    primes, offsets, rows = E.engram_layout(w.vocab_size, w.layers, w.max_ngram, w.n_heads)
+    case = make_case(w, rows, device)
+    r = OracleRunner(w, case, args.cpu_tokens)
+    for _ in range(args.warmup):
+        r.step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r.step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = len(r.sel) * w.layers / dt
+    return {
+        "impl": "reference",
+        "metric": "engram_tokens_per_s_per_layer",
+        "value": round(value, 2),
+        "unit": "tokens/s per layer",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "tokens": w.tokens, "layers": w.layers},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s per layer", "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": f"{len(r.sel)} of {w.tokens} tokens per step (hash over all), numpy fp64"},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s per layer", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_fp8_t256")
+    ap.add_argument("--cpu-tokens", type=int, default=32)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["hash", "gather", "project", "gate"],
+                    help="profiling: run one stage alone")
+    ap.add_argument("--table-rows", type=int, default=0,
+                    help="profiling: shrink the table to about this many rows per layer")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        torch.distributed.init_process_group(backend)
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py needs a CUDA device for --impl ours")
+        torch.cuda.set_device(local)
+        if args.only:
+            run_only(args, torch.device("cuda", local))
+            return
+        line = run_ours(args, rank, world, torch.device("cuda", local))
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -105,8 +105,8 @@ def _gather_case(fmt, rows, T, C, D, seed):
     ids = torch.randint(0, rows, (T, C), generator=g, dtype=torch.int32)
     ids[0, 0] = rows                # out of range -> zero row
     ids[T // 2, C - 1] = -7
-    ids[1, 1] = rows - 1
-    ids[2, 2] = 0
+    ids[(T - 1) // 2, 1] = rows - 1   # last and first rows of the table
+    ids[T - 1, C // 2] = 0
     return table, scales, ids
 
 

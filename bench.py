@@ -144,7 +144,7 @@ class Path:
         T, L, Cc, K, N = w.tokens, w.layers, w.cols, w.K, w.N
         self.ids = torch.empty((T, L, Cc), dtype=torch.int32, device=d)
         self.A = torch.empty((T, K), dtype=torch.bfloat16, device=d)
-        self.kv = torch.empty((T, N), dtype=torch.bfloat16, device=d)
+        self.kv = torch.empty((T, N), dtype=torch.float32, device=d)
         self.err = torch.zeros(1, dtype=torch.int32, device=d)
         self.table_rows = rows
 
@@ -187,13 +187,13 @@ def stage_model(w, name, peaks_d):
     if name.startswith("gather"):
         return {"bytes": T * Cc * (row + 4) + 2 * T * K, "flops": 0, "bound": "hbm"}
     if name.startswith("project"):
-        by = 2 * N * K + 2 * T * K + 2 * T * N
+        by = 2 * N * K + 2 * T * K + 4 * T * N
         fl = 2 * T * N * K
         t_hbm = by / (peaks_d["hbm_gbs"] * 1e9)
         t_tc = fl / (peaks_d["bf16_tflops"] * 1e12)
         return {"bytes": by, "flops": fl, "bound": "hbm" if t_hbm >= t_tc else "tensor"}
     if name.startswith("gate"):
-        return {"bytes": 8 * hc * H * T + 2 * N * T + 4 * hc * H, "flops": 8 * hc * H * T, "bound": "hbm"}
+        return {"bytes": 8 * hc * H * T + 4 * N * T + 4 * hc * H, "flops": 8 * hc * H * T, "bound": "hbm"}
     raise ValueError(name)
 
 

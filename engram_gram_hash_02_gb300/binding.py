@@ -211,8 +211,8 @@ def engram_project(A, wkv, out=None, err=None, stream=None):
     if K != K2:
         raise ValueError(f"A is [T, {K}] but wkv is [{N}, {K2}]")
     if out is None:
-        out = torch.empty((T, N), dtype=torch.bfloat16, device=A.device)
-    _u16(out, "out")
+        out = torch.empty((T, N), dtype=torch.float32, device=A.device)
+    _dev(out, torch.float32, "out")
     _opt(err, torch.int32, "err")
     _check("engram_project", lib().engram_project(_ptr(A), _ptr(wkv), _ptr(out), T, K, N, None, 0, _ptr(err),
                                                    _stream(stream)))
@@ -222,7 +222,7 @@ def engram_project(A, wkv, out=None, err=None, stream=None):
 def engram_gate(dims: EngramDims, streams, kv, q_weight, k_weight, token_mask=None, stream=None):
     """Updates ``streams`` (fp32 [T, hc, H]) in place and returns it."""
     _dev(streams, torch.float32, "streams")
-    _u16(kv, "kv")
+    _dev(kv, torch.float32, "kv")
     _u16(q_weight, "q_weight")
     _u16(k_weight, "k_weight")
     _opt(token_mask, torch.uint8, "token_mask")

@@ -92,7 +92,7 @@ static int check_gather(int32_t fmt, const int32_t* ids, int64_t ids_stride_t, i
   return ENGRAM_OK;
 }
 
-static int check_project(const uint16_t* A, const uint16_t* wkv, const uint16_t* kv, int64_t T, int32_t K,
+static int check_project(const uint16_t* A, const uint16_t* wkv, const float* kv, int64_t T, int32_t K,
                          int32_t N) {
   ENGRAM_CHECK_ARG(T >= 0 && T < (int64_t)1 << 31, "T must be in [0, 2^31)");
   ENGRAM_CHECK_ARG(K >= 8 && K % 8 == 0, "K must be a positive multiple of 8 (got %d)", K);
@@ -102,7 +102,7 @@ static int check_project(const uint16_t* A, const uint16_t* wkv, const uint16_t*
   return ENGRAM_OK;
 }
 
-static int check_gate(const EngramDims* d, const float* streams, const uint16_t* kv, const uint16_t* qw,
+static int check_gate(const EngramDims* d, const float* streams, const float* kv, const uint16_t* qw,
                       const uint16_t* kw, int64_t T) {
   int rc = check_dims(d, false, true);
   if (rc) return rc;
@@ -178,7 +178,7 @@ int engram_gather_dequant(int32_t fmt, const int32_t* ids, int64_t ids_stride_t,
   return e == cudaSuccess ? ENGRAM_OK : fail_cuda(e, "engram_gather_dequant: launch");
 }
 
-int engram_project(const uint16_t* A, const uint16_t* wkv, uint16_t* kv, int64_t T, int32_t K, int32_t N,
+int engram_project(const uint16_t* A, const uint16_t* wkv, float* kv, int64_t T, int32_t K, int32_t N,
                    void* workspace, size_t ws_bytes, int32_t* err_flag, engram_stream_t stream) {
   (void)workspace;
   (void)ws_bytes;
@@ -189,7 +189,7 @@ int engram_project(const uint16_t* A, const uint16_t* wkv, uint16_t* kv, int64_t
   return launch_gemm(p, static_cast<cudaStream_t>(stream));
 }
 
-int engram_gate(const EngramDims* dims, float* streams, const uint16_t* kv, const uint16_t* q_weight,
+int engram_gate(const EngramDims* dims, float* streams, const float* kv, const uint16_t* q_weight,
                 const uint16_t* k_weight, const uint8_t* token_mask, int64_t T, engram_stream_t stream) {
   if (T == 0) return check_dims(dims, false, true);
   int rc = check_gate(dims, streams, kv, q_weight, k_weight, T);
@@ -204,7 +204,7 @@ size_t engram_forward_workspace_bytes(const EngramDims* d, int64_t T) {
   const int64_t C = (int64_t)(d->max_ngram - 1) * d->n_heads;
   const int64_t K = C * d->head_dim;
   const int64_t N = (int64_t)d->hidden * (d->hc + 1);
-  return round256((size_t)(T * d->layers * C * 4)) + round256((size_t)(T * K * 2)) + round256((size_t)(T * N * 2));
+  return round256((size_t)(T * d->layers * C * 4)) + round256((size_t)(T * K * 2)) + round256((size_t)(T * N * 4));
 }
 
 int engram_forward(const EngramDims* dims, const EngramHashTables* tables, const EngramLayerWeights* layers,
@@ -230,16 +230,16 @@ int engram_forward(const EngramDims* dims, const EngramHashTables* tables, const
     rc = check_gather(w.table_format, reinterpret_cast<const int32_t*>(16), (int64_t)L * C, T, C, dims->head_dim,
                       w.table, w.table_scales, w.table_rows, reinterpret_cast<const uint16_t*>(workspace));
     if (rc) return rc;
-    rc = check_project(reinterpret_cast<const uint16_t*>(workspace), w.wkv, reinterpret_cast<const uint16_t*>(workspace),
+    rc = check_project(reinterpret_cast<const uint16_t*>(workspace), w.wkv, reinterpret_cast<const float*>(workspace),
                        T, (int32_t)K, (int32_t)N);
     if (rc) return rc;
-    rc = check_gate(dims, streams[l], reinterpret_cast<const uint16_t*>(workspace), w.q_weight, w.k_weight, T);
+    rc = check_gate(dims, streams[l], reinterpret_cast<const float*>(workspace), w.q_weight, w.k_weight, T);
     if (rc) return rc;
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* ids = out_ids != nullptr ? out_ids : reinterpret_cast<int32_t*>(ws);
   uint16_t* A = reinterpret_cast<uint16_t*>(ws + round256((size_t)(T * L * C * 4)));
-  uint16_t* kv = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(A) + round256((size_t)(T * K * 2)));
+  float* kv = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(A) + round256((size_t)(T * K * 2)));
 
   rc = engram_hash(dims, tok->input_ids, T, tok->cu_seqlens, tok->num_seqs, tok->sequence_ids, tok->token_mask,
                    tok->lookback_ids, tables->token_map, tables->multipliers, tables->primes, tables->offsets, ids,

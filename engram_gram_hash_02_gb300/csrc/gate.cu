@@ -6,18 +6,20 @@
 // the wkv output, clamp 1e-6) and the Atlas "engram_v41" page (stage 4: in place on the
 // fp32 highway [T, hc, H]).
 //
-// One CTA per token. Each thread owns two groups of 8 consecutive hidden elements of every
-// stream; it reads the streams, keys and norm weights once (16-byte loads), accumulates the
-// three reductions per stream (sum h^2, sum key^2, sum h*q*key*k), and keeps the streams in
-// registers. A warp-shuffle + shared-memory reduction gives the hc gates; the threads then
-// add g_j * value to their registers and write the streams back. HBM traffic is one read and
-// one write of the highway plus one read of kv, the minimum.
+// One CTA per (token, stream). Each thread owns two groups of 8 consecutive hidden elements;
+// it reads its part of the stream, the key, the value and the two norm weights once (16-byte
+// loads, all issued before any arithmetic), accumulates sum h^2, sum key^2 and
+// sum h*q*key*k, and keeps the stream and the value in registers. A warp-shuffle + shared
+// memory reduction gives the gate; the threads add g * value and write the stream back.
+// Stream traffic is one read and one write, the minimum; the value is read once per stream
+// (hc-1 of those reads hit L2).
 #include "internal.cuh"
 
 namespace engram {
 namespace {
 
-constexpr int kItems = 2;  // groups of 8 elements per thread per stream
+constexpr int kItems = 2;      // groups of 8 elements per thread
+constexpr int kMaxThreads = 512;
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -29,83 +31,82 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
   f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
 }
 
-template <int HC>
-__global__ void __launch_bounds__(512)
+__device__ __forceinline__ void load8(const float* p, float (&f)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+__global__ void __launch_bounds__(kMaxThreads)
 gate_kernel(const GateParams p) {
-  const int64_t t = blockIdx.x;
+  const int64_t t = blockIdx.x / p.hc;
+  const int j = blockIdx.x - (int)(t * p.hc);
   if (p.token_mask != nullptr && __ldg(p.token_mask + t) == 0) return;  // gate shut: untouched
 
   const int H = p.H;
-  const int G = H >> 3;                                  // groups of 8 per stream
-  float* __restrict__ h = p.streams + t * HC * (int64_t)H;
-  const uint16_t* __restrict__ kv = p.kv + t * (HC + 1) * (int64_t)H;
+  const int G = H >> 3;                                  // groups of 8
+  float* __restrict__ h = p.streams + (t * p.hc + j) * (int64_t)H;
+  const float* __restrict__ key = p.kv + t * (int64_t)(p.hc + 1) * H + (int64_t)j * H;
+  const float* __restrict__ val = p.kv + t * (int64_t)(p.hc + 1) * H + (int64_t)p.hc * H;
+  const uint16_t* __restrict__ qw = p.q_weight + (int64_t)j * H;
+  const uint16_t* __restrict__ kw = p.k_weight + (int64_t)j * H;
 
-  float hv[HC][kItems][8];
-  float ssh[HC], ssk[HC], dot[HC];
-#pragma unroll
-  for (int j = 0; j < HC; ++j) ssh[j] = ssk[j] = dot[j] = 0.f;
-
+  float hv[kItems][8], kv[kItems][8], vv[kItems][8];
+  uint4 qraw[kItems], kraw[kItems];
 #pragma unroll
   for (int it = 0; it < kItems; ++it) {
     const int g = threadIdx.x + it * blockDim.x;
     if (g < G) {
+      load8(h + 8 * g, hv[it]);
+      load8(key + 8 * g, kv[it]);
+      load8(val + 8 * g, vv[it]);
+      qraw[it] = __ldg(reinterpret_cast<const uint4*>(qw + 8 * g));
+      kraw[it] = __ldg(reinterpret_cast<const uint4*>(kw + 8 * g));
+    } else {
 #pragma unroll
-      for (int j = 0; j < HC; ++j) {
-        const float4 a = *reinterpret_cast<const float4*>(h + j * H + 8 * g);
-        const float4 b = *reinterpret_cast<const float4*>(h + j * H + 8 * g + 4);
-        hv[j][it][0] = a.x; hv[j][it][1] = a.y; hv[j][it][2] = a.z; hv[j][it][3] = a.w;
-        hv[j][it][4] = b.x; hv[j][it][5] = b.y; hv[j][it][6] = b.z; hv[j][it][7] = b.w;
-        float key[8], qw[8], kw[8];
-        unpack8(__ldg(reinterpret_cast<const uint4*>(kv + j * H + 8 * g)), key);
-        unpack8(__ldg(reinterpret_cast<const uint4*>(p.q_weight + j * H + 8 * g)), qw);
-        unpack8(__ldg(reinterpret_cast<const uint4*>(p.k_weight + j * H + 8 * g)), kw);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float x = hv[j][it][e];
-          ssh[j] = fmaf(x, x, ssh[j]);
-          ssk[j] = fmaf(key[e], key[e], ssk[j]);
-          dot[j] = fmaf(x * qw[e], key[e] * kw[e], dot[j]);
-        }
-      }
+      for (int e = 0; e < 8; ++e) hv[it][e] = kv[it][e] = vv[it][e] = 0.f;
+      qraw[it] = kraw[it] = make_uint4(0, 0, 0, 0);
     }
   }
-  uint4 vraw[kItems];
+  float ssh = 0.f, ssk = 0.f, dot = 0.f;
 #pragma unroll
   for (int it = 0; it < kItems; ++it) {
-    const int g = threadIdx.x + it * blockDim.x;
-    vraw[it] = g < G ? __ldg(reinterpret_cast<const uint4*>(kv + HC * H + 8 * g)) : make_uint4(0, 0, 0, 0);
+    float q[8], k[8];
+    unpack8(qraw[it], q);
+    unpack8(kraw[it], k);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float x = hv[it][e], y = kv[it][e];
+      ssh = fmaf(x, x, ssh);
+      ssk = fmaf(y, y, ssk);
+      dot = fmaf(x * q[e], y * k[e], dot);
+    }
   }
 
-  // ---- block reduction of 3*HC partial sums ------------------------------------------------
-  __shared__ float red[32][3 * HC];
-  __shared__ float gate[HC];
+  // ---- block reduction of the three sums -------------------------------------------------------
+  __shared__ float red[kMaxThreads / 32][3];
+  __shared__ float gate;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-  for (int j = 0; j < HC; ++j) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      ssh[j] += __shfl_xor_sync(0xffffffffu, ssh[j], off);
-      ssk[j] += __shfl_xor_sync(0xffffffffu, ssk[j], off);
-      dot[j] += __shfl_xor_sync(0xffffffffu, dot[j], off);
-    }
+  for (int off = 16; off > 0; off >>= 1) {
+    ssh += __shfl_xor_sync(0xffffffffu, ssh, off);
+    ssk += __shfl_xor_sync(0xffffffffu, ssk, off);
+    dot += __shfl_xor_sync(0xffffffffu, dot, off);
   }
   if (lane == 0) {
-#pragma unroll
-    for (int j = 0; j < HC; ++j) {
-      red[warp][3 * j] = ssh[j];
-      red[warp][3 * j + 1] = ssk[j];
-      red[warp][3 * j + 2] = dot[j];
-    }
+    red[warp][0] = ssh;
+    red[warp][1] = ssk;
+    red[warp][2] = dot;
   }
   __syncthreads();
-  if (threadIdx.x < HC) {
-    const int j = threadIdx.x;
+  if (threadIdx.x == 0) {
     const int nw = blockDim.x >> 5;
     float a = 0.f, b = 0.f, c = 0.f;
     for (int w = 0; w < nw; ++w) {
-      a += red[w][3 * j];
-      b += red[w][3 * j + 1];
-      c += red[w][3 * j + 2];
+      a += red[w][0];
+      b += red[w][1];
+      c += red[w][2];
     }
     const float invH = 1.0f / (float)H;
     const float rh = rsqrtf(a * invH + p.eps);
@@ -114,55 +115,38 @@ gate_kernel(const GateParams p) {
     float ss = 0.f;                                      // sign(0) = 0
     if (s > 0.f) ss = sqrtf(fmaxf(s, p.clamp));
     else if (s < 0.f) ss = -sqrtf(fmaxf(-s, p.clamp));
-    gate[j] = 1.0f / (1.0f + expf(-ss));
+    gate = 1.0f / (1.0f + expf(-ss));
   }
   __syncthreads();
+  const float g = gate;
 
-  // ---- h_j += g_j * value ---------------------------------------------------------------------
+  // ---- h += g * value ----------------------------------------------------------------------------
 #pragma unroll
   for (int it = 0; it < kItems; ++it) {
-    const int g = threadIdx.x + it * blockDim.x;
-    if (g < G) {
-      float v[8];
-      unpack8(vraw[it], v);
-#pragma unroll
-      for (int j = 0; j < HC; ++j) {
-        const float gj = gate[j];
-        float4 a, b;
-        a.x = fmaf(gj, v[0], hv[j][it][0]); a.y = fmaf(gj, v[1], hv[j][it][1]);
-        a.z = fmaf(gj, v[2], hv[j][it][2]); a.w = fmaf(gj, v[3], hv[j][it][3]);
-        b.x = fmaf(gj, v[4], hv[j][it][4]); b.y = fmaf(gj, v[5], hv[j][it][5]);
-        b.z = fmaf(gj, v[6], hv[j][it][6]); b.w = fmaf(gj, v[7], hv[j][it][7]);
-        *reinterpret_cast<float4*>(h + j * H + 8 * g) = a;
-        *reinterpret_cast<float4*>(h + j * H + 8 * g + 4) = b;
-      }
+    const int gi = threadIdx.x + it * blockDim.x;
+    if (gi < G) {
+      float4 a, b;
+      a.x = fmaf(g, vv[it][0], hv[it][0]); a.y = fmaf(g, vv[it][1], hv[it][1]);
+      a.z = fmaf(g, vv[it][2], hv[it][2]); a.w = fmaf(g, vv[it][3], hv[it][3]);
+      b.x = fmaf(g, vv[it][4], hv[it][4]); b.y = fmaf(g, vv[it][5], hv[it][5]);
+      b.z = fmaf(g, vv[it][6], hv[it][6]); b.w = fmaf(g, vv[it][7], hv[it][7]);
+      *reinterpret_cast<float4*>(h + 8 * gi) = a;
+      *reinterpret_cast<float4*>(h + 8 * gi + 4) = b;
     }
   }
-}
-
-template <int HC>
-cudaError_t launch_hc(const GateParams& p, cudaStream_t stream) {
-  const int groups = p.H / 8;
-  int threads = (groups + kItems - 1) / kItems;
-  threads = ((threads + 31) / 32) * 32;
-  gate_kernel<HC><<<(unsigned)p.T, threads, 0, stream>>>(p);
-  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_gate(const GateParams& p, cudaStream_t stream) {
-  switch (p.hc) {
-    case 1: return launch_hc<1>(p, stream);
-    case 2: return launch_hc<2>(p, stream);
-    case 3: return launch_hc<3>(p, stream);
-    case 4: return launch_hc<4>(p, stream);
-    case 5: return launch_hc<5>(p, stream);
-    case 6: return launch_hc<6>(p, stream);
-    case 7: return launch_hc<7>(p, stream);
-    case 8: return launch_hc<8>(p, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  const int groups = p.H / 8;
+  int threads = (groups + kItems - 1) / kItems;
+  threads = ((threads + 31) / 32) * 32;
+  if (threads > kMaxThreads) return cudaErrorInvalidValue;
+  const int64_t blocks = p.T * p.hc;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+  gate_kernel<<<(unsigned)blocks, threads, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace engram

@@ -2,7 +2,7 @@
 //
 // The projection of the vLLM "deepseek_v41.common.engram" page (Engram.__init__: wkv maps
 // n_hash_cols*head_dim -> dim*(hc+1); Engram.forward) and of the Atlas "engram_v41" page
-// (stage 3: dense bf16 GEMM). bf16 operands, fp32 accumulation in tensor memory, bf16 out.
+// (stage 3: dense bf16 GEMM). bf16 operands, fp32 accumulation in tensor memory, fp32 out.
 //
 // One CTA computes a tile of up to 256 rows (two 128-row accumulators) x BN columns:
 //   warp 0      TMA producer: 128B-swizzled K-major tiles of A (128 rows x 64) and of wkv
@@ -10,7 +10,7 @@
 //   warp 1      allocates tensor memory; one lane issues tcgen05.mma (M=128, N=BN, K=16,
 //               kind::f16) per 16-wide k step and releases a stage with tcgen05.commit.
 //   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator (each warp its 32-lane quarter),
-//               bf16 round, 16-byte stores to kv.
+//               16-byte stores of fp32 kv (kept in fp32 for the gate's reductions).
 // Both tiles of a 256-row block share each wkv tile, so wkv is read from memory once per
 // column block. BN is picked per shape so the number of tiles fills the SMs in few waves.
 //
@@ -149,14 +149,9 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo_f32), __uint_as_float(hi_f32));
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
 wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                uint16_t* __restrict__ D, const GemmArgs a) {
+                float* __restrict__ D, const GemmArgs a) {
   // a timeout anywhere in this launch (or an earlier one sharing the flag word) voids the
   // result: later CTAs do no work instead of each waiting out its own time limit
   if (a.err != nullptr && (*reinterpret_cast<volatile int32_t*>(a.err) & ENGRAM_ERR_PIPE_TIMEOUT)) return;
@@ -268,21 +263,18 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       for (int ms = 0; ms < a.msub; ++ms) {
         const int64_t row = (int64_t)m0 + ms * 128 + q * 32 + lane;
         const bool row_ok = row < a.M;
-        uint16_t* drow = D + row * (int64_t)a.N;
+        float* drow = D + row * (int64_t)a.N;
         for (int c = 0; c < a.BN; c += 16) {
           uint32_t r[16];
           tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ms * a.acc_stride + c), r);
           tmem_ld_wait();
           const int col = n0 + c;
           if (row_ok && col < a.N) {
-            uint4 lo, hi;
-            lo.x = pack_bf16x2(r[0], r[1]);   lo.y = pack_bf16x2(r[2], r[3]);
-            lo.z = pack_bf16x2(r[4], r[5]);   lo.w = pack_bf16x2(r[6], r[7]);
-            hi.x = pack_bf16x2(r[8], r[9]);   hi.y = pack_bf16x2(r[10], r[11]);
-            hi.z = pack_bf16x2(r[12], r[13]); hi.w = pack_bf16x2(r[14], r[15]);
             uint4* dst = reinterpret_cast<uint4*>(drow + col);
-            dst[0] = lo;
-            dst[1] = hi;
+            dst[0] = make_uint4(r[0], r[1], r[2], r[3]);
+            dst[1] = make_uint4(r[4], r[5], r[6], r[7]);
+            dst[2] = make_uint4(r[8], r[9], r[10], r[11]);
+            dst[3] = make_uint4(r[12], r[13], r[14], r[15]);
           }
         }
       }

@@ -5,8 +5,9 @@
 // boundaries) and the vLLM "deepseek_v41.common.engram" page (NgramHashState.forward,
 // EngramLayout, compute_hash_multipliers; lookback ids before each chunk).
 //
-// Lane k < max_ngram decides whether window slot k may be read (its position is alive and
-// in t's document, or a live lookback entry) and loads its compressed id; a ballot turns the
+// Lane k < max_ngram loads window slot k (issued speculatively, alongside the block's staging
+// of cu_seqlens in shared memory), then decides whether the slot may be read (its position is
+// alive and in t's document, or a live lookback entry); a ballot turns the
 // per-slot verdicts into the walk back from t (slot k is open only if slots 0..k all are);
 // shuffles hand every lane the window. Lanes then take the (layer, column) pairs: each mixes
 // its n-gram's slots with XOR of id * multiplier and reduces modulo its head's prime.
@@ -16,51 +17,70 @@ namespace engram {
 namespace {
 
 constexpr int kWarpsPerBlock = 8;
+constexpr int kSmemCu = 2048;   // cu_seqlens entries staged in shared memory (else searched in global)
 
-__device__ __forceinline__ int32_t find_sequence(const int32_t* __restrict__ cu, int32_t S, int64_t t) {
-  // largest s in [0, S) with cu[s] <= t (empty sequences before t are skipped)
+// largest s in [0, S) with cu[s] <= t (empty sequences before t are skipped)
+template <typename Load>
+__device__ __forceinline__ int32_t find_sequence(Load cu, int32_t S, int64_t t) {
   int32_t lo = 0, hi = S - 1;
   while (lo < hi) {
-    int32_t mid = (lo + hi + 1) >> 1;
-    if ((int64_t)__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
+    const int32_t mid = (lo + hi + 1) >> 1;
+    if ((int64_t)cu(mid) <= t) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
 
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 hash_kernel(const HashParams p) {
+  __shared__ int32_t s_cu[kSmemCu];
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-  if (t >= p.T) return;
+  const bool live = t < p.T;
   const int O = p.max_ngram - 1;
+  const bool cu_in_smem = p.cu_seqlens != nullptr && p.S + 1 <= kSmemCu;
+
+  // ---- speculative loads of slot k = lane (issued before the sequence start is known) --------
+  const int64_t pos = t - lane;
+  const bool slot = live && lane < p.max_ngram && pos >= 0;
+  int32_t raw = -1, sid = 1, sid_next = 1;
+  bool alive = true;
+  if (slot) {
+    raw = __ldg(p.input_ids + pos);
+    if (p.token_mask != nullptr) alive = __ldg(p.token_mask + pos) != 0;
+    if (p.sequence_ids != nullptr) {
+      sid = __ldg(p.sequence_ids + pos);
+      sid_next = lane > 0 ? __ldg(p.sequence_ids + pos + 1) : sid;
+    }
+  }
+  const bool raw_ok = raw >= 0 && raw < p.raw_vocab;
+  const int32_t mapped = (slot && raw_ok) ? __ldg(p.token_map + raw) : p.pad_id;
+
+  if (cu_in_smem) {
+    for (int i = threadIdx.x; i <= p.S; i += blockDim.x) s_cu[i] = __ldg(p.cu_seqlens + i);
+    __syncthreads();
+  }
+  if (!live) return;
 
   int32_t s = 0;
   int64_t start = 0;
-  if (p.cu_seqlens != nullptr) {
-    s = find_sequence(p.cu_seqlens, p.S, t);
+  if (cu_in_smem) {
+    s = find_sequence([&](int32_t i) { return s_cu[i]; }, p.S, t);
+    start = s_cu[s];
+  } else if (p.cu_seqlens != nullptr) {
+    s = find_sequence([&](int32_t i) { return __ldg(p.cu_seqlens + i); }, p.S, t);
     start = __ldg(p.cu_seqlens + s);
   }
 
-  // ---- slot k = lane: may it be read, and what does it hold -------------------------
+  // ---- slot k = lane: may it be read, and what does it hold --------------------------------
   bool ok = false;
   int64_t val = p.pad_id;
   if (lane < p.max_ngram) {
-    const int64_t pos = t - lane;
     if (pos >= start) {
-      const int32_t raw = __ldg(p.input_ids + pos);
-      if (raw >= 0 && raw < p.raw_vocab) {
-        val = __ldg(p.token_map + raw);
-      } else if (lane == 0 && p.err != nullptr) {
-        atomicOr(p.err, ENGRAM_ERR_RAW_ID);   // hashes as pad_id
-      }
-      ok = (p.token_mask == nullptr || __ldg(p.token_mask + pos) != 0);
-      if (p.sequence_ids != nullptr) {
-        const int32_t sid = __ldg(p.sequence_ids + pos);
-        ok = ok && sid != 0;
-        if (lane > 0) ok = ok && sid == __ldg(p.sequence_ids + pos + 1);
-      }
+      val = mapped;                                   // pad_id for a raw id outside the map
+      if (lane == 0 && !raw_ok && p.err != nullptr) atomicOr(p.err, ENGRAM_ERR_RAW_ID);
+      ok = alive && sid != 0 && (lane == 0 || sid == sid_next);
     } else if (p.lookback_ids != nullptr) {
-      const int64_t i = pos - start + O;       // index into the sequence's lookback row
+      const int64_t i = pos - start + O;              // index into the sequence's lookback row
       if (i >= 0) {
         const int32_t id = __ldg(p.lookback_ids + (int64_t)s * O + i);
         ok = id >= 0;

@@ -63,7 +63,7 @@ cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
 struct GemmParams {
   const uint16_t* A;
   const uint16_t* B;
-  uint16_t* D;
+  float* D;
   int64_t M;
   int32_t K, N;
   int32_t* err;
@@ -73,7 +73,7 @@ int launch_gemm(const GemmParams& p, cudaStream_t stream);
 
 struct GateParams {
   float* streams;
-  const uint16_t* kv;
+  const float* kv;
   const uint16_t* q_weight;
   const uint16_t* k_weight;
   const uint8_t* token_mask;

@@ -141,15 +141,17 @@ int engram_gather_dequant(int32_t fmt, const int32_t* ids, int64_t ids_stride_t,
 
 /*
  * Stage 3: wkv projection kv = A * wkv^T ([vLLM] Engram.__init__ (wkv) and Engram.forward;
- * [Atlas] stage 3). bf16 operands, fp32 accumulation on tcgen05 tensor cores, bf16 output.
+ * [Atlas] stage 3). bf16 operands, fp32 accumulation on tcgen05 tensor cores, fp32 output
+ * (the pages keep kv in the model dtype; fp32 keeps the gate's reductions exact to the
+ * accumulator, which matters for the larger Q2_K rows).
  *   A    device bf16 [T, K] row-major       wkv device bf16 [N, K] row-major (nn.Linear layout)
- *   kv   device bf16 [T, N] row-major; columns [j*H, (j+1)*H) are stream j's key, [hc*H, N)
+ *   kv   device fp32 [T, N] row-major; columns [j*H, (j+1)*H) are stream j's key, [hc*H, N)
  *        the shared value
  * K % 8 == 0, N % 16 == 0, all three 16-byte aligned. workspace/ws_bytes are unused (pass
  * NULL/0). ENGRAM_ERR_PIPE_TIMEOUT in err_flag means the result is invalid; while that bit is
  * set in the word passed, later calls with the same word skip the work.
  */
-int engram_project(const uint16_t* A, const uint16_t* wkv, uint16_t* kv, int64_t T, int32_t K,
+int engram_project(const uint16_t* A, const uint16_t* wkv, float* kv, int64_t T, int32_t K,
                    int32_t N, void* workspace, size_t ws_bytes, int32_t* err_flag,
                    engram_stream_t stream);
 
@@ -165,12 +167,12 @@ void engram_set_gemm_tile(int32_t bn);
  *   h_j = h_j + g * value
  * Masked tokens are not read or written.
  *   streams   device fp32 [T, hc, H] (in/out), 16-byte aligned
- *   kv        device bf16 [T, (hc+1)*H] (output of engram_project)
+ *   kv        device fp32 [T, (hc+1)*H] (output of engram_project)
  *   q_weight, k_weight device bf16 [hc, H]
  *   token_mask device uint8 [T] or NULL
  * H % 8 == 0, 8 <= H <= 8192, 1 <= hc <= 8.
  */
-int engram_gate(const EngramDims* dims, float* streams, const uint16_t* kv,
+int engram_gate(const EngramDims* dims, float* streams, const float* kv,
                 const uint16_t* q_weight, const uint16_t* k_weight, const uint8_t* token_mask,
                 int64_t T, engram_stream_t stream);
 
@@ -205,7 +207,7 @@ typedef struct EngramTokens {
 } EngramTokens;
 
 /* Bytes of device workspace engram_forward needs for T tokens (256-byte aligned pieces:
- * hash ids [T, layers, C] int32, rows [T, C*head_dim] bf16, kv [T, (hc+1)*H] bf16). */
+ * hash ids [T, layers, C] int32, rows [T, C*head_dim] bf16, kv [T, (hc+1)*H] fp32). */
 size_t engram_forward_workspace_bytes(const EngramDims* dims, int64_t T);
 
 /*

@@ -83,7 +83,7 @@ def gpu_forward(w, case, setup, device="cuda", with_err=True):
     id_bytes = ((T * w.layers * w.cols * 4 + 255) // 256) * 256
     a_bytes = ((T * K * 2 + 255) // 256) * 256
     A_last = ws[id_bytes:id_bytes + T * K * 2].view(torch.bfloat16).view(T, K)
-    kv_last = ws[id_bytes + a_bytes:id_bytes + a_bytes + T * N * 2].view(torch.bfloat16).view(T, N)
+    kv_last = ws[id_bytes + a_bytes:id_bytes + a_bytes + T * N * 4].view(torch.float32).view(T, N)
     return {"ids": out_ids, "streams": streams, "A_last": A_last, "kv_last": kv_last,
             "err": int(err.item()) if err is not None else 0, "dims": dims}
 
@@ -142,9 +142,13 @@ def check_streams(got: np.ndarray, ref: np.ndarray, h0: np.ndarray, what=""):
     return max_abs, rel, upd_rel
 
 
-def check_kv(got_bits: np.ndarray, ref: np.ndarray, what=""):
-    g = O.bf16_bits_to_f64(got_bits)
+def check_kv(got, ref: np.ndarray, what=""):
+    """fp32 kv from the tensor cores against the fp64 product of the same bf16 operands.
+    Products of bf16 values are exact in fp32; what remains is fp32 summation over K terms:
+    a random walk of about sqrt(K) * 2^-24 * rms (~5e-6 rms at K = 6144). The bound allows
+    20x that plus 2^-14 relative."""
+    g = np.asarray(got, dtype=np.float64)
     rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
-    tol = 2.0 ** -8 * np.abs(ref) + 1e-3 * rms
+    tol = 2.0 ** -14 * np.abs(ref) + 1e-4 * rms
     bad = np.abs(g - ref) > tol
     assert not bad.any(), f"{what}: {int(bad.sum())} of {bad.size} kv outside tolerance; worst {float(np.abs(g - ref).max()):.3g}"

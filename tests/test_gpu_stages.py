@@ -155,10 +155,10 @@ def test_project_vs_fp64(T, K, N):
     ref = O.project(H.bits16(A), H.bits16(W))
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    H.check_kv(H.bits16(kv), ref, f"T={T} K={K} N={N}")
-    # the library GEMM and torch's bf16 matmul agree to bf16 rounding
+    H.check_kv(kv.cpu().numpy(), ref, f"T={T} K={K} N={N}")
+    # the library GEMM and torch's fp32 matmul of the same bf16 values agree to fp32 summation order
     tm = (A.float() @ W.float().t())
-    assert torch.allclose(kv.float(), tm, rtol=2 ** -7, atol=1e-3 * float(tm.pow(2).mean().sqrt()))
+    assert torch.allclose(kv, tm, rtol=1e-4, atol=1e-4 * float(tm.pow(2).mean().sqrt()))
 
 
 @pytest.mark.parametrize("bn", [16, 48, 128, 144, 256])
@@ -173,19 +173,17 @@ def test_project_tile_widths(bn):
         torch.cuda.synchronize()
     finally:
         E().set_gemm_tile(0)
-    H.check_kv(H.bits16(kv), O.project(H.bits16(A), H.bits16(W)), f"bn={bn}")
+    H.check_kv(kv.cpu().numpy(), O.project(H.bits16(A), H.bits16(W)), f"bn={bn}")
 
 
 def test_project_integer_exact():
-    # small integers: every partial sum is exact in fp32, and |kv| < 256 is exact in bf16
+    # small integers: every product and partial sum is exact in fp32
     g = torch.Generator(device=DEV).manual_seed(3)
     A = torch.randint(-3, 4, (200, 256), generator=g, device=DEV).to(torch.bfloat16)
     W = torch.randint(-3, 4, (320, 256), generator=g, device=DEV).to(torch.bfloat16)
     ref = O.project(H.bits16(A), H.bits16(W))
     kv = E().engram_project(A, W)
-    got = O.bf16_bits_to_f64(H.bits16(kv))
-    small = np.abs(ref) < 256
-    assert np.array_equal(got[small], ref[small])
+    assert np.array_equal(kv.cpu().numpy().astype(np.float64), ref)
 
 
 # ------------------------------------------------------------------------------------------- gate
@@ -195,7 +193,7 @@ def test_project_integer_exact():
 def test_gate_vs_oracle(T, hc, H_, masked):
     g = torch.Generator(device=DEV).manual_seed(T + hc + H_)
     h = torch.randn(T, hc, H_, generator=g, device=DEV)
-    kv = (torch.randn(T, (hc + 1) * H_, generator=g, device=DEV) * 0.03).to(torch.bfloat16)
+    kv = torch.randn(T, (hc + 1) * H_, generator=g, device=DEV) * 0.03
     q = (1 + 0.1 * torch.randn(hc, H_, generator=g, device=DEV)).to(torch.bfloat16)
     k = (1 + 0.1 * torch.randn(hc, H_, generator=g, device=DEV)).to(torch.bfloat16)
     mask = None
@@ -204,7 +202,7 @@ def test_gate_vs_oracle(T, hc, H_, masked):
     h0 = h.cpu().numpy().astype(np.float64)
     dims = E().make_dims(1, 3, 4, 64, H_, hc, 10, 10, 0, 1e-6, 1e-6)
     E().engram_gate(dims, h, kv, q, k, token_mask=mask)
-    ref, _ = O.gate(h0, O.bf16_bits_to_f64(H.bits16(kv)), H.bits16(q), H.bits16(k), 1e-6, 1e-6,
+    ref, _ = O.gate(h0, kv.cpu().numpy().astype(np.float64), H.bits16(q), H.bits16(k), 1e-6, 1e-6,
                     None if mask is None else mask.cpu().numpy())
     got = h.cpu().numpy()
     if mask is not None:
@@ -217,8 +215,8 @@ def test_gate_zero_value_bit_unchanged():
     T, hc, H_ = 8, 4, 512
     h = torch.randn(T, hc, H_, device=DEV)
     before = h.clone()
-    kv = torch.zeros(T, (hc + 1) * H_, device=DEV, dtype=torch.bfloat16)
-    kv[:, : hc * H_] = torch.randn(T, hc * H_, device=DEV).to(torch.bfloat16)
+    kv = torch.zeros(T, (hc + 1) * H_, device=DEV)
+    kv[:, : hc * H_] = torch.randn(T, hc * H_, device=DEV)
     q = torch.ones(hc, H_, device=DEV, dtype=torch.bfloat16)
     dims = E().make_dims(1, 3, 4, 64, H_, hc, 10, 10, 0)
     E().engram_gate(dims, h, kv, q, q)
@@ -235,7 +233,7 @@ def test_bad_arguments_return_einval():
         E().engram_project(A, W)
     assert ei.value.code == -1
     h = torch.zeros(2, 4, 256, device=DEV)
-    kv = torch.zeros(2, 5 * 256, device=DEV, dtype=torch.bfloat16)
+    kv = torch.zeros(2, 5 * 256, device=DEV)
     q = torch.zeros(4, 256, device=DEV, dtype=torch.bfloat16)
     bad = E().make_dims(1, 3, 4, 64, 256, 9, 10, 10, 0)          # hc > 8
     with pytest.raises(E().EngramError):

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libengram.so")
 TABLE_BF16, TABLE_FP8_E8M0, TABLE_Q2K = 0, 1, 2
 TABLE_FORMATS = {"bf16": TABLE_BF16, "fp8": TABLE_FP8_E8M0, "q2k": TABLE_Q2K}
 ERR_RAW_ID, ERR_ROW_ID, ERR_PIPE_TIMEOUT = 1, 2, 4
+NOALLOC_SCRATCH_BYTES = 32 << 20   # ENGRAM_NOALLOC_SCRATCH_BYTES
 INT64_MAX = (1 << 63) - 1
 
 
@@ -79,6 +80,7 @@ def lib() -> C.CDLL:
         L.engram_forward_workspace_bytes.argtypes = [P, I64]
         L.engram_forward_workspace_bytes.restype = SZ
         L.engram_forward.argtypes = [P, P, P, P, P, P, SZ, P, P, P]
+        L.engram_forward_noalloc.argtypes = [P, P, P, P, P, P, P, P]
         L.engram_set_gemm_tile.argtypes = [I32]
         L.engram_set_gemm_tile.restype = None
         _lib = L
@@ -302,6 +304,14 @@ class ForwardPlan:
         _check("engram_forward", lib().engram_forward(
             C.byref(self.dims), C.byref(self._tables), self._layers, C.byref(self._tokens), self._streams,
             _ptr(self.workspace), self._ws_bytes, _ptr(self._out_ids), _ptr(self._err), _stream(stream)))
+
+
+    def run_noalloc(self, stream=None):
+        """The same pass through engram_forward_noalloc: scratch in the library's static device
+        array instead of self.workspace (for callers that may not allocate)."""
+        _check("engram_forward_noalloc", lib().engram_forward_noalloc(
+            C.byref(self.dims), C.byref(self._tables), self._layers, C.byref(self._tokens), self._streams,
+            _ptr(self._out_ids), _ptr(self._err), _stream(stream)))
 
 
 def engram_forward(dims: EngramDims, tables: HashTables, layers: list, input_ids, streams: list, **kw):

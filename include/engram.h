@@ -224,6 +224,30 @@ int engram_forward(const EngramDims* dims, const EngramHashTables* tables,
                    float* const* streams, void* workspace, size_t ws_bytes, int32_t* out_ids,
                    int32_t* err_flag, engram_stream_t stream);
 
+/* Size of the static device scratch of engram_forward_noalloc: 32 MiB, held by every GPU that
+ * loads the library until the process exits. */
+#define ENGRAM_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * engram_forward without a workspace argument, for callers that may not allocate device memory:
+ * e.g. an engine whose pool owns all the device memory it may touch and lends a plugin only its
+ * own tensors, or a real-time loop that cannot take cudaMalloc's implicit synchronisation.
+ * No page counterpart: the pages have no such entry point; the path computed is engram_forward's.
+ *   Arguments as engram_forward, minus workspace/ws_bytes. The hash ids, rows and kv live in one
+ *   static device array of ENGRAM_NOALLOC_SCRATCH_BYTES; a call whose
+ *   engram_forward_workspace_bytes(dims, T) exceeds it returns ENGRAM_EINVAL and launches nothing
+ *   (the decode step of 256 tokens, 24 hash columns of 256, hidden 4096, hc 4 needs 24.1 MB).
+ *   The first call on each device looks up the array's device address (cudaGetSymbolAddress, with
+ *   that device current): make that first call before any stream capture.
+ *   Calls allocate nothing (no cudaMalloc, cudaFree or allocating library routine). All calls share
+ *   the array and it keeps the last call's contents; nothing in it needs to start at zero. Calls
+ *   whose work overlaps on the GPU (other streams or threads) race on it: order them.
+ */
+int engram_forward_noalloc(const EngramDims* dims, const EngramHashTables* tables,
+                           const EngramLayerWeights* layers, const EngramTokens* tokens,
+                           float* const* streams, int32_t* out_ids, int32_t* err_flag,
+                           engram_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,5 +23,6 @@ from .binding import (  # noqa: F401
     hash_multipliers,
     lib,
     make_dims,
+    set_gemm_cluster,
     set_gemm_tile,
 )

@@ -83,6 +83,8 @@ def lib() -> C.CDLL:
         L.engram_forward_noalloc.argtypes = [P, P, P, P, P, P, P, P]
         L.engram_set_gemm_tile.argtypes = [I32]
         L.engram_set_gemm_tile.restype = None
+        L.engram_set_gemm_cluster.argtypes = [I32]
+        L.engram_set_gemm_cluster.restype = None
         _lib = L
     return _lib
 
@@ -236,6 +238,10 @@ def engram_gate(dims: EngramDims, streams, kv, q_weight, k_weight, token_mask=No
 
 def set_gemm_tile(bn: int = 0):
     lib().engram_set_gemm_tile(int(bn))
+
+
+def set_gemm_cluster(c: int = 0):
+    lib().engram_set_gemm_cluster(int(c))
 
 
 # ---------------------------------------------------------------------------------------------

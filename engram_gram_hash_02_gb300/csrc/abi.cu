@@ -39,6 +39,7 @@ int num_sms() {
 }
 
 void set_gemm_bn_override(int bn);
+void set_gemm_cluster_override(int c);
 
 static int check_dims(const EngramDims* d, bool need_hash, bool need_gate) {
   ENGRAM_CHECK_ARG(d != nullptr, "dims is NULL");
@@ -128,10 +129,12 @@ void engram_set_gemm_tile(int32_t bn) {
   set_gemm_bn_override((bn >= 16 && bn <= 256 && bn % 16 == 0) ? bn : 0);
 }
 
-int engram_hash(const EngramDims* dims, const int32_t* input_ids, int64_t T, const int32_t* cu_seqlens,
-                int32_t S, const int32_t* sequence_ids, const uint8_t* token_mask, const int32_t* lookback_ids,
-                const int32_t* token_map, const int64_t* multipliers, const int64_t* primes,
-                const int64_t* offsets, int32_t* out_ids, int32_t* err_flag, engram_stream_t stream) {
+void engram_set_gemm_cluster(int32_t c) { set_gemm_cluster_override((c == 1 || c == 2 || c == 4) ? c : 0); }
+
+static int hash_impl(const EngramDims* dims, const int32_t* input_ids, int64_t T, const int32_t* cu_seqlens,
+                     int32_t S, const int32_t* sequence_ids, const uint8_t* token_mask, const int32_t* lookback_ids,
+                     const int32_t* token_map, const int64_t* multipliers, const int64_t* primes,
+                     const int64_t* offsets, int32_t* out_ids, int32_t* err_flag, engram_stream_t stream, bool pdl) {
   int rc = check_dims(dims, true, false);
   if (rc) return rc;
   ENGRAM_CHECK_ARG(T >= 0 && T < (int64_t)1 << 34, "T must be in [0, 2^34)");
@@ -163,40 +166,64 @@ int engram_hash(const EngramDims* dims, const int32_t* input_ids, int64_t T, con
   p.cols = (dims->max_ngram - 1) * dims->n_heads;
   p.raw_vocab = dims->raw_vocab;
   p.pad_id = dims->pad_id;
-  cudaError_t e = launch_hash(p, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_hash(p, static_cast<cudaStream_t>(stream), pdl);
   return e == cudaSuccess ? ENGRAM_OK : fail_cuda(e, "engram_hash: launch");
+}
+
+int engram_hash(const EngramDims* dims, const int32_t* input_ids, int64_t T, const int32_t* cu_seqlens,
+                int32_t S, const int32_t* sequence_ids, const uint8_t* token_mask, const int32_t* lookback_ids,
+                const int32_t* token_map, const int64_t* multipliers, const int64_t* primes,
+                const int64_t* offsets, int32_t* out_ids, int32_t* err_flag, engram_stream_t stream) {
+  return hash_impl(dims, input_ids, T, cu_seqlens, S, sequence_ids, token_mask, lookback_ids, token_map, multipliers,
+                   primes, offsets, out_ids, err_flag, stream, false);
+}
+
+static int gather_impl(int32_t fmt, const int32_t* ids, int64_t ids_stride_t, int64_t T, int32_t C,
+                       int32_t head_dim, const void* table, const uint8_t* scales, int64_t num_rows, uint16_t* out,
+                       int32_t* err_flag, engram_stream_t stream, bool pdl) {
+  if (T == 0) return ENGRAM_OK;
+  int rc = check_gather(fmt, ids, ids_stride_t, T, C, head_dim, table, scales, num_rows, out);
+  if (rc) return rc;
+  GatherParams p{fmt, ids, ids_stride_t, T, C, head_dim, table, scales, num_rows, out, err_flag};
+  cudaError_t e = launch_gather(p, static_cast<cudaStream_t>(stream), pdl);
+  return e == cudaSuccess ? ENGRAM_OK : fail_cuda(e, "engram_gather_dequant: launch");
 }
 
 int engram_gather_dequant(int32_t fmt, const int32_t* ids, int64_t ids_stride_t, int64_t T, int32_t C,
                           int32_t head_dim, const void* table, const uint8_t* scales, int64_t num_rows,
                           uint16_t* out, int32_t* err_flag, engram_stream_t stream) {
+  return gather_impl(fmt, ids, ids_stride_t, T, C, head_dim, table, scales, num_rows, out, err_flag, stream, false);
+}
+
+static int project_impl(const uint16_t* A, const uint16_t* wkv, float* kv, int64_t T, int32_t K, int32_t N,
+                        int32_t* err_flag, engram_stream_t stream, bool pdl) {
   if (T == 0) return ENGRAM_OK;
-  int rc = check_gather(fmt, ids, ids_stride_t, T, C, head_dim, table, scales, num_rows, out);
+  int rc = check_project(A, wkv, kv, T, K, N);
   if (rc) return rc;
-  GatherParams p{fmt, ids, ids_stride_t, T, C, head_dim, table, scales, num_rows, out, err_flag};
-  cudaError_t e = launch_gather(p, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? ENGRAM_OK : fail_cuda(e, "engram_gather_dequant: launch");
+  GemmParams p{A, wkv, kv, T, K, N, err_flag};
+  return launch_gemm(p, static_cast<cudaStream_t>(stream), pdl);
 }
 
 int engram_project(const uint16_t* A, const uint16_t* wkv, float* kv, int64_t T, int32_t K, int32_t N,
                    void* workspace, size_t ws_bytes, int32_t* err_flag, engram_stream_t stream) {
   (void)workspace;
   (void)ws_bytes;
-  if (T == 0) return ENGRAM_OK;
-  int rc = check_project(A, wkv, kv, T, K, N);
-  if (rc) return rc;
-  GemmParams p{A, wkv, kv, T, K, N, err_flag};
-  return launch_gemm(p, static_cast<cudaStream_t>(stream));
+  return project_impl(A, wkv, kv, T, K, N, err_flag, stream, false);
 }
 
-int engram_gate(const EngramDims* dims, float* streams, const float* kv, const uint16_t* q_weight,
-                const uint16_t* k_weight, const uint8_t* token_mask, int64_t T, engram_stream_t stream) {
+static int gate_impl(const EngramDims* dims, float* streams, const float* kv, const uint16_t* q_weight,
+                     const uint16_t* k_weight, const uint8_t* token_mask, int64_t T, engram_stream_t stream, bool pdl) {
   if (T == 0) return check_dims(dims, false, true);
   int rc = check_gate(dims, streams, kv, q_weight, k_weight, T);
   if (rc) return rc;
   GateParams p{streams, kv, q_weight, k_weight, token_mask, T, dims->hidden, dims->hc, dims->eps, dims->clamp};
-  cudaError_t e = launch_gate(p, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_gate(p, static_cast<cudaStream_t>(stream), pdl);
   return e == cudaSuccess ? ENGRAM_OK : fail_cuda(e, "engram_gate: launch");
+}
+
+int engram_gate(const EngramDims* dims, float* streams, const float* kv, const uint16_t* q_weight,
+                const uint16_t* k_weight, const uint8_t* token_mask, int64_t T, engram_stream_t stream) {
+  return gate_impl(dims, streams, kv, q_weight, k_weight, token_mask, T, stream, false);
 }
 
 size_t engram_forward_workspace_bytes(const EngramDims* d, int64_t T) {
@@ -241,18 +268,19 @@ int engram_forward(const EngramDims* dims, const EngramHashTables* tables, const
   uint16_t* A = reinterpret_cast<uint16_t*>(ws + round256((size_t)(T * L * C * 4)));
   float* kv = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(A) + round256((size_t)(T * K * 2)));
 
-  rc = engram_hash(dims, tok->input_ids, T, tok->cu_seqlens, tok->num_seqs, tok->sequence_ids, tok->token_mask,
-                   tok->lookback_ids, tables->token_map, tables->multipliers, tables->primes, tables->offsets, ids,
-                   err_flag, stream);
+  // each launch may start while its predecessor finishes (programmatic dependent launch)
+  rc = hash_impl(dims, tok->input_ids, T, tok->cu_seqlens, tok->num_seqs, tok->sequence_ids, tok->token_mask,
+                 tok->lookback_ids, tables->token_map, tables->multipliers, tables->primes, tables->offsets, ids,
+                 err_flag, stream, true);
   if (rc) return rc;
   for (int l = 0; l < L; ++l) {
     const EngramLayerWeights& w = layers[l];
-    rc = engram_gather_dequant(w.table_format, ids + (int64_t)l * C, (int64_t)L * C, T, C, dims->head_dim, w.table,
-                               w.table_scales, w.table_rows, A, err_flag, stream);
+    rc = gather_impl(w.table_format, ids + (int64_t)l * C, (int64_t)L * C, T, C, dims->head_dim, w.table,
+                     w.table_scales, w.table_rows, A, err_flag, stream, true);
     if (rc) return rc;
-    rc = engram_project(A, w.wkv, kv, T, (int32_t)K, (int32_t)N, nullptr, 0, err_flag, stream);
+    rc = project_impl(A, w.wkv, kv, T, (int32_t)K, (int32_t)N, err_flag, stream, true);
     if (rc) return rc;
-    rc = engram_gate(dims, streams[l], kv, w.q_weight, w.k_weight, tok->token_mask, T, stream);
+    rc = gate_impl(dims, streams[l], kv, w.q_weight, w.k_weight, tok->token_mask, T, stream, true);
     if (rc) return rc;
   }
   return ENGRAM_OK;

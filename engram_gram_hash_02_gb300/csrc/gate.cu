@@ -42,7 +42,10 @@ __global__ void __launch_bounds__(kMaxThreads)
 gate_kernel(const GateParams p) {
   const int64_t t = blockIdx.x / p.hc;
   const int j = blockIdx.x - (int)(t * p.hc);
-  if (p.token_mask != nullptr && __ldg(p.token_mask + t) == 0) return;  // gate shut: untouched
+  if (p.token_mask != nullptr && __ldg(p.token_mask + t) == 0) {   // gate shut: untouched
+    pdl_wait();
+    return;
+  }
 
   const int H = p.H;
   const int G = H >> 3;                                  // groups of 8
@@ -52,6 +55,7 @@ gate_kernel(const GateParams p) {
   const uint16_t* __restrict__ qw = p.q_weight + (int64_t)j * H;
   const uint16_t* __restrict__ kw = p.k_weight + (int64_t)j * H;
 
+  // the stream and the norm weights do not come from the projection: load them first
   float hv[kItems][8], kv[kItems][8], vv[kItems][8];
   uint4 qraw[kItems], kraw[kItems];
 #pragma unroll
@@ -59,14 +63,25 @@ gate_kernel(const GateParams p) {
     const int g = threadIdx.x + it * blockDim.x;
     if (g < G) {
       load8(h + 8 * g, hv[it]);
-      load8(key + 8 * g, kv[it]);
-      load8(val + 8 * g, vv[it]);
       qraw[it] = __ldg(reinterpret_cast<const uint4*>(qw + 8 * g));
       kraw[it] = __ldg(reinterpret_cast<const uint4*>(kw + 8 * g));
     } else {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) hv[it][e] = kv[it][e] = vv[it][e] = 0.f;
+      for (int e = 0; e < 8; ++e) hv[it][e] = 0.f;
       qraw[it] = kraw[it] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  pdl_wait();                                            // kv comes from the projection
+  pdl_trigger();
+#pragma unroll
+  for (int it = 0; it < kItems; ++it) {
+    const int g = threadIdx.x + it * blockDim.x;
+    if (g < G) {
+      load8(key + 8 * g, kv[it]);
+      load8(val + 8 * g, vv[it]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) kv[it][e] = vv[it][e] = 0.f;
     }
   }
   float ssh = 0.f, ssk = 0.f, dot = 0.f;
@@ -138,15 +153,14 @@ gate_kernel(const GateParams p) {
 
 }  // namespace
 
-cudaError_t launch_gate(const GateParams& p, cudaStream_t stream) {
+cudaError_t launch_gate(const GateParams& p, cudaStream_t stream, bool pdl) {
   const int groups = p.H / 8;
   int threads = (groups + kItems - 1) / kItems;
   threads = ((threads + 31) / 32) * 32;
   if (threads > kMaxThreads) return cudaErrorInvalidValue;
   const int64_t blocks = p.T * p.hc;
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-  gate_kernel<<<(unsigned)blocks, threads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_k(gate_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream, pdl, p);
 }
 
 }  // namespace engram

@@ -52,6 +52,8 @@ __device__ __forceinline__ void flag(int32_t* err, int32_t bit) {
 // ---- FP8-E4M3 + E8M0 ------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads)
 gather_fp8_kernel(const GatherParams p) {
+  pdl_wait();                                    // ids come from the hash kernel
+  pdl_trigger();
   const int chunks_per_row = p.D >> 4;                 // 16 values per chunk
   const int64_t total = p.T * p.C * chunks_per_row;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
@@ -110,6 +112,8 @@ gather_fp8_kernel(const GatherParams p) {
 // ---- bf16 rows: copy ----------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads)
 gather_bf16_kernel(const GatherParams p) {
+  pdl_wait();
+  pdl_trigger();
   const int chunks_per_row = p.D >> 3;                 // 8 values per chunk
   const int64_t total = p.T * p.C * chunks_per_row;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
@@ -148,6 +152,8 @@ gather_bf16_kernel(const GatherParams p) {
 // Lane L writes elements 8L..8L+7: half = L/16, bit pair j = (L/4)%4, l0 = 8*(L%4), b = L/2.
 __global__ void __launch_bounds__(kThreads)
 gather_q2k_kernel(const GatherParams p) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
@@ -218,22 +224,21 @@ unsigned grid_for(int64_t work_items, int64_t per_block) {
 
 }  // namespace
 
-cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream) {
+cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl) {
   const int64_t rows = p.T * p.C;
   switch (p.fmt) {
     case ENGRAM_TABLE_FP8_E8M0:
-      gather_fp8_kernel<<<grid_for(rows * (p.D / 16), kThreads * kChunksPerThread), kThreads, 0, stream>>>(p);
-      break;
+      return launch_k(gather_fp8_kernel, dim3(grid_for(rows * (p.D / 16), kThreads * kChunksPerThread)),
+                      dim3(kThreads), 0, stream, pdl, p);
     case ENGRAM_TABLE_BF16:
-      gather_bf16_kernel<<<grid_for(rows * (p.D / 8), kThreads * kChunksPerThread), kThreads, 0, stream>>>(p);
-      break;
+      return launch_k(gather_bf16_kernel, dim3(grid_for(rows * (p.D / 8), kThreads * kChunksPerThread)),
+                      dim3(kThreads), 0, stream, pdl, p);
     case ENGRAM_TABLE_Q2K:
-      gather_q2k_kernel<<<grid_for(rows, (kThreads / 32) * kQ2kRowsPerWarp), kThreads, 0, stream>>>(p);
-      break;
+      return launch_k(gather_q2k_kernel, dim3(grid_for(rows, (kThreads / 32) * kQ2kRowsPerWarp)), dim3(kThreads),
+                      0, stream, pdl, p);
     default:
       return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace engram

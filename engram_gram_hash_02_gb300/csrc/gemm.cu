@@ -6,7 +6,9 @@
 //
 // One CTA computes a tile of up to 256 rows (two 128-row accumulators) x BN columns:
 //   warp 0      TMA producer: 128B-swizzled K-major tiles of A (128 rows x 64) and of wkv
-//               (BN rows x 64) into a ring of shared-memory stages, mbarrier complete_tx.
+//               (BN rows x 64) into a ring of shared-memory stages, mbarrier complete_tx. Under
+//               programmatic dependent launch the first ring of wkv tiles is requested before
+//               waiting for the kernel that writes A.
 //   warp 1      allocates tensor memory; one lane issues tcgen05.mma (M=128, N=BN, K=16,
 //               kind::f16) per 16-wide k step and releases a stage with tcgen05.commit.
 //   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator (each warp its 32-lane quarter),
@@ -14,7 +16,7 @@
 // Both tiles of a 256-row block share each wkv tile, so wkv is read from memory once per
 // column block. BN is picked per shape so the number of tiles fills the SMs in few waves.
 //
-// Every mbarrier wait is bounded (2 s of %globaltimer); on expiry the CTA raises an abort
+// Every mbarrier wait is bounded (~2 s of SM clock cycles); on expiry the CTA raises an abort
 // flag, reports ENGRAM_ERR_PIPE_TIMEOUT, drains its in-flight copies and MMAs (again
 // bounded), frees its tensor memory and exits.
 #include <cuda.h>
@@ -31,7 +33,7 @@ constexpr int kUmmaK = 16;                 // k per tcgen05.mma for 16-bit opera
 constexpr int kThreads = 192;
 constexpr int kMaxStages = 8;
 constexpr int kATileBytes = 128 * kBK * 2;  // 16 KB
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint64_t kWaitLimitCycles = 4000000000ull;  // wait bound in SM cycles: ~2 s at 2 GHz
 constexpr int kSmemBudget = 232448;        // 227 KB opt-in maximum per CTA
 
 struct Ctl {
@@ -44,6 +46,7 @@ struct Ctl {
 
 struct GemmArgs {
   int32_t M, K, N;
+  int32_t cluster;
   int32_t BN, msub, stages, num_kb;
   int32_t m_tiles, n_tiles, group_m;
   int32_t stage_bytes;
@@ -55,11 +58,6 @@ struct GemmArgs {
 // ---- PTX wrappers ------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
 }
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -78,16 +76,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait: false if this CTA aborted (here or in another role).
+// Bounded wait: false if this CTA aborted (here or in another role). The bound counts SM clock
+// cycles (clock64 is a cheap local register; %globaltimer is slow to read on this part and would
+// sit on the pipeline's critical path).
 __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int32_t* abort_flag,
-                                       int32_t* err, uint64_t limit_ns) {
+                                       int32_t* err, uint64_t limit_cycles) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
+  const uint64_t t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 31u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > limit_ns) {
+      if ((uint64_t)clock64() - t0 > limit_cycles) {
         *abort_flag = 1;
         if (err != nullptr) atomicOr(err, ENGRAM_ERR_PIPE_TIMEOUT);
         return false;
@@ -149,12 +149,39 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// A slice multicast into the same offset of every CTA in `mask`, each signalling its own barrier
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x,
+                                               int32_t y, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
+      : "memory");
+}
+// release a stage in every CTA of the cluster once this CTA's MMAs have read it
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 float* __restrict__ D, const GemmArgs a) {
-  // a timeout anywhere in this launch (or an earlier one sharing the flag word) voids the
-  // result: later CTAs do no work instead of each waiting out its own time limit
-  if (a.err != nullptr && (*reinterpret_cast<volatile int32_t*>(a.err) & ENGRAM_ERR_PIPE_TIMEOUT)) return;
+  const int c = a.cluster;                     // CTAs sharing one row block (launch cluster size)
+  // A timeout anywhere in an earlier launch sharing the flag word voids the result: skip the
+  // work instead of waiting out the time limits again. (Clustered CTAs must all take part.)
+  if (c == 1 && a.err != nullptr && (*reinterpret_cast<volatile int32_t*>(a.err) & ENGRAM_ERR_PIPE_TIMEOUT)) return;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t tiles = (raw_base + 1023u) & ~1023u;          // swizzled tiles need 1 KB alignment
@@ -163,22 +190,27 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = c > 1 ? cluster_ctarank() : 0;
+  const uint16_t all_ctas = (uint16_t)((1u << c) - 1u);
 
-  // grouped raster: consecutive CTAs sweep group_m row blocks of one column block
-  const int tile = blockIdx.x;
-  const int per_group = a.group_m * a.n_tiles;
-  const int first_m = (tile / per_group) * a.group_m;
+  // grouped raster over clusters: consecutive clusters sweep group_m row blocks of one group of
+  // c column blocks; the CTAs of a cluster share the row block and take adjacent column blocks
+  const int ct = blockIdx.x / c;
+  const int n_clusters = a.n_tiles / c;        // n_tiles is padded to a multiple of c
+  const int per_group = a.group_m * n_clusters;
+  const int first_m = (ct / per_group) * a.group_m;
   const int gsize = min(a.m_tiles - first_m, a.group_m);
-  const int in_group = tile % per_group;
+  const int in_group = ct % per_group;
   const int m_blk = first_m + in_group % gsize;
-  const int n_blk = in_group / gsize;
+  const int n_blk = (in_group / gsize) * c + (int)rank;
   const int m0 = m_blk * 128 * a.msub;
   const int n0 = n_blk * a.BN;
+  const int a_rows = 128 / c;                  // rows of each 128-row A tile this CTA loads
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
-      mbar_init(smem_u32(&ctl->empty[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), (uint32_t)c);   // one release per consumer in the cluster
     }
     mbar_init(smem_u32(&ctl->acc_full), 1);
     ctl->abort_flag = 0;
@@ -197,38 +229,69 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
-  __syncthreads();
+  if (c > 1) cluster_sync_all();               // peers' barriers exist before anyone multicasts
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      int issued = 0;
-      bool ok = true;
-      for (int kb = 0; kb < a.num_kb; ++kb) {
+      auto load_a = [&](int kb) {
         const int s = kb % a.stages;
-        const uint32_t ph = (uint32_t)(kb / a.stages) & 1u;
-        if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, a.err, kWaitLimitNs)) {
-          ok = false;
-          break;
+        const uint32_t full = smem_u32(&ctl->full[s]);
+        const uint32_t st = tiles + (uint32_t)(s * a.stage_bytes);
+        for (int ms = 0; ms < a.msub; ++ms) {
+          const uint32_t dst = st + ms * kATileBytes + rank * (uint32_t)(a_rows * kBK * 2);
+          const int y = m0 + ms * 128 + (int)rank * a_rows;
+          if (c > 1) tma_load_2d_mc(dst, &tmA, full, kb * kBK, y, all_ctas);
+          else tma_load_2d(dst, &tmA, full, kb * kBK, y);
         }
+      };
+      auto load_b = [&](int kb) {
+        const int s = kb % a.stages;
         const uint32_t full = smem_u32(&ctl->full[s]);
         const uint32_t st = tiles + (uint32_t)(s * a.stage_bytes);
         mbar_expect_tx(full, (uint32_t)a.stage_bytes);
-        tma_load_2d(st, &tmA, full, kb * kBK, m0);
-        if (a.msub == 2) tma_load_2d(st + kATileBytes, &tmA, full, kb * kBK, m0 + 128);
         tma_load_2d(st + a.msub * kATileBytes, &tmB, full, kb * kBK, n0);
+      };
+      // wkv does not come from the preceding kernel: fill the ring's weight halves before waiting
+      // for the gathered rows (A) to be complete
+      const int early = a.num_kb < a.stages ? a.num_kb : a.stages;
+      for (int kb = 0; kb < early; ++kb) load_b(kb);
+      pdl_wait();
+      pdl_trigger();
+      for (int kb = 0; kb < early; ++kb) load_a(kb);
+      int issued = early;
+      bool ok = true;
+      for (int kb = early; kb < a.num_kb; ++kb) {
+        const int s = kb % a.stages;
+        const uint32_t ph = (uint32_t)(kb / a.stages) & 1u;
+        // every consumer in the cluster has released stage s (the A slices land in all of them)
+        if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, a.err, kWaitLimitCycles)) {
+          ok = false;
+          break;
+        }
+        load_b(kb);
+        load_a(kb);
         issued = kb + 1;
       }
-      if (!ok) {
+      if (ok) {
+        // producer tail: wait until every consumer in the cluster has released the last stages,
+        // so no peer's release can arrive here after this CTA has exited
+        for (int kb = a.num_kb; kb < a.num_kb + a.stages; ++kb) {
+          const int s = kb % a.stages;
+          const uint32_t ph = (uint32_t)(kb / a.stages) & 1u;
+          if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, a.err, kWaitLimitCycles)) break;
+        }
+      } else {
         // drain: the copies still in flight must land before shared memory goes away
         const int first = issued > a.stages ? issued - a.stages : 0;
         for (int kb = first; kb < issued; ++kb) {
           const int s = kb % a.stages;
           const uint32_t ph = (uint32_t)(kb / a.stages) & 1u;
           volatile int32_t never = 0;
-          mbar_wait(smem_u32(&ctl->full[s]), ph, &never, nullptr, kWaitLimitNs / 4);
+          mbar_wait(smem_u32(&ctl->full[s]), ph, &never, nullptr, kWaitLimitCycles / 4);
         }
       }
     }
@@ -238,7 +301,7 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       for (int kb = 0; kb < a.num_kb; ++kb) {
         const int s = kb % a.stages;
         const uint32_t ph = (uint32_t)(kb / a.stages) & 1u;
-        if (!mbar_wait(smem_u32(&ctl->full[s]), ph, abort_flag, a.err, kWaitLimitNs)) break;
+        if (!mbar_wait(smem_u32(&ctl->full[s]), ph, abort_flag, a.err, kWaitLimitCycles)) break;
         tc_fence_after();
         const uint32_t st = tiles + (uint32_t)(s * a.stage_bytes);
         const uint32_t b_addr = st + (uint32_t)(a.msub * kATileBytes);
@@ -250,31 +313,39 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             tc_mma(tmem + ms * a.acc_stride, adesc, bdesc, a.idesc, (kb | k) != 0 ? 1u : 0u);
           }
         }
-        tc_commit(smem_u32(&ctl->empty[s]));   // stage free once these MMAs have read it
+        if (c > 1) tc_commit_mc(smem_u32(&ctl->empty[s]), all_ctas);
+        else tc_commit(smem_u32(&ctl->empty[s]));   // stage free once these MMAs have read it
       }
       tc_commit(smem_u32(&ctl->acc_full));     // accumulators final (or drained, on abort)
     }
   } else {
-    // ---------------- epilogue: TMEM -> registers -> bf16 -> global ----------------
+    // ---------------- epilogue: TMEM -> registers -> fp32 kv ----------------
     const int q = warp & 3;                    // TMEM lane quarter this warp may access
-    const bool ok = mbar_wait(smem_u32(&ctl->acc_full), 0, abort_flag, a.err, kWaitLimitNs);
+    pdl_wait();                                // kv may still be read by an earlier kernel
+    const bool ok = mbar_wait(smem_u32(&ctl->acc_full), 0, abort_flag, a.err, kWaitLimitCycles);
     tc_fence_after();
     if (ok && *abort_flag == 0) {
       for (int ms = 0; ms < a.msub; ++ms) {
         const int64_t row = (int64_t)m0 + ms * 128 + q * 32 + lane;
         const bool row_ok = row < a.M;
         float* drow = D + row * (int64_t)a.N;
-        for (int c = 0; c < a.BN; c += 16) {
-          uint32_t r[16];
-          tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ms * a.acc_stride + c), r);
+        const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ms * a.acc_stride);
+        for (int c0 = 0; c0 < a.BN; c0 += 32) {
+          uint32_t r[32];
+          const bool two = c0 + 16 < a.BN;
+          tmem_ld16(tbase + c0, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
+          if (two) tmem_ld16(tbase + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
           tmem_ld_wait();
-          const int col = n0 + c;
-          if (row_ok && col < a.N) {
-            uint4* dst = reinterpret_cast<uint4*>(drow + col);
-            dst[0] = make_uint4(r[0], r[1], r[2], r[3]);
-            dst[1] = make_uint4(r[4], r[5], r[6], r[7]);
-            dst[2] = make_uint4(r[8], r[9], r[10], r[11]);
-            dst[3] = make_uint4(r[12], r[13], r[14], r[15]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int col = n0 + c0 + 16 * h;
+            if (row_ok && col < a.N && (h == 0 || two)) {
+              uint4* dst = reinterpret_cast<uint4*>(drow + col);
+              dst[0] = make_uint4(r[16 * h + 0], r[16 * h + 1], r[16 * h + 2], r[16 * h + 3]);
+              dst[1] = make_uint4(r[16 * h + 4], r[16 * h + 5], r[16 * h + 6], r[16 * h + 7]);
+              dst[2] = make_uint4(r[16 * h + 8], r[16 * h + 9], r[16 * h + 10], r[16 * h + 11]);
+              dst[3] = make_uint4(r[16 * h + 12], r[16 * h + 13], r[16 * h + 14], r[16 * h + 15]);
+            }
           }
         }
       }
@@ -288,7 +359,7 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (*abort_flag) {
       // make sure no MMA is still writing the accumulators we are about to free
       volatile int32_t never = 0;
-      mbar_wait(smem_u32(&ctl->acc_full), 0, &never, nullptr, kWaitLimitNs / 4);
+      mbar_wait(smem_u32(&ctl->acc_full), 0, &never, nullptr, kWaitLimitCycles / 4);
     }
     __syncwarp();
     tc_fence_after();
@@ -330,7 +401,8 @@ bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, uint32_t
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int g_bn_override = 0;  // engram_set_gemm_tile
+int g_bn_override = 0;       // engram_set_gemm_tile
+int g_cluster_override = 0;  // engram_set_gemm_cluster
 
 int pick_bn(int64_t m_tiles, int N, int sms) {
   if (g_bn_override > 0) return g_bn_override;
@@ -355,11 +427,62 @@ uint32_t pow2_at_least(uint32_t x) {
   return p;
 }
 
+cudaError_t launch(const CUtensorMap& mA, const CUtensorMap& mB, float* D, const GemmArgs& a, int64_t grid,
+                   int smem, cudaStream_t stream, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)a.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, wkv_gemm_kernel, mA, mB, D, a);
+}
+
+// Largest cluster (<= 4) whose clusters all fit on the GPU at once, or 2 when more than one
+// wave is needed anyway; 1 when there is only one column tile.
+int pick_cluster(int n_tiles, int64_t m_tiles, int smem) {
+  if (g_cluster_override > 0) return g_cluster_override;
+  if (n_tiles < 2) return 1;
+  int best = 1;
+  for (int c = 2; c <= 4; c *= 2) {
+    if (n_tiles < c) break;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)c, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)c;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, wkv_gemm_kernel, &cfg) != cudaSuccess || active <= 0) {
+      cudaGetLastError();
+      break;
+    }
+    const int64_t clusters = m_tiles * ((n_tiles + c - 1) / c);
+    if (clusters <= active) best = c;          // one wave of clusters
+    else if (c == 2) best = 2;                 // several waves: pairs still halve A's L2 reads
+  }
+  return best;
+}
+
 }  // namespace
 
 void set_gemm_bn_override(int bn) { g_bn_override = bn; }
+void set_gemm_cluster_override(int c) { g_cluster_override = c; }
 
-int launch_gemm(const GemmParams& p, cudaStream_t stream) {
+int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl) {
   const int sms = num_sms();
   GemmArgs a{};
   a.M = (int32_t)p.M;
@@ -368,7 +491,7 @@ int launch_gemm(const GemmParams& p, cudaStream_t stream) {
   a.msub = p.M > 128 ? 2 : 1;
   a.m_tiles = (int32_t)((p.M + 128 * a.msub - 1) / (128 * a.msub));
   a.BN = pick_bn(a.m_tiles, p.N, sms);
-  a.n_tiles = (p.N + a.BN - 1) / a.BN;
+  const int n_tiles = (p.N + a.BN - 1) / a.BN;
   a.group_m = 16;
   a.num_kb = (p.K + kBK - 1) / kBK;
   a.stage_bytes = a.msub * kATileBytes + a.BN * kBK * 2;
@@ -386,28 +509,32 @@ int launch_gemm(const GemmParams& p, cudaStream_t stream) {
             | ((uint32_t)(a.BN >> 3) << 17)   // N
             | ((uint32_t)(128 >> 4) << 24);   // M = 128; A and B K-major (bits 15, 16 = 0)
   a.err = p.err;
-
-  CUtensorMap mA, mB;
-  if (!make_map(&mA, p.A, p.M, p.K, 128) || !make_map(&mB, p.B, p.N, p.K, (uint32_t)a.BN)) {
-    set_error("engram_project: cuTensorMapEncodeTiled failed (driver entry point missing or bad layout)");
-    return ENGRAM_ECUDA;
-  }
   const int smem = 1024 + a.stages * a.stage_bytes + ctl_bytes;
+
   static bool configured[64] = {false};     // the attribute is per device
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !configured[dev]) {
     cudaError_t e = cudaFuncSetAttribute(wkv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
     if (e != cudaSuccess) return fail_cuda(e, "engram_project: cudaFuncSetAttribute");
+    e = cudaFuncSetAttribute(wkv_gemm_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return fail_cuda(e, "engram_project: cudaFuncSetAttribute (cluster)");
     if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
+  a.cluster = pick_cluster(n_tiles, a.m_tiles, smem);
+  a.n_tiles = ((n_tiles + a.cluster - 1) / a.cluster) * a.cluster;   // padded tiles store nothing
+
+  CUtensorMap mA, mB;
+  if (!make_map(&mA, p.A, p.M, p.K, (uint32_t)(128 / a.cluster)) || !make_map(&mB, p.B, p.N, p.K, (uint32_t)a.BN)) {
+    set_error("engram_project: cuTensorMapEncodeTiled failed (driver entry point missing or bad layout)");
+    return ENGRAM_ECUDA;
   }
   const int64_t grid = (int64_t)a.m_tiles * a.n_tiles;
   if (grid > 0x7fffffff) {
     set_error("engram_project: too many tiles");
     return ENGRAM_EINVAL;
   }
-  wkv_gemm_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(mA, mB, p.D, a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch(mA, mB, p.D, a, grid, smem, stream, pdl);
   if (e != cudaSuccess) return fail_cuda(e, "engram_project: launch");
   return ENGRAM_OK;
 }

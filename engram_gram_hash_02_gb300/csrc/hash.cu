@@ -33,6 +33,8 @@ __device__ __forceinline__ int32_t find_sequence(Load cu, int32_t S, int64_t t) 
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 hash_kernel(const HashParams p) {
   __shared__ int32_t s_cu[kSmemCu];
+  pdl_wait();                                    // inputs may come from the preceding kernel
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const bool live = t < p.T;
@@ -119,10 +121,9 @@ hash_kernel(const HashParams p) {
 
 }  // namespace
 
-cudaError_t launch_hash(const HashParams& p, cudaStream_t stream) {
+cudaError_t launch_hash(const HashParams& p, cudaStream_t stream, bool pdl) {
   const int64_t blocks = (p.T + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  hash_kernel<<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_k(hash_kernel, dim3((unsigned)blocks), dim3(kWarpsPerBlock * 32), 0, stream, pdl, p);
 }
 
 }  // namespace engram

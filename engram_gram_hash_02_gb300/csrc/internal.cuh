@@ -26,6 +26,32 @@ inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 
 int num_sms();  // of the current device, cached per device
 
+// ---- programmatic dependent launch ----------------------------------------------------------
+// Inside engram_forward each kernel is launched so that it may start while its predecessor on
+// the stream is still running. Every kernel runs pdl_wait() (all prerequisite grids complete and
+// their writes visible) before it reads anything a predecessor wrote or writes anything a
+// predecessor reads, and every CTA runs it before exiting; pdl_trigger() comes only after the
+// wait, so a dependent grid starts only once every earlier kernel but its immediate predecessor
+// has finished. Launched without the attribute (the single-stage entry points), both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename Kernel, typename... Args>
+cudaError_t launch_k(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                     Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // ---- launchers (validated arguments only) ---------------------------------------------
 struct HashParams {
   const int32_t* input_ids;
@@ -44,7 +70,7 @@ struct HashParams {
   int32_t layers, max_ngram, n_heads, cols;
   int32_t raw_vocab, pad_id;
 };
-cudaError_t launch_hash(const HashParams& p, cudaStream_t stream);
+cudaError_t launch_hash(const HashParams& p, cudaStream_t stream, bool pdl = false);
 
 struct GatherParams {
   int32_t fmt;
@@ -58,7 +84,7 @@ struct GatherParams {
   uint16_t* out;
   int32_t* err;
 };
-cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream);
+cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl = false);
 
 struct GemmParams {
   const uint16_t* A;
@@ -69,7 +95,7 @@ struct GemmParams {
   int32_t* err;
 };
 // returns ENGRAM_OK or an error code (sets the message)
-int launch_gemm(const GemmParams& p, cudaStream_t stream);
+int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl = false);
 
 struct GateParams {
   float* streams;
@@ -81,6 +107,6 @@ struct GateParams {
   int32_t H, hc;
   float eps, clamp;
 };
-cudaError_t launch_gate(const GateParams& p, cudaStream_t stream);
+cudaError_t launch_gate(const GateParams& p, cudaStream_t stream, bool pdl = false);
 
 }  // namespace engram

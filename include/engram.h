@@ -158,6 +158,9 @@ int engram_project(const uint16_t* A, const uint16_t* wkv, float* kv, int64_t T,
 /* Tuning knob for engram_project: force the tile width (columns per CTA, a multiple of 16 in
  * [16, 256]); 0 restores the automatic choice. Process-wide; not thread-safe against calls. */
 void engram_set_gemm_tile(int32_t bn);
+/* Tuning knob for engram_project: CTAs per cluster that share (multicast) each A tile, 1, 2 or 4;
+ * 0 restores the automatic choice. Process-wide. */
+void engram_set_gemm_cluster(int32_t c);
 
 /*
  * Stage 4: gate, in place on the fp32 highway ([NeMo] _engram_gate_core; [vLLM]

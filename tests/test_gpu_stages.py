@@ -161,19 +161,25 @@ def test_project_vs_fp64(T, K, N):
     assert torch.allclose(kv, tm, rtol=1e-4, atol=1e-4 * float(tm.pow(2).mean().sqrt()))
 
 
-@pytest.mark.parametrize("bn", [16, 48, 128, 144, 256])
-def test_project_tile_widths(bn):
+@pytest.mark.parametrize("bn,cluster", [(16, 1), (48, 2), (128, 4), (144, 2), (144, 4), (256, 1), (256, 2),
+                                        (96, 4)])
+def test_project_tile_widths_and_clusters(bn, cluster):
+    # N = 1440 gives 10, 30, 12, 10, 6 or 15 column tiles: clusters of 2 and 4 pad the last group
     T, K, N = 260, 640, 1440
-    g = torch.Generator(device=DEV).manual_seed(bn)
+    g = torch.Generator(device=DEV).manual_seed(bn * 10 + cluster)
     A = (torch.randn(T, K, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
     W = (torch.randn(N, K, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
     try:
         E().set_gemm_tile(bn)
-        kv = E().engram_project(A, W)
+        E().set_gemm_cluster(cluster)
+        kv = E().engram_project(A, W, err=err)
         torch.cuda.synchronize()
     finally:
         E().set_gemm_tile(0)
-    H.check_kv(kv.cpu().numpy(), O.project(H.bits16(A), H.bits16(W)), f"bn={bn}")
+        E().set_gemm_cluster(0)
+    assert int(err.item()) == 0
+    H.check_kv(kv.cpu().numpy(), O.project(H.bits16(A), H.bits16(W)), f"bn={bn} cluster={cluster}")
 
 
 def test_project_integer_exact():

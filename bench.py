@@ -149,6 +149,7 @@ class Path:
         self.A = torch.empty((T, K), dtype=torch.bfloat16, device=d)
         self.kv = torch.empty((T, N), dtype=torch.float32, device=d)
         self.err = torch.zeros(1, dtype=torch.int32, device=d)
+        self.gemm_ws = torch.empty(max(256, E.project_workspace_bytes(T, K, N)), dtype=torch.uint8, device=d)
         self.table_rows = rows
 
     @staticmethod
@@ -172,7 +173,7 @@ class Path:
         for l, lw in enumerate(self.layers):
             g_args = (B.TABLE_FORMATS[lw.fmt], self.ids.data_ptr() + 4 * l * Cc, L * Cc, T, Cc, w.head_dim,
                       p(lw.table), p(lw.scales), int(lw.num_rows), p(self.A), p(self.err), s)
-            pr_args = (p(self.A), p(lw.wkv), p(self.kv), T, K, N, None, 0, p(self.err), s)
+            pr_args = (p(self.A), p(lw.wkv), p(self.kv), T, K, N, p(self.gemm_ws), self.gemm_ws.numel(), p(self.err), s)
             ga_args = (C.byref(dims), p(self.streams[l]), p(self.kv), p(lw.q_weight), p(lw.k_weight),
                        p(self.mask), T, s)
             calls.append((f"gather{l}", lambda a=g_args: lib.engram_gather_dequant(*a)))

@@ -23,6 +23,7 @@ from .binding import (  # noqa: F401
     hash_multipliers,
     lib,
     make_dims,
-    set_gemm_cluster,
+    project_workspace_bytes,
+    set_gemm_schedule,
     set_gemm_tile,
 )

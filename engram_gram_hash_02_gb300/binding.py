@@ -83,8 +83,10 @@ def lib() -> C.CDLL:
         L.engram_forward_noalloc.argtypes = [P, P, P, P, P, P, P, P]
         L.engram_set_gemm_tile.argtypes = [I32]
         L.engram_set_gemm_tile.restype = None
-        L.engram_set_gemm_cluster.argtypes = [I32]
-        L.engram_set_gemm_cluster.restype = None
+        L.engram_set_gemm_schedule.argtypes = [I32]
+        L.engram_set_gemm_schedule.restype = None
+        L.engram_project_workspace_bytes.argtypes = [I64, I32, I32]
+        L.engram_project_workspace_bytes.restype = SZ
         _lib = L
     return _lib
 
@@ -207,7 +209,9 @@ def engram_gather_dequant(fmt: str, ids, table, scales, num_rows: int, head_dim:
     return out
 
 
-def engram_project(A, wkv, out=None, err=None, stream=None):
+def engram_project(A, wkv, out=None, err=None, workspace="auto", stream=None):
+    """workspace: a uint8 CUDA tensor, None (no workspace), or "auto" (allocated at the size
+    engram_project_workspace_bytes asks for)."""
     _u16(A, "A")
     _u16(wkv, "wkv")
     T, K = A.shape
@@ -218,8 +222,12 @@ def engram_project(A, wkv, out=None, err=None, stream=None):
         out = torch.empty((T, N), dtype=torch.float32, device=A.device)
     _dev(out, torch.float32, "out")
     _opt(err, torch.int32, "err")
-    _check("engram_project", lib().engram_project(_ptr(A), _ptr(wkv), _ptr(out), T, K, N, None, 0, _ptr(err),
-                                                   _stream(stream)))
+    if isinstance(workspace, str):
+        nbytes = project_workspace_bytes(T, K, N) if T > 0 else 0
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=A.device) if nbytes else None
+    ws_bytes = 0 if workspace is None else workspace.numel()
+    _check("engram_project", lib().engram_project(_ptr(A), _ptr(wkv), _ptr(out), T, K, N, _ptr(workspace), ws_bytes,
+                                                   _ptr(err), _stream(stream)))
     return out
 
 
@@ -240,8 +248,13 @@ def set_gemm_tile(bn: int = 0):
     lib().engram_set_gemm_tile(int(bn))
 
 
-def set_gemm_cluster(c: int = 0):
-    lib().engram_set_gemm_cluster(int(c))
+def set_gemm_schedule(s: int = 0):
+    """0 automatic, 1 data-parallel tiles, 2 stream-K (when the workspace allows)."""
+    lib().engram_set_gemm_schedule(int(s))
+
+
+def project_workspace_bytes(T: int, K: int, N: int) -> int:
+    return int(lib().engram_project_workspace_bytes(T, K, N))
 
 
 # ---------------------------------------------------------------------------------------------
@@ -299,6 +312,9 @@ class ForwardPlan:
         self._streams = (C.c_void_p * len(streams))(*[s.data_ptr() for s in streams])
         need = forward_workspace_bytes(dims, T)
         if workspace is None:
+            # the minimum plus the projection's stream-K scratch
+            K, N = dims.cols * dims.head_dim, dims.hidden * (dims.hc + 1)
+            need += project_workspace_bytes(T, K, N) if T > 0 else 0
             workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=input_ids.device)
         self.workspace = workspace
         self._ws_bytes = workspace.numel() * workspace.element_size()

@@ -39,7 +39,7 @@ int num_sms() {
 }
 
 void set_gemm_bn_override(int bn);
-void set_gemm_cluster_override(int c);
+void set_gemm_schedule_override(int s);
 
 static int check_dims(const EngramDims* d, bool need_hash, bool need_gate) {
   ENGRAM_CHECK_ARG(d != nullptr, "dims is NULL");
@@ -129,7 +129,12 @@ void engram_set_gemm_tile(int32_t bn) {
   set_gemm_bn_override((bn >= 16 && bn <= 256 && bn % 16 == 0) ? bn : 0);
 }
 
-void engram_set_gemm_cluster(int32_t c) { set_gemm_cluster_override((c == 1 || c == 2 || c == 4) ? c : 0); }
+void engram_set_gemm_schedule(int32_t s) { set_gemm_schedule_override((s == 1 || s == 2) ? s : 0); }
+
+size_t engram_project_workspace_bytes(int64_t T, int32_t K, int32_t N) {
+  if (T <= 0 || T >= ((int64_t)1 << 31) || K < 8 || K % 8 != 0 || N < 16 || N % 16 != 0) return 0;
+  return gemm_workspace_bytes(T, K, N);
+}
 
 static int hash_impl(const EngramDims* dims, const int32_t* input_ids, int64_t T, const int32_t* cu_seqlens,
                      int32_t S, const int32_t* sequence_ids, const uint8_t* token_mask, const int32_t* lookback_ids,
@@ -196,19 +201,18 @@ int engram_gather_dequant(int32_t fmt, const int32_t* ids, int64_t ids_stride_t,
 }
 
 static int project_impl(const uint16_t* A, const uint16_t* wkv, float* kv, int64_t T, int32_t K, int32_t N,
-                        int32_t* err_flag, engram_stream_t stream, bool pdl) {
+                        void* workspace, size_t ws_bytes, int32_t* err_flag, engram_stream_t stream, bool pdl) {
   if (T == 0) return ENGRAM_OK;
   int rc = check_project(A, wkv, kv, T, K, N);
   if (rc) return rc;
-  GemmParams p{A, wkv, kv, T, K, N, err_flag};
+  ENGRAM_CHECK_ARG(workspace == nullptr || aligned(workspace, 256), "engram_project: workspace must be 256-byte aligned");
+  GemmParams p{A, wkv, kv, T, K, N, err_flag, workspace, workspace != nullptr ? ws_bytes : 0};
   return launch_gemm(p, static_cast<cudaStream_t>(stream), pdl);
 }
 
 int engram_project(const uint16_t* A, const uint16_t* wkv, float* kv, int64_t T, int32_t K, int32_t N,
                    void* workspace, size_t ws_bytes, int32_t* err_flag, engram_stream_t stream) {
-  (void)workspace;
-  (void)ws_bytes;
-  return project_impl(A, wkv, kv, T, K, N, err_flag, stream, false);
+  return project_impl(A, wkv, kv, T, K, N, workspace, ws_bytes, err_flag, stream, false);
 }
 
 static int gate_impl(const EngramDims* dims, float* streams, const float* kv, const uint16_t* q_weight,
@@ -267,6 +271,9 @@ int engram_forward(const EngramDims* dims, const EngramHashTables* tables, const
   int32_t* ids = out_ids != nullptr ? out_ids : reinterpret_cast<int32_t*>(ws);
   uint16_t* A = reinterpret_cast<uint16_t*>(ws + round256((size_t)(T * L * C * 4)));
   float* kv = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(A) + round256((size_t)(T * K * 2)));
+  // workspace beyond the minimum goes to the projection (stream-K partials)
+  void* gemm_ws = ws_bytes > need ? static_cast<void*>(ws + need) : nullptr;
+  const size_t gemm_ws_bytes = ws_bytes > need ? ws_bytes - need : 0;
 
   // each launch may start while its predecessor finishes (programmatic dependent launch)
   rc = hash_impl(dims, tok->input_ids, T, tok->cu_seqlens, tok->num_seqs, tok->sequence_ids, tok->token_mask,
@@ -278,7 +285,7 @@ int engram_forward(const EngramDims* dims, const EngramHashTables* tables, const
     rc = gather_impl(w.table_format, ids + (int64_t)l * C, (int64_t)L * C, T, C, dims->head_dim, w.table,
                      w.table_scales, w.table_rows, A, err_flag, stream, true);
     if (rc) return rc;
-    rc = project_impl(A, w.wkv, kv, T, (int32_t)K, (int32_t)N, err_flag, stream, true);
+    rc = project_impl(A, w.wkv, kv, T, (int32_t)K, (int32_t)N, gemm_ws, gemm_ws_bytes, err_flag, stream, true);
     if (rc) return rc;
     rc = gate_impl(dims, streams[l], kv, w.q_weight, w.k_weight, tok->token_mask, T, stream, true);
     if (rc) return rc;

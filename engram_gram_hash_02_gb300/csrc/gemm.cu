@@ -4,23 +4,36 @@
 // n_hash_cols*head_dim -> dim*(hc+1); Engram.forward) and of the Atlas "engram_v41" page
 // (stage 3: dense bf16 GEMM). bf16 operands, fp32 accumulation in tensor memory, fp32 out.
 //
-// One CTA computes a tile of up to 256 rows (two 128-row accumulators) x BN columns:
+// A persistent kernel, one CTA per SM, 6 warps:
 //   warp 0      TMA producer: 128B-swizzled K-major tiles of A (128 rows x 64) and of wkv
-//               (BN rows x 64) into a ring of shared-memory stages, mbarrier complete_tx. Under
+//               (BN rows x 64) into a ring of shared-memory stages (mbarrier complete_tx). Under
 //               programmatic dependent launch the first ring of wkv tiles is requested before
 //               waiting for the kernel that writes A.
 //   warp 1      allocates tensor memory; one lane issues tcgen05.mma (M=128, N=BN, K=16,
-//               kind::f16) per 16-wide k step and releases a stage with tcgen05.commit.
-//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator (each warp its 32-lane quarter),
-//               16-byte stores of fp32 kv (kept in fp32 for the gate's reductions).
-// Both tiles of a 256-row block share each wkv tile, so wkv is read from memory once per
-// column block. BN is picked per shape so the number of tiles fills the SMs in few waves.
+//               kind::f16) and releases each stage with tcgen05.commit.
+//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulators (each warp its 32-lane quarter),
+//               transposed through a small shared tile so stores to kv are coalesced rows.
+// Every item accumulates into two TMEM accumulators, which the tensor core runs as independent
+// chains (back-to-back MMAs into one accumulator wait on each other): the two 128-row halves of
+// a 256-row tile, or, for tiles of at most 128 rows, the even and odd k steps of one tile
+// (summed in the epilogue).
 //
-// Every mbarrier wait is bounded (~2 s of SM clock cycles); on expiry the CTA raises an abort
-// flag, reports ENGRAM_ERR_PIPE_TIMEOUT, drains its in-flight copies and MMAs (again
+// Schedules (items are (tile, k-range) pairs; the roles walk the same sequence):
+//   data-parallel  CTA c takes tiles c, c + grid, ... over the whole K (many tiles);
+//   stream-K       the tiles x k-blocks are split evenly over all CTAs, so a shape with fewer
+//                  tiles than SMs (the decode step: 80 tiles of 256 x 256) still keeps every SM
+//                  streaming wkv. A tile cut between CTAs is finished by the CTA holding its last
+//                  k-block (the owner): the others write fp32 partials to the caller's workspace
+//                  and publish an epoch-tagged flag; the owner adds them in CTA order
+//                  (deterministic). Each CTA runs its segments last-first, so partials are
+//                  produced early and consumed late. All CTAs are co-resident (grid <= SMs).
+//
+// Every wait (mbarrier or flag) is bounded (~2 s of SM clock cycles); on expiry the CTA raises
+// an abort flag, reports ENGRAM_ERR_PIPE_TIMEOUT, drains its in-flight copies and MMAs (again
 // bounded), frees its tensor memory and exits.
 #include <cuda.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "internal.cuh"
@@ -31,29 +44,94 @@ namespace {
 constexpr int kBK = 64;                    // k elements per stage (128 bytes = one swizzle row)
 constexpr int kUmmaK = 16;                 // k per tcgen05.mma for 16-bit operands
 constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
 constexpr int kMaxStages = 8;
 constexpr int kATileBytes = 128 * kBK * 2;  // 16 KB
 constexpr uint64_t kWaitLimitCycles = 4000000000ull;  // wait bound in SM cycles: ~2 s at 2 GHz
 constexpr int kSmemBudget = 232448;        // 227 KB opt-in maximum per CTA
+constexpr unsigned long long kFlagMagic = 0x5EA5C0DEull;
+constexpr int kEpiChunk = 32;                        // columns staged per warp and step
+constexpr int kEpiStride = kEpiChunk + 4;            // padded row (floats): conflict-free 16-B access
+constexpr int kEpiBytes = 4 * 32 * kEpiStride * 4;   // four epilogue warps x 32 rows
 
 struct Ctl {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  uint64_t acc_full;
+  uint64_t acc_full;                       // MMA -> epilogue: the item's accumulators are final
+  uint64_t acc_empty;                      // epilogue -> MMA: tensor memory drained
   uint32_t tmem_base;
   int32_t abort_flag;
 };
 
 struct GemmArgs {
   int32_t M, K, N;
-  int32_t cluster;
   int32_t BN, msub, stages, num_kb;
   int32_t m_tiles, n_tiles, group_m;
   int32_t stage_bytes;
   uint32_t idesc;
   uint32_t tmem_cols, acc_stride;
+  int32_t stream_k;                        // 0: data-parallel tiles, 1: stream-K
+  int64_t total_units;                     // tiles * num_kb
+  float* partial;                          // [grid][msub*128][BN] fp32 (stream-K)
+  unsigned long long* flags;               // [grid] (stream-K)
+  unsigned long long epoch;
   int32_t* err;
 };
+
+struct Item {
+  int tile, k0, k1;
+};
+
+// The sequence of items of CTA b. Every role constructs one and walks it in the same order.
+struct Schedule {
+  const GemmArgs& a;
+  int b, grid;
+  int next_tile;                           // data-parallel
+  int64_t u_begin, u_end, cursor;          // stream-K: this CTA's unit range, walked backwards
+  __device__ Schedule(const GemmArgs& args, int block, int g) : a(args), b(block), grid(g) {
+    next_tile = block;
+    const int64_t base = a.total_units / g, rem = a.total_units % g;
+    u_begin = (int64_t)block * base + (block < rem ? block : rem);
+    u_end = u_begin + base + (block < rem ? 1 : 0);
+    cursor = u_end;
+  }
+  __device__ bool next(Item& it) {
+    if (!a.stream_k) {
+      if (next_tile >= a.m_tiles * a.n_tiles) return false;
+      it.tile = next_tile;
+      it.k0 = 0;
+      it.k1 = a.num_kb;
+      next_tile += grid;
+      return true;
+    }
+    if (cursor <= u_begin) return false;
+    const int64_t last = cursor - 1;
+    const int tile = (int)(last / a.num_kb);
+    const int64_t tile_start = (int64_t)tile * a.num_kb;
+    const int64_t seg_start = tile_start > u_begin ? tile_start : u_begin;
+    it.tile = tile;
+    it.k0 = (int)(seg_start - tile_start);
+    it.k1 = (int)(cursor - tile_start);
+    cursor = seg_start;
+    return true;
+  }
+  // CTA whose unit range holds unit u
+  __device__ int owner_of(int64_t u) const {
+    const int64_t base = a.total_units / grid, rem = a.total_units % grid;
+    const int64_t big = rem * (base + 1);
+    return u < big ? (int)(u / (base + 1)) : (int)(rem + (u - big) / base);
+  }
+};
+
+__device__ __forceinline__ void tile_origin(const GemmArgs& a, int tile, int& m0, int& n0) {
+  // grouped raster: consecutive tiles sweep group_m row blocks of one column block
+  const int per_group = a.group_m * a.n_tiles;
+  const int first_m = (tile / per_group) * a.group_m;
+  const int gsize = min(a.m_tiles - first_m, a.group_m);
+  const int in_group = tile % per_group;
+  m0 = (first_m + in_group % gsize) * 128 * a.msub;
+  n0 = (in_group / gsize) * a.BN;
+}
 
 // ---- PTX wrappers ------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -64,6 +142,9 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -126,7 +207,7 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
       : "memory");
 }
 // 32 lanes x 16 columns of 32-bit accumulator: thread i gets lane (quarter*32 + i)
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -136,6 +217,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void epi_bar() {  // the 128 epilogue threads only
+  asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 
 // Shared-memory matrix descriptor: K-major operand stored as 128-byte rows with the 128B
 // swizzle (what TMA writes with CU_TENSOR_MAP_SWIZZLE_128B); 8-row groups 1024 bytes apart.
@@ -149,70 +241,31 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// A slice multicast into the same offset of every CTA in `mask`, each signalling its own barrier
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x,
-                                               int32_t y, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
-      : "memory");
-}
-// release a stage in every CTA of the cluster once this CTA's MMAs have read it
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
 wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 float* __restrict__ D, const GemmArgs a) {
-  const int c = a.cluster;                     // CTAs sharing one row block (launch cluster size)
   // A timeout anywhere in an earlier launch sharing the flag word voids the result: skip the
-  // work instead of waiting out the time limits again. (Clustered CTAs must all take part.)
-  if (c == 1 && a.err != nullptr && (*reinterpret_cast<volatile int32_t*>(a.err) & ENGRAM_ERR_PIPE_TIMEOUT)) return;
+  // work instead of waiting out the time limits again.
+  if (a.err != nullptr && (*reinterpret_cast<volatile int32_t*>(a.err) & ENGRAM_ERR_PIPE_TIMEOUT)) {
+    pdl_wait();
+    return;
+  }
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t tiles = (raw_base + 1023u) & ~1023u;          // swizzled tiles need 1 KB alignment
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem_raw + (tiles - raw_base) + a.stages * a.stage_bytes);
+  float* epi_stage = reinterpret_cast<float*>(smem_raw + (tiles - raw_base) + a.stages * a.stage_bytes);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem_raw + (tiles - raw_base) + a.stages * a.stage_bytes + kEpiBytes);
   volatile int32_t* abort_flag = &ctl->abort_flag;
-
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = c > 1 ? cluster_ctarank() : 0;
-  const uint16_t all_ctas = (uint16_t)((1u << c) - 1u);
-
-  // grouped raster over clusters: consecutive clusters sweep group_m row blocks of one group of
-  // c column blocks; the CTAs of a cluster share the row block and take adjacent column blocks
-  const int ct = blockIdx.x / c;
-  const int n_clusters = a.n_tiles / c;        // n_tiles is padded to a multiple of c
-  const int per_group = a.group_m * n_clusters;
-  const int first_m = (ct / per_group) * a.group_m;
-  const int gsize = min(a.m_tiles - first_m, a.group_m);
-  const int in_group = ct % per_group;
-  const int m_blk = first_m + in_group % gsize;
-  const int n_blk = (in_group / gsize) * c + (int)rank;
-  const int m0 = m_blk * 128 * a.msub;
-  const int n0 = n_blk * a.BN;
-  const int a_rows = 128 / c;                  // rows of each 128-row A tile this CTA loads
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
-      mbar_init(smem_u32(&ctl->empty[s]), (uint32_t)c);   // one release per consumer in the cluster
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
     }
     mbar_init(smem_u32(&ctl->acc_full), 1);
+    mbar_init(smem_u32(&ctl->acc_empty), kEpiThreads);
     ctl->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -229,126 +282,225 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
-  if (c > 1) cluster_sync_all();               // peers' barriers exist before anyone multicasts
-  else __syncthreads();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      auto load_a = [&](int kb) {
-        const int s = kb % a.stages;
-        const uint32_t full = smem_u32(&ctl->full[s]);
-        const uint32_t st = tiles + (uint32_t)(s * a.stage_bytes);
-        for (int ms = 0; ms < a.msub; ++ms) {
-          const uint32_t dst = st + ms * kATileBytes + rank * (uint32_t)(a_rows * kBK * 2);
-          const int y = m0 + ms * 128 + (int)rank * a_rows;
-          if (c > 1) tma_load_2d_mc(dst, &tmA, full, kb * kBK, y, all_ctas);
-          else tma_load_2d(dst, &tmA, full, kb * kBK, y);
-        }
-      };
-      auto load_b = [&](int kb) {
-        const int s = kb % a.stages;
+      auto load_b = [&](int it, int kb, int n0) {
+        const int s = it % a.stages;
         const uint32_t full = smem_u32(&ctl->full[s]);
         const uint32_t st = tiles + (uint32_t)(s * a.stage_bytes);
         mbar_expect_tx(full, (uint32_t)a.stage_bytes);
         tma_load_2d(st + a.msub * kATileBytes, &tmB, full, kb * kBK, n0);
       };
+      auto load_a = [&](int it, int kb, int m0) {
+        const int s = it % a.stages;
+        const uint32_t full = smem_u32(&ctl->full[s]);
+        const uint32_t st = tiles + (uint32_t)(s * a.stage_bytes);
+        for (int ms = 0; ms < a.msub; ++ms) tma_load_2d(st + ms * kATileBytes, &tmA, full, kb * kBK, m0 + ms * 128);
+      };
       // wkv does not come from the preceding kernel: fill the ring's weight halves before waiting
       // for the gathered rows (A) to be complete
-      const int early = a.num_kb < a.stages ? a.num_kb : a.stages;
-      for (int kb = 0; kb < early; ++kb) load_b(kb);
+      int early = 0;
+      {
+        Schedule sch(a, blockIdx.x, gridDim.x);
+        Item item;
+        while (early < a.stages && sch.next(item)) {
+          int m0, n0;
+          tile_origin(a, item.tile, m0, n0);
+          for (int kb = item.k0; kb < item.k1 && early < a.stages; ++kb) load_b(early++, kb, n0);
+        }
+      }
       pdl_wait();
       pdl_trigger();
-      for (int kb = 0; kb < early; ++kb) load_a(kb);
-      int issued = early;
+      int it = 0, issued = 0;
       bool ok = true;
-      for (int kb = early; kb < a.num_kb; ++kb) {
-        const int s = kb % a.stages;
-        const uint32_t ph = (uint32_t)(kb / a.stages) & 1u;
-        // every consumer in the cluster has released stage s (the A slices land in all of them)
-        if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, a.err, kWaitLimitCycles)) {
-          ok = false;
-          break;
+      Schedule sch(a, blockIdx.x, gridDim.x);
+      Item item;
+      while (ok && sch.next(item)) {
+        int m0, n0;
+        tile_origin(a, item.tile, m0, n0);
+        for (int kb = item.k0; kb < item.k1; ++kb, ++it) {
+          if (it < early) {
+            load_a(it, kb, m0);
+          } else {
+            const int s = it % a.stages;
+            const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+            if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, a.err, kWaitLimitCycles)) {
+              ok = false;
+              break;
+            }
+            load_b(it, kb, n0);
+            load_a(it, kb, m0);
+          }
+          issued = it + 1;
         }
-        load_b(kb);
-        load_a(kb);
-        issued = kb + 1;
       }
-      if (ok) {
-        // producer tail: wait until every consumer in the cluster has released the last stages,
-        // so no peer's release can arrive here after this CTA has exited
-        for (int kb = a.num_kb; kb < a.num_kb + a.stages; ++kb) {
-          const int s = kb % a.stages;
-          const uint32_t ph = (uint32_t)(kb / a.stages) & 1u;
-          if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, a.err, kWaitLimitCycles)) break;
-        }
-      } else {
+      if (!ok) {
         // drain: the copies still in flight must land before shared memory goes away
         const int first = issued > a.stages ? issued - a.stages : 0;
-        for (int kb = first; kb < issued; ++kb) {
-          const int s = kb % a.stages;
-          const uint32_t ph = (uint32_t)(kb / a.stages) & 1u;
+        for (int j = first; j < issued; ++j) {
           volatile int32_t never = 0;
-          mbar_wait(smem_u32(&ctl->full[s]), ph, &never, nullptr, kWaitLimitCycles / 4);
+          mbar_wait(smem_u32(&ctl->full[j % a.stages]), (uint32_t)(j / a.stages) & 1u, &never, nullptr,
+                    kWaitLimitCycles / 4);
         }
       }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      for (int kb = 0; kb < a.num_kb; ++kb) {
-        const int s = kb % a.stages;
-        const uint32_t ph = (uint32_t)(kb / a.stages) & 1u;
-        if (!mbar_wait(smem_u32(&ctl->full[s]), ph, abort_flag, a.err, kWaitLimitCycles)) break;
-        tc_fence_after();
-        const uint32_t st = tiles + (uint32_t)(s * a.stage_bytes);
-        const uint32_t b_addr = st + (uint32_t)(a.msub * kATileBytes);
-#pragma unroll
-        for (int k = 0; k < kBK / kUmmaK; ++k) {
-          const uint64_t bdesc = smem_desc_sw128(b_addr + k * kUmmaK * 2);
-          for (int ms = 0; ms < a.msub; ++ms) {
-            const uint64_t adesc = smem_desc_sw128(st + ms * kATileBytes + k * kUmmaK * 2);
-            tc_mma(tmem + ms * a.acc_stride, adesc, bdesc, a.idesc, (kb | k) != 0 ? 1u : 0u);
-          }
+      Schedule sch(a, blockIdx.x, gridDim.x);
+      Item item;
+      int it = 0, n_items = 0;
+      bool ok = true;
+      while (ok && sch.next(item)) {
+        // the epilogue has drained the previous item's accumulators
+        if (!mbar_wait(smem_u32(&ctl->acc_empty), (uint32_t)(n_items & 1) ^ 1u, abort_flag, a.err,
+                       kWaitLimitCycles)) {
+          ok = false;
+          break;
         }
-        if (c > 1) tc_commit_mc(smem_u32(&ctl->empty[s]), all_ctas);
-        else tc_commit(smem_u32(&ctl->empty[s]));   // stage free once these MMAs have read it
+        tc_fence_after();
+        for (int kb = item.k0; kb < item.k1; ++kb, ++it) {
+          const int s = it % a.stages;
+          const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+          if (!mbar_wait(smem_u32(&ctl->full[s]), ph, abort_flag, a.err, kWaitLimitCycles)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = tiles + (uint32_t)(s * a.stage_bytes);
+          const uint32_t b_addr = st + (uint32_t)(a.msub * kATileBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k) {
+            const uint64_t bdesc = smem_desc_sw128(b_addr + k * kUmmaK * 2);
+            if (a.msub == 2) {
+              // two chains: the two 128-row halves
+              for (int ms = 0; ms < 2; ++ms) {
+                const uint64_t adesc = smem_desc_sw128(st + ms * kATileBytes + k * kUmmaK * 2);
+                tc_mma(tmem + ms * a.acc_stride, adesc, bdesc, a.idesc, (kb > item.k0 || k > 0) ? 1u : 0u);
+              }
+            } else {
+              // two chains: even and odd k steps of the same tile
+              const uint64_t adesc = smem_desc_sw128(st + k * kUmmaK * 2);
+              tc_mma(tmem + (k & 1) * a.acc_stride, adesc, bdesc, a.idesc, (kb > item.k0 || k > 1) ? 1u : 0u);
+            }
+          }
+          tc_commit(smem_u32(&ctl->empty[s]));   // stage free once these MMAs have read it
+        }
+        tc_commit(smem_u32(&ctl->acc_full));     // this item's accumulators final (or drained)
+        ++n_items;
       }
-      tc_commit(smem_u32(&ctl->acc_full));     // accumulators final (or drained, on abort)
+      if (!ok) tc_commit(smem_u32(&ctl->acc_full));
     }
   } else {
-    // ---------------- epilogue: TMEM -> registers -> fp32 kv ----------------
+    // ---------------- epilogue: TMEM -> registers -> shared tile -> fp32 kv / partials --------
     const int q = warp & 3;                    // TMEM lane quarter this warp may access
+    const int et = threadIdx.x - 64;           // 0..127
     pdl_wait();                                // kv may still be read by an earlier kernel
-    const bool ok = mbar_wait(smem_u32(&ctl->acc_full), 0, abort_flag, a.err, kWaitLimitCycles);
-    tc_fence_after();
-    if (ok && *abort_flag == 0) {
-      for (int ms = 0; ms < a.msub; ++ms) {
-        const int64_t row = (int64_t)m0 + ms * 128 + q * 32 + lane;
-        const bool row_ok = row < a.M;
-        float* drow = D + row * (int64_t)a.N;
-        const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ms * a.acc_stride);
-        for (int c0 = 0; c0 < a.BN; c0 += 32) {
-          uint32_t r[32];
-          const bool two = c0 + 16 < a.BN;
-          tmem_ld16(tbase + c0, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
-          if (two) tmem_ld16(tbase + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
-          tmem_ld_wait();
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int col = n0 + c0 + 16 * h;
-            if (row_ok && col < a.N && (h == 0 || two)) {
-              uint4* dst = reinterpret_cast<uint4*>(drow + col);
-              dst[0] = make_uint4(r[16 * h + 0], r[16 * h + 1], r[16 * h + 2], r[16 * h + 3]);
-              dst[1] = make_uint4(r[16 * h + 4], r[16 * h + 5], r[16 * h + 6], r[16 * h + 7]);
-              dst[2] = make_uint4(r[16 * h + 8], r[16 * h + 9], r[16 * h + 10], r[16 * h + 11]);
-              dst[3] = make_uint4(r[16 * h + 12], r[16 * h + 13], r[16 * h + 14], r[16 * h + 15]);
+    Schedule sch(a, blockIdx.x, gridDim.x);
+    Item item;
+    int n_items = 0;
+    const int rows_per_item = 128 * a.msub;
+    // Each warp owns 32 rows (its TMEM lane quarter) of each 128-row half. Per 32-column chunk,
+    // tcgen05.ld gives every thread 32 columns of its row; the chunk is transposed through a
+    // padded shared tile so that 8 lanes write (or read) 128 contiguous bytes of one row.
+    float* stg = epi_stage + q * 32 * kEpiStride;
+    const int sr = lane >> 3;                  // row offset within a group of 4
+    const int sc = (lane & 7) * 4;             // column of this lane's float4
+    while (sch.next(item)) {
+      const bool ok = mbar_wait(smem_u32(&ctl->acc_full), (uint32_t)(n_items & 1), abort_flag, a.err,
+                                kWaitLimitCycles);
+      tc_fence_after();
+      if (!ok || *abort_flag) break;
+      int m0, n0;
+      tile_origin(a, item.tile, m0, n0);
+      const bool whole = item.k0 == 0 && item.k1 == a.num_kb;
+      const bool owner = !whole && item.k1 == a.num_kb;
+      const bool contributor = !whole && !owner;
+      // contributors to this tile (owner only): the CTAs holding its units [0, k0)
+      int j_first = blockIdx.x, j_last = blockIdx.x - 1;
+      if (owner) {
+        j_first = sch.owner_of((int64_t)item.tile * a.num_kb);
+        j_last = blockIdx.x - 1;
+        bool flags_ok = true;
+        const unsigned long long want = (a.epoch << 32) | kFlagMagic;
+        for (int j = j_first; j <= j_last && flags_ok; ++j) {
+          const uint64_t t0 = clock64();
+          while (ld_acquire(a.flags + j) != want) {
+            if (*abort_flag || (uint64_t)clock64() - t0 > kWaitLimitCycles) {
+              *abort_flag = 1;
+              if (a.err != nullptr) atomicOr(a.err, ENGRAM_ERR_PIPE_TIMEOUT);
+              flags_ok = false;
+              break;
             }
           }
         }
+        if (!flags_ok) break;
       }
+      for (int ms = 0; ms < a.msub; ++ms) {
+        const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ms * a.acc_stride);
+        const int row0 = ms * 128 + q * 32;    // first row of this warp (within the item)
+        for (int c0 = 0; c0 < a.BN; c0 += kEpiChunk) {
+          const bool two = c0 + 16 < a.BN;     // BN is a multiple of 16
+          uint32_t r[32];
+          tmem_ld16(tbase + c0, &r[0]);
+          if (two) tmem_ld16(tbase + c0 + 16, &r[16]);
+          if (a.msub == 1) {                   // sum the even/odd k-step chains
+            uint32_t r2[32];
+            tmem_ld16(tbase + a.acc_stride + c0, &r2[0]);
+            if (two) tmem_ld16(tbase + a.acc_stride + c0 + 16, &r2[16]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
+          } else {
+            tmem_ld_wait();
+          }
+          const int ncol = two ? 32 : 16;
+          float4* my = reinterpret_cast<float4*>(stg + lane * kEpiStride);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (i * 4 < ncol)
+              my[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                  __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+          __syncwarp();
+          if (sc < ncol) {
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              const int wr = g * 4 + sr;       // row within the warp's 32
+              const int lrow = row0 + wr;      // row within the item
+              float4 v = *reinterpret_cast<const float4*>(stg + wr * kEpiStride + sc);
+              if (contributor) {
+                *reinterpret_cast<float4*>(a.partial + ((int64_t)blockIdx.x * rows_per_item + lrow) * a.BN + c0 + sc) = v;
+                continue;
+              }
+              if (owner) {
+                for (int j = j_first; j <= j_last; ++j) {   // fixed order: deterministic sums
+                  const float4 pv = __ldcg(reinterpret_cast<const float4*>(
+                      a.partial + ((int64_t)j * rows_per_item + lrow) * a.BN + c0 + sc));
+                  v.x += pv.x; v.y += pv.y; v.z += pv.z; v.w += pv.w;
+                }
+              }
+              const int64_t row = (int64_t)m0 + lrow;
+              const int col = n0 + c0 + sc;
+              if (row < a.M && col < a.N) *reinterpret_cast<float4*>(D + row * (int64_t)a.N + col) = v;
+            }
+          }
+          __syncwarp();
+        }
+      }
+      if (contributor) {
+        // publish the partial: every epilogue thread's stores before the flag
+        __threadfence();
+        epi_bar();
+        if (et == 0) st_release(a.flags + blockIdx.x, (a.epoch << 32) | kFlagMagic);
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&ctl->acc_empty));  // tensor memory may take the next item
+      ++n_items;
     }
   }
 
@@ -359,7 +511,8 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (*abort_flag) {
       // make sure no MMA is still writing the accumulators we are about to free
       volatile int32_t never = 0;
-      mbar_wait(smem_u32(&ctl->acc_full), 0, &never, nullptr, kWaitLimitCycles / 4);
+      for (int ph = 0; ph < 2; ++ph)
+        mbar_wait(smem_u32(&ctl->acc_full), (uint32_t)ph, &never, nullptr, kWaitLimitCycles / 8);
     }
     __syncwarp();
     tc_fence_after();
@@ -401,18 +554,24 @@ bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, uint32_t
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int g_bn_override = 0;       // engram_set_gemm_tile
-int g_cluster_override = 0;  // engram_set_gemm_cluster
+int g_bn_override = 0;      // engram_set_gemm_tile
+int g_sched_override = 0;   // engram_set_gemm_schedule: 0 auto, 1 data-parallel, 2 stream-K
+std::atomic<unsigned long long> g_epoch{1};
 
-int pick_bn(int64_t m_tiles, int N, int sms) {
-  if (g_bn_override > 0) return g_bn_override;
+uint32_t pow2_at_least(uint32_t x) {
+  uint32_t p = 32;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+// tile width for the data-parallel schedule: few waves of tiles over the SMs
+int pick_bn_dp(int64_t m_tiles, int N, int sms) {
   int best = 256;
   double best_cost = 1e300;
   for (int bn = 256; bn >= 64; bn -= 16) {
     const int64_t tiles = m_tiles * ((N + bn - 1) / bn);
     const int64_t waves = (tiles + sms - 1) / sms;
-    // a wave costs about its tile width plus a fixed share for the A operand and setup
-    const double cost = (double)waves * (bn + 48);
+    const double cost = (double)waves * (bn + 48);   // a wave ~ its tile width + fixed overhead
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = bn;
@@ -421,120 +580,107 @@ int pick_bn(int64_t m_tiles, int N, int sms) {
   return best;
 }
 
-uint32_t pow2_at_least(uint32_t x) {
-  uint32_t p = 32;
-  while (p < x) p <<= 1;
-  return p;
+struct Plan {
+  GemmArgs a;
+  int grid;
+  int smem;
+  size_t ws_needed;   // workspace of the stream-K schedule (0 when data-parallel)
+};
+
+size_t sk_workspace(int sms, int msub, int bn) {
+  return (((size_t)sms * 8 + 255) & ~(size_t)255) + (size_t)sms * (size_t)(128 * msub) * (size_t)bn * 4;
 }
 
-cudaError_t launch(const CUtensorMap& mA, const CUtensorMap& mB, float* D, const GemmArgs& a, int64_t grid,
-                   int smem, cudaStream_t stream, bool pdl) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)a.cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, wkv_gemm_kernel, mA, mB, D, a);
-}
-
-// Largest cluster (<= 4) whose clusters all fit on the GPU at once, or 2 when more than one
-// wave is needed anyway; 1 when there is only one column tile.
-int pick_cluster(int n_tiles, int64_t m_tiles, int smem) {
-  if (g_cluster_override > 0) return g_cluster_override;
-  if (n_tiles < 2) return 1;
-  int best = 1;
-  for (int c = 2; c <= 4; c *= 2) {
-    if (n_tiles < c) break;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)c, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)c;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int active = 0;
-    if (cudaOccupancyMaxActiveClusters(&active, wkv_gemm_kernel, &cfg) != cudaSuccess || active <= 0) {
-      cudaGetLastError();
-      break;
-    }
-    const int64_t clusters = m_tiles * ((n_tiles + c - 1) / c);
-    if (clusters <= active) best = c;          // one wave of clusters
-    else if (c == 2) best = 2;                 // several waves: pairs still halve A's L2 reads
+// Data-parallel by default; stream-K (256-wide tiles) when asked for, the data-parallel schedule
+// would leave SMs idle, and the caller's workspace holds the partials.
+bool plan_gemm(int64_t M, int K, int N, int sms, size_t ws_bytes, Plan& P) {
+  GemmArgs& a = P.a;
+  a = GemmArgs{};
+  a.M = (int32_t)M;
+  a.K = K;
+  a.N = N;
+  a.msub = M > 128 ? 2 : 1;
+  a.m_tiles = (int32_t)((M + 128 * a.msub - 1) / (128 * a.msub));
+  a.num_kb = (K + kBK - 1) / kBK;
+  a.group_m = 16;
+  const int bn_sk = N >= 256 ? 256 : ((N + 15) / 16) * 16;
+  const int64_t tiles_sk = (int64_t)a.m_tiles * ((N + bn_sk - 1) / bn_sk);
+  const size_t sk_ws = sk_workspace(sms, a.msub, bn_sk);
+  // stream-K is opt-in (engram_set_gemm_schedule(2)): measured slower than data-parallel so far
+  bool sk = g_sched_override == 2 && a.num_kb >= 2 && tiles_sk < 2 * (int64_t)sms;
+  if (g_bn_override > 0 && g_bn_override != bn_sk) sk = false;
+  if (sk && ws_bytes < sk_ws) sk = false;       // no room for partials: data-parallel
+  a.stream_k = sk ? 1 : 0;
+  a.BN = sk ? bn_sk : (g_bn_override > 0 ? g_bn_override : pick_bn_dp(a.m_tiles, N, sms));
+  a.n_tiles = (N + a.BN - 1) / a.BN;
+  const int64_t n_tiles_total = (int64_t)a.m_tiles * a.n_tiles;
+  if (n_tiles_total > 0x7fffffff) return false;
+  a.total_units = n_tiles_total * a.num_kb;
+  if (sk) {
+    P.grid = a.total_units < sms ? (int)a.total_units : sms;
+  } else {
+    P.grid = n_tiles_total < sms ? (int)n_tiles_total : sms;
   }
-  return best;
+  a.stage_bytes = a.msub * kATileBytes + a.BN * kBK * 2;
+  a.stages = (kSmemBudget - 1024 - kEpiBytes - (int)sizeof(Ctl)) / a.stage_bytes;
+  if (a.stages > kMaxStages) a.stages = kMaxStages;
+  if (a.stages < 2) return false;
+  a.acc_stride = pow2_at_least((uint32_t)a.BN);
+  a.tmem_cols = a.acc_stride * 2;              // two accumulators (chains) per item
+  if (a.tmem_cols > 512) return false;
+  a.idesc = (1u << 4)                          // accumulate in f32
+            | (1u << 7) | (1u << 10)           // A and B are bf16
+            | ((uint32_t)(a.BN >> 3) << 17)    // N
+            | ((uint32_t)(128 >> 4) << 24);    // M = 128; A and B K-major (bits 15, 16 = 0)
+  P.smem = 1024 + a.stages * a.stage_bytes + kEpiBytes + (int)sizeof(Ctl);
+  P.ws_needed = sk ? sk_ws : 0;
+  return true;
 }
 
 }  // namespace
 
 void set_gemm_bn_override(int bn) { g_bn_override = bn; }
-void set_gemm_cluster_override(int c) { g_cluster_override = c; }
+void set_gemm_schedule_override(int s) { g_sched_override = s; }
+
+// Workspace that lets the projection of this shape use the stream-K schedule (0 if it never would)
+size_t gemm_workspace_bytes(int64_t M, int K, int N) {
+  Plan P;
+  const int saved = g_sched_override;
+  g_sched_override = 2;
+  const bool ok = plan_gemm(M, K, N, num_sms(), (size_t)-1, P);
+  g_sched_override = saved;
+  return ok ? P.ws_needed : 0;
+}
 
 int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl) {
-  const int sms = num_sms();
-  GemmArgs a{};
-  a.M = (int32_t)p.M;
-  a.K = p.K;
-  a.N = p.N;
-  a.msub = p.M > 128 ? 2 : 1;
-  a.m_tiles = (int32_t)((p.M + 128 * a.msub - 1) / (128 * a.msub));
-  a.BN = pick_bn(a.m_tiles, p.N, sms);
-  const int n_tiles = (p.N + a.BN - 1) / a.BN;
-  a.group_m = 16;
-  a.num_kb = (p.K + kBK - 1) / kBK;
-  a.stage_bytes = a.msub * kATileBytes + a.BN * kBK * 2;
-  const int ctl_bytes = (int)sizeof(Ctl);
-  a.stages = (kSmemBudget - 1024 - ctl_bytes) / a.stage_bytes;
-  if (a.stages > kMaxStages) a.stages = kMaxStages;
-  if (a.stages < 2) {
-    set_error("engram_project: tile of %d columns does not fit shared memory", a.BN);
+  Plan P;
+  if (!plan_gemm(p.M, p.K, p.N, num_sms(), p.workspace != nullptr ? p.ws_bytes : 0, P)) {
+    set_error("engram_project: no tile plan fits (T %lld, K %d, N %d)", (long long)p.M, p.K, p.N);
     return ENGRAM_EINVAL;
   }
-  a.acc_stride = pow2_at_least((uint32_t)a.BN);
-  a.tmem_cols = a.acc_stride * a.msub;
-  a.idesc = (1u << 4)                         // accumulate in f32
-            | (1u << 7) | (1u << 10)          // A and B are bf16
-            | ((uint32_t)(a.BN >> 3) << 17)   // N
-            | ((uint32_t)(128 >> 4) << 24);   // M = 128; A and B K-major (bits 15, 16 = 0)
+  GemmArgs a = P.a;
   a.err = p.err;
-  const int smem = 1024 + a.stages * a.stage_bytes + ctl_bytes;
-
+  if (a.stream_k) {
+    uint8_t* ws = static_cast<uint8_t*>(p.workspace);
+    a.flags = reinterpret_cast<unsigned long long*>(ws);
+    a.partial = reinterpret_cast<float*>(ws + (((size_t)num_sms() * 8 + 255) & ~(size_t)255));
+    a.epoch = g_epoch.fetch_add(1) & 0xffffffffull;
+  }
   static bool configured[64] = {false};     // the attribute is per device
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !configured[dev]) {
     cudaError_t e = cudaFuncSetAttribute(wkv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
     if (e != cudaSuccess) return fail_cuda(e, "engram_project: cudaFuncSetAttribute");
-    e = cudaFuncSetAttribute(wkv_gemm_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return fail_cuda(e, "engram_project: cudaFuncSetAttribute (cluster)");
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  a.cluster = pick_cluster(n_tiles, a.m_tiles, smem);
-  a.n_tiles = ((n_tiles + a.cluster - 1) / a.cluster) * a.cluster;   // padded tiles store nothing
-
   CUtensorMap mA, mB;
-  if (!make_map(&mA, p.A, p.M, p.K, (uint32_t)(128 / a.cluster)) || !make_map(&mB, p.B, p.N, p.K, (uint32_t)a.BN)) {
+  if (!make_map(&mA, p.A, p.M, p.K, 128) || !make_map(&mB, p.B, p.N, p.K, (uint32_t)a.BN)) {
     set_error("engram_project: cuTensorMapEncodeTiled failed (driver entry point missing or bad layout)");
     return ENGRAM_ECUDA;
   }
-  const int64_t grid = (int64_t)a.m_tiles * a.n_tiles;
-  if (grid > 0x7fffffff) {
-    set_error("engram_project: too many tiles");
-    return ENGRAM_EINVAL;
-  }
-  cudaError_t e = launch(mA, mB, p.D, a, grid, smem, stream, pdl);
+  cudaError_t e = launch_k(wkv_gemm_kernel, dim3((unsigned)P.grid), dim3(kThreads), (size_t)P.smem, stream, pdl, mA,
+                           mB, p.D, a);
   if (e != cudaSuccess) return fail_cuda(e, "engram_project: launch");
   return ENGRAM_OK;
 }

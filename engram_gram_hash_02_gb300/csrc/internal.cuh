@@ -93,9 +93,12 @@ struct GemmParams {
   int64_t M;
   int32_t K, N;
   int32_t* err;
+  void* workspace;      // stream-K partials and flags (may be NULL)
+  size_t ws_bytes;
 };
 // returns ENGRAM_OK or an error code (sets the message)
 int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl = false);
+size_t gemm_workspace_bytes(int64_t M, int K, int N);
 
 struct GateParams {
   float* streams;

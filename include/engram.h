@@ -147,20 +147,30 @@ int engram_gather_dequant(int32_t fmt, const int32_t* ids, int64_t ids_stride_t,
  *   A    device bf16 [T, K] row-major       wkv device bf16 [N, K] row-major (nn.Linear layout)
  *   kv   device fp32 [T, N] row-major; columns [j*H, (j+1)*H) are stream j's key, [hc*H, N)
  *        the shared value
- * K % 8 == 0, N % 16 == 0, all three 16-byte aligned. workspace/ws_bytes are unused (pass
- * NULL/0). ENGRAM_ERR_PIPE_TIMEOUT in err_flag means the result is invalid; while that bit is
- * set in the word passed, later calls with the same word skip the work.
+ * K % 8 == 0, N % 16 == 0, all three 16-byte aligned.
+ *   workspace  device, 256-byte aligned, or NULL. Used only by the stream-K schedule (opt-in,
+ *              engram_set_gemm_schedule(2)): with at least engram_project_workspace_bytes(T, K, N)
+ *              bytes, shapes with fewer 256-wide tiles than twice the SM count split the
+ *              k-blocks of all tiles evenly over the SMs and combine cut tiles from fp32 partials
+ *              kept here (in a fixed order, so results are deterministic). Otherwise each CTA runs
+ *              whole tiles. Nothing in it needs to start at zero.
+ * ENGRAM_ERR_PIPE_TIMEOUT in err_flag means the result is invalid; while that bit is set in the
+ * word passed, later calls with the same word skip the work.
  */
 int engram_project(const uint16_t* A, const uint16_t* wkv, float* kv, int64_t T, int32_t K,
                    int32_t N, void* workspace, size_t ws_bytes, int32_t* err_flag,
                    engram_stream_t stream);
 
+/* Workspace bytes that let engram_project run the stream-K schedule for this shape on the current
+ * device (0: the shape always runs the data-parallel schedule, or bad sizes). */
+size_t engram_project_workspace_bytes(int64_t T, int32_t K, int32_t N);
+
 /* Tuning knob for engram_project: force the tile width (columns per CTA, a multiple of 16 in
  * [16, 256]); 0 restores the automatic choice. Process-wide; not thread-safe against calls. */
 void engram_set_gemm_tile(int32_t bn);
-/* Tuning knob for engram_project: CTAs per cluster that share (multicast) each A tile, 1, 2 or 4;
- * 0 restores the automatic choice. Process-wide. */
-void engram_set_gemm_cluster(int32_t c);
+/* Tuning knob for engram_project: 1 forces the data-parallel tile schedule, 2 the stream-K
+ * schedule (when the workspace allows), 0 restores the automatic choice. Process-wide. */
+void engram_set_gemm_schedule(int32_t s);
 
 /*
  * Stage 4: gate, in place on the fp32 highway ([NeMo] _engram_gate_core; [vLLM]
@@ -209,15 +219,18 @@ typedef struct EngramTokens {
   const int32_t* lookback_ids;
 } EngramTokens;
 
-/* Bytes of device workspace engram_forward needs for T tokens (256-byte aligned pieces:
- * hash ids [T, layers, C] int32, rows [T, C*head_dim] bf16, kv [T, (hc+1)*H] fp32). */
+/* Minimum bytes of device workspace engram_forward needs for T tokens (256-byte aligned pieces:
+ * hash ids [T, layers, C] int32, rows [T, C*head_dim] bf16, kv [T, (hc+1)*H] fp32). Workspace
+ * beyond the minimum is handed to the projection: add engram_project_workspace_bytes(T,
+ * C*head_dim, (hc+1)*H) for its stream-K schedule. */
 size_t engram_forward_workspace_bytes(const EngramDims* dims, int64_t T);
 
 /*
  * The whole path: one hash launch for all layers, then per layer gather -> project -> gate.
  *   layers     host array [dims->layers] of per-layer weights
  *   streams    host array [dims->layers] of device fp32 [T, hc, H] highways, updated in place
- *   workspace  device, >= engram_forward_workspace_bytes(dims, T), 256-byte aligned
+ *   workspace  device, >= engram_forward_workspace_bytes(dims, T), 256-byte aligned (see there
+ *              for the optional extra that speeds up the projection)
  *   out_ids    device int32 [T, layers, C] or NULL: if given, the hash writes the ids there
  *              (and the workspace's id region goes unused)
  * Launches 1 + 3*layers kernels on `stream`.

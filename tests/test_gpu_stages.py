@@ -161,25 +161,58 @@ def test_project_vs_fp64(T, K, N):
     assert torch.allclose(kv, tm, rtol=1e-4, atol=1e-4 * float(tm.pow(2).mean().sqrt()))
 
 
-@pytest.mark.parametrize("bn,cluster", [(16, 1), (48, 2), (128, 4), (144, 2), (144, 4), (256, 1), (256, 2),
-                                        (96, 4)])
-def test_project_tile_widths_and_clusters(bn, cluster):
-    # N = 1440 gives 10, 30, 12, 10, 6 or 15 column tiles: clusters of 2 and 4 pad the last group
-    T, K, N = 260, 640, 1440
-    g = torch.Generator(device=DEV).manual_seed(bn * 10 + cluster)
+@pytest.mark.parametrize("bn", [16, 48, 128, 144, 256, 96])
+@pytest.mark.parametrize("T", [260, 100])
+def test_project_tile_widths_data_parallel(bn, T):
+    # N = 1440 is 90, 30, 12, 10, 6 or 15 column tiles; T 260 is two 256-row blocks, T 100 one
+    # 128-row block split into even / odd k-step chains
+    K, N = 640, 1440
+    g = torch.Generator(device=DEV).manual_seed(bn * 10 + T)
     A = (torch.randn(T, K, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
     W = (torch.randn(N, K, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     try:
         E().set_gemm_tile(bn)
-        E().set_gemm_cluster(cluster)
+        E().set_gemm_schedule(1)
         kv = E().engram_project(A, W, err=err)
         torch.cuda.synchronize()
     finally:
         E().set_gemm_tile(0)
-        E().set_gemm_cluster(0)
+        E().set_gemm_schedule(0)
     assert int(err.item()) == 0
-    H.check_kv(kv.cpu().numpy(), O.project(H.bits16(A), H.bits16(W)), f"bn={bn} cluster={cluster}")
+    H.check_kv(kv.cpu().numpy(), O.project(H.bits16(A), H.bits16(W)), f"bn={bn} T={T}")
+
+
+@pytest.mark.parametrize("T,K,N", [
+    (64, 512, 1280),       # 5 tiles x 8 k-blocks over 40 CTAs: every tile cut 8 ways
+    (256, 1024, 4096),     # 16 tiles x 16 k-blocks: tiles cut across ~10 CTAs
+    (300, 6144, 1296),     # 2 row blocks (ragged), ragged last column tile
+    (1, 6144, 2560),
+    (256, 6144, 20480),    # the decode projection
+])
+def test_project_stream_k_matches_fp64_and_is_deterministic(T, K, N):
+    g = torch.Generator(device=DEV).manual_seed(T + K + N)
+    A = (torch.randn(T, K, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    W = (torch.randn(N, K, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    nbytes = E().project_workspace_bytes(T, K, N)
+    assert nbytes > 0, "this shape should qualify for stream-K"
+    ws = torch.full((nbytes,), 0xAB, dtype=torch.uint8, device=DEV)      # stale contents must not matter
+    try:
+        E().set_gemm_schedule(2)
+        kv1 = E().engram_project(A, W, err=err, workspace=ws)
+        kv2 = E().engram_project(A, W, err=err, workspace=ws)
+        E().set_gemm_schedule(1)
+        kv_dp = E().engram_project(A, W, err=err, workspace=None)
+        torch.cuda.synchronize()
+    finally:
+        E().set_gemm_schedule(0)
+    assert int(err.item()) == 0
+    assert torch.equal(kv1, kv2)                     # fixed summation order
+    rows = np.arange(T) if T <= 300 else np.random.default_rng(0).choice(T, 64, replace=False)
+    ref = O.project(H.bits16(A)[rows], H.bits16(W))
+    H.check_kv(kv1.cpu().numpy()[rows], ref, f"stream-K T={T} K={K} N={N}")
+    H.check_kv(kv_dp.cpu().numpy()[rows], ref, f"data-parallel T={T} K={K} N={N}")
 
 
 def test_project_integer_exact():

@@ -12,7 +12,7 @@
 //   warp 1      allocates tensor memory; one lane issues tcgen05.mma (M=128, N=BN, K=16,
 //               kind::f16) and releases each stage with tcgen05.commit.
 //   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulators (each warp its 32-lane quarter),
-//               transposed through a small shared tile so stores to kv are coalesced rows.
+//               staged as 32 x 32 swizzled shared tiles and written with TMA bulk tensor stores.
 // Every item accumulates into two TMEM accumulators, which the tensor core runs as independent
 // chains (back-to-back MMAs into one accumulator wait on each other): the two 128-row halves of
 // a 256-row tile, or, for tiles of at most 128 rows, the even and odd k steps of one tile
@@ -50,9 +50,9 @@ constexpr int kATileBytes = 128 * kBK * 2;  // 16 KB
 constexpr uint64_t kWaitLimitCycles = 4000000000ull;  // wait bound in SM cycles: ~2 s at 2 GHz
 constexpr int kSmemBudget = 232448;        // 227 KB opt-in maximum per CTA
 constexpr unsigned long long kFlagMagic = 0x5EA5C0DEull;
-constexpr int kEpiChunk = 32;                        // columns staged per warp and step
-constexpr int kEpiStride = kEpiChunk + 4;            // padded row (floats): conflict-free 16-B access
-constexpr int kEpiBytes = 4 * 32 * kEpiStride * 4;   // four epilogue warps x 32 rows
+constexpr int kEpiChunk = 32;                        // columns per warp and step (128 bytes of fp32)
+constexpr int kEpiWarpBytes = 32 * kEpiChunk * 4;    // one 32 x 32 fp32 staging tile (4 KB)
+constexpr int kEpiBytes = 4 * kEpiWarpBytes;         // four epilogue warps
 
 struct Ctl {
   uint64_t full[kMaxStages];
@@ -243,6 +243,7 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
 
 __global__ void __launch_bounds__(kThreads, 1)
 wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmP,
                 float* __restrict__ D, const GemmArgs a) {
   // A timeout anywhere in an earlier launch sharing the flag word voids the result: skip the
   // work instead of waiting out the time limits again.
@@ -253,7 +254,7 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t tiles = (raw_base + 1023u) & ~1023u;          // swizzled tiles need 1 KB alignment
-  float* epi_stage = reinterpret_cast<float*>(smem_raw + (tiles - raw_base) + a.stages * a.stage_bytes);
+  const uint32_t epi_stage = tiles + (uint32_t)(a.stages * a.stage_bytes);   // 1 KB aligned
   Ctl* ctl = reinterpret_cast<Ctl*>(smem_raw + (tiles - raw_base) + a.stages * a.stage_bytes + kEpiBytes);
   volatile int32_t* abort_flag = &ctl->abort_flag;
   const int warp = threadIdx.x >> 5;
@@ -273,6 +274,8 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    prefetch_tmap(&tmD);
+    if (a.stream_k) prefetch_tmap(&tmP);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -406,11 +409,11 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     int n_items = 0;
     const int rows_per_item = 128 * a.msub;
     // Each warp owns 32 rows (its TMEM lane quarter) of each 128-row half. Per 32-column chunk,
-    // tcgen05.ld gives every thread 32 columns of its row; the chunk is transposed through a
-    // padded shared tile so that 8 lanes write (or read) 128 contiguous bytes of one row.
-    float* stg = epi_stage + q * 32 * kEpiStride;
-    const int sr = lane >> 3;                  // row offset within a group of 4
-    const int sc = (lane & 7) * 4;             // column of this lane's float4
+    // tcgen05.ld gives every thread 32 columns of its row; the thread writes them into the warp's
+    // 32 x 128-byte staging tile in the 128B-swizzled order (16-byte piece i of row r at piece
+    // i ^ (r % 8): conflict-free), and one lane stores the tile with a TMA bulk tensor store. A
+    // 16-column tail (tile widths that are odd multiples of 16) is stored by the threads.
+    const uint32_t stg = epi_stage + (uint32_t)(q * kEpiWarpBytes);
     while (sch.next(item)) {
       const bool ok = mbar_wait(smem_u32(&ctl->acc_full), (uint32_t)(n_items & 1), abort_flag, a.err,
                                 kWaitLimitCycles);
@@ -444,6 +447,7 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       for (int ms = 0; ms < a.msub; ++ms) {
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ms * a.acc_stride);
         const int row0 = ms * 128 + q * 32;    // first row of this warp (within the item)
+        const int lrow = row0 + lane;          // this thread's row (within the item)
         for (int c0 = 0; c0 < a.BN; c0 += kEpiChunk) {
           const bool two = c0 + 16 < a.BN;     // BN is a multiple of 16
           uint32_t r[32];
@@ -459,39 +463,68 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           } else {
             tmem_ld_wait();
           }
-          const int ncol = two ? 32 : 16;
-          float4* my = reinterpret_cast<float4*>(stg + lane * kEpiStride);
+          const int npc = two ? 8 : 4;         // 16-byte pieces in this chunk
+          if (owner) {
+            // add the contributors' partials in CTA order (deterministic); loads batched per CTA
+            for (int j = j_first; j <= j_last; ++j) {
+              const float4* src = reinterpret_cast<const float4*>(
+                  a.partial + ((int64_t)j * rows_per_item + lrow) * a.BN + c0);
+              float4 pv[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if (i * 4 < ncol)
-              my[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                  __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
-          __syncwarp();
-          if (sc < ncol) {
+              for (int i = 0; i < 8; ++i) pv[i] = i < npc ? __ldcg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
-              const int wr = g * 4 + sr;       // row within the warp's 32
-              const int lrow = row0 + wr;      // row within the item
-              float4 v = *reinterpret_cast<const float4*>(stg + wr * kEpiStride + sc);
-              if (contributor) {
-                *reinterpret_cast<float4*>(a.partial + ((int64_t)blockIdx.x * rows_per_item + lrow) * a.BN + c0 + sc) = v;
-                continue;
+              for (int i = 0; i < 8; ++i) {
+                r[4 * i] = __float_as_uint(__uint_as_float(r[4 * i]) + pv[i].x);
+                r[4 * i + 1] = __float_as_uint(__uint_as_float(r[4 * i + 1]) + pv[i].y);
+                r[4 * i + 2] = __float_as_uint(__uint_as_float(r[4 * i + 2]) + pv[i].z);
+                r[4 * i + 3] = __float_as_uint(__uint_as_float(r[4 * i + 3]) + pv[i].w);
               }
-              if (owner) {
-                for (int j = j_first; j <= j_last; ++j) {   // fixed order: deterministic sums
-                  const float4 pv = __ldcg(reinterpret_cast<const float4*>(
-                      a.partial + ((int64_t)j * rows_per_item + lrow) * a.BN + c0 + sc));
-                  v.x += pv.x; v.y += pv.y; v.z += pv.z; v.w += pv.w;
-                }
-              }
-              const int64_t row = (int64_t)m0 + lrow;
-              const int col = n0 + c0 + sc;
-              if (row < a.M && col < a.N) *reinterpret_cast<float4*>(D + row * (int64_t)a.N + col) = v;
             }
           }
+          if (!two) {
+            // 16-column tail: plain stores of this thread's row
+            float* dst = contributor ? a.partial + ((int64_t)blockIdx.x * rows_per_item + lrow) * a.BN + c0
+                                     : D + ((int64_t)m0 + lrow) * a.N + n0 + c0;
+            const bool ok_row = contributor || ((int64_t)m0 + lrow < a.M && n0 + c0 < a.N);
+            if (ok_row) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                reinterpret_cast<float4*>(dst)[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                                                __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+            }
+            continue;
+          }
+          // the previous TMA store from this staging tile has read it
+          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
           __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t addr = stg + (uint32_t)(lane * 128 + ((i ^ (lane & 7)) * 16));
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r[4 * i]), "r"(r[4 * i + 1]),
+                         "r"(r[4 * i + 2]), "r"(r[4 * i + 3])
+                         : "memory");
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the TMA unit
+          __syncwarp();
+          if (lane == 0) {
+            const CUtensorMap* map = contributor ? &tmP : &tmD;
+            const int x = contributor ? c0 : n0 + c0;
+            const int y = contributor ? (int)blockIdx.x * rows_per_item + row0 : m0 + row0;
+            asm volatile(
+                "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                    reinterpret_cast<uint64_t>(map)),
+                "r"(x), "r"(y), "r"(stg)
+                : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          }
         }
       }
+      // this item's stores are complete (global writes done) before the tile or flag moves on
+      if (lane == 0) {
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+      __syncwarp();
       if (contributor) {
         // publish the partial: every epilogue thread's stores before the flag
         __threadfence();
@@ -539,6 +572,20 @@ EncodeTiledFn encode_fn() {
       fn = reinterpret_cast<EncodeTiledFn>(p);
   });
   return fn;
+}
+
+// 2-D fp32 map over a row-major [rows, cols] matrix; box = 32 x 32 with the 128B swizzle (the
+// epilogue's staging tiles)
+bool make_map_f32(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+  cuuint32_t box[2] = {(cuuint32_t)kEpiChunk, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 2-D bf16 map over a row-major [rows, K] matrix; box = 64 k x box_rows rows, 128B swizzle
@@ -674,13 +721,17 @@ int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl) {
     if (e != cudaSuccess) return fail_cuda(e, "engram_project: cudaFuncSetAttribute");
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  CUtensorMap mA, mB;
-  if (!make_map(&mA, p.A, p.M, p.K, 128) || !make_map(&mB, p.B, p.N, p.K, (uint32_t)a.BN)) {
+  CUtensorMap mA, mB, mD, mP;
+  bool maps_ok = make_map(&mA, p.A, p.M, p.K, 128) && make_map(&mB, p.B, p.N, p.K, (uint32_t)a.BN) &&
+                 make_map_f32(&mD, p.D, p.M, p.N);
+  if (a.stream_k) maps_ok = maps_ok && make_map_f32(&mP, a.partial, (int64_t)P.grid * 128 * a.msub, a.BN);
+  else mP = mD;
+  if (!maps_ok) {
     set_error("engram_project: cuTensorMapEncodeTiled failed (driver entry point missing or bad layout)");
     return ENGRAM_ECUDA;
   }
   cudaError_t e = launch_k(wkv_gemm_kernel, dim3((unsigned)P.grid), dim3(kThreads), (size_t)P.smem, stream, pdl, mA,
-                           mB, p.D, a);
+                           mB, mD, mP, p.D, a);
   if (e != cudaSuccess) return fail_cuda(e, "engram_project: launch");
   return ENGRAM_OK;
 }

@@ -22,11 +22,13 @@
 //   data-parallel  CTA c takes tiles c, c + grid, ... over the whole K (many tiles);
 //   stream-K       the tiles x k-blocks are split evenly over all CTAs, so a shape with fewer
 //                  tiles than SMs (the decode step: 80 tiles of 256 x 256) still keeps every SM
-//                  streaming wkv. A tile cut between CTAs is finished by the CTA holding its last
-//                  k-block (the owner): the others write fp32 partials to the caller's workspace
-//                  and publish an epoch-tagged flag; the owner adds them in CTA order
-//                  (deterministic). Each CTA runs its segments last-first, so partials are
-//                  produced early and consumed late. All CTAs are co-resident (grid <= SMs).
+//                  streaming wkv. A tile cut between CTAs is summed into kv in unit order: the
+//                  CTA holding its first segment stores it (TMA store) and publishes an
+//                  epoch-tagged flag in the caller's workspace; the CTA holding the next segment
+//                  waits for that flag and adds its part with a TMA bulk reduce-add, and so on
+//                  (fixed order: deterministic). Each CTA runs its segments last-first, so the
+//                  segment others wait for is done early. All CTAs are co-resident (grid <= SMs)
+//                  and wait only on lower-numbered CTAs.
 //
 // Every wait (mbarrier or flag) is bounded (~2 s of SM clock cycles); on expiry the CTA raises
 // an abort flag, reports ENGRAM_ERR_PIPE_TIMEOUT, drains its in-flight copies and MMAs (again
@@ -72,7 +74,6 @@ struct GemmArgs {
   uint32_t tmem_cols, acc_stride;
   int32_t stream_k;                        // 0: data-parallel tiles, 1: stream-K
   int64_t total_units;                     // tiles * num_kb
-  float* partial;                          // [grid][msub*128][BN] fp32 (stream-K)
   unsigned long long* flags;               // [grid] (stream-K)
   unsigned long long epoch;
   int32_t* err;
@@ -114,12 +115,6 @@ struct Schedule {
     it.k1 = (int)(cursor - tile_start);
     cursor = seg_start;
     return true;
-  }
-  // CTA whose unit range holds unit u
-  __device__ int owner_of(int64_t u) const {
-    const int64_t base = a.total_units / grid, rem = a.total_units % grid;
-    const int64_t big = rem * (base + 1);
-    return u < big ? (int)(u / (base + 1)) : (int)(rem + (u - big) / base);
   }
 };
 
@@ -243,7 +238,7 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
 
 __global__ void __launch_bounds__(kThreads, 1)
 wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmP,
+                const __grid_constant__ CUtensorMap tmD,
                 float* __restrict__ D, const GemmArgs a) {
   // A timeout anywhere in an earlier launch sharing the flag word voids the result: skip the
   // work instead of waiting out the time limits again.
@@ -275,7 +270,6 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmD);
-    if (a.stream_k) prefetch_tmap(&tmP);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -400,14 +394,13 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       if (!ok) tc_commit(smem_u32(&ctl->acc_full));
     }
   } else {
-    // ---------------- epilogue: TMEM -> registers -> shared tile -> fp32 kv / partials --------
+    // ---------------- epilogue: TMEM -> registers -> shared tile -> fp32 kv --------------------
     const int q = warp & 3;                    // TMEM lane quarter this warp may access
     const int et = threadIdx.x - 64;           // 0..127
     pdl_wait();                                // kv may still be read by an earlier kernel
     Schedule sch(a, blockIdx.x, gridDim.x);
     Item item;
     int n_items = 0;
-    const int rows_per_item = 128 * a.msub;
     // Each warp owns 32 rows (its TMEM lane quarter) of each 128-row half. Per 32-column chunk,
     // tcgen05.ld gives every thread 32 columns of its row; the thread writes them into the warp's
     // 32 x 128-byte staging tile in the 128B-swizzled order (16-byte piece i of row r at piece
@@ -421,28 +414,24 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       if (!ok || *abort_flag) break;
       int m0, n0;
       tile_origin(a, item.tile, m0, n0);
-      const bool whole = item.k0 == 0 && item.k1 == a.num_kb;
-      const bool owner = !whole && item.k1 == a.num_kb;
-      const bool contributor = !whole && !owner;
-      // contributors to this tile (owner only): the CTAs holding its units [0, k0)
-      int j_first = blockIdx.x, j_last = blockIdx.x - 1;
-      if (owner) {
-        j_first = sch.owner_of((int64_t)item.tile * a.num_kb);
-        j_last = blockIdx.x - 1;
-        bool flags_ok = true;
-        const unsigned long long want = (a.epoch << 32) | kFlagMagic;
-        for (int j = j_first; j <= j_last && flags_ok; ++j) {
-          const uint64_t t0 = clock64();
-          while (ld_acquire(a.flags + j) != want) {
-            if (*abort_flag || (uint64_t)clock64() - t0 > kWaitLimitCycles) {
-              *abort_flag = 1;
-              if (a.err != nullptr) atomicOr(a.err, ENGRAM_ERR_PIPE_TIMEOUT);
-              flags_ok = false;
-              break;
-            }
+      // A tile cut between CTAs is summed into kv in unit order: the CTA holding its first
+      // segment stores it, each later segment waits for the CTA just before it (which holds the
+      // previous segment) and adds into kv. Fixed order, so results are deterministic.
+      const bool adder = item.k0 > 0;                        // later segment: reduce-add into kv
+      const bool publish = item.k1 < a.num_kb;               // a later segment follows: signal it
+      const unsigned long long want = (a.epoch << 32) | kFlagMagic;
+      if (adder) {
+        const uint64_t t0 = clock64();
+        while (ld_acquire(a.flags + blockIdx.x - 1) != want) {     // every lane acquires
+          if (*abort_flag || (uint64_t)clock64() - t0 > kWaitLimitCycles) {
+            *abort_flag = 1;
+            if (a.err != nullptr) atomicOr(a.err, ENGRAM_ERR_PIPE_TIMEOUT);
+            break;
           }
         }
-        if (!flags_ok) break;
+        asm volatile("fence.proxy.async.global;" ::: "memory");   // order before our TMA adds
+        __syncwarp();
+        if (*abort_flag) break;
       }
       for (int ms = 0; ms < a.msub; ++ms) {
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ms * a.acc_stride);
@@ -464,33 +453,19 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             tmem_ld_wait();
           }
           const int npc = two ? 8 : 4;         // 16-byte pieces in this chunk
-          if (owner) {
-            // add the contributors' partials in CTA order (deterministic); loads batched per CTA
-            for (int j = j_first; j <= j_last; ++j) {
-              const float4* src = reinterpret_cast<const float4*>(
-                  a.partial + ((int64_t)j * rows_per_item + lrow) * a.BN + c0);
-              float4 pv[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) pv[i] = i < npc ? __ldcg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                r[4 * i] = __float_as_uint(__uint_as_float(r[4 * i]) + pv[i].x);
-                r[4 * i + 1] = __float_as_uint(__uint_as_float(r[4 * i + 1]) + pv[i].y);
-                r[4 * i + 2] = __float_as_uint(__uint_as_float(r[4 * i + 2]) + pv[i].z);
-                r[4 * i + 3] = __float_as_uint(__uint_as_float(r[4 * i + 3]) + pv[i].w);
-              }
-            }
-          }
           if (!two) {
-            // 16-column tail: plain stores of this thread's row
-            float* dst = contributor ? a.partial + ((int64_t)blockIdx.x * rows_per_item + lrow) * a.BN + c0
-                                     : D + ((int64_t)m0 + lrow) * a.N + n0 + c0;
-            const bool ok_row = contributor || ((int64_t)m0 + lrow < a.M && n0 + c0 < a.N);
-            if (ok_row) {
+            // 16-column tail: this thread's row by plain stores (or atomic adds)
+            float* dst = D + ((int64_t)m0 + lrow) * a.N + n0 + c0;
+            if ((int64_t)m0 + lrow < a.M && n0 + c0 < a.N) {
+              if (adder) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                reinterpret_cast<float4*>(dst)[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                                                __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                for (int i = 0; i < 16; ++i) atomicAdd(dst + i, __uint_as_float(r[i]));
+              } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  reinterpret_cast<float4*>(dst)[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                                                  __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+              }
             }
             continue;
           }
@@ -507,14 +482,17 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the TMA unit
           __syncwarp();
           if (lane == 0) {
-            const CUtensorMap* map = contributor ? &tmP : &tmD;
-            const int x = contributor ? c0 : n0 + c0;
-            const int y = contributor ? (int)blockIdx.x * rows_per_item + row0 : m0 + row0;
-            asm volatile(
-                "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                    reinterpret_cast<uint64_t>(map)),
-                "r"(x), "r"(y), "r"(stg)
-                : "memory");
+            const uint64_t map = reinterpret_cast<uint64_t>(&tmD);
+            if (adder)
+              asm volatile(
+                  "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map),
+                  "r"(n0 + c0), "r"(m0 + row0), "r"(stg)
+                  : "memory");
+            else
+              asm volatile(
+                  "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map),
+                  "r"(n0 + c0), "r"(m0 + row0), "r"(stg)
+                  : "memory");
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
           }
         }
@@ -525,11 +503,11 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         asm volatile("fence.proxy.async.global;" ::: "memory");
       }
       __syncwarp();
-      if (contributor) {
-        // publish the partial: every epilogue thread's stores before the flag
+      if (publish) {
+        // this segment is in kv (every warp's stores complete): let the next segment's CTA add
         __threadfence();
         epi_bar();
-        if (et == 0) st_release(a.flags + blockIdx.x, (a.epoch << 32) | kFlagMagic);
+        if (et == 0) st_release(a.flags + blockIdx.x, want);
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&ctl->acc_empty));  // tensor memory may take the next item
@@ -634,12 +612,10 @@ struct Plan {
   size_t ws_needed;   // workspace of the stream-K schedule (0 when data-parallel)
 };
 
-size_t sk_workspace(int sms, int msub, int bn) {
-  return (((size_t)sms * 8 + 255) & ~(size_t)255) + (size_t)sms * (size_t)(128 * msub) * (size_t)bn * 4;
-}
+size_t sk_workspace(int sms) { return ((size_t)sms * 8 + 255) & ~(size_t)255; }   // one flag per CTA
 
 // Data-parallel by default; stream-K (256-wide tiles) when asked for, the data-parallel schedule
-// would leave SMs idle, and the caller's workspace holds the partials.
+// would leave SMs idle, and the caller's workspace holds the flags.
 bool plan_gemm(int64_t M, int K, int N, int sms, size_t ws_bytes, Plan& P) {
   GemmArgs& a = P.a;
   a = GemmArgs{};
@@ -652,11 +628,11 @@ bool plan_gemm(int64_t M, int K, int N, int sms, size_t ws_bytes, Plan& P) {
   a.group_m = 16;
   const int bn_sk = N >= 256 ? 256 : ((N + 15) / 16) * 16;
   const int64_t tiles_sk = (int64_t)a.m_tiles * ((N + bn_sk - 1) / bn_sk);
-  const size_t sk_ws = sk_workspace(sms, a.msub, bn_sk);
+  const size_t sk_ws = sk_workspace(sms);
   // stream-K is opt-in (engram_set_gemm_schedule(2)): measured slower than data-parallel so far
   bool sk = g_sched_override == 2 && a.num_kb >= 2 && tiles_sk < 2 * (int64_t)sms;
   if (g_bn_override > 0 && g_bn_override != bn_sk) sk = false;
-  if (sk && ws_bytes < sk_ws) sk = false;       // no room for partials: data-parallel
+  if (sk && ws_bytes < sk_ws) sk = false;       // no room for the flags: data-parallel
   a.stream_k = sk ? 1 : 0;
   a.BN = sk ? bn_sk : (g_bn_override > 0 ? g_bn_override : pick_bn_dp(a.m_tiles, N, sms));
   a.n_tiles = (N + a.BN - 1) / a.BN;
@@ -710,7 +686,6 @@ int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl) {
   if (a.stream_k) {
     uint8_t* ws = static_cast<uint8_t*>(p.workspace);
     a.flags = reinterpret_cast<unsigned long long*>(ws);
-    a.partial = reinterpret_cast<float*>(ws + (((size_t)num_sms() * 8 + 255) & ~(size_t)255));
     a.epoch = g_epoch.fetch_add(1) & 0xffffffffull;
   }
   static bool configured[64] = {false};     // the attribute is per device
@@ -721,17 +696,14 @@ int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl) {
     if (e != cudaSuccess) return fail_cuda(e, "engram_project: cudaFuncSetAttribute");
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  CUtensorMap mA, mB, mD, mP;
-  bool maps_ok = make_map(&mA, p.A, p.M, p.K, 128) && make_map(&mB, p.B, p.N, p.K, (uint32_t)a.BN) &&
-                 make_map_f32(&mD, p.D, p.M, p.N);
-  if (a.stream_k) maps_ok = maps_ok && make_map_f32(&mP, a.partial, (int64_t)P.grid * 128 * a.msub, a.BN);
-  else mP = mD;
-  if (!maps_ok) {
+  CUtensorMap mA, mB, mD;
+  if (!make_map(&mA, p.A, p.M, p.K, 128) || !make_map(&mB, p.B, p.N, p.K, (uint32_t)a.BN) ||
+      !make_map_f32(&mD, p.D, p.M, p.N)) {
     set_error("engram_project: cuTensorMapEncodeTiled failed (driver entry point missing or bad layout)");
     return ENGRAM_ECUDA;
   }
   cudaError_t e = launch_k(wkv_gemm_kernel, dim3((unsigned)P.grid), dim3(kThreads), (size_t)P.smem, stream, pdl, mA,
-                           mB, mD, mP, p.D, a);
+                           mB, mD, p.D, a);
   if (e != cudaSuccess) return fail_cuda(e, "engram_project: launch");
   return ENGRAM_OK;
 }

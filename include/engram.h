@@ -150,10 +150,10 @@ int engram_gather_dequant(int32_t fmt, const int32_t* ids, int64_t ids_stride_t,
  * K % 8 == 0, N % 16 == 0, all three 16-byte aligned.
  *   workspace  device, 256-byte aligned, or NULL. Used only by the stream-K schedule (opt-in,
  *              engram_set_gemm_schedule(2)): with at least engram_project_workspace_bytes(T, K, N)
- *              bytes, shapes with fewer 256-wide tiles than twice the SM count split the
- *              k-blocks of all tiles evenly over the SMs and combine cut tiles from fp32 partials
- *              kept here (in a fixed order, so results are deterministic). Otherwise each CTA runs
- *              whole tiles. Nothing in it needs to start at zero.
+ *              bytes (one flag per SM), shapes with fewer 256-wide tiles than twice the SM count
+ *              split the k-blocks of all tiles evenly over the SMs; a tile cut between CTAs is
+ *              summed into kv segment by segment in a fixed order (deterministic results).
+ *              Otherwise each CTA runs whole tiles. Nothing in it needs to start at zero.
  * ENGRAM_ERR_PIPE_TIMEOUT in err_flag means the result is invalid; while that bit is set in the
  * word passed, later calls with the same word skip the work.
  */

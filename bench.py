@@ -51,6 +51,24 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest of a per-rank number over all ranks: the job takes as long as its slowest
+    replica.  Identity outside torch.distributed."""
+    if not torch.distributed.is_available() or not torch.distributed.is_initialized():
+        return float(x)
+    if torch.distributed.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world: int, units_per_rank: int, ms: float) -> float:
+    """Whole-job units/s when each of `world` replicas processes `units_per_rank` units and the
+    slowest takes `ms` milliseconds."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 def src_sha(name: str) -> str:
     with open(os.path.join(ROOT, "engram_gram_hash_02_gb300", "csrc", name), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -274,20 +292,14 @@ def run_ours(args, rank, world, device):
     per_step_serial = np.array([e[0].elapsed_time(e[-1]) for e in ev])
     per_kernel = {name: float(np.mean([e[i].elapsed_time(e[i + 1]) for e in ev]))
                   for i, (name, _) in enumerate(calls)}
-    ms = float(per_step.mean())
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(float(per_step.mean()), device)
     tokens = w.tokens * w.layers
-    value = world * tokens / (ms / 1e3)
+    value = replica_throughput(world, tokens, ms)
 
     # ---- end to end through the public API with host buffers -------------------------------
     e2e = run_e2e(args, path, stream, device) if not args.no_e2e else None
-    if world > 1 and e2e is not None:
-        t = torch.tensor([e2e["ms"]], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e["ms"] = float(t.item())
+    if e2e is not None:
+        e2e["ms"] = max_over_ranks(e2e["ms"], device)
 
     if rank != 0:
         return None
@@ -309,9 +321,15 @@ def run_ours(args, rank, world, device):
     stages = {}
     for name, t in per_kernel.items():
         m = stage_model(w, name, pk)
-        stages[name] = {"us": round(t * 1e3, 2), "GB/s": round(m["bytes"] / (t / 1e3) / 1e9, 1)}
+        gbs = m["bytes"] / (t / 1e3) / 1e9
+        stages[name] = {"us": round(t * 1e3, 2), "GB/s": round(gbs, 1), "bound": m["bound"]}
         if m["flops"] and name.startswith("project"):
-            stages[name]["TFLOP/s"] = round(m["flops"] / (t / 1e3) / 1e12, 1)
+            tfs = m["flops"] / (t / 1e3) / 1e12
+            stages[name]["TFLOP/s"] = round(tfs, 1)
+            if m["bound"] == "tensor":
+                stages[name]["frac"] = round(tfs / pk["bf16_tflops"], 4)
+        if m["bound"] == "hbm":
+            stages[name]["frac"] = round(gbs / pk["hbm_gbs"], 4)
     line = {
         "metric": "engram_tokens_per_s_per_layer",
         "value": round(value, 1),
@@ -341,7 +359,7 @@ def run_ours(args, rank, world, device):
         "wall_s_timed": round(wall, 4),
     }
     if e2e is not None:
-        line["e2e"] = {"value": round(world * tokens / (e2e["ms"] / 1e3), 1), "unit": "tokens/s per layer",
+        line["e2e"] = {"value": round(replica_throughput(world, tokens, e2e["ms"]), 1), "unit": "tokens/s per layer",
                        "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                        "ms_per_step": round(e2e["ms"], 5)}
     if world == 1 and not args.no_cpu_baseline:
@@ -489,9 +507,9 @@ def run_reference(args, rank, world):
         return None
     w = get_workload(args.workload)
     device = "cuda" if torch.cuda.is_available() else "cpu"
-    import engram_gram_hash_02_gb300 as E
-    primes, offsets, rows = E.engram_layout(w.vocab_size, w.layers, w.max_ngram, w.n_heads)
-    case = make_case(w, rows, device)
+    from oracle import engram_oracle as O
+    _, _, rows = O.layout(w.vocab_size, w.layers, w.max_ngram, w.n_heads)
+    case = make_case(w, [int(r) for r in np.asarray(rows).reshape(-1)], device)
     r = OracleRunner(w, case, args.cpu_tokens)
     for _ in range(args.warmup):
         r.step()

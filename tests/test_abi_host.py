@@ -1,0 +1,107 @@
+"""The C-ABI library on a machine without a GPU: it builds, loads, exports every function the
+header declares, and its host-only parts behave (layout, argument checks that fire before any
+CUDA call).  No kernel is launched here."""
+import ctypes
+import re
+from pathlib import Path
+
+import numpy as np
+import pytest
+
+from oracle import engram_oracle as O
+
+ROOT = Path(__file__).resolve().parents[1]
+HEADER = ROOT / "include" / "engram.h"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from engram_gram_hash_02_gb300 import build as B
+    from engram_gram_hash_02_gb300 import binding
+    B.build()
+    return binding.lib()
+
+
+def declared_functions():
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)          # drop comments
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b(engram_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary_calls():
+    names = declared_functions()
+    for want in ("engram_hash", "engram_gather_dequant", "engram_project", "engram_gate", "engram_forward",
+                 "engram_forward_workspace_bytes", "engram_forward_noalloc", "engram_layout",
+                 "engram_last_error"):
+        assert want in names, want
+
+
+def test_library_exports_every_declared_function(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"declared in engram.h but not exported: {missing}"
+
+
+def test_version_string(lib):
+    v = lib.engram_version().decode()
+    assert "sm_103a" in v
+
+
+def _c_layout(lib, vocab, L, ng, hh):
+    C = (ng - 1) * hh
+    p = np.zeros(L * C, np.int64)
+    o = np.zeros(L * C, np.int64)
+    r = np.zeros(L, np.int64)
+    rc = lib.engram_layout(vocab, L, ng, hh, p.ctypes.data, o.ctypes.data, r.ctypes.data)
+    return rc, p.reshape(L, C), o.reshape(L, C), r
+
+
+@pytest.mark.parametrize("vocab,L,ng,hh", [(4001, 1, 3, 4), (1 << 20, 1, 4, 8), (1 << 19, 2, 4, 8), (97, 3, 5, 2)])
+def test_host_layout_equals_oracle(lib, vocab, L, ng, hh):
+    rc, p, o, r = _c_layout(lib, vocab, L, ng, hh)
+    assert rc == 0
+    op, oo, orows = O.layout(vocab, L, ng, hh)               # oracle: [L, orders, heads]
+    assert np.array_equal(p, np.asarray(op).reshape(L, -1))
+    assert np.array_equal(o, np.asarray(oo).reshape(L, -1))
+    assert np.array_equal(r, np.asarray(orows).reshape(L))
+
+
+def test_host_layout_rejects_bad_arguments(lib):
+    rc, *_ = _c_layout(lib, 0, 1, 3, 4)
+    assert rc == -1
+    assert "engram_layout" in lib.engram_last_error().decode()
+
+
+def test_argument_checks_fire_before_any_cuda_call(lib):
+    from engram_gram_hash_02_gb300 import binding as Bd
+    stream = None
+    # projection: NULL operands
+    rc = lib.engram_project(None, None, None, 4, 64, 64, None, 0, None, stream)
+    assert rc == -1 and "non-NULL" in lib.engram_last_error().decode()
+    # projection: K not a multiple of 8
+    rc = lib.engram_project(None, None, None, 4, 60, 64, None, 0, None, stream)
+    assert rc == -1 and "K must be" in lib.engram_last_error().decode()
+    # gather: unknown table format
+    buf = (ctypes.c_uint8 * 4096)()
+    addr = (ctypes.addressof(buf) + 15) & ~15
+    rc = lib.engram_gather_dequant(7, addr, 8, 1, 8, 64, addr, addr, 10, addr, None, stream)
+    assert rc == -1 and "unknown table format" in lib.engram_last_error().decode()
+    # gate: hidden not a multiple of 8
+    dims = Bd.EngramDims(1, 3, 4, 64, 7, 4, 16, 16, 0, 1e-6, 1e-6)
+    rc = lib.engram_gate(ctypes.byref(dims), addr, addr, addr, addr, None, 1, stream)
+    assert rc == -1 and "hidden" in lib.engram_last_error().decode()
+    # hash: pad id outside the compressed vocabulary
+    dims = Bd.EngramDims(1, 3, 4, 64, 256, 4, 16, 16, 99, 1e-6, 1e-6)
+    rc = lib.engram_hash(ctypes.byref(dims), addr, 1, addr, 1, None, None, None, addr, addr, addr, addr, addr,
+                         None, stream)
+    assert rc == -1 and "pad_id" in lib.engram_last_error().decode()
+
+
+def test_forward_workspace_covers_ids_rows_and_kv(lib):
+    from engram_gram_hash_02_gb300 import binding as Bd
+    dims = Bd.EngramDims(1, 4, 8, 256, 4096, 4, 163840, 131072, 0, 1e-6, 1e-6)
+    T = 256
+    C, K, N = 24, 24 * 256, 4096 * 5
+    need = lib.engram_forward_workspace_bytes(ctypes.byref(dims), T)
+    assert need >= 4 * T * C + 2 * T * K + 4 * T * N
+    assert need % 256 == 0

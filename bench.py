@@ -193,7 +193,7 @@ class Path:
                       p(lw.table), p(lw.scales), int(lw.num_rows), p(self.A), p(self.err), s)
             pr_args = (p(self.A), p(lw.wkv), p(self.kv), T, K, N, p(self.gemm_ws), self.gemm_ws.numel(), p(self.err), s)
             ga_args = (C.byref(dims), p(self.streams[l]), p(self.kv), p(lw.q_weight), p(lw.k_weight),
-                       p(self.mask), T, s)
+                       p(self.mask), T, p(self.err), s)
             calls.append((f"gather{l}", lambda a=g_args: lib.engram_gather_dequant(*a)))
             calls.append((f"project{l}", lambda a=pr_args: lib.engram_project(*a)))
             calls.append((f"gate{l}", lambda a=ga_args: lib.engram_gate(*a)))

@@ -76,7 +76,7 @@ def lib() -> C.CDLL:
         L.engram_hash.argtypes = [P, P, I64, P, I32, P, P, P, P, P, P, P, P, P, P]
         L.engram_gather_dequant.argtypes = [I32, P, I64, I64, I32, I32, P, P, I64, P, P, P]
         L.engram_project.argtypes = [P, P, P, I64, I32, I32, P, SZ, P, P]
-        L.engram_gate.argtypes = [P, P, P, P, P, P, I64, P]
+        L.engram_gate.argtypes = [P, P, P, P, P, P, I64, P, P]
         L.engram_forward_workspace_bytes.argtypes = [P, I64]
         L.engram_forward_workspace_bytes.restype = SZ
         L.engram_forward.argtypes = [P, P, P, P, P, P, SZ, P, P, P]
@@ -231,16 +231,17 @@ def engram_project(A, wkv, out=None, err=None, workspace="auto", stream=None):
     return out
 
 
-def engram_gate(dims: EngramDims, streams, kv, q_weight, k_weight, token_mask=None, stream=None):
+def engram_gate(dims: EngramDims, streams, kv, q_weight, k_weight, token_mask=None, err=None, stream=None):
     """Updates ``streams`` (fp32 [T, hc, H]) in place and returns it."""
     _dev(streams, torch.float32, "streams")
     _dev(kv, torch.float32, "kv")
     _u16(q_weight, "q_weight")
     _u16(k_weight, "k_weight")
     _opt(token_mask, torch.uint8, "token_mask")
+    _opt(err, torch.int32, "err")
     T = streams.shape[0]
     _check("engram_gate", lib().engram_gate(C.byref(dims), _ptr(streams), _ptr(kv), _ptr(q_weight),
-                                             _ptr(k_weight), _ptr(token_mask), T, _stream(stream)))
+                                             _ptr(k_weight), _ptr(token_mask), T, _ptr(err), _stream(stream)))
     return streams
 
 

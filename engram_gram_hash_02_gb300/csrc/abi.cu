@@ -216,18 +216,21 @@ int engram_project(const uint16_t* A, const uint16_t* wkv, float* kv, int64_t T,
 }
 
 static int gate_impl(const EngramDims* dims, float* streams, const float* kv, const uint16_t* q_weight,
-                     const uint16_t* k_weight, const uint8_t* token_mask, int64_t T, engram_stream_t stream, bool pdl) {
+                     const uint16_t* k_weight, const uint8_t* token_mask, int64_t T, int32_t* err_flag,
+                     engram_stream_t stream, bool pdl) {
   if (T == 0) return check_dims(dims, false, true);
   int rc = check_gate(dims, streams, kv, q_weight, k_weight, T);
   if (rc) return rc;
-  GateParams p{streams, kv, q_weight, k_weight, token_mask, T, dims->hidden, dims->hc, dims->eps, dims->clamp};
+  GateParams p{streams, kv, q_weight, k_weight, token_mask, T, dims->hidden, dims->hc, dims->eps, dims->clamp,
+               err_flag};
   cudaError_t e = launch_gate(p, static_cast<cudaStream_t>(stream), pdl);
   return e == cudaSuccess ? ENGRAM_OK : fail_cuda(e, "engram_gate: launch");
 }
 
 int engram_gate(const EngramDims* dims, float* streams, const float* kv, const uint16_t* q_weight,
-                const uint16_t* k_weight, const uint8_t* token_mask, int64_t T, engram_stream_t stream) {
-  return gate_impl(dims, streams, kv, q_weight, k_weight, token_mask, T, stream, false);
+                const uint16_t* k_weight, const uint8_t* token_mask, int64_t T, int32_t* err_flag,
+                engram_stream_t stream) {
+  return gate_impl(dims, streams, kv, q_weight, k_weight, token_mask, T, err_flag, stream, false);
 }
 
 size_t engram_forward_workspace_bytes(const EngramDims* d, int64_t T) {
@@ -287,7 +290,7 @@ int engram_forward(const EngramDims* dims, const EngramHashTables* tables, const
     if (rc) return rc;
     rc = project_impl(A, w.wkv, kv, T, (int32_t)K, (int32_t)N, gemm_ws, gemm_ws_bytes, err_flag, stream, true);
     if (rc) return rc;
-    rc = gate_impl(dims, streams[l], kv, w.q_weight, w.k_weight, tok->token_mask, T, stream, true);
+    rc = gate_impl(dims, streams[l], kv, w.q_weight, w.k_weight, tok->token_mask, T, err_flag, stream, true);
     if (rc) return rc;
   }
   return ENGRAM_OK;

@@ -6,161 +6,259 @@
 // the wkv output, clamp 1e-6) and the Atlas "engram_v41" page (stage 4: in place on the
 // fp32 highway [T, hc, H]).
 //
-// One CTA per (token, stream). Each thread owns two groups of 8 consecutive hidden elements;
-// it reads its part of the stream, the key, the value and the two norm weights once (16-byte
-// loads, all issued before any arithmetic), accumulates sum h^2, sum key^2 and
-// sum h*q*key*k, and keeps the stream and the value in registers. A warp-shuffle + shared
-// memory reduction gives the gate; the threads add g * value and write the stream back.
-// Stream traffic is one read and one write, the minimum; the value is read once per stream
-// (hc-1 of those reads hit L2).
+// A persistent kernel: a few CTAs per SM, each walking a fixed share of the (token, stream)
+// items (item i = t * hc + j; CTA b takes b, b + grid, ...; masked tokens are skipped before
+// anything is loaded). Per item, one thread issues three 1-D bulk copies (cp.async.bulk) of
+// the stream row h_j, the key_j and the shared value (4H bytes each, contiguous) into one of
+// two shared-memory buffers, completing on that buffer's mbarrier; the copies of the next item
+// are in flight while the CTA works on the current one. The CTA reads h and the key from shared
+// memory to form sum h^2, sum key^2 and
+// sum h*q*key*k, reduces them with warp shuffles, computes the gate, and writes h + g * value
+// back with coalesced 16-byte stores. HBM traffic is the minimum: h read and written once, key
+// read once, the value once per stream (hc - 1 of those from L2). The grid is a multiple of hc,
+// so a CTA only ever sees one stream j: each thread loads its slice of q_weight[j] and
+// k_weight[j] into registers once, keeping that latency off the per-item path.
+//
+// Under programmatic dependent launch the first items' stream rows are requested before
+// waiting for the projection; every CTA waits once (not once per item). Waits on the buffers
+// are bounded (~2 s of SM clock cycles); on expiry the CTA reports ENGRAM_ERR_PIPE_TIMEOUT,
+// waits (bounded) for its copies in flight and exits.
 #include "internal.cuh"
 
 namespace engram {
 namespace {
 
-constexpr int kItems = 2;      // groups of 8 elements per thread
+constexpr int kBufs = 2;
+constexpr int kChunks = 4;                             // float4 chunks of a row per thread (H <= 16 * threads)
 constexpr int kMaxThreads = 512;
+constexpr int kMaxCtasPerSm = 8;
+constexpr int kSmemBudget = 232448;                    // opt-in maximum per CTA
+constexpr uint64_t kWaitLimitCycles = 4000000000ull;   // ~2 s at 2 GHz
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// bounded wait on a buffer's mbarrier; false on expiry (or when another thread gave up)
+__device__ __noinline__ bool wait_buffer(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint64_t limit) {
+  const uint64_t t0 = clock64();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 15u && (*abort_flag || (uint64_t)clock64() - t0 > limit)) return false;
+  }
+}
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
-  f[0] = bf16lo(v.x); f[1] = bf16hi(v.x);
-  f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
-  f[4] = bf16lo(v.z); f[5] = bf16hi(v.z);
-  f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
-}
-
-__device__ __forceinline__ void load8(const float* p, float (&f)[8]) {
-  const float4 a = *reinterpret_cast<const float4*>(p);
-  const float4 b = *reinterpret_cast<const float4*>(p + 4);
-  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-}
-
-__global__ void __launch_bounds__(kMaxThreads)
-gate_kernel(const GateParams p) {
-  const int64_t t = blockIdx.x / p.hc;
-  const int j = blockIdx.x - (int)(t * p.hc);
-  if (p.token_mask != nullptr && __ldg(p.token_mask + t) == 0) {   // gate shut: untouched
-    pdl_wait();
-    return;
+// The CTA's items in order, masked tokens skipped: every thread walks the same sequence.
+struct Items {
+  const GateParams& p;
+  int64_t total, stride;
+  __device__ Items(const GateParams& params, int64_t s) : p(params), total(params.T * params.hc), stride(s) {}
+  __device__ int64_t next(int64_t i) const {   // first unmasked item >= i on this CTA's stride
+    for (; i < total; i += stride) {
+      if (p.token_mask == nullptr || __ldg(p.token_mask + i / p.hc) != 0) return i;
+    }
+    return -1;
   }
+};
+
+__global__ void __launch_bounds__(kMaxThreads, 1)
+gate_kernel(const GateParams p) {
+  extern __shared__ __align__(128) float buf[];          // kBufs x [h | key | value], H floats each
+  __shared__ __align__(8) uint64_t full[kBufs];
+  __shared__ float red[kMaxThreads / 32][3];
+  __shared__ float gate_s;
+  __shared__ int abort_s;
 
   const int H = p.H;
-  const int G = H >> 3;                                  // groups of 8
-  float* __restrict__ h = p.streams + (t * p.hc + j) * (int64_t)H;
-  const float* __restrict__ key = p.kv + t * (int64_t)(p.hc + 1) * H + (int64_t)j * H;
-  const float* __restrict__ val = p.kv + t * (int64_t)(p.hc + 1) * H + (int64_t)p.hc * H;
-  const uint16_t* __restrict__ qw = p.q_weight + (int64_t)j * H;
-  const uint16_t* __restrict__ kw = p.k_weight + (int64_t)j * H;
+  const int tid = threadIdx.x;
+  const uint32_t row_bytes = 4u * (uint32_t)H;
+  const int64_t N = (int64_t)(p.hc + 1) * H;
+  const Items items(p, gridDim.x);
 
-  // the stream and the norm weights do not come from the projection: load them first
-  float hv[kItems][8], kv[kItems][8], vv[kItems][8];
-  uint4 qraw[kItems], kraw[kItems];
-#pragma unroll
-  for (int it = 0; it < kItems; ++it) {
-    const int g = threadIdx.x + it * blockDim.x;
-    if (g < G) {
-      load8(h + 8 * g, hv[it]);
-      qraw[it] = __ldg(reinterpret_cast<const uint4*>(qw + 8 * g));
-      kraw[it] = __ldg(reinterpret_cast<const uint4*>(kw + 8 * g));
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) hv[it][e] = 0.f;
-      qraw[it] = kraw[it] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    for (int b = 0; b < kBufs; ++b)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&full[b])) : "memory");
+    abort_s = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  // ---- producer state (thread 0): items issued so far -------------------------------------
+  int64_t ahead = items.next(blockIdx.x);                // next item to issue
+  int issued = 0;
+  auto buffer = [&](int n) { return smem_u32(buf) + (uint32_t)((n % kBufs) * 3) * row_bytes; };
+  auto issue_h = [&](int64_t i, int n) {                 // stream row: not written by the projection
+    const uint32_t bar = smem_u32(&full[n % kBufs]);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(3u * row_bytes)
+                 : "memory");
+    bulk_copy(buffer(n), p.streams + i * (int64_t)H, row_bytes, bar);
+  };
+  auto issue_kv = [&](int64_t i, int n) {                // key and value: the projection's output
+    const uint32_t bar = smem_u32(&full[n % kBufs]);
+    const int64_t t = i / p.hc;
+    const int j = (int)(i - t * p.hc);
+    bulk_copy(buffer(n) + row_bytes, p.kv + t * N + (int64_t)j * H, row_bytes, bar);
+    bulk_copy(buffer(n) + 2u * row_bytes, p.kv + t * N + (int64_t)p.hc * H, row_bytes, bar);
+  };
+  int64_t first_items[kBufs];
+  if (tid == 0) {
+    for (int n = 0; n < kBufs && ahead >= 0; ++n) {
+      first_items[n] = ahead;
+      issue_h(ahead, n);
+      ahead = items.next(ahead + gridDim.x);
+      ++issued;
     }
   }
   pdl_wait();                                            // kv comes from the projection
-  pdl_trigger();
+  if (tid == 0) {
+    for (int n = 0; n < issued; ++n) issue_kv(first_items[n], n);
+  }
+
+  const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  const int H4 = H >> 2;
+  // this CTA's stream and its norm weights (grid % hc == 0: every item of the CTA has j = b % hc)
+  const int jc = (int)(blockIdx.x % (unsigned)p.hc);
+  uint2 qreg[kChunks], kreg[kChunks];
 #pragma unroll
-  for (int it = 0; it < kItems; ++it) {
-    const int g = threadIdx.x + it * blockDim.x;
-    if (g < G) {
-      load8(key + 8 * g, kv[it]);
-      load8(val + 8 * g, vv[it]);
+  for (int m = 0; m < kChunks; ++m) {
+    const int c = tid + m * (int)blockDim.x;
+    if (c < H4) {
+      qreg[m] = __ldg(reinterpret_cast<const uint2*>(p.q_weight + (int64_t)jc * H) + c);
+      kreg[m] = __ldg(reinterpret_cast<const uint2*>(p.k_weight + (int64_t)jc * H) + c);
     } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) kv[it][e] = vv[it][e] = 0.f;
+      qreg[m] = kreg[m] = make_uint2(0, 0);
     }
   }
-  float ssh = 0.f, ssk = 0.f, dot = 0.f;
+  int64_t cur = items.next(blockIdx.x);
+  for (int n = 0; cur >= 0; ++n) {
+    const int64_t nxt = items.next(cur + gridDim.x);
+    if (nxt < 0 && tid == 0) pdl_trigger();              // last item: the next kernel may launch
+    const bool ok = wait_buffer(smem_u32(&full[n % kBufs]), (uint32_t)(n / kBufs) & 1u, &abort_s, kWaitLimitCycles);
+    if (!ok) abort_s = 1;
+    const float4* hs = reinterpret_cast<const float4*>(buf + (size_t)(n % kBufs) * 3 * H);
+    const float4* ks = hs + H4;
+    const float4* vs = ks + H4;
+    float ssh = 0.f, ssk = 0.f, dot = 0.f;
 #pragma unroll
-  for (int it = 0; it < kItems; ++it) {
-    float q[8], k[8];
-    unpack8(qraw[it], q);
-    unpack8(kraw[it], k);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float x = hv[it][e], y = kv[it][e];
-      ssh = fmaf(x, x, ssh);
-      ssk = fmaf(y, y, ssk);
-      dot = fmaf(x * q[e], y * k[e], dot);
+    for (int m = 0; m < kChunks; ++m) {
+      const int c = tid + m * (int)blockDim.x;
+      if (c >= H4) break;
+      const float4 x = hs[c], y = ks[c];
+      const uint2 qr = qreg[m], kr = kreg[m];
+      ssh = fmaf(x.x, x.x, ssh); ssh = fmaf(x.y, x.y, ssh); ssh = fmaf(x.z, x.z, ssh); ssh = fmaf(x.w, x.w, ssh);
+      ssk = fmaf(y.x, y.x, ssk); ssk = fmaf(y.y, y.y, ssk); ssk = fmaf(y.z, y.z, ssk); ssk = fmaf(y.w, y.w, ssk);
+      dot = fmaf(x.x * bf16lo(qr.x), y.x * bf16lo(kr.x), dot);
+      dot = fmaf(x.y * bf16hi(qr.x), y.y * bf16hi(kr.x), dot);
+      dot = fmaf(x.z * bf16lo(qr.y), y.z * bf16lo(kr.y), dot);
+      dot = fmaf(x.w * bf16hi(qr.y), y.w * bf16hi(kr.y), dot);
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      ssh += __shfl_xor_sync(0xffffffffu, ssh, off);
+      ssk += __shfl_xor_sync(0xffffffffu, ssk, off);
+      dot += __shfl_xor_sync(0xffffffffu, dot, off);
+    }
+    if (lane == 0) {
+      red[warp][0] = ssh;
+      red[warp][1] = ssk;
+      red[warp][2] = dot;
+    }
+    __syncthreads();                                     // (1) partial sums and abort_s visible
+    if (abort_s) break;
+    if (tid == 0) {
+      float a = 0.f, b = 0.f, c = 0.f;
+      for (int w = 0; w < nwarps; ++w) {
+        a += red[w][0];
+        b += red[w][1];
+        c += red[w][2];
+      }
+      const float invH = 1.0f / (float)H;
+      const float rh = rsqrtf(a * invH + p.eps);
+      const float rk = rsqrtf(b * invH + p.eps);
+      const float s = c * rh * rk / sqrtf((float)H);
+      float ss = 0.f;                                    // sign(0) = 0
+      if (s > 0.f) ss = sqrtf(fmaxf(s, p.clamp));
+      else if (s < 0.f) ss = -sqrtf(fmaxf(-s, p.clamp));
+      gate_s = 1.0f / (1.0f + expf(-ss));
+    }
+    __syncthreads();                                     // (2) gate visible
+    const float g = gate_s;
+    float4* out = reinterpret_cast<float4*>(p.streams + cur * (int64_t)H);
+    for (int c = tid; c < H4; c += blockDim.x) {
+      const float4 x = hs[c], v = vs[c];
+      out[c] = make_float4(fmaf(g, v.x, x.x), fmaf(g, v.y, x.y), fmaf(g, v.z, x.z), fmaf(g, v.w, x.w));
+    }
+    __syncthreads();                                     // (3) buffer n % kBufs read by all
+    if (tid == 0 && ahead >= 0) {
+      // refill this buffer with the item kBufs places ahead (issued == n + kBufs here)
+      issue_h(ahead, issued);
+      issue_kv(ahead, issued);
+      ahead = items.next(ahead + gridDim.x);
+      ++issued;
+    }
+    cur = nxt;
   }
 
-  // ---- block reduction of the three sums -------------------------------------------------------
-  __shared__ float red[kMaxThreads / 32][3];
-  __shared__ float gate;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    ssh += __shfl_xor_sync(0xffffffffu, ssh, off);
-    ssk += __shfl_xor_sync(0xffffffffu, ssk, off);
-    dot += __shfl_xor_sync(0xffffffffu, dot, off);
-  }
-  if (lane == 0) {
-    red[warp][0] = ssh;
-    red[warp][1] = ssk;
-    red[warp][2] = dot;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const int nw = blockDim.x >> 5;
-    float a = 0.f, b = 0.f, c = 0.f;
-    for (int w = 0; w < nw; ++w) {
-      a += red[w][0];
-      b += red[w][1];
-      c += red[w][2];
+  if (abort_s) {
+    if (p.err != nullptr && tid == 0) atomicOr(p.err, ENGRAM_ERR_PIPE_TIMEOUT);
+    // copies still in flight must land before shared memory goes away: wait (bounded) on every
+    // buffer use issued but not consumed
+    if (tid == 0) {
+      volatile int never = 0;
+      for (int n = issued > kBufs ? issued - kBufs : 0; n < issued; ++n)
+        wait_buffer(smem_u32(&full[n % kBufs]), (uint32_t)(n / kBufs) & 1u, &never, kWaitLimitCycles / 4);
     }
-    const float invH = 1.0f / (float)H;
-    const float rh = rsqrtf(a * invH + p.eps);
-    const float rk = rsqrtf(b * invH + p.eps);
-    const float s = c * rh * rk / sqrtf((float)H);
-    float ss = 0.f;                                      // sign(0) = 0
-    if (s > 0.f) ss = sqrtf(fmaxf(s, p.clamp));
-    else if (s < 0.f) ss = -sqrtf(fmaxf(-s, p.clamp));
-    gate = 1.0f / (1.0f + expf(-ss));
-  }
-  __syncthreads();
-  const float g = gate;
-
-  // ---- h += g * value ----------------------------------------------------------------------------
-#pragma unroll
-  for (int it = 0; it < kItems; ++it) {
-    const int gi = threadIdx.x + it * blockDim.x;
-    if (gi < G) {
-      float4 a, b;
-      a.x = fmaf(g, vv[it][0], hv[it][0]); a.y = fmaf(g, vv[it][1], hv[it][1]);
-      a.z = fmaf(g, vv[it][2], hv[it][2]); a.w = fmaf(g, vv[it][3], hv[it][3]);
-      b.x = fmaf(g, vv[it][4], hv[it][4]); b.y = fmaf(g, vv[it][5], hv[it][5]);
-      b.z = fmaf(g, vv[it][6], hv[it][6]); b.w = fmaf(g, vv[it][7], hv[it][7]);
-      *reinterpret_cast<float4*>(h + 8 * gi) = a;
-      *reinterpret_cast<float4*>(h + 8 * gi + 4) = b;
-    }
+    __syncthreads();
   }
 }
 
 }  // namespace
 
 cudaError_t launch_gate(const GateParams& p, cudaStream_t stream, bool pdl) {
-  const int groups = p.H / 8;
-  int threads = (groups + kItems - 1) / kItems;
-  threads = ((threads + 31) / 32) * 32;
-  if (threads > kMaxThreads) return cudaErrorInvalidValue;
-  const int64_t blocks = p.T * p.hc;
-  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-  return launch_k(gate_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream, pdl, p);
+  const int H = p.H;
+  int threads = ((H / (4 * kChunks) + 31) / 32) * 32;   // every thread covers at most kChunks chunks
+  if (threads < 64) threads = 64;
+  if (threads > kMaxThreads) threads = kMaxThreads;
+  const size_t smem = (size_t)kBufs * 3 * 4 * (size_t)H;
+  if (smem > (size_t)kSmemBudget - 2048) return cudaErrorInvalidValue;
+  static bool configured[64] = {false};     // the attribute is per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget - 2048);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
+  int per_sm = 0;                           // resident CTAs per SM (registers, shared memory)
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gate_kernel, threads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm > kMaxCtasPerSm) per_sm = kMaxCtasPerSm;
+  if (per_sm < 1) per_sm = 1;
+  const int64_t items = p.T * p.hc;
+  // a multiple of hc (each CTA keeps one stream's norm weights), at most one CTA per item
+  int64_t grid = ((int64_t)num_sms() * per_sm / p.hc) * p.hc;
+  if (grid < p.hc) grid = p.hc;
+  if (grid > items) grid = items;                       // items = T * hc: still a multiple of hc
+  return launch_k(gate_kernel, dim3((unsigned)grid), dim3(threads), smem, stream, pdl, p);
 }
 
 }  // namespace engram

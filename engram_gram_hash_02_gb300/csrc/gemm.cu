@@ -155,9 +155,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Bounded wait: false if this CTA aborted (here or in another role). The bound counts SM clock
 // cycles (clock64 is a cheap local register; %globaltimer is slow to read on this part and would
 // sit on the pipeline's critical path).
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int32_t* abort_flag,
-                                       int32_t* err, uint64_t limit_cycles) {
-  if (mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int32_t* abort_flag,
+                                            int32_t* err, uint64_t limit_cycles) {
   const uint64_t t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -170,6 +169,13 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
       }
     }
   }
+}
+// The producer and MMA threads sit on the pipeline's critical path: the common case (phase
+// already complete) stays inline, the bounded spin is a call.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int32_t* abort_flag, int32_t* err,
+                                          uint64_t limit_cycles) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, err, limit_cycles);
 }
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int32_t x, int32_t y) {
@@ -312,7 +318,6 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
       }
       pdl_wait();
-      pdl_trigger();
       int it = 0, issued = 0;
       bool ok = true;
       Schedule sch(a, blockIdx.x, gridDim.x);
@@ -320,6 +325,13 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       while (ok && sch.next(item)) {
         int m0, n0;
         tile_origin(a, item.tile, m0, n0);
+        {
+          // the next kernel may start launching once this CTA is on its last item (earlier, its
+          // waiting CTAs would share the SM with a long main loop)
+          Schedule peek = sch;
+          Item tmp;
+          if (!peek.next(tmp)) pdl_trigger();
+        }
         for (int kb = item.k0; kb < item.k1; ++kb, ++it) {
           if (it < early) {
             load_a(it, kb, m0);
@@ -351,7 +363,9 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (lane == 0) {
       Schedule sch(a, blockIdx.x, gridDim.x);
       Item item;
-      int it = 0, n_items = 0;
+      int n_items = 0;
+      int slot = 0;                            // iteration mod stages
+      uint32_t round = 0;                      // (iteration / stages) & 1
       bool ok = true;
       while (ok && sch.next(item)) {
         // the epilogue has drained the previous item's accumulators
@@ -361,32 +375,36 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           break;
         }
         tc_fence_after();
-        for (int kb = item.k0; kb < item.k1; ++kb, ++it) {
-          const int s = it % a.stages;
-          const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
-          if (!mbar_wait(smem_u32(&ctl->full[s]), ph, abort_flag, a.err, kWaitLimitCycles)) {
+        for (int kb = item.k0; kb < item.k1; ++kb) {
+          if (!mbar_wait(smem_u32(&ctl->full[slot]), round, abort_flag, a.err, kWaitLimitCycles)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t st = tiles + (uint32_t)(s * a.stage_bytes);
-          const uint32_t b_addr = st + (uint32_t)(a.msub * kATileBytes);
+          // descriptors of the k = 0 slices; a k step of 16 elements (32 bytes) adds 2 to the
+          // encoded start address, the second 128-row half (16 KB) adds 1024
+          const uint32_t st = tiles + (uint32_t)(slot * a.stage_bytes);
+          const uint64_t a0 = smem_desc_sw128(st);
+          const uint64_t b0 = smem_desc_sw128(st + (uint32_t)(a.msub * kATileBytes));
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k) {
-            const uint64_t bdesc = smem_desc_sw128(b_addr + k * kUmmaK * 2);
+            const uint64_t bdesc = b0 + (uint64_t)(2 * k);
             if (a.msub == 2) {
               // two chains: the two 128-row halves
-              for (int ms = 0; ms < 2; ++ms) {
-                const uint64_t adesc = smem_desc_sw128(st + ms * kATileBytes + k * kUmmaK * 2);
-                tc_mma(tmem + ms * a.acc_stride, adesc, bdesc, a.idesc, (kb > item.k0 || k > 0) ? 1u : 0u);
-              }
+              const uint32_t acc = (kb > item.k0 || k > 0) ? 1u : 0u;
+              tc_mma(tmem, a0 + (uint64_t)(2 * k), bdesc, a.idesc, acc);
+              tc_mma(tmem + a.acc_stride, a0 + (uint64_t)(2 * k + (kATileBytes >> 4)), bdesc, a.idesc, acc);
             } else {
               // two chains: even and odd k steps of the same tile
-              const uint64_t adesc = smem_desc_sw128(st + k * kUmmaK * 2);
-              tc_mma(tmem + (k & 1) * a.acc_stride, adesc, bdesc, a.idesc, (kb > item.k0 || k > 1) ? 1u : 0u);
+              tc_mma(tmem + (k & 1) * a.acc_stride, a0 + (uint64_t)(2 * k), bdesc, a.idesc,
+                     (kb > item.k0 || k > 1) ? 1u : 0u);
             }
           }
-          tc_commit(smem_u32(&ctl->empty[s]));   // stage free once these MMAs have read it
+          tc_commit(smem_u32(&ctl->empty[slot]));   // stage free once these MMAs have read it
+          if (++slot == a.stages) {
+            slot = 0;
+            round ^= 1u;
+          }
         }
         tc_commit(smem_u32(&ctl->acc_full));     // this item's accumulators final (or drained)
         ++n_items;

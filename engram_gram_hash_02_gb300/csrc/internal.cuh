@@ -109,6 +109,7 @@ struct GateParams {
   int64_t T;
   int32_t H, hc;
   float eps, clamp;
+  int32_t* err;
 };
 cudaError_t launch_gate(const GateParams& p, cudaStream_t stream, bool pdl = false);
 

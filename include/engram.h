@@ -183,11 +183,14 @@ void engram_set_gemm_schedule(int32_t s);
  *   kv        device fp32 [T, (hc+1)*H] (output of engram_project)
  *   q_weight, k_weight device bf16 [hc, H]
  *   token_mask device uint8 [T] or NULL
- * H % 8 == 0, 8 <= H <= 8192, 1 <= hc <= 8.
+ *   err_flag  device int32 or NULL: ENGRAM_ERR_PIPE_TIMEOUT if a copy into shared memory never
+ *             completed (the streams of the items not yet processed are then unchanged)
+ * H % 8 == 0, 8 <= H <= 8192, 1 <= hc <= 8. A persistent kernel (a few CTAs per SM), each
+ * CTA streaming its (token, stream) rows through shared memory with bulk copies.
  */
 int engram_gate(const EngramDims* dims, float* streams, const float* kv,
                 const uint16_t* q_weight, const uint16_t* k_weight, const uint8_t* token_mask,
-                int64_t T, engram_stream_t stream);
+                int64_t T, int32_t* err_flag, engram_stream_t stream);
 
 /* Per-layer resident weights ([Atlas] EngramLayerWeights; [vLLM] Engram parameters). */
 typedef struct EngramLayerWeights {

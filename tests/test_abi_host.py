@@ -88,7 +88,7 @@ def test_argument_checks_fire_before_any_cuda_call(lib):
     assert rc == -1 and "unknown table format" in lib.engram_last_error().decode()
     # gate: hidden not a multiple of 8
     dims = Bd.EngramDims(1, 3, 4, 64, 7, 4, 16, 16, 0, 1e-6, 1e-6)
-    rc = lib.engram_gate(ctypes.byref(dims), addr, addr, addr, addr, None, 1, stream)
+    rc = lib.engram_gate(ctypes.byref(dims), addr, addr, addr, addr, None, 1, None, stream)
     assert rc == -1 and "hidden" in lib.engram_last_error().decode()
     # hash: pad id outside the compressed vocabulary
     dims = Bd.EngramDims(1, 3, 4, 64, 256, 4, 16, 16, 99, 1e-6, 1e-6)

@@ -227,8 +227,12 @@ def test_project_integer_exact():
 
 # ------------------------------------------------------------------------------------------- gate
 
+# The gate kernel is persistent (a few CTAs per SM, two shared-memory buffers each): the larger
+# cases give every CTA many items, so the buffers are reused across several phases.
 @pytest.mark.parametrize("T,hc,H_,masked", [(64, 4, 256, False), (37, 4, 4096, True), (5, 4, 7168, True),
-                                            (9, 2, 1000, False), (3, 1, 8, True), (16, 8, 512, False)])
+                                            (9, 2, 1000, False), (3, 1, 8, True), (16, 8, 512, False),
+                                            (700, 4, 4096, True), (120, 4, 8192, False), (90, 4, 7168, True),
+                                            (3000, 8, 64, True)])
 def test_gate_vs_oracle(T, hc, H_, masked):
     g = torch.Generator(device=DEV).manual_seed(T + hc + H_)
     h = torch.randn(T, hc, H_, generator=g, device=DEV)
@@ -248,6 +252,19 @@ def test_gate_vs_oracle(T, hc, H_, masked):
         keep = mask.cpu().numpy() == 0
         assert np.array_equal(got[keep], h0[keep].astype(np.float32))   # bit-unchanged
     H.check_streams(got, ref, h0, f"gate T={T} hc={hc} H={H_}")
+
+
+def test_gate_all_masked_leaves_streams_bit_unchanged():
+    T, hc, H_ = 500, 4, 4096
+    h = torch.randn(T, hc, H_, device=DEV)
+    before = h.clone()
+    kv = torch.randn(T, (hc + 1) * H_, device=DEV)
+    q = torch.ones(hc, H_, device=DEV, dtype=torch.bfloat16)
+    mask = torch.zeros(T, dtype=torch.uint8, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    dims = E().make_dims(1, 3, 4, 64, H_, hc, 10, 10, 0)
+    E().engram_gate(dims, h, kv, q, q, token_mask=mask, err=err)
+    assert torch.equal(h, before) and int(err.item()) == 0
 
 
 def test_gate_zero_value_bit_unchanged():

@@ -356,6 +356,99 @@ def project(a_bits, wkv_bits):
 
 
 # ---------------------------------------------------------------------------
+# Stage 3, FP8 operand variant: MXFP8 operands
+#
+# The FP8 table rows already are e4m3 codes with one power-of-two (E8M0) scale
+# per 32 values ([vLLM] ``ParallelEngramEmbedding``: weight float8_e4m3fn plus a
+# ue8m0 scale per 32-element block).  The variant feeds those codes and scales
+# to the projection as they are, and stores wkv the same way: per row and per
+# block of 32 along K, one scale byte and 32 e4m3 codes.  The pages do not
+# print a weight encoder; the reading is the rule the table's scale convention
+# implies: the scale is the smallest power of two 2**e with
+# max|w| / 2**e <= 448 (so no value saturates), byte = 127 + e, and each code
+# is w / 2**e rounded to nearest, ties to even.  An all-zero block gets byte 127
+# and zero codes.  Dequantised values are exact in bf16 and fp32.
+# ---------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def float_to_e4m3(x):
+    """fp64 values -> OCP E4M3 (fn) codes, round to nearest, ties to even.
+    Magnitudes above 448 saturate to 448 (the format has no infinities); NaN
+    becomes 0x7F.  Subnormals are multiples of 2**-9 below 2**-6."""
+    x = np.asarray(x, dtype=np.float64)
+    sign = np.signbit(x).astype(np.int64) << 7
+    a = np.abs(x)
+    nan = np.isnan(x)
+    a = np.where(nan, 0.0, a)
+    code = np.zeros(a.shape, dtype=np.int64)
+    sub = a < 2.0 ** -6
+    # subnormal range: q = rint(a / 2**-9) in 0..8; code 8 is 2**-6, the first normal
+    code = np.where(sub, np.rint(a * 2.0 ** 9).astype(np.int64), code)
+    mant, ex = np.frexp(np.where(sub, 1.0, a))                 # a = mant * 2**ex, mant in [0.5, 1)
+    E = ex.astype(np.int64) - 1                                # a = (2 * mant) * 2**E
+    q = np.rint((2.0 * mant - 1.0) * 8.0).astype(np.int64)     # 3 mantissa bits, ties to even
+    E = np.where(q == 8, E + 1, E)
+    q = np.where(q == 8, 0, q)
+    normal = (E + 7) << 3 | q
+    over = (E + 7 > 15) | ((E + 7 == 15) & (q == 7))
+    normal = np.where(over, 0x7E, normal)
+    code = np.where(sub, code, normal)
+    code = np.where(nan, 0x7F, code | sign)
+    return code.astype(np.uint8)
+
+
+def mxfp8_quantize(w_bits, block: int = E8M0_BLOCK):
+    """bf16 bits [N, K] -> (e4m3 codes uint8 [N, K], scale bytes uint8 [N, K/32])
+    under the reading stated above.  K must be a multiple of 32."""
+    w = bf16_bits_to_f64(w_bits)
+    N, K = w.shape
+    assert K % block == 0
+    wb = w.reshape(N, K // block, block)
+    amax = np.abs(wb).max(axis=2)                              # [N, K/32]
+    e = np.zeros(amax.shape, dtype=np.int64)
+    nz = amax > 0
+    # smallest e with amax / 2**e <= 448: start from the binary exponent and correct
+    _, ex = np.frexp(np.where(nz, amax / E4M3_MAX, 1.0))       # amax/448 = m * 2**ex, m in [0.5, 1)
+    e = np.where(nz, ex.astype(np.int64), 0)                   # 2**ex >= amax/448 > 2**(ex-1)
+    e = np.where(nz & (np.ldexp(E4M3_MAX, (e - 1)) >= amax), e - 1, e)
+    e = np.clip(e, -127, 127)
+    codes = float_to_e4m3(wb / np.exp2(e.astype(np.float64))[:, :, None]).reshape(N, K)
+    return codes, (e + 127).astype(np.uint8)
+
+
+def mxfp8_dequant(codes, scale_bytes, block: int = E8M0_BLOCK):
+    """fp64 values of MXFP8 data: e4m3 value times 2**(byte - 127), per block of
+    32 along the last axis."""
+    v = e4m3_to_float(codes)
+    s = np.exp2(np.asarray(scale_bytes, dtype=np.float64) - 127.0)
+    return v * np.repeat(s, block, axis=-1)
+
+
+def gather_fp8_raw(weight, scales, ids, num_rows: int):
+    """FP8 variant of stage 2: ids [T, C] -> (codes [T, C*D], scales [T, C*D/32]),
+    the table's bytes copied without dequantisation; ids outside [0, num_rows)
+    give a zero row (codes 0, scale byte 127)."""
+    ids = np.asarray(ids, dtype=np.int64)
+    T, C = ids.shape
+    weight = np.asarray(weight, dtype=np.uint8)
+    scales = np.asarray(scales, dtype=np.uint8)
+    flat = ids.reshape(-1)
+    ok = (flat >= 0) & (flat < num_rows)
+    safe = np.where(ok, flat, 0)
+    codes = np.where(ok[:, None], weight[safe], np.uint8(0)).astype(np.uint8)
+    sc = np.where(ok[:, None], scales[safe], np.uint8(127)).astype(np.uint8)
+    return codes.reshape(T, -1), sc.reshape(T, -1), int((~ok).sum())
+
+
+def project_mxfp8(a_codes, a_scales, w_codes, w_scales):
+    """kv[t, n] = sum_k A[t, k] * W[n, k] in fp64 from MXFP8 operands (each value
+    its code times its block's power-of-two scale)."""
+    return mxfp8_dequant(a_codes, a_scales) @ mxfp8_dequant(w_codes, w_scales).T
+
+
+# ---------------------------------------------------------------------------
 # Stage 4: gate
 # ---------------------------------------------------------------------------
 

@@ -16,14 +16,18 @@ from .binding import (  # noqa: F401
     engram_forward,
     engram_gate,
     engram_gather_dequant,
+    engram_gather_fp8_codes,
     engram_hash,
     engram_layout,
     engram_project,
+    engram_project_mxfp8,
     forward_workspace_bytes,
     hash_multipliers,
     lib,
     make_dims,
     project_workspace_bytes,
+    quantize_mxfp8,
+    set_gemm_mx_tile,
     set_gemm_schedule,
     set_gemm_tile,
 )

@@ -18,6 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libengram.so")
 
 TABLE_BF16, TABLE_FP8_E8M0, TABLE_Q2K = 0, 1, 2
+WKV_BF16, WKV_MXFP8 = 0, 1
 TABLE_FORMATS = {"bf16": TABLE_BF16, "fp8": TABLE_FP8_E8M0, "q2k": TABLE_Q2K}
 ERR_RAW_ID, ERR_ROW_ID, ERR_PIPE_TIMEOUT = 1, 2, 4
 NOALLOC_SCRATCH_BYTES = 32 << 20   # ENGRAM_NOALLOC_SCRATCH_BYTES
@@ -44,7 +45,7 @@ class EngramDims(C.Structure):
 class _LayerWeights(C.Structure):
     _fields_ = [("table_format", C.c_int32), ("table", C.c_void_p), ("table_scales", C.c_void_p),
                 ("table_rows", C.c_int64), ("wkv", C.c_void_p), ("q_weight", C.c_void_p),
-                ("k_weight", C.c_void_p)]
+                ("k_weight", C.c_void_p), ("wkv_format", C.c_int32), ("wkv_scales", C.c_void_p)]
 
 
 class _HashTables(C.Structure):
@@ -87,6 +88,11 @@ def lib() -> C.CDLL:
         L.engram_set_gemm_schedule.restype = None
         L.engram_project_workspace_bytes.argtypes = [I64, I32, I32]
         L.engram_project_workspace_bytes.restype = SZ
+        L.engram_quantize_mxfp8.argtypes = [P, I64, I32, P, P, P]
+        L.engram_gather_fp8_codes.argtypes = [P, I64, I64, I32, I32, P, P, I64, P, P, P, P]
+        L.engram_project_mxfp8.argtypes = [P, P, P, P, P, I64, I32, I32, P, P]
+        L.engram_set_gemm_mx_tile.argtypes = [I32]
+        L.engram_set_gemm_mx_tile.restype = None
         _lib = L
     return _lib
 
@@ -254,6 +260,56 @@ def set_gemm_schedule(s: int = 0):
     lib().engram_set_gemm_schedule(int(s))
 
 
+def quantize_mxfp8(w: torch.Tensor, codes=None, scales=None, stream=None):
+    """bf16 [N, K] -> (e4m3 codes uint8 [N, K], scale bytes uint8 [N, K/32]) (engram_quantize_mxfp8)."""
+    _u16(w, "w")
+    N, K = w.shape
+    codes = torch.empty(N, K, dtype=torch.uint8, device=w.device) if codes is None else _dev(codes, torch.uint8, "codes")
+    scales = (torch.empty(N, K // 32, dtype=torch.uint8, device=w.device) if scales is None
+              else _dev(scales, torch.uint8, "scales"))
+    _check("engram_quantize_mxfp8", lib().engram_quantize_mxfp8(_ptr(w), N, K, _ptr(codes), _ptr(scales),
+                                                               _stream(stream)))
+    return codes, scales
+
+
+def engram_gather_fp8_codes(ids, table, table_scales, num_rows: int, head_dim: int, codes=None, scales=None,
+                            err=None, stream=None):
+    """FP8 rows by id without dequantisation. ids int32 [T, C] (or a [T, L*C] slice: the row
+    stride is ids.stride(0)) -> (codes uint8 [T, C*head_dim], scales uint8 [T, C*head_dim/32])."""
+    if not isinstance(ids, torch.Tensor) or ids.dtype != torch.int32 or not ids.is_cuda or ids.stride(1) != 1:
+        raise ValueError("ids must be a CUDA int32 tensor with unit column stride")
+    T, Cc = ids.shape
+    _dev(table, torch.uint8, "table")
+    _dev(table_scales, torch.uint8, "table_scales")
+    _opt(err, torch.int32, "err")
+    codes = (torch.empty(T, Cc * head_dim, dtype=torch.uint8, device=ids.device) if codes is None
+             else _dev(codes, torch.uint8, "codes"))
+    scales = (torch.empty(T, Cc * head_dim // 32, dtype=torch.uint8, device=ids.device) if scales is None
+              else _dev(scales, torch.uint8, "scales"))
+    _check("engram_gather_fp8_codes", lib().engram_gather_fp8_codes(
+        _ptr(ids), ids.stride(0), T, Cc, head_dim, _ptr(table), _ptr(table_scales), int(num_rows), _ptr(codes),
+        _ptr(scales), _ptr(err), _stream(stream)))
+    return codes, scales
+
+
+def engram_project_mxfp8(a_codes, a_scales, w_codes, w_scales, out=None, err=None, stream=None):
+    """kv fp32 [T, N] = A * W^T from MXFP8 operands (engram_project_mxfp8)."""
+    for t, n in ((a_codes, "a_codes"), (a_scales, "a_scales"), (w_codes, "w_codes"), (w_scales, "w_scales")):
+        _dev(t, torch.uint8, n)
+    T, K = a_codes.shape
+    N = w_codes.shape[0]
+    out = torch.empty(T, N, dtype=torch.float32, device=a_codes.device) if out is None else _dev(out, torch.float32, "out")
+    _opt(err, torch.int32, "err")
+    _check("engram_project_mxfp8", lib().engram_project_mxfp8(_ptr(a_codes), _ptr(a_scales), _ptr(w_codes),
+                                                             _ptr(w_scales), _ptr(out), T, K, N, _ptr(err),
+                                                             _stream(stream)))
+    return out
+
+
+def set_gemm_mx_tile(bn: int = 0):
+    lib().engram_set_gemm_mx_tile(int(bn))
+
+
 def project_workspace_bytes(T: int, K: int, N: int) -> int:
     return int(lib().engram_project_workspace_bytes(T, K, N))
 
@@ -264,6 +320,8 @@ def project_workspace_bytes(T: int, K: int, N: int) -> int:
 
 @dataclass
 class LayerWeights:
+    """One layer's resident weights. ``wkv`` is bf16 [N, K], or e4m3 codes (uint8 [N, K]) with
+    ``wkv_scales`` (uint8 [N, K/32]) for the FP8 variant (see ``quantize_mxfp8``)."""
     fmt: str
     table: torch.Tensor
     scales: torch.Tensor | None
@@ -271,6 +329,7 @@ class LayerWeights:
     wkv: torch.Tensor
     q_weight: torch.Tensor
     k_weight: torch.Tensor
+    wkv_scales: torch.Tensor | None = None
 
 
 @dataclass
@@ -303,8 +362,13 @@ class ForwardPlan:
                                    _ptr(tables.offsets))
         arr = (_LayerWeights * len(layers))()
         for i, w in enumerate(layers):
+            mx = w.wkv_scales is not None
+            if mx:
+                _dev(w.wkv, torch.uint8, "wkv (MXFP8 codes)")
+                _dev(w.wkv_scales, torch.uint8, "wkv_scales")
             arr[i] = _LayerWeights(TABLE_FORMATS[w.fmt], _ptr(w.table), _ptr(w.scales), int(w.num_rows),
-                                   _ptr(w.wkv), _ptr(w.q_weight), _ptr(w.k_weight))
+                                   _ptr(w.wkv), _ptr(w.q_weight), _ptr(w.k_weight), WKV_MXFP8 if mx else WKV_BF16,
+                                   _ptr(w.wkv_scales))
             _dev(streams[i], torch.float32, f"streams[{i}]")
         self._layers = arr
         S = 1 if cu_seqlens is None else cu_seqlens.numel() - 1

@@ -39,6 +39,7 @@ int num_sms() {
 }
 
 void set_gemm_bn_override(int bn);
+void set_gemm_mx_bn_override(int bn);
 void set_gemm_schedule_override(int s);
 
 static int check_dims(const EngramDims* d, bool need_hash, bool need_gate) {
@@ -233,6 +234,74 @@ int engram_gate(const EngramDims* dims, float* streams, const float* kv, const u
   return gate_impl(dims, streams, kv, q_weight, k_weight, token_mask, T, err_flag, stream, false);
 }
 
+// ---- FP8 (MXFP8) operand variant ------------------------------------------------------------
+
+int engram_quantize_mxfp8(const uint16_t* w, int64_t N, int32_t K, uint8_t* codes, uint8_t* scales,
+                          engram_stream_t stream) {
+  ENGRAM_CHECK_ARG(N >= 0 && K >= 32 && K % 32 == 0, "engram_quantize_mxfp8: need N >= 0 and K a multiple of 32 (got %d)", K);
+  if (N == 0) return ENGRAM_OK;
+  ENGRAM_CHECK_ARG(w && codes && scales, "engram_quantize_mxfp8: w, codes and scales must be non-NULL");
+  cudaError_t e = launch_quantize_mxfp8(w, N, K, codes, scales, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ENGRAM_OK : fail_cuda(e, "engram_quantize_mxfp8: launch");
+}
+
+static int check_gather_codes(const int32_t* ids, int64_t ids_stride_t, int64_t T, int32_t C, int32_t D,
+                              const void* table, const uint8_t* scales, int64_t num_rows, const uint8_t* codes,
+                              const uint8_t* out_scales) {
+  ENGRAM_CHECK_ARG(T >= 0, "T must be >= 0");
+  ENGRAM_CHECK_ARG(C >= 1 && ids_stride_t >= C, "need C >= 1 and ids_stride_t >= C");
+  ENGRAM_CHECK_ARG(D >= 32 && D % 32 == 0, "FP8 head_dim must be a multiple of 32 (got %d)", D);
+  ENGRAM_CHECK_ARG(num_rows >= 0, "num_rows must be >= 0");
+  ENGRAM_CHECK_ARG(ids && table && scales && codes && out_scales, "ids, table, scales and outputs must be non-NULL");
+  ENGRAM_CHECK_ARG(aligned(table, 16) && aligned(codes, 16), "table and codes must be 16-byte aligned");
+  return ENGRAM_OK;
+}
+
+static int gather_codes_impl(const int32_t* ids, int64_t ids_stride_t, int64_t T, int32_t C, int32_t D,
+                             const void* table, const uint8_t* scales, int64_t num_rows, uint8_t* codes,
+                             uint8_t* out_scales, int32_t* err_flag, engram_stream_t stream, bool pdl) {
+  if (T == 0) return ENGRAM_OK;
+  int rc = check_gather_codes(ids, ids_stride_t, T, C, D, table, scales, num_rows, codes, out_scales);
+  if (rc) return rc;
+  GatherCodesParams p{ids, ids_stride_t, T, C, D, table, scales, num_rows, codes, out_scales, err_flag};
+  cudaError_t e = launch_gather_codes(p, static_cast<cudaStream_t>(stream), pdl);
+  return e == cudaSuccess ? ENGRAM_OK : fail_cuda(e, "engram_gather_fp8_codes: launch");
+}
+
+int engram_gather_fp8_codes(const int32_t* ids, int64_t ids_stride_t, int64_t T, int32_t C, int32_t head_dim,
+                            const void* table, const uint8_t* table_scales, int64_t num_rows, uint8_t* codes,
+                            uint8_t* scales, int32_t* err_flag, engram_stream_t stream) {
+  return gather_codes_impl(ids, ids_stride_t, T, C, head_dim, table, table_scales, num_rows, codes, scales, err_flag,
+                           stream, false);
+}
+
+static int check_project_mx(const uint8_t* A, const uint8_t* SA, const uint8_t* W, const uint8_t* SW, const float* kv,
+                            int64_t T, int32_t K, int32_t N) {
+  ENGRAM_CHECK_ARG(T >= 0 && T < (int64_t)1 << 31, "T must be in [0, 2^31)");
+  ENGRAM_CHECK_ARG(K >= 128 && K % 128 == 0, "MXFP8 projection: K must be a positive multiple of 128 (got %d)", K);
+  ENGRAM_CHECK_ARG(N >= 16 && N % 16 == 0, "N must be a positive multiple of 16 (got %d)", N);
+  ENGRAM_CHECK_ARG(A && SA && W && SW && kv, "A, A_scales, W, W_scales and kv must be non-NULL");
+  ENGRAM_CHECK_ARG(aligned(A, 16) && aligned(W, 16) && aligned(kv, 16), "A, W and kv must be 16-byte aligned");
+  ENGRAM_CHECK_ARG(aligned(SA, 4) && aligned(SW, 4), "A_scales and W_scales must be 4-byte aligned");
+  return ENGRAM_OK;
+}
+
+static int project_mx_impl(const uint8_t* A, const uint8_t* SA, const uint8_t* W, const uint8_t* SW, float* kv,
+                           int64_t T, int32_t K, int32_t N, int32_t* err_flag, engram_stream_t stream, bool pdl) {
+  if (T == 0) return ENGRAM_OK;
+  int rc = check_project_mx(A, SA, W, SW, kv, T, K, N);
+  if (rc) return rc;
+  GemmMxParams p{A, SA, W, SW, kv, T, K, N, err_flag};
+  return launch_gemm_mx(p, static_cast<cudaStream_t>(stream), pdl);
+}
+
+int engram_project_mxfp8(const uint8_t* A, const uint8_t* A_scales, const uint8_t* W, const uint8_t* W_scales,
+                         float* kv, int64_t T, int32_t K, int32_t N, int32_t* err_flag, engram_stream_t stream) {
+  return project_mx_impl(A, A_scales, W, W_scales, kv, T, K, N, err_flag, stream, false);
+}
+
+void engram_set_gemm_mx_tile(int32_t bn) { set_gemm_mx_bn_override((bn >= 16 && bn <= 256 && bn % 16 == 0) ? bn : 0); }
+
 size_t engram_forward_workspace_bytes(const EngramDims* d, int64_t T) {
   if (d == nullptr || T < 0) return 0;
   const int64_t C = (int64_t)(d->max_ngram - 1) * d->n_heads;
@@ -264,8 +333,17 @@ int engram_forward(const EngramDims* dims, const EngramHashTables* tables, const
     rc = check_gather(w.table_format, reinterpret_cast<const int32_t*>(16), (int64_t)L * C, T, C, dims->head_dim,
                       w.table, w.table_scales, w.table_rows, reinterpret_cast<const uint16_t*>(workspace));
     if (rc) return rc;
-    rc = check_project(reinterpret_cast<const uint16_t*>(workspace), w.wkv, reinterpret_cast<const float*>(workspace),
-                       T, (int32_t)K, (int32_t)N);
+    if (w.wkv_format == ENGRAM_WKV_MXFP8) {
+      ENGRAM_CHECK_ARG(w.table_format == ENGRAM_TABLE_FP8_E8M0,
+                       "layer %d: MXFP8 wkv needs an FP8+E8M0 table (its rows are the A operand)", l);
+      rc = check_project_mx(static_cast<const uint8_t*>(workspace), static_cast<const uint8_t*>(workspace),
+                            reinterpret_cast<const uint8_t*>(w.wkv), w.wkv_scales,
+                            reinterpret_cast<const float*>(workspace), T, (int32_t)K, (int32_t)N);
+    } else {
+      ENGRAM_CHECK_ARG(w.wkv_format == ENGRAM_WKV_BF16, "layer %d: unknown wkv format %d", l, w.wkv_format);
+      rc = check_project(reinterpret_cast<const uint16_t*>(workspace), w.wkv, reinterpret_cast<const float*>(workspace),
+                         T, (int32_t)K, (int32_t)N);
+    }
     if (rc) return rc;
     rc = check_gate(dims, streams[l], reinterpret_cast<const float*>(workspace), w.q_weight, w.k_weight, T);
     if (rc) return rc;
@@ -285,11 +363,24 @@ int engram_forward(const EngramDims* dims, const EngramHashTables* tables, const
   if (rc) return rc;
   for (int l = 0; l < L; ++l) {
     const EngramLayerWeights& w = layers[l];
-    rc = gather_impl(w.table_format, ids + (int64_t)l * C, (int64_t)L * C, T, C, dims->head_dim, w.table,
-                     w.table_scales, w.table_rows, A, err_flag, stream, true);
-    if (rc) return rc;
-    rc = project_impl(A, w.wkv, kv, T, (int32_t)K, (int32_t)N, gemm_ws, gemm_ws_bytes, err_flag, stream, true);
-    if (rc) return rc;
+    if (w.wkv_format == ENGRAM_WKV_MXFP8) {
+      // FP8 variant: the rows' codes and scales are the A operand as they are (the A region holds
+      // T*K codes, then the T*K/32 scale bytes)
+      uint8_t* codes = reinterpret_cast<uint8_t*>(A);
+      uint8_t* sa = codes + round256((size_t)(T * K));
+      rc = gather_codes_impl(ids + (int64_t)l * C, (int64_t)L * C, T, C, dims->head_dim, w.table, w.table_scales,
+                             w.table_rows, codes, sa, err_flag, stream, true);
+      if (rc) return rc;
+      rc = project_mx_impl(codes, sa, reinterpret_cast<const uint8_t*>(w.wkv), w.wkv_scales, kv, T, (int32_t)K,
+                           (int32_t)N, err_flag, stream, true);
+      if (rc) return rc;
+    } else {
+      rc = gather_impl(w.table_format, ids + (int64_t)l * C, (int64_t)L * C, T, C, dims->head_dim, w.table,
+                       w.table_scales, w.table_rows, A, err_flag, stream, true);
+      if (rc) return rc;
+      rc = project_impl(A, w.wkv, kv, T, (int32_t)K, (int32_t)N, gemm_ws, gemm_ws_bytes, err_flag, stream, true);
+      if (rc) return rc;
+    }
     rc = gate_impl(dims, streams[l], kv, w.q_weight, w.k_weight, tok->token_mask, T, err_flag, stream, true);
     if (rc) return rc;
   }

@@ -1,0 +1,435 @@
+// Stage 3, FP8 operand variant: kv[T, N] = A[T, K] * W[N, K]^T with both operands MXFP8 (e4m3
+// codes plus one power-of-two scale byte per 32 values along K), on tcgen05 tensor cores with
+// block scaling (tcgen05.mma kind::mxf8f6f4.block_scale.scale_vec::1X), fp32 out.
+//
+// The A operand is the FP8 table rows of the vLLM "deepseek_v41.common.engram" page
+// (ParallelEngramEmbedding: float8_e4m3fn weight, ue8m0 scale per 32 values) gathered without
+// dequantisation; W is wkv encoded the same way. Each product a * 2^sa * b * 2^sb is exact, so the
+// result is the projection of the dequantised operands with fp32 accumulation.
+//
+// A persistent data-parallel kernel, one CTA per SM, 10 warps:
+//   warp 0      TMA producer: 128B-swizzled K-major tiles of codes, 128 k per stage (one swizzle
+//               row per matrix row): A (128 rows per half) and W (BN rows). Under programmatic
+//               dependent launch the first ring of W tiles is requested before waiting for the
+//               kernel that writes A.
+//   warp 1      allocates all 512 tensor-memory columns; one lane issues the MMAs: per stage four
+//               k steps of 32, step s reading scale byte s of each 32-bit scale word.
+//   warps 2..5  epilogue: fp32 accumulators -> swizzled shared tile -> TMA bulk tensor store.
+//   warps 6..9  scale writers: per stage, each warp loads the stage's scale words of its TMEM lane
+//               quarter and stores them into that stage's scale slot with tcgen05.st. Layout
+//               (measured on this part): A row m reads lane m, column m / 32 of its slot; B row n
+//               reads, for accumulator lanes in quarter q, lane 32q + n % 32, column n / 32. So
+//               every quarter holds lane r, column c = scale word of A row r + 32c (per 128-row
+//               half) and of B row r + 32c.
+// Accumulators: two independent chains (the two 128-row halves of a 256-row tile, or for tiles of
+// at most 128 rows the even and odd k steps, summed in the epilogue) when tensor memory allows,
+// else one. All waits are bounded (~2 s of SM clock cycles); on expiry the CTA reports
+// ENGRAM_ERR_PIPE_TIMEOUT, drains what is in flight (bounded), frees tensor memory and exits.
+#include <mutex>
+
+#include "tc_common.cuh"
+
+namespace engram {
+namespace {
+
+constexpr int kStageK = 128;                 // k per stage: one 128-byte swizzle row of codes
+constexpr int kThreads = 320;
+constexpr int kEpiThreads = 128;
+constexpr int kMaxStages = 8;
+constexpr int kATileBytes = 128 * kStageK;   // 16 KB: 128 rows x 128 codes
+constexpr int kTmemCols = 512;
+
+struct MxCtl {
+  uint64_t full[kMaxStages];                 // TMA -> MMA: the stage's A and W codes landed
+  uint64_t empty[kMaxStages];                // MMA -> TMA / scale writers: stage and scale slot read
+  uint64_t sf_full[kMaxStages];              // scale writers -> MMA: the slot's scales are in TMEM
+  uint64_t acc_full;
+  uint64_t acc_empty;
+  uint32_t tmem_base;
+  int32_t abort_flag;
+};
+
+struct MxArgs {
+  int32_t M, K, N;
+  int32_t BN, msub, chains, stages, num_kb;
+  int32_t m_tiles, n_tiles, group_m;
+  int32_t a_bytes, b_bytes;
+  uint32_t idesc;
+  uint32_t acc_stride;                       // column of the second accumulator chain
+  uint32_t sf_base, sf_slot_w, sfb_off;      // scale slots: base column, width, W's offset in a slot
+  const uint32_t* sfa;                       // [M, K/128] scale words (bytes of 4 consecutive blocks)
+  const uint32_t* sfb;                       // [N, K/128]
+  int32_t* err;
+};
+
+__device__ __forceinline__ void mx_tile_origin(const MxArgs& a, int tile, int& m0, int& n0) {
+  const int per_group = a.group_m * a.n_tiles;
+  const int first_m = (tile / per_group) * a.group_m;
+  const int gsize = min(a.m_tiles - first_m, a.group_m);
+  const int in_group = tile % per_group;
+  m0 = (first_m + in_group % gsize) * 128 * a.msub;
+  n0 = (in_group / gsize) * a.BN;
+}
+
+__device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+wkv_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmD, float* __restrict__ D, const MxArgs a) {
+  if (a.err != nullptr && (*reinterpret_cast<volatile int32_t*>(a.err) & ENGRAM_ERR_PIPE_TIMEOUT)) {
+    pdl_wait();
+    return;
+  }
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t tiles = (raw_base + 1023u) & ~1023u;
+  const uint32_t stage_bytes = (uint32_t)(a.a_bytes + a.b_bytes);
+  const uint32_t epi_stage = tiles + (uint32_t)a.stages * stage_bytes;
+  MxCtl* ctl = reinterpret_cast<MxCtl*>(smem_raw + (epi_stage - raw_base) + kEpiBytes);
+  volatile int32_t* abort_flag = &ctl->abort_flag;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_tiles_total = a.m_tiles * a.n_tiles;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+      mbar_init(smem_u32(&ctl->sf_full[s]), 4);
+    }
+    mbar_init(smem_u32(&ctl->acc_full), 1);
+    mbar_init(smem_u32(&ctl->acc_empty), kEpiThreads);
+    ctl->abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmD);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&ctl->tmem_base)),
+                 "n"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      auto load_b = [&](int it, int kb, int n0) {
+        const int s = it % a.stages;
+        const uint32_t full = smem_u32(&ctl->full[s]);
+        mbar_expect_tx(full, stage_bytes);
+        tma_load_2d(tiles + (uint32_t)s * stage_bytes + (uint32_t)a.a_bytes, &tmB, full, kb * kStageK, n0);
+      };
+      auto load_a = [&](int it, int kb, int m0) {
+        const int s = it % a.stages;
+        const uint32_t full = smem_u32(&ctl->full[s]);
+        const uint32_t st = tiles + (uint32_t)s * stage_bytes;
+        for (int ms = 0; ms < a.msub; ++ms) tma_load_2d(st + ms * kATileBytes, &tmA, full, kb * kStageK, m0 + ms * 128);
+      };
+      // W does not come from the preceding kernel: fill the ring's W halves first
+      int early = 0;
+      for (int tile = blockIdx.x; tile < n_tiles_total && early < a.stages; tile += gridDim.x) {
+        int m0, n0;
+        mx_tile_origin(a, tile, m0, n0);
+        for (int kb = 0; kb < a.num_kb && early < a.stages; ++kb) load_b(early++, kb, n0);
+      }
+      pdl_wait();
+      int it = 0, issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < n_tiles_total; tile += gridDim.x) {
+        int m0, n0;
+        mx_tile_origin(a, tile, m0, n0);
+        if (tile + (int)gridDim.x >= n_tiles_total) pdl_trigger();   // last tile of this CTA
+        for (int kb = 0; kb < a.num_kb; ++kb, ++it) {
+          if (it < early) {
+            load_a(it, kb, m0);
+          } else {
+            const int s = it % a.stages;
+            const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+            if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, a.err, kWaitLimitCycles)) {
+              ok = false;
+              break;
+            }
+            load_b(it, kb, n0);
+            load_a(it, kb, m0);
+          }
+          issued = it + 1;
+        }
+      }
+      if (!ok) {
+        const int first = issued > a.stages ? issued - a.stages : 0;
+        for (int j = first; j < issued; ++j) {
+          volatile int32_t never = 0;
+          mbar_wait(smem_u32(&ctl->full[j % a.stages]), (uint32_t)(j / a.stages) & 1u, &never, nullptr,
+                    kWaitLimitCycles / 4);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      int n_items = 0, slot = 0;
+      uint32_t round = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < n_tiles_total; tile += gridDim.x) {
+        if (!mbar_wait(smem_u32(&ctl->acc_empty), (uint32_t)(n_items & 1) ^ 1u, abort_flag, a.err,
+                       kWaitLimitCycles)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < a.num_kb; ++kb) {
+          if (!mbar_wait(smem_u32(&ctl->full[slot]), round, abort_flag, a.err, kWaitLimitCycles) ||
+              !mbar_wait(smem_u32(&ctl->sf_full[slot]), round, abort_flag, a.err, kWaitLimitCycles)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = tiles + (uint32_t)slot * stage_bytes;
+          const uint64_t a0 = smem_desc_sw128(st);
+          const uint64_t b0 = smem_desc_sw128(st + (uint32_t)a.a_bytes);
+          const uint32_t sfa = tmem + a.sf_base + (uint32_t)slot * a.sf_slot_w;
+          const uint32_t sfb = sfa + a.sfb_off;
+#pragma unroll
+          for (int k = 0; k < kStageK / 32; ++k) {
+            // k step of 32 codes = 32 bytes = 2 in the encoded start address; scale byte k
+            const uint32_t idk = a.idesc | ((uint32_t)k << 29) | ((uint32_t)k << 4);
+            const uint64_t bdesc = b0 + (uint64_t)(2 * k);
+            if (a.msub == 2) {
+              const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
+              tc_mma_mx(tmem, a0 + (uint64_t)(2 * k), bdesc, idk, sfa, sfb, acc);
+              tc_mma_mx(tmem + a.acc_stride, a0 + (uint64_t)(2 * k + (kATileBytes >> 4)), bdesc, idk, sfa + 4, sfb, acc);
+            } else if (a.chains == 2) {
+              tc_mma_mx(tmem + (k & 1) * a.acc_stride, a0 + (uint64_t)(2 * k), bdesc, idk, sfa, sfb,
+                        (kb > 0 || k > 1) ? 1u : 0u);
+            } else {
+              tc_mma_mx(tmem, a0 + (uint64_t)(2 * k), bdesc, idk, sfa, sfb, (kb > 0 || k > 0) ? 1u : 0u);
+            }
+          }
+          tc_commit(smem_u32(&ctl->empty[slot]));   // stage and scale slot free once read
+          if (++slot == a.stages) {
+            slot = 0;
+            round ^= 1u;
+          }
+        }
+        tc_commit(smem_u32(&ctl->acc_full));
+        ++n_items;
+      }
+      if (!ok) tc_commit(smem_u32(&ctl->acc_full));
+    }
+  } else if (warp < 6) {
+    // ---------------- epilogue ----------------
+    const int q = warp & 3;
+    pdl_wait();                                // kv may still be read by an earlier kernel
+    const uint32_t stg = epi_stage + (uint32_t)(q * kEpiWarpBytes);
+    int n_items = 0;
+    for (int tile = blockIdx.x; tile < n_tiles_total; tile += gridDim.x) {
+      const bool ok = mbar_wait(smem_u32(&ctl->acc_full), (uint32_t)(n_items & 1), abort_flag, a.err,
+                                kWaitLimitCycles);
+      tc_fence_after();
+      if (!ok || *abort_flag) break;
+      int m0, n0;
+      mx_tile_origin(a, tile, m0, n0);
+      store_accumulators(&tmD, D, a.M, a.N, tmem, q, lane, stg, a.msub, a.msub == 1 && a.chains == 2, a.acc_stride,
+                         a.BN, m0, n0, false);
+      if (lane == 0) {
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // staging tile reusable
+      }
+      __syncwarp();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&ctl->acc_empty));  // tensor memory may take the next tile
+      ++n_items;
+    }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
+  } else {
+    // ---------------- scale writers ----------------
+    const int q = warp & 3;                    // TMEM lane quarter of this warp
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    pdl_wait();                                // A's scales come from the preceding kernel
+    int slot = 0;
+    uint32_t round = 0, it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < n_tiles_total; tile += gridDim.x) {
+      int m0, n0;
+      mx_tile_origin(a, tile, m0, n0);
+      for (int kb = 0; kb < a.num_kb; ++kb, ++it) {
+        // scale words of this stage: A rows m0 + 128h + lane + 32c, W rows n0 + lane + 32c
+        uint32_t va[2][4], vb[8];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int64_t row = (int64_t)m0 + 128 * h + lane + 32 * c;
+            va[h][c] = (h < a.msub && row < a.M) ? __ldg(a.sfa + row * a.num_kb + kb) : 0u;
+          }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int r = lane + 32 * c;
+          vb[c] = (r < a.BN && n0 + r < a.N) ? __ldg(a.sfb + (int64_t)(n0 + r) * a.num_kb + kb) : 0u;
+        }
+        if (it >= (uint32_t)a.stages &&
+            !mbar_wait(smem_u32(&ctl->empty[slot]), round ^ 1u, abort_flag, a.err, kWaitLimitCycles)) {
+          ok = false;
+          break;
+        }
+        const uint32_t col = a.sf_base + (uint32_t)slot * a.sf_slot_w;
+        tmem_st4(lane_base + col, va[0]);
+        if (a.msub == 2) tmem_st4(lane_base + col + 4, va[1]);
+        tmem_st8(lane_base + col + a.sfb_off, vb);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->sf_full[slot]));
+        if (++slot == a.stages) {
+          slot = 0;
+          round ^= 1u;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    if (*abort_flag) {
+      volatile int32_t never = 0;
+      for (int ph = 0; ph < 2; ++ph)
+        mbar_wait(smem_u32(&ctl->acc_full), (uint32_t)ph, &never, nullptr, kWaitLimitCycles / 8);
+    }
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
+  }
+}
+
+struct MxPlan {
+  MxArgs a;
+  int grid, smem;
+};
+
+int g_mx_bn_override = 0;
+
+// tile width: few waves of tiles over the SMs, within tensor memory (accumulator chains plus one
+// scale slot per stage) and shared memory
+bool plan_mx(int64_t M, int K, int N, int sms, MxPlan& P) {
+  MxArgs& a = P.a;
+  a = MxArgs{};
+  a.M = (int32_t)M;
+  a.K = K;
+  a.N = N;
+  a.msub = M > 128 ? 2 : 1;
+  a.m_tiles = (int32_t)((M + 128 * a.msub - 1) / (128 * a.msub));
+  a.num_kb = K / kStageK;
+  a.group_m = 16;
+  a.a_bytes = a.msub * kATileBytes;
+  a.sf_slot_w = (uint32_t)(4 * a.msub + 8);
+  a.sfb_off = (uint32_t)(4 * a.msub);
+  const int avail = kSmemBudget - 1024 - kEpiBytes - (int)sizeof(MxCtl);
+  int best = 0, best_chains = 0, best_stages = 0;
+  double best_cost = 1e300;
+  for (int bn = 256; bn >= 16; bn -= 16) {
+    if (g_mx_bn_override > 0 && bn != g_mx_bn_override) continue;
+    int stages = avail / (a.a_bytes + bn * kStageK);
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages < 2) continue;
+    const int stride = ((bn + 31) / 32) * 32;
+    int chains = 2;
+    if (2 * stride + stages * (int)a.sf_slot_w > kTmemCols) {
+      if (a.msub == 2) continue;             // both halves need their own accumulator
+      chains = 1;
+      if (stride + stages * (int)a.sf_slot_w > kTmemCols) continue;
+    }
+    const int64_t tiles = (int64_t)a.m_tiles * ((N + bn - 1) / bn);
+    const int64_t waves = (tiles + sms - 1) / sms;
+    const double cost = (double)waves * (bn + 48);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = bn;
+      best_chains = chains;
+      best_stages = stages;
+    }
+  }
+  if (best == 0) return false;
+  a.BN = best;
+  a.chains = best_chains;
+  a.stages = best_stages;
+  a.b_bytes = a.BN * kStageK;
+  a.acc_stride = (uint32_t)(((a.BN + 31) / 32) * 32);
+  a.sf_base = (uint32_t)a.chains * a.acc_stride;
+  a.n_tiles = (N + a.BN - 1) / a.BN;
+  const int64_t tiles = (int64_t)a.m_tiles * a.n_tiles;
+  if (tiles > 0x7fffffff) return false;
+  P.grid = tiles < sms ? (int)tiles : sms;
+  a.idesc = ((uint32_t)(a.BN >> 3) << 17)    // N
+            | (1u << 23)                     // scales are UE8M0
+            | ((uint32_t)(128 >> 4) << 24);  // M = 128; A and W e4m3 (format 0), K-major
+  P.smem = 1024 + a.stages * (a.a_bytes + a.b_bytes) + kEpiBytes + (int)sizeof(MxCtl);
+  return true;
+}
+
+}  // namespace
+
+void set_gemm_mx_bn_override(int bn) { g_mx_bn_override = bn; }
+
+int launch_gemm_mx(const GemmMxParams& p, cudaStream_t stream, bool pdl) {
+  MxPlan P;
+  if (!plan_mx(p.M, p.K, p.N, num_sms(), P)) {
+    set_error("engram_project_mxfp8: no tile plan fits (T %lld, K %d, N %d)", (long long)p.M, p.K, p.N);
+    return ENGRAM_EINVAL;
+  }
+  MxArgs a = P.a;
+  a.err = p.err;
+  a.sfa = reinterpret_cast<const uint32_t*>(p.SA);
+  a.sfb = reinterpret_cast<const uint32_t*>(p.SB);
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    cudaError_t e =
+        cudaFuncSetAttribute(wkv_gemm_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+    if (e != cudaSuccess) return fail_cuda(e, "engram_project_mxfp8: cudaFuncSetAttribute");
+    if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
+  CUtensorMap mA, mB, mD;
+  if (!make_map_u8(&mA, p.A, p.M, p.K, 128) || !make_map_u8(&mB, p.B, p.N, p.K, (uint32_t)a.BN) ||
+      !make_map_f32(&mD, p.D, p.M, p.N)) {
+    set_error("engram_project_mxfp8: cuTensorMapEncodeTiled failed (driver entry point missing or bad layout)");
+    return ENGRAM_ECUDA;
+  }
+  cudaError_t e = launch_k(wkv_gemm_mx_kernel, dim3((unsigned)P.grid), dim3(kThreads), (size_t)P.smem, stream, pdl,
+                           mA, mB, mD, p.D, a);
+  if (e != cudaSuccess) return fail_cuda(e, "engram_project_mxfp8: launch");
+  return ENGRAM_OK;
+}
+
+}  // namespace engram

@@ -93,12 +93,41 @@ struct GemmParams {
   int64_t M;
   int32_t K, N;
   int32_t* err;
-  void* workspace;      // stream-K partials and flags (may be NULL)
+  void* workspace;      // stream-K flags (may be NULL)
   size_t ws_bytes;
 };
 // returns ENGRAM_OK or an error code (sets the message)
 int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl = false);
 size_t gemm_workspace_bytes(int64_t M, int K, int N);
+
+// ---- FP8 (MXFP8) operand variant of the projection -----------------------------------------
+struct GatherCodesParams {
+  const int32_t* ids;
+  int64_t ids_stride_t;
+  int64_t T;
+  int32_t C, D;
+  const void* table;          // e4m3 codes [rows, D]
+  const uint8_t* scales;      // [rows, D/32]
+  int64_t num_rows;
+  uint8_t* codes;             // [T, C*D]
+  uint8_t* out_scales;        // [T, C*D/32]
+  int32_t* err;
+};
+cudaError_t launch_gather_codes(const GatherCodesParams& p, cudaStream_t stream, bool pdl = false);
+cudaError_t launch_quantize_mxfp8(const uint16_t* w, int64_t N, int32_t K, uint8_t* codes, uint8_t* scales,
+                                  cudaStream_t stream);
+
+struct GemmMxParams {
+  const uint8_t* A;           // e4m3 codes [M, K]
+  const uint8_t* SA;          // scale bytes [M, K/32]
+  const uint8_t* B;           // e4m3 codes [N, K]
+  const uint8_t* SB;          // scale bytes [N, K/32]
+  float* D;                   // [M, N]
+  int64_t M;
+  int32_t K, N;
+  int32_t* err;
+};
+int launch_gemm_mx(const GemmMxParams& p, cudaStream_t stream, bool pdl = false);
 
 struct GateParams {
   float* streams;

@@ -43,7 +43,7 @@ extern "C" {
 /* bits of the device err_flag word */
 #define ENGRAM_ERR_RAW_ID 1        /* raw input id outside [0, raw_vocab): used pad_id */
 #define ENGRAM_ERR_ROW_ID 2        /* row id outside [0, num_rows): wrote a zero row */
-#define ENGRAM_ERR_PIPE_TIMEOUT 4  /* a GEMM pipeline wait ran past its time limit */
+#define ENGRAM_ERR_PIPE_TIMEOUT 4  /* a pipeline wait (GEMM, gate) ran past its time limit */
 
 typedef void* engram_stream_t; /* a cudaStream_t */
 
@@ -52,6 +52,12 @@ enum EngramTableFmt {
   ENGRAM_TABLE_BF16 = 0,    /* bf16 [rows, head_dim] */
   ENGRAM_TABLE_FP8_E8M0 = 1,/* e4m3 [rows, head_dim] + one E8M0 byte per 32 values [rows, head_dim/32] */
   ENGRAM_TABLE_Q2K = 2      /* one 84-byte Q2_K super-block per 256-wide row [rows, 84] */
+};
+
+/* wkv formats (EngramLayerWeights.wkv_format). */
+enum EngramWkvFmt {
+  ENGRAM_WKV_BF16 = 0,      /* bf16 [N, K] */
+  ENGRAM_WKV_MXFP8 = 1      /* e4m3 codes [N, K] + one power-of-two scale byte per 32 along K [N, K/32] */
 };
 
 /*
@@ -173,6 +179,44 @@ void engram_set_gemm_tile(int32_t bn);
 void engram_set_gemm_schedule(int32_t s);
 
 /*
+ * FP8 operand variant of stage 3 (MXFP8). The FP8 table of [vLLM] ParallelEngramEmbedding
+ * (float8_e4m3fn weight, one ue8m0 scale per 32 values) already is an MXFP8 operand; this
+ * variant gathers its rows without dequantising them and multiplies them with a wkv stored the
+ * same way on the tensor cores' block-scaled path (tcgen05.mma kind::mxf8f6f4), fp32 out. The
+ * result equals the projection of the dequantised operands with fp32 accumulation. It needs no
+ * workspace. Scale bytes are E8M0 exponents (value = code * 2^(byte - 127)).
+ */
+
+/* wkv bf16 [N, K] -> MXFP8: codes uint8 [N, K] (e4m3) and scales uint8 [N, K/32]. Per row and
+ * block of 32 along K, the scale is the smallest power of two 2^e with max|w| / 2^e <= 448 (byte
+ * 127 + e; the table's own scale convention, so no value saturates) and each code is w / 2^e
+ * rounded to the nearest e4m3 value, ties to even; an all-zero block gets byte 127 and zero codes.
+ * K % 32 == 0. Device pointers; deterministic. */
+int engram_quantize_mxfp8(const uint16_t* w, int64_t N, int32_t K, uint8_t* codes, uint8_t* scales,
+                          engram_stream_t stream);
+
+/* Stage 2 for the FP8 variant: like engram_gather_dequant for an FP8_E8M0 table, but the rows'
+ * codes and scale bytes are copied as they are: codes uint8 [T, C*head_dim], scales uint8
+ * [T, C*head_dim/32]. Ids outside [0, num_rows) give a zero row (codes 0, scale byte 127) and set
+ * ENGRAM_ERR_ROW_ID. head_dim % 32 == 0; table and codes 16-byte aligned. */
+int engram_gather_fp8_codes(const int32_t* ids, int64_t ids_stride_t, int64_t T, int32_t C,
+                            int32_t head_dim, const void* table, const uint8_t* table_scales,
+                            int64_t num_rows, uint8_t* codes, uint8_t* scales, int32_t* err_flag,
+                            engram_stream_t stream);
+
+/* Stage 3, FP8 variant: kv fp32 [T, N] = A * W^T with A codes [T, K] + A_scales [T, K/32] (from
+ * engram_gather_fp8_codes) and W codes [N, K] + W_scales [N, K/32] (from engram_quantize_mxfp8).
+ * K % 128 == 0, N % 16 == 0; A, W, kv 16-byte aligned, scales 4-byte aligned. err_flag as for
+ * engram_project. */
+int engram_project_mxfp8(const uint8_t* A, const uint8_t* A_scales, const uint8_t* W,
+                         const uint8_t* W_scales, float* kv, int64_t T, int32_t K, int32_t N,
+                         int32_t* err_flag, engram_stream_t stream);
+
+/* Tuning knob for engram_project_mxfp8: force the tile width (a multiple of 16 in [16, 256] that
+ * fits tensor memory); 0 restores the automatic choice. Process-wide. */
+void engram_set_gemm_mx_tile(int32_t bn);
+
+/*
  * Stage 4: gate, in place on the fp32 highway ([NeMo] _engram_gate_core; [vLLM]
  * Engram.forward; [Atlas] stage 4). For each token t with token_mask[t] != 0 and stream j:
  *   s   = <h_j * rsqrt(mean(h_j^2)+eps) * q_weight[j], key_j * rsqrt(mean(key_j^2)+eps) * k_weight[j]> / sqrt(H)
@@ -198,9 +242,11 @@ typedef struct EngramLayerWeights {
   const void* table;           /* device, see engram_gather_dequant */
   const uint8_t* table_scales; /* device, FP8_E8M0 only */
   int64_t table_rows;
-  const uint16_t* wkv;         /* device bf16 [(hc+1)*H, C*head_dim] */
+  const uint16_t* wkv;         /* device [(hc+1)*H, C*head_dim]: bf16, or e4m3 codes (MXFP8) */
   const uint16_t* q_weight;    /* device bf16 [hc, H] */
   const uint16_t* k_weight;    /* device bf16 [hc, H] */
+  int32_t wkv_format;          /* EngramWkvFmt; MXFP8 needs an FP8_E8M0 table and K % 128 == 0 */
+  const uint8_t* wkv_scales;   /* device [(hc+1)*H, C*head_dim/32], MXFP8 only */
 } EngramLayerWeights;
 
 /* Hash tables ([Atlas] EngramHashTables). All device memory. */

@@ -58,8 +58,9 @@ def build(name_or_w, device="cuda", seq_lens=None, seed=None):
     return w, case, (primes, offsets, rows, mult)
 
 
-def gpu_forward(w, case, setup, device="cuda", with_err=True):
-    """Run engram_forward on the device; returns ids, per-layer streams, the workspace views."""
+def gpu_forward(w, case, setup, device="cuda", with_err=True, mx=False):
+    """Run engram_forward on the device; returns ids, per-layer streams, the workspace views.
+    With ``mx`` the layers carry MXFP8 wkv (quantised on the device) and the FP8 variant runs."""
     import engram_gram_hash_02_gb300 as E
     primes, offsets, rows, mult = setup
     b = case.batch
@@ -67,8 +68,13 @@ def gpu_forward(w, case, setup, device="cuda", with_err=True):
     dims = dims_for(w, pad)
     tables = E.HashTables(to_device(b["token_map"], device), to_device(mult, device),
                           to_device(primes, device), to_device(offsets, device))
-    layers = [E.LayerWeights(t["fmt"], t["table"], t["scales"], t["num_rows"], case.wkv[l], case.q_weight[l],
-                             case.k_weight[l]) for l, t in enumerate(case.tables)]
+    layers = []
+    for l, t in enumerate(case.tables):
+        wkv, wsc = case.wkv[l], None
+        if mx:
+            wkv, wsc = E.quantize_mxfp8(case.wkv[l])
+        layers.append(E.LayerWeights(t["fmt"], t["table"], t["scales"], t["num_rows"], wkv, case.q_weight[l],
+                                     case.k_weight[l], wkv_scales=wsc))
     streams = [s.clone() for s in case.streams]
     err = torch.zeros(1, dtype=torch.int32, device=device) if with_err else None
     out_ids = torch.empty((w.tokens, w.layers, w.cols), dtype=torch.int32, device=device)
@@ -82,10 +88,24 @@ def gpu_forward(w, case, setup, device="cuda", with_err=True):
     T, K, N = w.tokens, w.K, w.N
     id_bytes = ((T * w.layers * w.cols * 4 + 255) // 256) * 256
     a_bytes = ((T * K * 2 + 255) // 256) * 256
-    A_last = ws[id_bytes:id_bytes + T * K * 2].view(torch.bfloat16).view(T, K)
     kv_last = ws[id_bytes + a_bytes:id_bytes + a_bytes + T * N * 4].view(torch.float32).view(T, N)
-    return {"ids": out_ids, "streams": streams, "A_last": A_last, "kv_last": kv_last,
-            "err": int(err.item()) if err is not None else 0, "dims": dims}
+    out = {"ids": out_ids, "streams": streams, "kv_last": kv_last, "err": int(err.item()) if err is not None else 0,
+           "dims": dims}
+    if mx:
+        code_bytes = ((T * K + 255) // 256) * 256
+        out["A_codes_last"] = ws[id_bytes:id_bytes + T * K].view(T, K)
+        out["A_scales_last"] = ws[id_bytes + code_bytes:id_bytes + code_bytes + T * K // 32].view(T, K // 32)
+    else:
+        out["A_last"] = ws[id_bytes:id_bytes + T * K * 2].view(torch.bfloat16).view(T, K)
+    return out
+
+
+def oracle_mxfp8_quantize(wkv: torch.Tensor, rows: int = 2048):
+    """The oracle's MXFP8 encoding of a bf16 weight, a block of rows at a time (rows are
+    independent; this bounds the fp64 temporaries)."""
+    bits = bits16(wkv)
+    parts = [O.mxfp8_quantize(bits[i:i + rows]) for i in range(0, bits.shape[0], rows)]
+    return np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts])
 
 
 def compact_table(tab: dict, ids: np.ndarray):
@@ -106,8 +126,9 @@ def compact_table(tab: dict, ids: np.ndarray):
     return t_np, s_np, remap.reshape(ids.shape), len(uniq)
 
 
-def oracle_forward(w, case, tokens=None):
-    """The oracle's whole path on the selected tokens (all if None), from its own layout."""
+def oracle_forward(w, case, tokens=None, mx=False):
+    """The oracle's whole path on the selected tokens (all if None), from its own layout. With
+    ``mx``, the FP8 variant: raw FP8 rows and the oracle's own MXFP8 encoding of wkv."""
     primes, offsets, rows, mult = oracle_setup(w)
     b = case.batch
     pad = pad_id_of(w, b["token_map"])
@@ -120,8 +141,14 @@ def oracle_forward(w, case, tokens=None):
     layers = []
     for l, tab in enumerate(case.tables):
         t_np, s_np, remap, nrows = compact_table(tab, ids[sel, l, :])
-        a_bits, n_oob = O.gather(tab["fmt"], t_np, s_np, remap, nrows, w.head_dim)
-        kv = O.project(a_bits, bits16(case.wkv[l]))
+        if mx:
+            codes, sc, n_oob = O.gather_fp8_raw(t_np, s_np, remap, nrows)
+            wc, ws_ = oracle_mxfp8_quantize(case.wkv[l])
+            kv = O.project_mxfp8(codes, sc, wc, ws_)
+            a_bits = (codes, sc)
+        else:
+            a_bits, n_oob = O.gather(tab["fmt"], t_np, s_np, remap, nrows, w.head_dim)
+            kv = O.project(a_bits, bits16(case.wkv[l]))
         h0 = case.streams[l][torch.from_numpy(sel).to(case.streams[l].device)].cpu().numpy()
         out, g = O.gate(h0, kv, bits16(case.q_weight[l]), bits16(case.k_weight[l]), w.eps, w.clamp,
                         None if mask is None else mask[sel])

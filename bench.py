@@ -132,7 +132,7 @@ class ClockSampler:
 class Path:
     """Device-resident workload plus pre-marshalled C-ABI calls for each stage."""
 
-    def __init__(self, w, device, table_rows=None):
+    def __init__(self, w, device, table_rows=None, wkv="bf16"):
         import ctypes as C
 
         import engram_gram_hash_02_gb300 as E
@@ -159,12 +159,23 @@ class Path:
         self.lookback = to_device(b["lookback_ids"], d)
         self.tables = E.HashTables(to_device(b["token_map"], d), to_device(mult, d), to_device(primes, d),
                                    to_device(offsets, d))
-        self.layers = [E.LayerWeights(t["fmt"], t["table"], t["scales"], t["num_rows"], case.wkv[l],
-                                      case.q_weight[l], case.k_weight[l]) for l, t in enumerate(case.tables)]
+        self.mx = wkv == "mxfp8"
+        if self.mx and any(t["fmt"] != "fp8" for t in case.tables):
+            raise SystemExit("--wkv mxfp8 needs an FP8+E8M0 table (its rows are the projection's A operand)")
+        self.layers = []
+        for l, t in enumerate(case.tables):
+            wkv_l, wsc = case.wkv[l], None
+            if self.mx:                   # weight preparation, once, outside every timed region
+                wkv_l, wsc = E.quantize_mxfp8(case.wkv[l])
+            self.layers.append(E.LayerWeights(t["fmt"], t["table"], t["scales"], t["num_rows"], wkv_l,
+                                              case.q_weight[l], case.k_weight[l], wkv_scales=wsc))
         self.streams = [s.clone() for s in case.streams]
         T, L, Cc, K, N = w.tokens, w.layers, w.cols, w.K, w.N
         self.ids = torch.empty((T, L, Cc), dtype=torch.int32, device=d)
         self.A = torch.empty((T, K), dtype=torch.bfloat16, device=d)
+        if self.mx:                       # FP8 variant: codes [T, K] and scales [T, K/32] of the rows
+            self.A_codes = torch.empty((T, K), dtype=torch.uint8, device=d)
+            self.A_scales = torch.empty(E.mx_scale_shape(T, K), dtype=torch.uint8, device=d)
         self.kv = torch.empty((T, N), dtype=torch.float32, device=d)
         self.err = torch.zeros(1, dtype=torch.int32, device=d)
         self.gemm_ws = torch.empty(max(256, E.project_workspace_bytes(T, K, N)), dtype=torch.uint8, device=d)
@@ -194,25 +205,43 @@ class Path:
             pr_args = (p(self.A), p(lw.wkv), p(self.kv), T, K, N, p(self.gemm_ws), self.gemm_ws.numel(), p(self.err), s)
             ga_args = (C.byref(dims), p(self.streams[l]), p(self.kv), p(lw.q_weight), p(lw.k_weight),
                        p(self.mask), T, p(self.err), s)
-            calls.append((f"gather{l}", lambda a=g_args: lib.engram_gather_dequant(*a)))
-            calls.append((f"project{l}", lambda a=pr_args: lib.engram_project(*a)))
+            if self.mx:
+                gc_args = (self.ids.data_ptr() + 4 * l * Cc, L * Cc, T, Cc, w.head_dim, p(lw.table), p(lw.scales),
+                           int(lw.num_rows), p(self.A_codes), p(self.A_scales), p(self.err), s)
+                pm_args = (p(self.A_codes), p(self.A_scales), p(lw.wkv), p(lw.wkv_scales), p(self.kv), T, K, N,
+                           p(self.err), s)
+                calls.append((f"gather{l}", lambda a=gc_args: lib.engram_gather_fp8_codes(*a)))
+                calls.append((f"project{l}", lambda a=pm_args: lib.engram_project_mxfp8(*a)))
+            else:
+                calls.append((f"gather{l}", lambda a=g_args: lib.engram_gather_dequant(*a)))
+                calls.append((f"project{l}", lambda a=pr_args: lib.engram_project(*a)))
             calls.append((f"gate{l}", lambda a=ga_args: lib.engram_gate(*a)))
         return calls
 
 
-def stage_model(w, name, peaks_d):
-    """Algorithmic bytes / flops of one launch of a stage at workload w."""
+# FP8 dense tensor peak: the measured bf16 peak times the nominal fp8 / bf16 ratio (4.5 / 2.25)
+FP8_OVER_BF16 = 2.0
+
+
+def tensor_peak(peaks_d, mx: bool) -> float:
+    return peaks_d["bf16_tflops"] * (FP8_OVER_BF16 if mx else 1.0)
+
+
+def stage_model(w, name, peaks_d, mx: bool = False):
+    """Algorithmic bytes / flops of one launch of a stage at workload w (``mx``: the FP8 variant,
+    MXFP8 codes plus one scale byte per 32 values for both projection operands)."""
     T, L, Cc, D, K, N, H, hc = w.tokens, w.layers, w.cols, w.head_dim, w.K, w.N, w.hidden, w.hc
     row = {"fp8": D + D // 32, "q2k": 84, "bf16": 2 * D}[w.table_format]
+    op = (K + K // 32) if mx else 2 * K              # bytes of one operand row
     if name == "hash":
         return {"bytes": 8 * T + 4 * T * L * Cc, "flops": 0, "bound": "alu"}
     if name.startswith("gather"):
-        return {"bytes": T * Cc * (row + 4) + 2 * T * K, "flops": 0, "bound": "hbm"}
+        return {"bytes": T * Cc * (row + 4) + T * op, "flops": 0, "bound": "hbm"}
     if name.startswith("project"):
-        by = 2 * N * K + 2 * T * K + 4 * T * N
+        by = N * op + T * op + 4 * T * N
         fl = 2 * T * N * K
         t_hbm = by / (peaks_d["hbm_gbs"] * 1e9)
-        t_tc = fl / (peaks_d["bf16_tflops"] * 1e12)
+        t_tc = fl / (tensor_peak(peaks_d, mx) * 1e12)
         return {"bytes": by, "flops": fl, "bound": "hbm" if t_hbm >= t_tc else "tensor"}
     if name.startswith("gate"):
         return {"bytes": 8 * hc * H * T + 4 * N * T + 4 * hc * H, "flops": 8 * hc * H * T, "bound": "hbm"}
@@ -228,7 +257,8 @@ def kernel_src(name):
 
 def run_ours(args, rank, world, device):
     w = get_workload(args.workload)
-    path = Path(w, device)
+    path = Path(w, device, wkv=args.wkv)
+    mx = path.mx
     stream = torch.cuda.current_stream()
     calls = path.stage_calls(stream)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
@@ -305,29 +335,29 @@ def run_ours(args, rank, world, device):
         return None
     pk, pk_kind = peaks()
     dom = max(per_kernel, key=per_kernel.get)
-    model = stage_model(w, dom, pk)
+    model = stage_model(w, dom, pk, mx)
     t_s = per_kernel[dom] / 1e3
     if model["bound"] == "tensor":
-        achieved, peak, unit = model["flops"] / t_s / 1e12, pk["bf16_tflops"], "TFLOP/s"
+        achieved, peak, unit = model["flops"] / t_s / 1e12, tensor_peak(pk, mx), "TFLOP/s"
     elif model["bound"] == "hbm":
         achieved, peak, unit = model["bytes"] / t_s / 1e9, pk["hbm_gbs"], "GB/s"
     else:
         achieved, peak, unit = model["bytes"] / t_s / 1e9, None, "GB/s"
-    key = f"{dom}@{w.name}"
+    key = f"{dom}@{w.name}" + ("@mxfp8" if mx else "")
     traffic = None
     rec = NCU_TRAFFIC.get(key)
     if rec and rec.get("src_sha") == src_sha(kernel_src(dom)):
         traffic = rec["bytes"]
     stages = {}
     for name, t in per_kernel.items():
-        m = stage_model(w, name, pk)
+        m = stage_model(w, name, pk, mx)
         gbs = m["bytes"] / (t / 1e3) / 1e9
         stages[name] = {"us": round(t * 1e3, 2), "GB/s": round(gbs, 1), "bound": m["bound"]}
         if m["flops"] and name.startswith("project"):
             tfs = m["flops"] / (t / 1e3) / 1e12
             stages[name]["TFLOP/s"] = round(tfs, 1)
             if m["bound"] == "tensor":
-                stages[name]["frac"] = round(tfs / pk["bf16_tflops"], 4)
+                stages[name]["frac"] = round(tfs / tensor_peak(pk, mx), 4)
         if m["bound"] == "hbm":
             stages[name]["frac"] = round(gbs / pk["hbm_gbs"], 4)
     line = {
@@ -342,17 +372,19 @@ def run_ours(args, rank, world, device):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "e4m3 x e4m3 (MXFP8), fp32 accumulate" if mx else "bf16",
         "data": "synthetic (seeded; tables, weights and ids drawn on device)",
         "config": {"workload": w.name, "tokens": w.tokens, "layers": w.layers, "hash_cols": w.cols,
                    "head_dim": w.head_dim, "table": w.table_format, "table_rows": int(sum(path.table_rows)),
                    "hidden": w.hidden, "hc": w.hc, "K": w.K, "N": w.N,
+                   "wkv": "mxfp8" if mx else "bf16",
                    "l2": "flushed before every timed step (512 MB write)", "parallelism": f"replicas{world}"},
         "gpu_launches": 2 * args.steps * len(calls),
         "stages": stages,
         "roofline": {"kernel": dom, "bound": model["bound"], "achieved": round(achieved, 1),
                      "peak": peak, "unit": unit, "frac": None if peak is None else round(achieved / peak, 4),
-                     "peak_source": f"{pk_kind} ({'hbm_gbs' if unit == 'GB/s' else 'bf16_tflops'}, burst)",
+                     "peak_source": f"{pk_kind} ({'hbm_gbs' if unit == 'GB/s' else 'bf16_tflops'}, burst)"
+                                    + (" x 2 (nominal fp8 / bf16)" if unit != 'GB/s' and mx else ""),
                      "algorithmic_bytes": model["bytes"], "algorithmic_flops": model["flops"],
                      "traffic": traffic},
         "clocks": clocks,
@@ -369,7 +401,7 @@ def run_ours(args, rank, world, device):
 
 def run_only(args, device):
     """Run one stage alone (for short profiler captures); prints its mean time."""
-    path = Path(get_workload(args.workload), device, args.table_rows)
+    path = Path(get_workload(args.workload), device, args.table_rows, wkv=args.wkv)
     w = path.w
     stream = torch.cuda.current_stream()
     all_calls = path.stage_calls(stream)
@@ -548,6 +580,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_fp8_t256")
+    ap.add_argument("--wkv", choices=["bf16", "mxfp8"], default="bf16",
+                    help="wkv format: bf16 (the workloads' own), or MXFP8 (the FP8 operand variant)")
     ap.add_argument("--cpu-tokens", type=int, default=32)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

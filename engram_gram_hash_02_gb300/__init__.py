@@ -25,6 +25,7 @@ from .binding import (  # noqa: F401
     hash_multipliers,
     lib,
     make_dims,
+    mx_scale_shape,
     project_workspace_bytes,
     quantize_mxfp8,
     set_gemm_mx_tile,

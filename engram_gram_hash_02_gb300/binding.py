@@ -260,12 +260,19 @@ def set_gemm_schedule(s: int = 0):
     lib().engram_set_gemm_schedule(int(s))
 
 
+def mx_scale_shape(rows: int, K: int):
+    """Shape of an MXFP8 scale array: [ceil(K/128), rows rounded up to 4, 4] bytes; byte
+    (kb, r, j) is the scale of row r's block of 32 columns 4*kb + j."""
+    return ((K // 32 + 3) // 4, (rows + 3) // 4 * 4, 4)
+
+
 def quantize_mxfp8(w: torch.Tensor, codes=None, scales=None, stream=None):
-    """bf16 [N, K] -> (e4m3 codes uint8 [N, K], scale bytes uint8 [N, K/32]) (engram_quantize_mxfp8)."""
+    """bf16 [N, K] -> (e4m3 codes uint8 [N, K], scales uint8 ``mx_scale_shape(N, K)``)
+    (engram_quantize_mxfp8)."""
     _u16(w, "w")
     N, K = w.shape
     codes = torch.empty(N, K, dtype=torch.uint8, device=w.device) if codes is None else _dev(codes, torch.uint8, "codes")
-    scales = (torch.empty(N, K // 32, dtype=torch.uint8, device=w.device) if scales is None
+    scales = (torch.empty(mx_scale_shape(N, K), dtype=torch.uint8, device=w.device) if scales is None
               else _dev(scales, torch.uint8, "scales"))
     _check("engram_quantize_mxfp8", lib().engram_quantize_mxfp8(_ptr(w), N, K, _ptr(codes), _ptr(scales),
                                                                _stream(stream)))
@@ -275,7 +282,7 @@ def quantize_mxfp8(w: torch.Tensor, codes=None, scales=None, stream=None):
 def engram_gather_fp8_codes(ids, table, table_scales, num_rows: int, head_dim: int, codes=None, scales=None,
                             err=None, stream=None):
     """FP8 rows by id without dequantisation. ids int32 [T, C] (or a [T, L*C] slice: the row
-    stride is ids.stride(0)) -> (codes uint8 [T, C*head_dim], scales uint8 [T, C*head_dim/32])."""
+    stride is ids.stride(0)) -> (codes uint8 [T, C*head_dim], scales ``mx_scale_shape(T, C*head_dim)``)."""
     if not isinstance(ids, torch.Tensor) or ids.dtype != torch.int32 or not ids.is_cuda or ids.stride(1) != 1:
         raise ValueError("ids must be a CUDA int32 tensor with unit column stride")
     T, Cc = ids.shape
@@ -284,7 +291,7 @@ def engram_gather_fp8_codes(ids, table, table_scales, num_rows: int, head_dim: i
     _opt(err, torch.int32, "err")
     codes = (torch.empty(T, Cc * head_dim, dtype=torch.uint8, device=ids.device) if codes is None
              else _dev(codes, torch.uint8, "codes"))
-    scales = (torch.empty(T, Cc * head_dim // 32, dtype=torch.uint8, device=ids.device) if scales is None
+    scales = (torch.empty(mx_scale_shape(T, Cc * head_dim), dtype=torch.uint8, device=ids.device) if scales is None
               else _dev(scales, torch.uint8, "scales"))
     _check("engram_gather_fp8_codes", lib().engram_gather_fp8_codes(
         _ptr(ids), ids.stride(0), T, Cc, head_dim, _ptr(table), _ptr(table_scales), int(num_rows), _ptr(codes),

@@ -239,6 +239,7 @@ int engram_gate(const EngramDims* dims, float* streams, const float* kv, const u
 int engram_quantize_mxfp8(const uint16_t* w, int64_t N, int32_t K, uint8_t* codes, uint8_t* scales,
                           engram_stream_t stream) {
   ENGRAM_CHECK_ARG(N >= 0 && K >= 32 && K % 32 == 0, "engram_quantize_mxfp8: need N >= 0 and K a multiple of 32 (got %d)", K);
+  ENGRAM_CHECK_ARG(aligned(scales, 4), "engram_quantize_mxfp8: scales must be 4-byte aligned");
   if (N == 0) return ENGRAM_OK;
   ENGRAM_CHECK_ARG(w && codes && scales, "engram_quantize_mxfp8: w, codes and scales must be non-NULL");
   cudaError_t e = launch_quantize_mxfp8(w, N, K, codes, scales, static_cast<cudaStream_t>(stream));
@@ -253,7 +254,8 @@ static int check_gather_codes(const int32_t* ids, int64_t ids_stride_t, int64_t 
   ENGRAM_CHECK_ARG(D >= 32 && D % 32 == 0, "FP8 head_dim must be a multiple of 32 (got %d)", D);
   ENGRAM_CHECK_ARG(num_rows >= 0, "num_rows must be >= 0");
   ENGRAM_CHECK_ARG(ids && table && scales && codes && out_scales, "ids, table, scales and outputs must be non-NULL");
-  ENGRAM_CHECK_ARG(aligned(table, 16) && aligned(codes, 16), "table and codes must be 16-byte aligned");
+  ENGRAM_CHECK_ARG(aligned(table, 16) && aligned(codes, 16) && aligned(out_scales, 16),
+                   "table, codes and scales must be 16-byte aligned");
   return ENGRAM_OK;
 }
 
@@ -282,7 +284,7 @@ static int check_project_mx(const uint8_t* A, const uint8_t* SA, const uint8_t* 
   ENGRAM_CHECK_ARG(N >= 16 && N % 16 == 0, "N must be a positive multiple of 16 (got %d)", N);
   ENGRAM_CHECK_ARG(A && SA && W && SW && kv, "A, A_scales, W, W_scales and kv must be non-NULL");
   ENGRAM_CHECK_ARG(aligned(A, 16) && aligned(W, 16) && aligned(kv, 16), "A, W and kv must be 16-byte aligned");
-  ENGRAM_CHECK_ARG(aligned(SA, 4) && aligned(SW, 4), "A_scales and W_scales must be 4-byte aligned");
+  ENGRAM_CHECK_ARG(aligned(SA, 16) && aligned(SW, 16), "A_scales and W_scales must be 16-byte aligned");
   return ENGRAM_OK;
 }
 

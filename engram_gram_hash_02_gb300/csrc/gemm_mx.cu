@@ -9,14 +9,15 @@
 //
 // A persistent data-parallel kernel, one CTA per SM, 10 warps:
 //   warp 0      TMA producer: 128B-swizzled K-major tiles of codes, 128 k per stage (one swizzle
-//               row per matrix row): A (128 rows per half) and W (BN rows). Under programmatic
-//               dependent launch the first ring of W tiles is requested before waiting for the
-//               kernel that writes A.
+//               row per matrix row): A (128 rows per half) and W (BN rows), plus the stage's scale
+//               words of both (one contiguous run each in the [K/128][rows4] word layout, 1-D bulk
+//               copies). Under programmatic dependent launch the first ring of W tiles and scales
+//               is requested before waiting for the kernel that writes A.
 //   warp 1      allocates all 512 tensor-memory columns; one lane issues the MMAs: per stage four
 //               k steps of 32, step s reading scale byte s of each 32-bit scale word.
 //   warps 2..5  epilogue: fp32 accumulators -> swizzled shared tile -> TMA bulk tensor store.
-//   warps 6..9  scale writers: per stage, each warp loads the stage's scale words of its TMEM lane
-//               quarter and stores them into that stage's scale slot with tcgen05.st. Layout
+//   warps 6..9  scale writers: once a stage has landed, each warp moves its scale words from shared
+//               memory into that stage's scale slot of its TMEM lane quarter with tcgen05.st. Layout
 //               (measured on this part): A row m reads lane m, column m / 32 of its slot; B row n
 //               reads, for accumulator lanes in quarter q, lane 32q + n % 32, column n / 32. So
 //               every quarter holds lane r, column c = scale word of A row r + 32c (per 128-row
@@ -54,6 +55,8 @@ struct MxArgs {
   int32_t BN, msub, chains, stages, num_kb;
   int32_t m_tiles, n_tiles, group_m;
   int32_t a_bytes, b_bytes;
+  int32_t stage_bytes;                       // A + W codes + both scale runs, rounded to 1 KB
+  int32_t rows_a4, rows_b4;                  // rows of the scale word arrays (M, N rounded up to 4)
   uint32_t idesc;
   uint32_t acc_stride;                       // column of the second accumulator chain
   uint32_t sf_base, sf_slot_w, sfb_off;      // scale slots: base column, width, W's offset in a slot
@@ -81,6 +84,12 @@ __device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t adesc, uint6
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
+// 1-D bulk copy global -> shared, completing on an mbarrier (16-byte aligned, size a multiple of 16)
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
 __device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t* v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v[0]), "r"(v[1]),
                "r"(v[2]), "r"(v[3])
@@ -102,7 +111,9 @@ wkv_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t tiles = (raw_base + 1023u) & ~1023u;
-  const uint32_t stage_bytes = (uint32_t)(a.a_bytes + a.b_bytes);
+  const uint32_t stage_bytes = (uint32_t)a.stage_bytes;
+  const uint32_t sf_off = (uint32_t)(a.a_bytes + a.b_bytes);          // scale words within a stage
+  const uint32_t sfb_words_off = (uint32_t)(a.msub * 128) * 4u;
   const uint32_t epi_stage = tiles + (uint32_t)a.stages * stage_bytes;
   MxCtl* ctl = reinterpret_cast<MxCtl*>(smem_raw + (epi_stage - raw_base) + kEpiBytes);
   volatile int32_t* abort_flag = &ctl->abort_flag;
@@ -142,24 +153,32 @@ wkv_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      auto load_b = [&](int it, int kb, int n0) {
+      // W codes and W scales (not written by the preceding kernel); the stage's barrier expects
+      // every byte of the stage, including A's that load_a brings later
+      auto load_b = [&](int it, int kb, int m0, int n0) {
         const int s = it % a.stages;
         const uint32_t full = smem_u32(&ctl->full[s]);
-        mbar_expect_tx(full, stage_bytes);
-        tma_load_2d(tiles + (uint32_t)s * stage_bytes + (uint32_t)a.a_bytes, &tmB, full, kb * kStageK, n0);
+        const uint32_t st = tiles + (uint32_t)s * stage_bytes;
+        const int rows_a = min(a.msub * 128, a.rows_a4 - m0);
+        const int rows_b = min(a.BN, a.rows_b4 - n0);
+        mbar_expect_tx(full, (uint32_t)(a.a_bytes + a.b_bytes + 4 * rows_a + 4 * rows_b));
+        tma_load_2d(st + (uint32_t)a.a_bytes, &tmB, full, kb * kStageK, n0);
+        bulk_load(st + sf_off + sfb_words_off, a.sfb + (int64_t)kb * a.rows_b4 + n0, 4u * (uint32_t)rows_b, full);
       };
       auto load_a = [&](int it, int kb, int m0) {
         const int s = it % a.stages;
         const uint32_t full = smem_u32(&ctl->full[s]);
         const uint32_t st = tiles + (uint32_t)s * stage_bytes;
         for (int ms = 0; ms < a.msub; ++ms) tma_load_2d(st + ms * kATileBytes, &tmA, full, kb * kStageK, m0 + ms * 128);
+        const int rows_a = min(a.msub * 128, a.rows_a4 - m0);
+        bulk_load(st + sf_off, a.sfa + (int64_t)kb * a.rows_a4 + m0, 4u * (uint32_t)rows_a, full);
       };
       // W does not come from the preceding kernel: fill the ring's W halves first
       int early = 0;
       for (int tile = blockIdx.x; tile < n_tiles_total && early < a.stages; tile += gridDim.x) {
         int m0, n0;
         mx_tile_origin(a, tile, m0, n0);
-        for (int kb = 0; kb < a.num_kb && early < a.stages; ++kb) load_b(early++, kb, n0);
+        for (int kb = 0; kb < a.num_kb && early < a.stages; ++kb) load_b(early++, kb, m0, n0);
       }
       pdl_wait();
       int it = 0, issued = 0;
@@ -178,7 +197,7 @@ wkv_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
               ok = false;
               break;
             }
-            load_b(it, kb, n0);
+            load_b(it, kb, m0, n0);
             load_a(it, kb, m0);
           }
           issued = it + 1;
@@ -274,36 +293,42 @@ wkv_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     // ---------------- scale writers ----------------
     const int q = warp & 3;                    // TMEM lane quarter of this warp
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-    pdl_wait();                                // A's scales come from the preceding kernel
     int slot = 0;
-    uint32_t round = 0, it = 0;
+    uint32_t round = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < n_tiles_total; tile += gridDim.x) {
       int m0, n0;
       mx_tile_origin(a, tile, m0, n0);
-      for (int kb = 0; kb < a.num_kb; ++kb, ++it) {
-        // scale words of this stage: A rows m0 + 128h + lane + 32c, W rows n0 + lane + 32c
-        uint32_t va[2][4], vb[8];
+      for (int kb = 0; kb < a.num_kb; ++kb) {
+        // the stage (codes and scale words) has landed; its slot's previous MMAs are done, since
+        // the producer waited for them before loading
+        if (!mbar_wait(smem_u32(&ctl->full[slot]), round, abort_flag, a.err, kWaitLimitCycles)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sw = tiles + (uint32_t)slot * stage_bytes + sf_off;   // this stage's scale words
+        uint32_t va[8], vb[8];
+        // A row m0 + 128h + 32c + lane, W row n0 + 32c + lane; rows past the matrix read scale 1.0
+        // (their codes are zero-filled)
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const int64_t row = (int64_t)m0 + 128 * h + lane + 32 * c;
-            va[h][c] = (h < a.msub && row < a.M) ? __ldg(a.sfa + row * a.num_kb + kb) : 0u;
+            const int r = 128 * h + 32 * c + lane;
+            uint32_t v = 0x7F7F7F7Fu;
+            if (h < a.msub && m0 + r < a.M) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(sw + 4u * r));
+            va[4 * h + c] = v;
           }
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const int r = lane + 32 * c;
-          vb[c] = (r < a.BN && n0 + r < a.N) ? __ldg(a.sfb + (int64_t)(n0 + r) * a.num_kb + kb) : 0u;
-        }
-        if (it >= (uint32_t)a.stages &&
-            !mbar_wait(smem_u32(&ctl->empty[slot]), round ^ 1u, abort_flag, a.err, kWaitLimitCycles)) {
-          ok = false;
-          break;
+          const int r = 32 * c + lane;
+          uint32_t v = 0x7F7F7F7Fu;
+          if (r < a.BN && n0 + r < a.N) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(sw + sfb_words_off + 4u * r));
+          vb[c] = v;
         }
         const uint32_t col = a.sf_base + (uint32_t)slot * a.sf_slot_w;
-        tmem_st4(lane_base + col, va[0]);
-        if (a.msub == 2) tmem_st4(lane_base + col + 4, va[1]);
+        tmem_st4(lane_base + col, &va[0]);
+        if (a.msub == 2) tmem_st4(lane_base + col + 4, &va[4]);
         tmem_st8(lane_base + col + a.sfb_off, vb);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
@@ -330,6 +355,11 @@ wkv_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
   }
+}
+
+// one stage: A and W code tiles, then A's and W's scale words; 1 KB aligned for the next stage
+int mx_stage_bytes(int a_bytes, int msub, int bn) {
+  return ((a_bytes + bn * kStageK + 4 * (msub * 128 + bn)) + 1023) & ~1023;
 }
 
 struct MxPlan {
@@ -359,7 +389,7 @@ bool plan_mx(int64_t M, int K, int N, int sms, MxPlan& P) {
   double best_cost = 1e300;
   for (int bn = 256; bn >= 16; bn -= 16) {
     if (g_mx_bn_override > 0 && bn != g_mx_bn_override) continue;
-    int stages = avail / (a.a_bytes + bn * kStageK);
+    int stages = avail / mx_stage_bytes(a.a_bytes, a.msub, bn);
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) continue;
     const int stride = ((bn + 31) / 32) * 32;
@@ -384,6 +414,9 @@ bool plan_mx(int64_t M, int K, int N, int sms, MxPlan& P) {
   a.chains = best_chains;
   a.stages = best_stages;
   a.b_bytes = a.BN * kStageK;
+  a.stage_bytes = mx_stage_bytes(a.a_bytes, a.msub, a.BN);
+  a.rows_a4 = (int32_t)((M + 3) & ~(int64_t)3);
+  a.rows_b4 = (N + 3) & ~3;
   a.acc_stride = (uint32_t)(((a.BN + 31) / 32) * 32);
   a.sf_base = (uint32_t)a.chains * a.acc_stride;
   a.n_tiles = (N + a.BN - 1) / a.BN;
@@ -393,7 +426,7 @@ bool plan_mx(int64_t M, int K, int N, int sms, MxPlan& P) {
   a.idesc = ((uint32_t)(a.BN >> 3) << 17)    // N
             | (1u << 23)                     // scales are UE8M0
             | ((uint32_t)(128 >> 4) << 24);  // M = 128; A and W e4m3 (format 0), K-major
-  P.smem = 1024 + a.stages * (a.a_bytes + a.b_bytes) + kEpiBytes + (int)sizeof(MxCtl);
+  P.smem = 1024 + a.stages * a.stage_bytes + kEpiBytes + (int)sizeof(MxCtl);
   return true;
 }
 

@@ -10,6 +10,10 @@
 // of 32 along K, the scale is the smallest power of two 2^e with max|w| / 2^e <= 448, stored as
 // the byte 127 + e; each code is w / 2^e rounded to the nearest e4m3 value, ties to even. An
 // all-zero block gets byte 127 and zero codes.
+//
+// Scale layout of both operands (the projection's own, so a stage's scales are one contiguous
+// run it can bulk-copy): 32-bit words [K/128][rows4], rows4 = rows rounded up to a multiple of 4;
+// word (kb, r) holds the bytes of row r's blocks 4kb .. 4kb+3, lowest byte first.
 #include "internal.cuh"
 
 namespace engram {
@@ -37,6 +41,7 @@ __global__ void __launch_bounds__(kThreads)
 quantize_mxfp8_kernel(const uint16_t* __restrict__ w, int64_t N, int32_t K, uint8_t* __restrict__ codes,
                       uint8_t* __restrict__ scales) {
   const int64_t blocks = N * (K / 32);
+  const int64_t rows4 = (N + 3) & ~(int64_t)3;
   const int lane = threadIdx.x & 31;
   for (int64_t b = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5; b < blocks;
        b += ((int64_t)gridDim.x * kThreads) >> 5) {
@@ -55,7 +60,11 @@ quantize_mxfp8_kernel(const uint16_t* __restrict__ w, int64_t N, int32_t K, uint
       e = max(-127, min(127, e));
     }
     codes[idx] = (uint8_t)to_e4m3(ldexpf(x, -e));
-    if (lane == 0) scales[b] = (uint8_t)(127 + e);
+    if (lane == 0) {
+      const int64_t n = b / (K / 32);
+      const int blk = (int)(b - n * (K / 32));
+      scales[((int64_t)(blk >> 2) * rows4 + n) * 4 + (blk & 3)] = (uint8_t)(127 + e);
+    }
   }
 }
 
@@ -69,6 +78,7 @@ gather_fp8_codes_kernel(const GatherCodesParams p) {
   const int chunks_per_row = p.D >> 4;
   const int sblocks = p.D >> 5;
   const int64_t total = p.T * p.C * chunks_per_row;
+  const int64_t rows4 = (p.T + 3) & ~(int64_t)3;
   const uint8_t* __restrict__ weight = static_cast<const uint8_t*>(p.table);
   for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < total; i += (int64_t)gridDim.x * kThreads) {
     const int64_t r = i / chunks_per_row;
@@ -81,8 +91,12 @@ gather_fp8_codes_kernel(const GatherCodesParams p) {
     if (ok) v = ld_stream_v4(weight + id * p.D + (j << 4));
     else if (j == 0 && p.err != nullptr) atomicOr(p.err, ENGRAM_ERR_ROW_ID);
     *reinterpret_cast<uint4*>(p.codes + (i << 4)) = v;
-    // scale bytes: the row's D/32 bytes, copied by the threads of the first D/32 chunks
-    if (j < sblocks) p.out_scales[r * sblocks + j] = ok ? __ldg(p.scales + id * sblocks + j) : (uint8_t)127;
+    // scale bytes: the row's D/32 bytes, copied by the threads of the first D/32 chunks into the
+    // projection's word layout (block b of token t at byte 4 * ((b / 4) * rows4 + t) + b % 4)
+    if (j < sblocks) {
+      const int b = col * sblocks + j;
+      p.out_scales[((int64_t)(b >> 2) * rows4 + t) * 4 + (b & 3)] = ok ? __ldg(p.scales + id * sblocks + j) : (uint8_t)127;
+    }
   }
 }
 

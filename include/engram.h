@@ -185,29 +185,35 @@ void engram_set_gemm_schedule(int32_t s);
  * same way on the tensor cores' block-scaled path (tcgen05.mma kind::mxf8f6f4), fp32 out. The
  * result equals the projection of the dequantised operands with fp32 accumulation. It needs no
  * workspace. Scale bytes are E8M0 exponents (value = code * 2^(byte - 127)).
+ *
+ * Scale layout (both operands): the bytes of a matrix with R rows and K columns are stored as
+ * [ceil(K/128)][R4][4] with R4 = R rounded up to a multiple of 4: byte (kb, r, j) is the scale of
+ * row r's block of 32 columns 4*kb + j. Each 128-column step of the projection then reads one
+ * contiguous run per operand. Pad rows (r >= R) are ignored.
  */
 
-/* wkv bf16 [N, K] -> MXFP8: codes uint8 [N, K] (e4m3) and scales uint8 [N, K/32]. Per row and
+/* wkv bf16 [N, K] -> MXFP8: codes uint8 [N, K] (e4m3) and scales uint8 [ceil(K/128)][N4][4]. Per row and
  * block of 32 along K, the scale is the smallest power of two 2^e with max|w| / 2^e <= 448 (byte
  * 127 + e; the table's own scale convention, so no value saturates) and each code is w / 2^e
  * rounded to the nearest e4m3 value, ties to even; an all-zero block gets byte 127 and zero codes.
- * K % 32 == 0. Device pointers; deterministic. */
+ * K % 32 == 0; scales 4-byte aligned. Device pointers; deterministic. */
 int engram_quantize_mxfp8(const uint16_t* w, int64_t N, int32_t K, uint8_t* codes, uint8_t* scales,
                           engram_stream_t stream);
 
 /* Stage 2 for the FP8 variant: like engram_gather_dequant for an FP8_E8M0 table, but the rows'
- * codes and scale bytes are copied as they are: codes uint8 [T, C*head_dim], scales uint8
- * [T, C*head_dim/32]. Ids outside [0, num_rows) give a zero row (codes 0, scale byte 127) and set
- * ENGRAM_ERR_ROW_ID. head_dim % 32 == 0; table and codes 16-byte aligned. */
+ * codes and scale bytes are copied as they are: codes uint8 [T, C*head_dim], scales in the layout
+ * above, uint8 [ceil(C*head_dim/128)][T4][4]. Ids outside [0, num_rows) give a zero row (codes 0,
+ * scale byte 127) and set ENGRAM_ERR_ROW_ID. head_dim % 32 == 0; table, codes, scales 16-byte
+ * aligned. */
 int engram_gather_fp8_codes(const int32_t* ids, int64_t ids_stride_t, int64_t T, int32_t C,
                             int32_t head_dim, const void* table, const uint8_t* table_scales,
                             int64_t num_rows, uint8_t* codes, uint8_t* scales, int32_t* err_flag,
                             engram_stream_t stream);
 
-/* Stage 3, FP8 variant: kv fp32 [T, N] = A * W^T with A codes [T, K] + A_scales [T, K/32] (from
- * engram_gather_fp8_codes) and W codes [N, K] + W_scales [N, K/32] (from engram_quantize_mxfp8).
- * K % 128 == 0, N % 16 == 0; A, W, kv 16-byte aligned, scales 4-byte aligned. err_flag as for
- * engram_project. */
+/* Stage 3, FP8 variant: kv fp32 [T, N] = A * W^T with A codes [T, K] + A_scales [K/128][T4][4]
+ * (from engram_gather_fp8_codes) and W codes [N, K] + W_scales [K/128][N4][4] (from
+ * engram_quantize_mxfp8). K % 128 == 0, N % 16 == 0; all pointers 16-byte aligned. err_flag as
+ * for engram_project. */
 int engram_project_mxfp8(const uint8_t* A, const uint8_t* A_scales, const uint8_t* W,
                          const uint8_t* W_scales, float* kv, int64_t T, int32_t K, int32_t N,
                          int32_t* err_flag, engram_stream_t stream);
@@ -246,7 +252,7 @@ typedef struct EngramLayerWeights {
   const uint16_t* q_weight;    /* device bf16 [hc, H] */
   const uint16_t* k_weight;    /* device bf16 [hc, H] */
   int32_t wkv_format;          /* EngramWkvFmt; MXFP8 needs an FP8_E8M0 table and K % 128 == 0 */
-  const uint8_t* wkv_scales;   /* device [(hc+1)*H, C*head_dim/32], MXFP8 only */
+  const uint8_t* wkv_scales;   /* device, MXFP8 only: [C*head_dim/128][N4][4] (see engram_project_mxfp8) */
 } EngramLayerWeights;
 
 /* Hash tables ([Atlas] EngramHashTables). All device memory. */

@@ -93,11 +93,29 @@ def gpu_forward(w, case, setup, device="cuda", with_err=True, mx=False):
            "dims": dims}
     if mx:
         code_bytes = ((T * K + 255) // 256) * 256
+        shp = E.mx_scale_shape(T, K)
         out["A_codes_last"] = ws[id_bytes:id_bytes + T * K].view(T, K)
-        out["A_scales_last"] = ws[id_bytes + code_bytes:id_bytes + code_bytes + T * K // 32].view(T, K // 32)
+        sc = ws[id_bytes + code_bytes:id_bytes + code_bytes + shp[0] * shp[1] * shp[2]].view(shp)
+        out["A_scales_last"] = mx_words_to_rows(sc, T, K // 32)
     else:
         out["A_last"] = ws[id_bytes:id_bytes + T * K * 2].view(torch.bfloat16).view(T, K)
     return out
+
+
+def mx_words_to_rows(sc: torch.Tensor, rows: int, nblk: int) -> np.ndarray:
+    """MXFP8 scales in the projection's word layout [ceil(nblk/4), rows4, 4] -> bytes [rows, nblk]
+    (the oracle's layout)."""
+    a = sc.detach().cpu().numpy()
+    return a.transpose(1, 0, 2).reshape(a.shape[1], -1)[:rows, :nblk]
+
+
+def mx_rows_to_words(sc_rows: np.ndarray) -> np.ndarray:
+    """Bytes [rows, nblk] -> the word layout [ceil(nblk/4), rows4, 4] (pad entries 127)."""
+    R, nb = sc_rows.shape
+    R4, nb4 = (R + 3) // 4 * 4, (nb + 3) // 4 * 4
+    pad = np.full((R4, nb4), 127, dtype=np.uint8)
+    pad[:R, :nb] = sc_rows
+    return np.ascontiguousarray(pad.reshape(R4, nb4 // 4, 4).transpose(1, 0, 2))
 
 
 def oracle_mxfp8_quantize(wkv: torch.Tensor, rows: int = 2048):

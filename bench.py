@@ -39,6 +39,9 @@ L2_FLUSH_BYTES = 512 << 20
 NCU_TRAFFIC: dict = {
     # profiles/wkv_gemm_decode_fp8_t256.md: dram__bytes_read.sum + dram__bytes_write.sum
     "project0@decode_fp8_t256": {"bytes": 254888960 + 3356416, "src_sha": "cc823d9d72114c80"},
+    # profiles/wkv_gemm_mx_decode_fp8_t256.md (FP8 variant, --wkv mxfp8)
+    "project0@decode_fp8_t256@mxfp8": {"bytes": 131441408 + 3196160, "src_sha": "f0631574c6a8fe56",
+                                       "src": "gemm_mx.cu"},
 }
 
 
@@ -346,7 +349,7 @@ def run_ours(args, rank, world, device):
     key = f"{dom}@{w.name}" + ("@mxfp8" if mx else "")
     traffic = None
     rec = NCU_TRAFFIC.get(key)
-    if rec and rec.get("src_sha") == src_sha(kernel_src(dom)):
+    if rec and rec.get("src_sha") == src_sha(rec.get("src", kernel_src(dom))):
         traffic = rec["bytes"]
     stages = {}
     for name, t in per_kernel.items():

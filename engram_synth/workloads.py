@@ -145,6 +145,13 @@ WORKLOADS = {
         lookback=False,
     ),
 }
+# Small cases for the FP8 operand variant: the tiny config's token recipe (64 uniform ids, one
+# sequence, primes just above 4000) with FP8+E8M0 rows of 256 (K = 8 * 256 = 2048), and a
+# two-layer version of the decode step (layers 1 and 14) for the per-layer loop.
+WORKLOADS["tiny_fp8"] = replace(WORKLOADS["tiny_bf16"], name="tiny_fp8", seed=5, head_dim=256,
+                                table_format="fp8")
+WORKLOADS["decode_fp8_t256_2layer"] = replace(_DECODE, name="decode_fp8_t256_2layer", seed=6,
+                                              layer_ids=(1, 14))
 for _t in (1, 64, 1024):
     WORKLOADS[f"large_fp8_t{_t}"] = replace(
         WORKLOADS["large_fp8_t16384"], name=f"large_fp8_t{_t}", seq_lens=(_t,))

@@ -111,19 +111,77 @@ def test_project_mxfp8_rejects_bad_shapes():
     assert ei.value.code == -1
 
 
-@pytest.mark.parametrize("name", ["decode_fp8_t256", "large_fp8_t64"])
-def test_forward_mxfp8_matches_oracle(name):
+def _sample(w, case, n):
+    """All tokens up to n, else a seeded sample plus sequence starts, document starts and masked."""
+    T = w.tokens
+    if T <= n:
+        return None
+    rng = np.random.default_rng(77)
+    pick = set(rng.choice(T, size=n, replace=False).tolist())
+    pick.update(int(x) for x in case.batch["cu_seqlens"][:-1] if x < T)
+    sid = case.batch.get("sequence_ids")
+    if sid is not None:
+        pick.update(np.nonzero(np.diff(sid) != 0)[0][:64].tolist())
+    mask = case.batch.get("token_mask")
+    if mask is not None:
+        pick.update(np.nonzero(mask == 0)[0][:64].tolist())
+    pick.add(T - 1)
+    return np.array(sorted(pick), dtype=np.int64)
+
+
+@pytest.mark.parametrize("name,sample", [("tiny_fp8", 0), ("decode_fp8_t256", 0), ("decode_fp8_t256_2layer", 0),
+                                         ("large_fp8_t1", 0), ("large_fp8_t64", 0), ("large_fp8_t1024", 256),
+                                         ("prefill_fp8_t32768", 384)])
+def test_forward_mxfp8_matches_oracle(name, sample):
     w, case, setup = H.build(name)
     got = H.gpu_forward(w, case, setup, mx=True)
-    ref = H.oracle_forward(w, case, None, mx=True)
+    toks = _sample(w, case, sample) if sample else None
+    ref = H.oracle_forward(w, case, toks, mx=True)
     assert got["err"] == 0
     assert np.array_equal(got["ids"].cpu().numpy(), ref["ids"].astype(np.int32))
+    sel = ref["tokens"]
+    sel_t = torch.from_numpy(sel).to(DEV)
     last = ref["layers"][-1]
-    assert np.array_equal(got["A_codes_last"].cpu().numpy(), last["a_bits"][0])
-    assert np.array_equal(got["A_scales_last"], last["a_bits"][1])
-    H.check_kv(got["kv_last"].cpu().numpy(), last["kv"], f"{name} mx kv")
+    assert np.array_equal(got["A_codes_last"].index_select(0, sel_t).cpu().numpy(), last["a_bits"][0])
+    assert np.array_equal(got["A_scales_last"][sel], last["a_bits"][1])
+    H.check_kv(got["kv_last"].index_select(0, sel_t).cpu().numpy(), last["kv"], f"{name} mx kv")
     for l, lref in enumerate(ref["layers"]):
-        H.check_streams(got["streams"][l].cpu().numpy(), lref["streams"], lref["streams_in"], f"{name} mx layer {l}")
+        h = got["streams"][l].index_select(0, sel_t).cpu().numpy()
+        H.check_streams(h, lref["streams"], lref["streams_in"], f"{name} mx layer {l}")
+    mask = case.batch.get("token_mask")
+    if mask is not None:                                   # masked tokens bit-unchanged
+        keep = mask[sel] == 0
+        for l in range(w.layers):
+            h = got["streams"][l].index_select(0, sel_t).cpu().numpy()
+            assert np.array_equal(h[keep], case.streams[l].index_select(0, sel_t).cpu().numpy()[keep])
+
+
+def test_noalloc_forward_with_mxfp8_matches_workspace_forward():
+    import engram_gram_hash_02_gb300 as Em
+    from engram_synth.case import to_device
+    w, case, setup = H.build("decode_fp8_t256")
+    primes, offsets, rows, mult = setup
+    b = case.batch
+    dims = H.dims_for(w, H.pad_id_of(w, b["token_map"]))
+    tables = Em.HashTables(to_device(b["token_map"], DEV), to_device(mult, DEV), to_device(primes, DEV),
+                           to_device(offsets, DEV))
+    layers = []
+    for l, t in enumerate(case.tables):
+        codes, sc = Em.quantize_mxfp8(case.wkv[l])
+        layers.append(Em.LayerWeights(t["fmt"], t["table"], t["scales"], t["num_rows"], codes, case.q_weight[l],
+                                      case.k_weight[l], wkv_scales=sc))
+    outs = []
+    for noalloc in (False, True, True):
+        streams = [s.clone() for s in case.streams]
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        plan = Em.ForwardPlan(dims, tables, layers, to_device(b["input_ids"], DEV), streams,
+                              cu_seqlens=to_device(b["cu_seqlens"], DEV), lookback_ids=to_device(b["lookback_ids"], DEV),
+                              err=err)
+        plan.run_noalloc() if noalloc else plan.run()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        outs.append(streams[0])
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])   # same kernels, same order
 
 
 def test_forward_mxfp8_needs_an_fp8_table():

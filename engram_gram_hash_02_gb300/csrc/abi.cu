@@ -137,10 +137,13 @@ size_t engram_project_workspace_bytes(int64_t T, int32_t K, int32_t N) {
   return gemm_workspace_bytes(T, K, N);
 }
 
-static int hash_impl(const EngramDims* dims, const int32_t* input_ids, int64_t T, const int32_t* cu_seqlens,
-                     int32_t S, const int32_t* sequence_ids, const uint8_t* token_mask, const int32_t* lookback_ids,
-                     const int32_t* token_map, const int64_t* multipliers, const int64_t* primes,
-                     const int64_t* offsets, int32_t* out_ids, int32_t* err_flag, engram_stream_t stream, bool pdl) {
+// Checks the hash arguments and fills its launch parameters (rc != 0: nothing to launch; T == 0
+// returns ENGRAM_OK with p.T == 0).
+static int hash_params(const EngramDims* dims, const int32_t* input_ids, int64_t T, const int32_t* cu_seqlens,
+                       int32_t S, const int32_t* sequence_ids, const uint8_t* token_mask, const int32_t* lookback_ids,
+                       const int32_t* token_map, const int64_t* multipliers, const int64_t* primes,
+                       const int64_t* offsets, int32_t* out_ids, int32_t* err_flag, HashParams& p) {
+  p = HashParams{};
   int rc = check_dims(dims, true, false);
   if (rc) return rc;
   ENGRAM_CHECK_ARG(T >= 0 && T < (int64_t)1 << 34, "T must be in [0, 2^34)");
@@ -152,7 +155,6 @@ static int hash_impl(const EngramDims* dims, const int32_t* input_ids, int64_t T
   } else {
     S = 1;
   }
-  HashParams p{};
   p.input_ids = input_ids;
   p.cu_seqlens = cu_seqlens;
   p.sequence_ids = sequence_ids;
@@ -172,6 +174,17 @@ static int hash_impl(const EngramDims* dims, const int32_t* input_ids, int64_t T
   p.cols = (dims->max_ngram - 1) * dims->n_heads;
   p.raw_vocab = dims->raw_vocab;
   p.pad_id = dims->pad_id;
+  return ENGRAM_OK;
+}
+
+static int hash_impl(const EngramDims* dims, const int32_t* input_ids, int64_t T, const int32_t* cu_seqlens,
+                     int32_t S, const int32_t* sequence_ids, const uint8_t* token_mask, const int32_t* lookback_ids,
+                     const int32_t* token_map, const int64_t* multipliers, const int64_t* primes,
+                     const int64_t* offsets, int32_t* out_ids, int32_t* err_flag, engram_stream_t stream, bool pdl) {
+  HashParams p;
+  int rc = hash_params(dims, input_ids, T, cu_seqlens, S, sequence_ids, token_mask, lookback_ids, token_map,
+                       multipliers, primes, offsets, out_ids, err_flag, p);
+  if (rc || T == 0) return rc;
   cudaError_t e = launch_hash(p, static_cast<cudaStream_t>(stream), pdl);
   return e == cudaSuccess ? ENGRAM_OK : fail_cuda(e, "engram_hash: launch");
 }
@@ -359,27 +372,54 @@ int engram_forward(const EngramDims* dims, const EngramHashTables* tables, const
   const size_t gemm_ws_bytes = ws_bytes > need ? ws_bytes - need : 0;
 
   // each launch may start while its predecessor finishes (programmatic dependent launch)
-  rc = hash_impl(dims, tok->input_ids, T, tok->cu_seqlens, tok->num_seqs, tok->sequence_ids, tok->token_mask,
-                 tok->lookback_ids, tables->token_map, tables->multipliers, tables->primes, tables->offsets, ids,
-                 err_flag, stream, true);
+  HashParams hp;
+  rc = hash_params(dims, tok->input_ids, T, tok->cu_seqlens, tok->num_seqs, tok->sequence_ids, tok->token_mask,
+                   tok->lookback_ids, tables->token_map, tables->multipliers, tables->primes, tables->offsets, ids,
+                   err_flag, hp);
   if (rc) return rc;
+  // an FP8 table in the first layer: hash and that layer's gather in one kernel
+  const bool fused = layers[0].table_format == ENGRAM_TABLE_FP8_E8M0;
+  if (fused) {
+    HashGatherParams g{};
+    g.h = hp;
+    g.table = layers[0].table;
+    g.scales = layers[0].table_scales;
+    g.num_rows = layers[0].table_rows;
+    g.D = dims->head_dim;
+    if (layers[0].wkv_format == ENGRAM_WKV_MXFP8) {
+      g.out_codes = reinterpret_cast<uint8_t*>(A);
+      g.out_scales = g.out_codes + round256((size_t)(T * K));
+    } else {
+      g.out_bf16 = A;
+    }
+    cudaError_t e = launch_hash_gather(g, static_cast<cudaStream_t>(stream), true);
+    if (e != cudaSuccess) return fail_cuda(e, "engram_forward: hash + gather launch");
+  } else {
+    cudaError_t e = launch_hash(hp, static_cast<cudaStream_t>(stream), true);
+    if (e != cudaSuccess) return fail_cuda(e, "engram_hash: launch");
+  }
   for (int l = 0; l < L; ++l) {
     const EngramLayerWeights& w = layers[l];
+    const bool gathered = fused && l == 0;
     if (w.wkv_format == ENGRAM_WKV_MXFP8) {
       // FP8 variant: the rows' codes and scales are the A operand as they are (the A region holds
       // T*K codes, then the T*K/32 scale bytes)
       uint8_t* codes = reinterpret_cast<uint8_t*>(A);
       uint8_t* sa = codes + round256((size_t)(T * K));
-      rc = gather_codes_impl(ids + (int64_t)l * C, (int64_t)L * C, T, C, dims->head_dim, w.table, w.table_scales,
-                             w.table_rows, codes, sa, err_flag, stream, true);
-      if (rc) return rc;
+      if (!gathered) {
+        rc = gather_codes_impl(ids + (int64_t)l * C, (int64_t)L * C, T, C, dims->head_dim, w.table, w.table_scales,
+                               w.table_rows, codes, sa, err_flag, stream, true);
+        if (rc) return rc;
+      }
       rc = project_mx_impl(codes, sa, reinterpret_cast<const uint8_t*>(w.wkv), w.wkv_scales, kv, T, (int32_t)K,
                            (int32_t)N, err_flag, stream, true);
       if (rc) return rc;
     } else {
-      rc = gather_impl(w.table_format, ids + (int64_t)l * C, (int64_t)L * C, T, C, dims->head_dim, w.table,
-                       w.table_scales, w.table_rows, A, err_flag, stream, true);
-      if (rc) return rc;
+      if (!gathered) {
+        rc = gather_impl(w.table_format, ids + (int64_t)l * C, (int64_t)L * C, T, C, dims->head_dim, w.table,
+                         w.table_scales, w.table_rows, A, err_flag, stream, true);
+        if (rc) return rc;
+      }
       rc = project_impl(A, w.wkv, kv, T, (int32_t)K, (int32_t)N, gemm_ws, gemm_ws_bytes, err_flag, stream, true);
       if (rc) return rc;
     }

@@ -12,7 +12,7 @@
 // the quants, scale nibbles and d/dmin of its 8 outputs.
 #include <cuda_fp8.h>
 
-#include "internal.cuh"
+#include "hash_token.cuh"
 
 namespace engram {
 namespace {
@@ -222,7 +222,75 @@ unsigned grid_for(int64_t work_items, int64_t per_block) {
   return (unsigned)(b < cap ? b : cap);
 }
 
+// ---- hash fused with the first layer's FP8 gather (engram_forward) ----------------------------
+// One CTA per token: warp 0 hashes the token (its window loads in flight while the block stages
+// cu_seqlens), the ids go to the global id buffer and to shared memory, then all threads fetch
+// the layer-0 rows, 16 bytes per thread and step, dequantised to bf16 or copied as codes.
+constexpr int kHgThreads = 128;
+
+__global__ void __launch_bounds__(kHgThreads)
+hash_gather_fp8_kernel(const HashGatherParams p) {
+  __shared__ int32_t s_cu[kSmemCu];
+  __shared__ int32_t s_ids[256];
+  pdl_wait();                                    // inputs may come from the preceding kernel
+  pdl_trigger();
+  const int64_t t = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const bool hasher = threadIdx.x < 32;
+  TokenLoads L;
+  if (hasher) L = hash_token_loads(p.h, t, lane);
+  const bool cu_in_smem = stage_cu(p.h, s_cu);
+  if (hasher) hash_token_finish(p.h, t, lane, L, cu_in_smem, s_cu, s_ids);
+  __syncthreads();
+
+  const int C = p.h.cols;
+  const int cpr = p.D >> 4;                     // 16-byte chunks per row
+  const int sblocks = p.D >> 5;
+  const int64_t K = (int64_t)C * p.D;
+  const int64_t rows4 = (p.h.T + 3) & ~(int64_t)3;
+  const uint8_t* __restrict__ weight = static_cast<const uint8_t*>(p.table);
+  for (int i = threadIdx.x; i < C * cpr; i += kHgThreads) {
+    const int col = i / cpr;
+    const int j = i - col * cpr;
+    const int64_t id = s_ids[col];              // layer 0: (layer, column) index = column
+    const bool ok = id >= 0 && id < p.num_rows;
+    if (!ok && j == 0) flag(p.h.err, ENGRAM_ERR_ROW_ID);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (ok) v = ld_stream_v4(weight + id * p.D + (j << 4));
+    const int64_t e0 = t * K + (int64_t)col * p.D + (j << 4);   // first element of this chunk
+    if (p.out_bf16 != nullptr) {
+      uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+      if (ok) {
+        const float scale = __uint_as_float((uint32_t)__ldg(p.scales + id * sblocks + (j >> 1)) << 23);
+        lo.x = dequant_pair(v.x, scale);
+        lo.y = dequant_pair(v.x >> 16, scale);
+        lo.z = dequant_pair(v.y, scale);
+        lo.w = dequant_pair(v.y >> 16, scale);
+        hi.x = dequant_pair(v.z, scale);
+        hi.y = dequant_pair(v.z >> 16, scale);
+        hi.z = dequant_pair(v.w, scale);
+        hi.w = dequant_pair(v.w >> 16, scale);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + e0);
+      dst[0] = lo;
+      dst[1] = hi;
+    } else {
+      *reinterpret_cast<uint4*>(p.out_codes + e0) = v;
+      if (j < sblocks) {
+        const int b = col * sblocks + j;          // block of 32 along K
+        p.out_scales[((int64_t)(b >> 2) * rows4 + t) * 4 + (b & 3)] =
+            ok ? __ldg(p.scales + id * sblocks + j) : (uint8_t)127;
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_hash_gather(const HashGatherParams& p, cudaStream_t stream, bool pdl) {
+  if (p.h.T > 0x7fffffff) return cudaErrorInvalidValue;
+  return launch_k(hash_gather_fp8_kernel, dim3((unsigned)p.h.T), dim3(kHgThreads), 0, stream, pdl, p);
+}
 
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl) {
   const int64_t rows = p.T * p.C;

@@ -72,6 +72,21 @@ struct HashParams {
 };
 cudaError_t launch_hash(const HashParams& p, cudaStream_t stream, bool pdl = false);
 
+// Hash fused with the first layer's gather of an FP8_E8M0 table (engram_forward): one CTA per
+// token hashes it (all layers' ids to h.out) and gathers its layer-0 rows, dequantised to bf16
+// (out_bf16) or as codes and scale words (out_codes / out_scales, the FP8 variant's layout).
+struct HashGatherParams {
+  HashParams h;
+  const void* table;          // e4m3 codes [num_rows, D]
+  const uint8_t* scales;      // [num_rows, D/32]
+  int64_t num_rows;
+  int32_t D;
+  uint16_t* out_bf16;         // [T, C*D] or NULL
+  uint8_t* out_codes;         // [T, C*D] or NULL
+  uint8_t* out_scales;        // [ceil(C*D/128)][T4][4] or NULL
+};
+cudaError_t launch_hash_gather(const HashGatherParams& p, cudaStream_t stream, bool pdl = false);
+
 struct GatherParams {
   int32_t fmt;
   const int32_t* ids;

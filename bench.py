@@ -251,6 +251,12 @@ def stage_model(w, name, peaks_d, mx: bool = False):
     raise ValueError(name)
 
 
+def forward_launches(w) -> int:
+    """Kernels one engram_forward call launches: hash (fused with the first layer's gather when
+    that layer's table is FP8), then per layer gather, projection and gate."""
+    return 1 + 3 * w.layers - (1 if w.table_format == "fp8" else 0)
+
+
 def kernel_src(name):
     for pre, src in (("hash", "hash.cu"), ("gather", "gather.cu"), ("project", "gemm.cu"), ("gate", "gate.cu")):
         if name.startswith(pre):
@@ -382,7 +388,7 @@ def run_ours(args, rank, world, device):
                    "hidden": w.hidden, "hc": w.hc, "K": w.K, "N": w.N,
                    "wkv": "mxfp8" if mx else "bf16",
                    "l2": "flushed before every timed step (512 MB write)", "parallelism": f"replicas{world}"},
-        "gpu_launches": 2 * args.steps * len(calls),
+        "gpu_launches": args.steps * (forward_launches(w) + len(calls)),
         "stages": stages,
         "roofline": {"kernel": dom, "bound": model["bound"], "achieved": round(achieved, 1),
                      "peak": peak, "unit": unit, "frac": None if peak is None else round(achieved / peak, 4),
@@ -396,7 +402,8 @@ def run_ours(args, rank, world, device):
     if e2e is not None:
         line["e2e"] = {"value": round(replica_throughput(world, tokens, e2e["ms"]), 1), "unit": "tokens/s per layer",
                        "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                       "ms_per_step": round(e2e["ms"], 5)}
+                       "ms_per_step": round(e2e["ms"], 5),
+                       "pipelining": f"{e2e['slots']} buffer slots; copies in / forward / copies out on 3 streams"}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, path.case, args.cpu_tokens)
     return line
@@ -431,44 +438,74 @@ def run_only(args, device):
         raise SystemExit(f"device error flag {err}")
 
 
-def run_e2e(args, path, stream, device):
+def run_e2e(args, path, stream, device, slots: int = 3):
     """engram_forward with per-step host->device copies of the inputs (pinned) and a
-    device->host read of the updated streams, all inside the timed region."""
+    device->host read of the updated streams, all inside the timed region. Steps are pipelined
+    the way a serving loop runs them: `slots` sets of device buffers, copies in on one stream,
+    the forward pass on the compute stream, copies out on a third, so step k+1's inputs move while
+    step k computes and step k-1's result comes back. Every step copies its own inputs in and its
+    own result out."""
     E, w = path.E, path.w
-    host = {}
-    for name in ("input_ids", "cu", "sid", "mask", "lookback"):
-        t = getattr(path, name)
-        if t is not None:
-            host[name] = t.cpu().pin_memory()
-    h_streams = [s.cpu().pin_memory() for s in path.case.streams]
-    out_streams = [torch.empty_like(s).pin_memory() for s in h_streams]
-    plan = E.ForwardPlan(path.dims, path.tables, path.layers, path.input_ids, path.streams,
-                         cu_seqlens=path.cu, sequence_ids=path.sid, token_mask=path.mask,
-                         lookback_ids=path.lookback, out_ids=path.ids, err=path.err)
-    h2d = sum(t.numel() * t.element_size() for t in host.values()) + sum(
-        s.numel() * s.element_size() for s in h_streams)
-    d2h = sum(s.numel() * s.element_size() for s in h_streams)
+    names = [n for n in ("input_ids", "cu", "sid", "mask", "lookback") if getattr(path, n) is not None]
+    host_in = {n: getattr(path, n).cpu().pin_memory() for n in names}
+    host_streams = [s.cpu().pin_memory() for s in path.case.streams]
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    buf = []
+    for _ in range(slots):
+        dev_in = {n: torch.empty_like(getattr(path, n)) for n in names}
+        dev_streams = [torch.empty_like(s) for s in path.streams]
+        plan = E.ForwardPlan(path.dims, path.tables, path.layers, dev_in["input_ids"], dev_streams,
+                             cu_seqlens=dev_in.get("cu"), sequence_ids=dev_in.get("sid"),
+                             token_mask=dev_in.get("mask"), lookback_ids=dev_in.get("lookback"), err=path.err)
+        out_host = [torch.empty_like(s).pin_memory() for s in host_streams]
+        ev = {k: torch.cuda.Event() for k in ("in", "comp", "out")}
+        buf.append({"in": dev_in, "streams": dev_streams, "plan": plan, "out": out_host, "ev": ev})
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + sum(
+        s.numel() * s.element_size() for s in host_streams)
+    d2h = sum(s.numel() * s.element_size() for s in host_streams)
+    for b in buf:
+        b["ev"]["out"].record(s_out)
 
-    def step():
-        for name, t in host.items():
-            getattr(path, name).copy_(t, non_blocking=True)
-        for l, s in enumerate(h_streams):
-            path.streams[l].copy_(s, non_blocking=True)
-        plan.run(stream)
-        for l, s in enumerate(out_streams):
-            s.copy_(path.streams[l], non_blocking=True)
+    def step(k):
+        b = buf[k % slots]
+        s_in.wait_event(b["ev"]["out"])          # this slot's previous result has been copied out
+        with torch.cuda.stream(s_in):
+            for n in names:
+                b["in"][n].copy_(host_in[n], non_blocking=True)
+            for l, hs in enumerate(host_streams):
+                b["streams"][l].copy_(hs, non_blocking=True)
+        b["ev"]["in"].record(s_in)
+        stream.wait_event(b["ev"]["in"])
+        b["plan"].run(stream)
+        b["ev"]["comp"].record(stream)
+        s_out.wait_event(b["ev"]["comp"])
+        with torch.cuda.stream(s_out):
+            for l, o in enumerate(b["out"]):
+                o.copy_(b["streams"][l], non_blocking=True)
+        b["ev"]["out"].record(s_out)
 
-    for _ in range(max(3, args.warmup)):
-        step()
+    for k in range(max(3, args.warmup)):
+        step(k)
     torch.cuda.synchronize()
     n = args.steps
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(n):
-        step()
-    b.record(stream)
-    b.synchronize()
-    return {"ms": a.elapsed_time(b) / n, "h2d": int(h2d), "d2h": int(d2h)}
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(s_in)
+    for k in range(n):
+        step(k)
+    s_out.wait_stream(s_in)
+    s_out.wait_stream(stream)
+    t1.record(s_out)
+    t1.synchronize()
+    # the last step's result equals a plain run's (same inputs every step)
+    ref = [s.clone() for s in path.case.streams]
+    chk = E.ForwardPlan(path.dims, path.tables, path.layers, path.input_ids, ref, cu_seqlens=path.cu,
+                        sequence_ids=path.sid, token_mask=path.mask, lookback_ids=path.lookback, err=path.err)
+    chk.run(stream)
+    torch.cuda.synchronize()
+    last = buf[(n - 1) % slots]["out"]
+    if not all(torch.equal(o, r.cpu()) for o, r in zip(last, ref)):
+        raise RuntimeError("pipelined end-to-end result differs from a plain forward pass")
+    return {"ms": t0.elapsed_time(t1) / n, "h2d": int(h2d), "d2h": int(d2h), "slots": slots}
 
 
 # ------------------------------------------------------------------------------------------------

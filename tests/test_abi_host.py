@@ -105,3 +105,31 @@ def test_forward_workspace_covers_ids_rows_and_kv(lib):
     need = lib.engram_forward_workspace_bytes(ctypes.byref(dims), T)
     assert need >= 4 * T * C + 2 * T * K + 4 * T * N
     assert need % 256 == 0
+
+
+def test_fp8_variant_argument_checks_fire_before_any_cuda_call(lib):
+    buf = (ctypes.c_uint8 * 4096)()
+    addr = (ctypes.addressof(buf) + 15) & ~15
+    stream = None
+    # encoder: K not a multiple of 32
+    rc = lib.engram_quantize_mxfp8(addr, 4, 33, addr, addr, stream)
+    assert rc == -1 and "multiple of 32" in lib.engram_last_error().decode()
+    # projection: K not a multiple of 128
+    rc = lib.engram_project_mxfp8(addr, addr, addr, addr, addr, 4, 96, 32, None, stream)
+    assert rc == -1 and "multiple of 128" in lib.engram_last_error().decode()
+    # projection: scales must be 16-byte aligned (the stage's scale words are bulk-copied)
+    rc = lib.engram_project_mxfp8(addr, addr + 4, addr, addr, addr, 4, 128, 32, None, stream)
+    assert rc == -1 and "16-byte aligned" in lib.engram_last_error().decode()
+    # raw FP8 gather: head_dim not a multiple of 32
+    rc = lib.engram_gather_fp8_codes(addr, 8, 1, 8, 48, addr, addr, 10, addr, addr, None, stream)
+    assert rc == -1 and "multiple of 32" in lib.engram_last_error().decode()
+    # T = 0 and N = 0 are no-ops
+    assert lib.engram_project_mxfp8(None, None, None, None, None, 0, 128, 32, None, stream) == 0
+    assert lib.engram_quantize_mxfp8(None, 0, 64, None, None, stream) == 0
+
+
+def test_mx_scale_shape():
+    from engram_gram_hash_02_gb300 import binding as Bd
+    assert Bd.mx_scale_shape(256, 6144) == (48, 256, 4)
+    assert Bd.mx_scale_shape(1, 6144) == (48, 4, 4)          # rows padded to a multiple of 4
+    assert Bd.mx_scale_shape(5, 96) == (1, 8, 4)             # 3 blocks of 32 -> one word per row

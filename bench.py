@@ -252,9 +252,11 @@ def stage_model(w, name, peaks_d, mx: bool = False):
 
 
 def forward_launches(w) -> int:
-    """Kernels one engram_forward call launches: hash (fused with the first layer's gather when
-    that layer's table is FP8), then per layer gather, projection and gate."""
-    return 1 + 3 * w.layers - (1 if w.table_format == "fp8" else 0)
+    """Kernels one engram_forward call launches: the hash (which also gathers the rows of up to 8
+    leading FP8 layers), one gather launch per 8 remaining layers of the workload's one format,
+    then per layer the projection and the gate."""
+    fused = min(w.layers, 8) if w.table_format == "fp8" else 0
+    return 1 + -(-(w.layers - fused) // 8) + 2 * w.layers
 
 
 def kernel_src(name):

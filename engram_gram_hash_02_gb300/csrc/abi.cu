@@ -317,12 +317,21 @@ int engram_project_mxfp8(const uint8_t* A, const uint8_t* A_scales, const uint8_
 
 void engram_set_gemm_mx_tile(int32_t bn) { set_gemm_mx_bn_override((bn >= 16 && bn <= 256 && bn % 16 == 0) ? bn : 0); }
 
+// One layer's gathered operand in the engram_forward workspace: bf16 rows [T, K], or for the
+// FP8 variant the codes [T, K] followed (256-byte aligned) by the scale words [ceil(K/128)][T4][4].
+static size_t a_slot_bytes(int64_t T, int64_t K) {
+  const size_t rows = (size_t)(T * K * 2);
+  const size_t codes = round256((size_t)(T * K)) + (size_t)((K + 127) / 128) * (size_t)((T + 3) & ~(int64_t)3) * 4;
+  return round256(rows > codes ? rows : codes);
+}
+
 size_t engram_forward_workspace_bytes(const EngramDims* d, int64_t T) {
-  if (d == nullptr || T < 0) return 0;
+  if (d == nullptr || T < 0 || d->layers < 1) return 0;
   const int64_t C = (int64_t)(d->max_ngram - 1) * d->n_heads;
   const int64_t K = C * d->head_dim;
   const int64_t N = (int64_t)d->hidden * (d->hc + 1);
-  return round256((size_t)(T * d->layers * C * 4)) + round256((size_t)(T * K * 2)) + round256((size_t)(T * N * 4));
+  return round256((size_t)(T * d->layers * C * 4)) + (size_t)d->layers * a_slot_bytes(T, K) +
+         round256((size_t)(T * N * 4));
 }
 
 int engram_forward(const EngramDims* dims, const EngramHashTables* tables, const EngramLayerWeights* layers,
@@ -351,6 +360,10 @@ int engram_forward(const EngramDims* dims, const EngramHashTables* tables, const
     if (w.wkv_format == ENGRAM_WKV_MXFP8) {
       ENGRAM_CHECK_ARG(w.table_format == ENGRAM_TABLE_FP8_E8M0,
                        "layer %d: MXFP8 wkv needs an FP8+E8M0 table (its rows are the A operand)", l);
+      rc = check_gather_codes(reinterpret_cast<const int32_t*>(16), (int64_t)L * C, T, C, dims->head_dim, w.table,
+                              w.table_scales, w.table_rows, static_cast<const uint8_t*>(workspace),
+                              static_cast<const uint8_t*>(workspace));
+      if (rc) return rc;
       rc = check_project_mx(static_cast<const uint8_t*>(workspace), static_cast<const uint8_t*>(workspace),
                             reinterpret_cast<const uint8_t*>(w.wkv), w.wkv_scales,
                             reinterpret_cast<const float*>(workspace), T, (int32_t)K, (int32_t)N);
@@ -365,11 +378,16 @@ int engram_forward(const EngramDims* dims, const EngramHashTables* tables, const
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* ids = out_ids != nullptr ? out_ids : reinterpret_cast<int32_t*>(ws);
-  uint16_t* A = reinterpret_cast<uint16_t*>(ws + round256((size_t)(T * L * C * 4)));
-  float* kv = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(A) + round256((size_t)(T * K * 2)));
+  // one operand slot per layer (every layer's rows are gathered before the first projection), then kv
+  const size_t a_slot = a_slot_bytes(T, K);
+  uint8_t* const A0 = ws + round256((size_t)(T * L * C * 4));
+  auto rows_of = [&](int l) { return A0 + (size_t)l * a_slot; };                 // bf16 rows or codes
+  auto scales_of = [&](int l) { return rows_of(l) + round256((size_t)(T * K)); };  // FP8 variant
+  float* kv = reinterpret_cast<float*>(A0 + (size_t)L * a_slot);
   // workspace beyond the minimum goes to the projection (stream-K partials)
   void* gemm_ws = ws_bytes > need ? static_cast<void*>(ws + need) : nullptr;
   const size_t gemm_ws_bytes = ws_bytes > need ? ws_bytes - need : 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   // each launch may start while its predecessor finishes (programmatic dependent launch)
   HashParams hp;
@@ -377,52 +395,72 @@ int engram_forward(const EngramDims* dims, const EngramHashTables* tables, const
                    tok->lookback_ids, tables->token_map, tables->multipliers, tables->primes, tables->offsets, ids,
                    err_flag, hp);
   if (rc) return rc;
-  // an FP8 table in the first layer: hash and that layer's gather in one kernel
-  const bool fused = layers[0].table_format == ENGRAM_TABLE_FP8_E8M0;
-  if (fused) {
+  // the hash kernel also fetches the rows of the leading run of FP8 layers
+  int fused = 0;
+  while (fused < L && fused < kMaxGatherLayers && layers[fused].table_format == ENGRAM_TABLE_FP8_E8M0) ++fused;
+  if (fused > 0) {
     HashGatherParams g{};
     g.h = hp;
-    g.table = layers[0].table;
-    g.scales = layers[0].table_scales;
-    g.num_rows = layers[0].table_rows;
     g.D = dims->head_dim;
-    if (layers[0].wkv_format == ENGRAM_WKV_MXFP8) {
-      g.out_codes = reinterpret_cast<uint8_t*>(A);
-      g.out_scales = g.out_codes + round256((size_t)(T * K));
-    } else {
-      g.out_bf16 = A;
+    g.layers = fused;
+    for (int l = 0; l < fused; ++l) {
+      g.table[l] = layers[l].table;
+      g.scales[l] = layers[l].table_scales;
+      g.num_rows[l] = layers[l].table_rows;
+      if (layers[l].wkv_format == ENGRAM_WKV_MXFP8) {
+        g.out_codes[l] = rows_of(l);
+        g.out_scales[l] = scales_of(l);
+      } else {
+        g.out_bf16[l] = reinterpret_cast<uint16_t*>(rows_of(l));
+      }
     }
-    cudaError_t e = launch_hash_gather(g, static_cast<cudaStream_t>(stream), true);
+    cudaError_t e = launch_hash_gather(g, st, true);
     if (e != cudaSuccess) return fail_cuda(e, "engram_forward: hash + gather launch");
   } else {
-    cudaError_t e = launch_hash(hp, static_cast<cudaStream_t>(stream), true);
+    cudaError_t e = launch_hash(hp, st, true);
     if (e != cudaSuccess) return fail_cuda(e, "engram_hash: launch");
+  }
+  // the other layers' rows: one launch per run of consecutive layers with the same table format
+  // and operand kind (bf16 rows or FP8 codes), before the first projection
+  for (int l = fused; l < L;) {
+    const int fmt = layers[l].table_format;
+    const bool mx = layers[l].wkv_format == ENGRAM_WKV_MXFP8;
+    int e = l + 1;
+    while (e < L && e - l < kMaxGatherLayers && layers[e].table_format == fmt &&
+           (layers[e].wkv_format == ENGRAM_WKV_MXFP8) == mx)
+      ++e;
+    cudaError_t ce;
+    if (mx) {
+      GatherCodesLayers m{};
+      m.n = e - l;
+      for (int j = l; j < e; ++j)
+        m.l[j - l] = GatherCodesParams{ids + (int64_t)j * C, (int64_t)L * C, T, C, dims->head_dim, layers[j].table,
+                                       layers[j].table_scales, layers[j].table_rows, rows_of(j), scales_of(j),
+                                       err_flag};
+      ce = launch_gather_codes(m, st, true);
+    } else {
+      GatherLayers m{};
+      m.n = e - l;
+      for (int j = l; j < e; ++j)
+        m.l[j - l] = GatherParams{fmt, ids + (int64_t)j * C, (int64_t)L * C, T, C, dims->head_dim, layers[j].table,
+                                  layers[j].table_scales, layers[j].table_rows,
+                                  reinterpret_cast<uint16_t*>(rows_of(j)), err_flag};
+      ce = launch_gather(m, st, true);
+    }
+    if (ce != cudaSuccess) return fail_cuda(ce, "engram_forward: gather launch");
+    l = e;
   }
   for (int l = 0; l < L; ++l) {
     const EngramLayerWeights& w = layers[l];
-    const bool gathered = fused && l == 0;
     if (w.wkv_format == ENGRAM_WKV_MXFP8) {
-      // FP8 variant: the rows' codes and scales are the A operand as they are (the A region holds
-      // T*K codes, then the T*K/32 scale bytes)
-      uint8_t* codes = reinterpret_cast<uint8_t*>(A);
-      uint8_t* sa = codes + round256((size_t)(T * K));
-      if (!gathered) {
-        rc = gather_codes_impl(ids + (int64_t)l * C, (int64_t)L * C, T, C, dims->head_dim, w.table, w.table_scales,
-                               w.table_rows, codes, sa, err_flag, stream, true);
-        if (rc) return rc;
-      }
-      rc = project_mx_impl(codes, sa, reinterpret_cast<const uint8_t*>(w.wkv), w.wkv_scales, kv, T, (int32_t)K,
-                           (int32_t)N, err_flag, stream, true);
-      if (rc) return rc;
+      // FP8 variant: the rows' codes and scales are the A operand as they are
+      rc = project_mx_impl(rows_of(l), scales_of(l), reinterpret_cast<const uint8_t*>(w.wkv), w.wkv_scales, kv, T,
+                           (int32_t)K, (int32_t)N, err_flag, stream, true);
     } else {
-      if (!gathered) {
-        rc = gather_impl(w.table_format, ids + (int64_t)l * C, (int64_t)L * C, T, C, dims->head_dim, w.table,
-                         w.table_scales, w.table_rows, A, err_flag, stream, true);
-        if (rc) return rc;
-      }
-      rc = project_impl(A, w.wkv, kv, T, (int32_t)K, (int32_t)N, gemm_ws, gemm_ws_bytes, err_flag, stream, true);
-      if (rc) return rc;
+      rc = project_impl(reinterpret_cast<const uint16_t*>(rows_of(l)), w.wkv, kv, T, (int32_t)K, (int32_t)N, gemm_ws,
+                        gemm_ws_bytes, err_flag, stream, true);
     }
+    if (rc) return rc;
     rc = gate_impl(dims, streams[l], kv, w.q_weight, w.k_weight, tok->token_mask, T, err_flag, stream, true);
     if (rc) return rc;
   }

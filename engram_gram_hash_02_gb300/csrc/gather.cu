@@ -51,7 +51,8 @@ __device__ __forceinline__ void flag(int32_t* err, int32_t bit) {
 
 // ---- FP8-E4M3 + E8M0 ------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads)
-gather_fp8_kernel(const GatherParams p) {
+gather_fp8_kernel(const GatherLayers m) {
+  const GatherParams& p = m.l[blockIdx.y];
   pdl_wait();                                    // ids come from the hash kernel
   pdl_trigger();
   const int chunks_per_row = p.D >> 4;                 // 16 values per chunk
@@ -111,7 +112,8 @@ gather_fp8_kernel(const GatherParams p) {
 
 // ---- bf16 rows: copy ----------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads)
-gather_bf16_kernel(const GatherParams p) {
+gather_bf16_kernel(const GatherLayers m) {
+  const GatherParams& p = m.l[blockIdx.y];
   pdl_wait();
   pdl_trigger();
   const int chunks_per_row = p.D >> 3;                 // 8 values per chunk
@@ -151,7 +153,8 @@ gather_bf16_kernel(const GatherParams p) {
 // quant = (qs[32*(e/128) + e%32] >> 2*((e%128)/32)) & 3, then d*scale*q - dmin*min.
 // Lane L writes elements 8L..8L+7: half = L/16, bit pair j = (L/4)%4, l0 = 8*(L%4), b = L/2.
 __global__ void __launch_bounds__(kThreads)
-gather_q2k_kernel(const GatherParams p) {
+gather_q2k_kernel(const GatherLayers m) {
+  const GatherParams& p = m.l[blockIdx.y];
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
@@ -222,10 +225,11 @@ unsigned grid_for(int64_t work_items, int64_t per_block) {
   return (unsigned)(b < cap ? b : cap);
 }
 
-// ---- hash fused with the first layer's FP8 gather (engram_forward) ----------------------------
+// ---- hash fused with the leading FP8 layers' gathers (engram_forward) ---------------------------
 // One CTA per token: warp 0 hashes the token (its window loads in flight while the block stages
 // cu_seqlens), the ids go to the global id buffer and to shared memory, then all threads fetch
-// the layer-0 rows, 16 bytes per thread and step, dequantised to bf16 or copied as codes.
+// the token's rows of layers 0 .. layers-1, 16 bytes per thread and step, dequantised to bf16 or
+// copied as codes.
 constexpr int kHgThreads = 128;
 
 __global__ void __launch_bounds__(kHgThreads)
@@ -248,38 +252,45 @@ hash_gather_fp8_kernel(const HashGatherParams p) {
   const int sblocks = p.D >> 5;
   const int64_t K = (int64_t)C * p.D;
   const int64_t rows4 = (p.h.T + 3) & ~(int64_t)3;
-  const uint8_t* __restrict__ weight = static_cast<const uint8_t*>(p.table);
-  for (int i = threadIdx.x; i < C * cpr; i += kHgThreads) {
-    const int col = i / cpr;
-    const int j = i - col * cpr;
-    const int64_t id = s_ids[col];              // layer 0: (layer, column) index = column
-    const bool ok = id >= 0 && id < p.num_rows;
-    if (!ok && j == 0) flag(p.h.err, ENGRAM_ERR_ROW_ID);
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (ok) v = ld_stream_v4(weight + id * p.D + (j << 4));
-    const int64_t e0 = t * K + (int64_t)col * p.D + (j << 4);   // first element of this chunk
-    if (p.out_bf16 != nullptr) {
-      uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-      if (ok) {
-        const float scale = __uint_as_float((uint32_t)__ldg(p.scales + id * sblocks + (j >> 1)) << 23);
-        lo.x = dequant_pair(v.x, scale);
-        lo.y = dequant_pair(v.x >> 16, scale);
-        lo.z = dequant_pair(v.y, scale);
-        lo.w = dequant_pair(v.y >> 16, scale);
-        hi.x = dequant_pair(v.z, scale);
-        hi.y = dequant_pair(v.z >> 16, scale);
-        hi.z = dequant_pair(v.w, scale);
-        hi.w = dequant_pair(v.w >> 16, scale);
-      }
-      uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + e0);
-      dst[0] = lo;
-      dst[1] = hi;
-    } else {
-      *reinterpret_cast<uint4*>(p.out_codes + e0) = v;
-      if (j < sblocks) {
-        const int b = col * sblocks + j;          // block of 32 along K
-        p.out_scales[((int64_t)(b >> 2) * rows4 + t) * 4 + (b & 3)] =
-            ok ? __ldg(p.scales + id * sblocks + j) : (uint8_t)127;
+#pragma unroll 1
+  for (int l = 0; l < p.layers; ++l) {
+    const uint8_t* __restrict__ weight = static_cast<const uint8_t*>(p.table[l]);
+    const uint8_t* __restrict__ scales = p.scales[l];
+    const int64_t num_rows = p.num_rows[l];
+    uint16_t* const out_bf16 = p.out_bf16[l];
+    uint8_t* const out_codes = p.out_codes[l];
+    uint8_t* const out_scales = p.out_scales[l];
+    for (int i = threadIdx.x; i < C * cpr; i += kHgThreads) {
+      const int col = i / cpr;
+      const int j = i - col * cpr;
+      const int64_t id = s_ids[l * C + col];      // ids of token t in (layer, column) order
+      const bool ok = id >= 0 && id < num_rows;
+      if (!ok && j == 0) flag(p.h.err, ENGRAM_ERR_ROW_ID);
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (ok) v = ld_stream_v4(weight + id * p.D + (j << 4));
+      const int64_t e0 = t * K + (int64_t)col * p.D + (j << 4);   // first element of this chunk
+      if (out_bf16 != nullptr) {
+        uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+        if (ok) {
+          const float scale = __uint_as_float((uint32_t)__ldg(scales + id * sblocks + (j >> 1)) << 23);
+          lo.x = dequant_pair(v.x, scale);
+          lo.y = dequant_pair(v.x >> 16, scale);
+          lo.z = dequant_pair(v.y, scale);
+          lo.w = dequant_pair(v.y >> 16, scale);
+          hi.x = dequant_pair(v.z, scale);
+          hi.y = dequant_pair(v.z >> 16, scale);
+          hi.z = dequant_pair(v.w, scale);
+          hi.w = dequant_pair(v.w >> 16, scale);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(out_bf16 + e0);
+        dst[0] = lo;
+        dst[1] = hi;
+      } else {
+        *reinterpret_cast<uint4*>(out_codes + e0) = v;
+        if (j < sblocks) {
+          const int b = col * sblocks + j;          // block of 32 along K
+          out_scales[((int64_t)(b >> 2) * rows4 + t) * 4 + (b & 3)] = ok ? __ldg(scales + id * sblocks + j) : (uint8_t)127;
+        }
       }
     }
   }
@@ -292,18 +303,20 @@ cudaError_t launch_hash_gather(const HashGatherParams& p, cudaStream_t stream, b
   return launch_k(hash_gather_fp8_kernel, dim3((unsigned)p.h.T), dim3(kHgThreads), 0, stream, pdl, p);
 }
 
-cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl) {
+cudaError_t launch_gather(const GatherLayers& m, cudaStream_t stream, bool pdl) {
+  if (m.n < 1 || m.n > kMaxGatherLayers) return cudaErrorInvalidValue;
+  const GatherParams& p = m.l[0];                // every layer has p's format, T, C and D
   const int64_t rows = p.T * p.C;
   switch (p.fmt) {
     case ENGRAM_TABLE_FP8_E8M0:
-      return launch_k(gather_fp8_kernel, dim3(grid_for(rows * (p.D / 16), kThreads * kChunksPerThread)),
-                      dim3(kThreads), 0, stream, pdl, p);
+      return launch_k(gather_fp8_kernel, dim3(grid_for(rows * (p.D / 16), kThreads * kChunksPerThread), m.n),
+                      dim3(kThreads), 0, stream, pdl, m);
     case ENGRAM_TABLE_BF16:
-      return launch_k(gather_bf16_kernel, dim3(grid_for(rows * (p.D / 8), kThreads * kChunksPerThread)),
-                      dim3(kThreads), 0, stream, pdl, p);
+      return launch_k(gather_bf16_kernel, dim3(grid_for(rows * (p.D / 8), kThreads * kChunksPerThread), m.n),
+                      dim3(kThreads), 0, stream, pdl, m);
     case ENGRAM_TABLE_Q2K:
-      return launch_k(gather_q2k_kernel, dim3(grid_for(rows, (kThreads / 32) * kQ2kRowsPerWarp)), dim3(kThreads),
-                      0, stream, pdl, p);
+      return launch_k(gather_q2k_kernel, dim3(grid_for(rows, (kThreads / 32) * kQ2kRowsPerWarp), m.n),
+                      dim3(kThreads), 0, stream, pdl, m);
     default:
       return cudaErrorInvalidValue;
   }

@@ -72,18 +72,24 @@ struct HashParams {
 };
 cudaError_t launch_hash(const HashParams& p, cudaStream_t stream, bool pdl = false);
 
-// Hash fused with the first layer's gather of an FP8_E8M0 table (engram_forward): one CTA per
-// token hashes it (all layers' ids to h.out) and gathers its layer-0 rows, dequantised to bf16
-// (out_bf16) or as codes and scale words (out_codes / out_scales, the FP8 variant's layout).
+// Layers whose rows one gather launch fetches (engram_forward gathers every layer's rows right
+// after the hash, before the first projection)
+constexpr int kMaxGatherLayers = 8;
+
+// Hash fused with the gathers of the leading FP8_E8M0 layers (engram_forward): one CTA per token
+// hashes it (all layers' ids to h.out) and gathers its rows of layers 0 .. layers-1, dequantised to
+// bf16 (out_bf16[l]) or as codes and scale words (out_codes[l] / out_scales[l], the FP8 variant's
+// layout).
 struct HashGatherParams {
   HashParams h;
-  const void* table;          // e4m3 codes [num_rows, D]
-  const uint8_t* scales;      // [num_rows, D/32]
-  int64_t num_rows;
   int32_t D;
-  uint16_t* out_bf16;         // [T, C*D] or NULL
-  uint8_t* out_codes;         // [T, C*D] or NULL
-  uint8_t* out_scales;        // [ceil(C*D/128)][T4][4] or NULL
+  int32_t layers;                                  // 1 .. kMaxGatherLayers
+  const void* table[kMaxGatherLayers];             // e4m3 codes [num_rows, D]
+  const uint8_t* scales[kMaxGatherLayers];         // [num_rows, D/32]
+  int64_t num_rows[kMaxGatherLayers];
+  uint16_t* out_bf16[kMaxGatherLayers];            // [T, C*D] or NULL
+  uint8_t* out_codes[kMaxGatherLayers];            // [T, C*D] or NULL
+  uint8_t* out_scales[kMaxGatherLayers];           // [ceil(C*D/128)][T4][4] or NULL
 };
 cudaError_t launch_hash_gather(const HashGatherParams& p, cudaStream_t stream, bool pdl = false);
 
@@ -99,7 +105,18 @@ struct GatherParams {
   uint16_t* out;
   int32_t* err;
 };
-cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl = false);
+// n layers of the same format, T, C and D in one launch (grid y = layer)
+struct GatherLayers {
+  int32_t n;
+  GatherParams l[kMaxGatherLayers];
+};
+cudaError_t launch_gather(const GatherLayers& p, cudaStream_t stream, bool pdl = false);
+inline cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl = false) {
+  GatherLayers m{};
+  m.n = 1;
+  m.l[0] = p;
+  return launch_gather(m, stream, pdl);
+}
 
 struct GemmParams {
   const uint16_t* A;
@@ -128,7 +145,17 @@ struct GatherCodesParams {
   uint8_t* out_scales;        // [T, C*D/32]
   int32_t* err;
 };
-cudaError_t launch_gather_codes(const GatherCodesParams& p, cudaStream_t stream, bool pdl = false);
+struct GatherCodesLayers {
+  int32_t n;
+  GatherCodesParams l[kMaxGatherLayers];
+};
+cudaError_t launch_gather_codes(const GatherCodesLayers& p, cudaStream_t stream, bool pdl = false);
+inline cudaError_t launch_gather_codes(const GatherCodesParams& p, cudaStream_t stream, bool pdl = false) {
+  GatherCodesLayers m{};
+  m.n = 1;
+  m.l[0] = p;
+  return launch_gather_codes(m, stream, pdl);
+}
 cudaError_t launch_quantize_mxfp8(const uint16_t* w, int64_t N, int32_t K, uint8_t* codes, uint8_t* scales,
                                   cudaStream_t stream);
 

@@ -72,7 +72,8 @@ quantize_mxfp8_kernel(const uint16_t* __restrict__ w, int64_t N, int32_t K, uint
 // the chunk-0 thread also copies the row's scale bytes. Rows outside the table: codes 0, scale
 // byte 127 (a zero row).
 __global__ void __launch_bounds__(kThreads)
-gather_fp8_codes_kernel(const GatherCodesParams p) {
+gather_fp8_codes_kernel(const GatherCodesLayers m) {
+  const GatherCodesParams& p = m.l[blockIdx.y];
   pdl_wait();                                    // ids come from the hash kernel
   pdl_trigger();
   const int chunks_per_row = p.D >> 4;
@@ -113,13 +114,15 @@ cudaError_t launch_quantize_mxfp8(const uint16_t* w, int64_t N, int32_t K, uint8
                   scales);
 }
 
-cudaError_t launch_gather_codes(const GatherCodesParams& p, cudaStream_t stream, bool pdl) {
+cudaError_t launch_gather_codes(const GatherCodesLayers& m, cudaStream_t stream, bool pdl) {
+  if (m.n < 1 || m.n > kMaxGatherLayers) return cudaErrorInvalidValue;
+  const GatherCodesParams& p = m.l[0];           // every layer has p's T, C and D
   const int64_t total = p.T * p.C * (p.D >> 4);
   int64_t blocks = (total + kThreads - 1) / kThreads;
   const int64_t cap = (int64_t)num_sms() * 32;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  return launch_k(gather_fp8_codes_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, stream, pdl, p);
+  return launch_k(gather_fp8_codes_kernel, dim3((unsigned)blocks, (unsigned)m.n), dim3(kThreads), 0, stream, pdl, m);
 }
 
 }  // namespace engram

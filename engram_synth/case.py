@@ -25,20 +25,28 @@ class Case:
     extra: dict = field(default_factory=dict)
 
 
+def layer_formats(w) -> tuple:
+    """Table format of each layer: ``w.extra["layer_formats"]`` if given, else ``w.table_format``."""
+    fmts = tuple(w.extra.get("layer_formats", (w.table_format,) * w.layers))
+    if len(fmts) != w.layers:
+        raise ValueError(f"{w.name}: {len(fmts)} layer formats for {w.layers} layers")
+    return fmts
+
+
 def make_tables(w, rows_per_layer, device, seed: int):
     out = []
-    for layer, rows in enumerate(rows_per_layer):
+    for layer, (rows, fmt) in enumerate(zip(rows_per_layer, layer_formats(w))):
         s = seed * 100 + layer
         rows = int(rows)
-        if w.table_format == "fp8":
+        if fmt == "fp8":
             t, sc = gen.fp8_table(rows, w.head_dim, w.table_std, s, device)
-        elif w.table_format == "q2k":
+        elif fmt == "q2k":
             t, sc = gen.q2k_table(rows, s, device), None
-        elif w.table_format == "bf16":
+        elif fmt == "bf16":
             t, sc = gen.bf16_table(rows, w.head_dim, w.table_std, s, device), None
         else:
-            raise ValueError(w.table_format)
-        out.append({"fmt": w.table_format, "table": t, "scales": sc, "num_rows": rows})
+            raise ValueError(fmt)
+        out.append({"fmt": fmt, "table": t, "scales": sc, "num_rows": rows})
     return out
 
 

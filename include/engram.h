@@ -275,20 +275,27 @@ typedef struct EngramTokens {
 } EngramTokens;
 
 /* Minimum bytes of device workspace engram_forward needs for T tokens (256-byte aligned pieces:
- * hash ids [T, layers, C] int32, rows [T, C*head_dim] bf16, kv [T, (hc+1)*H] fp32). Workspace
- * beyond the minimum is handed to the projection: add engram_project_workspace_bytes(T,
- * C*head_dim, (hc+1)*H) for its stream-K schedule. */
+ * hash ids [T, layers, C] int32; one operand slot per layer, holding its rows [T, C*head_dim]
+ * bf16, or with an MXFP8 wkv its row codes [T, C*head_dim] and then the scale words
+ * [ceil(C*head_dim/128)][T4][4]; kv [T, (hc+1)*H] fp32). Workspace beyond the minimum is handed
+ * to the projection: add engram_project_workspace_bytes(T, C*head_dim, (hc+1)*H) for its
+ * stream-K schedule. */
 size_t engram_forward_workspace_bytes(const EngramDims* dims, int64_t T);
 
 /*
- * The whole path: one hash launch for all layers, then per layer gather -> project -> gate.
+ * The whole path. Every layer's rows are gathered before the first projection, as [vLLM]
+ * prepare_embeddings stages every layer's input before the decoder layers: one hash launch for
+ * all layers, which also fetches the rows of the leading run of FP8+E8M0 layers (at most 8), then
+ * one gather launch per run of consecutive remaining layers with the same table format and wkv
+ * format (at most 8 each); then per layer project -> gate.
  *   layers     host array [dims->layers] of per-layer weights
  *   streams    host array [dims->layers] of device fp32 [T, hc, H] highways, updated in place
  *   workspace  device, >= engram_forward_workspace_bytes(dims, T), 256-byte aligned (see there
  *              for the optional extra that speeds up the projection)
  *   out_ids    device int32 [T, layers, C] or NULL: if given, the hash writes the ids there
  *              (and the workspace's id region goes unused)
- * Launches 1 + 3*layers kernels on `stream`.
+ * Launches 1 + (gather launches) + 2*layers kernels on `stream`: 3 for one FP8 layer, 4 for one
+ * Q2_K or bf16 layer, 6 for two layers of one format.
  */
 int engram_forward(const EngramDims* dims, const EngramHashTables* tables,
                    const EngramLayerWeights* layers, const EngramTokens* tokens,

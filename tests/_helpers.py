@@ -58,9 +58,21 @@ def build(name_or_w, device="cuda", seq_lens=None, seed=None):
     return w, case, (primes, offsets, rows, mult)
 
 
+def _per_layer(flag, layers: int) -> list:
+    return [bool(f) for f in flag] if isinstance(flag, (list, tuple)) else [bool(flag)] * layers
+
+
+def a_slot_bytes(T: int, K: int) -> int:
+    """One layer's operand slot in the engram_forward workspace: bf16 rows [T, K], or the FP8
+    variant's codes [T, K] then (256-byte aligned) scale words [ceil(K/128), T4, 4]."""
+    r256 = lambda x: (x + 255) // 256 * 256
+    return r256(max(T * K * 2, r256(T * K) + (K + 127) // 128 * ((T + 3) // 4 * 4) * 4))
+
+
 def gpu_forward(w, case, setup, device="cuda", with_err=True, mx=False):
     """Run engram_forward on the device; returns ids, per-layer streams, the workspace views.
-    With ``mx`` the layers carry MXFP8 wkv (quantised on the device) and the FP8 variant runs."""
+    With ``mx`` (a bool, or one per layer) the layers carry MXFP8 wkv (quantised on the device)
+    and the FP8 variant runs for them."""
     import engram_gram_hash_02_gb300 as E
     primes, offsets, rows, mult = setup
     b = case.batch
@@ -68,10 +80,11 @@ def gpu_forward(w, case, setup, device="cuda", with_err=True, mx=False):
     dims = dims_for(w, pad)
     tables = E.HashTables(to_device(b["token_map"], device), to_device(mult, device),
                           to_device(primes, device), to_device(offsets, device))
+    mxl = _per_layer(mx, w.layers)
     layers = []
     for l, t in enumerate(case.tables):
         wkv, wsc = case.wkv[l], None
-        if mx:
+        if mxl[l]:
             wkv, wsc = E.quantize_mxfp8(case.wkv[l])
         layers.append(E.LayerWeights(t["fmt"], t["table"], t["scales"], t["num_rows"], wkv, case.q_weight[l],
                                      case.k_weight[l], wkv_scales=wsc))
@@ -85,20 +98,31 @@ def gpu_forward(w, case, setup, device="cuda", with_err=True, mx=False):
                             lookback_ids=to_device(b["lookback_ids"], device), out_ids=out_ids, err=err)
     torch.cuda.synchronize()
     ws = plan.workspace
-    T, K, N = w.tokens, w.K, w.N
-    id_bytes = ((T * w.layers * w.cols * 4 + 255) // 256) * 256
-    a_bytes = ((T * K * 2 + 255) // 256) * 256
-    kv_last = ws[id_bytes + a_bytes:id_bytes + a_bytes + T * N * 4].view(torch.float32).view(T, N)
+    T, K, N, L = w.tokens, w.K, w.N, w.layers
+    id_bytes = ((T * L * w.cols * 4 + 255) // 256) * 256
+    slot = a_slot_bytes(T, K)
+    kv0 = id_bytes + L * slot
+    kv_last = ws[kv0:kv0 + T * N * 4].view(torch.float32).view(T, N)
     out = {"ids": out_ids, "streams": streams, "kv_last": kv_last, "err": int(err.item()) if err is not None else 0,
-           "dims": dims}
-    if mx:
-        code_bytes = ((T * K + 255) // 256) * 256
-        shp = E.mx_scale_shape(T, K)
-        out["A_codes_last"] = ws[id_bytes:id_bytes + T * K].view(T, K)
-        sc = ws[id_bytes + code_bytes:id_bytes + code_bytes + shp[0] * shp[1] * shp[2]].view(shp)
-        out["A_scales_last"] = mx_words_to_rows(sc, T, K // 32)
+           "dims": dims, "A": [], "A_codes": [], "A_scales": []}
+    # every layer's gathered operand stays in its slot
+    code_bytes = ((T * K + 255) // 256) * 256
+    shp = E.mx_scale_shape(T, K)
+    for l in range(L):
+        a0 = id_bytes + l * slot
+        if mxl[l]:
+            out["A"].append(None)
+            out["A_codes"].append(ws[a0:a0 + T * K].view(T, K))
+            sc = ws[a0 + code_bytes:a0 + code_bytes + shp[0] * shp[1] * shp[2]].view(shp)
+            out["A_scales"].append(mx_words_to_rows(sc, T, K // 32))
+        else:
+            out["A"].append(ws[a0:a0 + T * K * 2].view(torch.bfloat16).view(T, K))
+            out["A_codes"].append(None)
+            out["A_scales"].append(None)
+    if mxl[-1]:
+        out["A_codes_last"], out["A_scales_last"] = out["A_codes"][-1], out["A_scales"][-1]
     else:
-        out["A_last"] = ws[id_bytes:id_bytes + T * K * 2].view(torch.bfloat16).view(T, K)
+        out["A_last"] = out["A"][-1]
     return out
 
 
@@ -146,7 +170,8 @@ def compact_table(tab: dict, ids: np.ndarray):
 
 def oracle_forward(w, case, tokens=None, mx=False):
     """The oracle's whole path on the selected tokens (all if None), from its own layout. With
-    ``mx``, the FP8 variant: raw FP8 rows and the oracle's own MXFP8 encoding of wkv."""
+    ``mx`` (a bool, or one per layer), the FP8 variant: raw FP8 rows and the oracle's own MXFP8
+    encoding of wkv."""
     primes, offsets, rows, mult = oracle_setup(w)
     b = case.batch
     pad = pad_id_of(w, b["token_map"])
@@ -156,10 +181,11 @@ def oracle_forward(w, case, tokens=None, mx=False):
     T = ids.shape[0]
     sel = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
     mask = b["token_mask"]
+    mxl = _per_layer(mx, w.layers)
     layers = []
     for l, tab in enumerate(case.tables):
         t_np, s_np, remap, nrows = compact_table(tab, ids[sel, l, :])
-        if mx:
+        if mxl[l]:
             codes, sc, n_oob = O.gather_fp8_raw(t_np, s_np, remap, nrows)
             wc, ws_ = oracle_mxfp8_quantize(case.wkv[l])
             kv = O.project_mxfp8(codes, sc, wc, ws_)

@@ -4,10 +4,13 @@ Every workload runs at its full size in the launch configuration the bench uses;
 checks all tokens where it finishes in seconds and a seeded sample (always including masked,
 document-start and sequence-start tokens) elsewhere.  Hash ids are compared for every token.
 """
+from dataclasses import replace
+
 import numpy as np
 import pytest
 import torch
 
+from engram_synth import get_workload
 from oracle import engram_oracle as O
 from tests import _helpers as H
 
@@ -49,9 +52,10 @@ def test_forward_matches_oracle(name, sample):
     for l, lref in enumerate(ref["layers"]):
         h = got["streams"][l].index_select(0, sel_t).cpu().numpy()
         H.check_streams(h, lref["streams"], lref["streams_in"], f"{name} layer {l}")
-    # the last layer's rows and kv are still in the workspace
+    # every layer's rows, and the last layer's kv, are still in the workspace
+    for l, lref in enumerate(ref["layers"]):
+        assert np.array_equal(H.bits16(got["A"][l].index_select(0, sel_t)), lref["a_bits"]), f"{name} rows {l}"
     last = ref["layers"][-1]
-    assert np.array_equal(H.bits16(got["A_last"].index_select(0, sel_t)), last["a_bits"])
     H.check_kv(got["kv_last"].index_select(0, sel_t).cpu().numpy(), last["kv"], f"{name} kv")
     mask = case.batch.get("token_mask")
     if mask is not None:
@@ -89,3 +93,41 @@ def test_forward_large_t16384_sampled():
     del case, got
     torch.cuda.empty_cache()
     assert O is not None
+
+
+# engram_forward gathers every layer's rows before the first projection: the hash kernel fetches
+# the leading run of FP8 layers (at most 8), then one gather launch per run of layers with the
+# same table format and operand kind (at most 8). These mixes reach each branch of that plan.
+@pytest.mark.parametrize("base,layer_ids,fmts,mx,sample", [
+    ("q2k_t8192", None, ("q2k", "fp8"), False, 384),           # no leading FP8 layer: two gather launches
+    ("decode_fp8_t256_2layer", None, ("fp8", "q2k"), False, 0),  # FP8 rows from the hash kernel, Q2_K after
+    ("decode_fp8_t256_2layer", None, None, (False, True), 0),    # one fused launch: bf16 rows, then codes
+    ("tiny_fp8", tuple(range(1, 11)), None, tuple(l % 2 == 1 for l in range(10)), 0),   # 8 fused + 2
+    ("tiny_fp8", tuple(range(1, 11)), ("q2k",) * 10, False, 0),  # gather launches of 8 and 2 layers
+])
+def test_forward_layer_mixes(base, layer_ids, fmts, mx, sample):
+    w = get_workload(base)
+    kw = {"name": f"{base}_mix"}
+    if layer_ids is not None:
+        kw["layer_ids"] = layer_ids
+    if fmts is not None:
+        kw["extra"] = {"layer_formats": fmts}
+    w = replace(w, **kw)
+    w, case, setup = H.build(w)
+    got = H.gpu_forward(w, case, setup, mx=mx)
+    toks = _sample(w, case, sample) if sample else None
+    ref = H.oracle_forward(w, case, toks, mx=mx)
+    assert got["err"] == 0
+    assert np.array_equal(got["ids"].cpu().numpy(), ref["ids"].astype(np.int32))
+    sel = ref["tokens"]
+    sel_t = torch.from_numpy(sel).to(got["ids"].device)
+    for l, lref in enumerate(ref["layers"]):
+        what = f"{w.name} layer {l}"
+        if got["A"][l] is not None:
+            assert np.array_equal(H.bits16(got["A"][l].index_select(0, sel_t)), lref["a_bits"]), what
+        else:
+            assert np.array_equal(got["A_codes"][l].index_select(0, sel_t).cpu().numpy(), lref["a_bits"][0]), what
+            assert np.array_equal(got["A_scales"][l][sel], lref["a_bits"][1]), what
+        h = got["streams"][l].index_select(0, sel_t).cpu().numpy()
+        H.check_streams(h, lref["streams"], lref["streams_in"], what)
+    H.check_kv(got["kv_last"].index_select(0, sel_t).cpu().numpy(), ref["layers"][-1]["kv"], f"{w.name} kv")

@@ -16,7 +16,13 @@
 // Every item accumulates into two TMEM accumulators, which the tensor core runs as independent
 // chains (back-to-back MMAs into one accumulator wait on each other): the two 128-row halves of
 // a 256-row tile, or, for tiles of at most 128 rows, the even and odd k steps of one tile
-// (summed in the epilogue).
+// (summed in the epilogue), or the two column halves of a split tile (below).
+//
+// Split tiles (129..256 tokens, when wkv is wide): instead of one CTA per 256-row x BN tile, two
+// CTAs per 128-row x 2*BN tile pair up on each column block (consecutive CTAs, so their wkv tiles
+// are read from HBM once and served twice by L2). A stage then holds a 16 KB token tile and a
+// 2*BN-row weight tile instead of 32 KB and BN rows: twice the weight bytes in flight per SM in
+// the same shared memory.
 //
 // Schedules (items are (tile, k-range) pairs; the roles walk the same sequence):
 //   data-parallel  CTA c takes tiles c, c + grid, ... over the whole K (many tiles);
@@ -63,6 +69,7 @@ struct Ctl {
 struct GemmArgs {
   int32_t M, K, N;
   int32_t BN, msub, stages, num_kb;
+  int32_t nsplit;                          // 2: tile = two column halves of BN/2, one MMA each
   int32_t m_tiles, n_tiles, group_m;
   int32_t stage_bytes;
   uint32_t idesc;
@@ -183,6 +190,8 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const uint32_t st = tiles + (uint32_t)(s * a.stage_bytes);
         mbar_expect_tx(full, (uint32_t)a.stage_bytes);
         tma_load_2d(st + a.msub * kATileBytes, &tmB, full, kb * kBK, n0);
+        if (a.nsplit == 2)
+          tma_load_2d(st + a.msub * kATileBytes + (a.BN >> 1) * (kBK * 2), &tmB, full, kb * kBK, n0 + (a.BN >> 1));
       };
       auto load_a = [&](int it, int kb, int m0) {
         const int s = it % a.stages;
@@ -274,7 +283,13 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k) {
             const uint64_t bdesc = b0 + (uint64_t)(2 * k);
-            if (a.msub == 2) {
+            if (a.nsplit == 2) {
+              // two chains: the two column halves (the second half's rows start BN/2 rows on)
+              const uint32_t acc = (kb > item.k0 || k > 0) ? 1u : 0u;
+              tc_mma(tmem, a0 + (uint64_t)(2 * k), bdesc, a.idesc, acc);
+              tc_mma(tmem + a.acc_stride, a0 + (uint64_t)(2 * k), bdesc + (uint64_t)(((a.BN >> 1) * kBK * 2) >> 4),
+                     a.idesc, acc);
+            } else if (a.msub == 2) {
               // two chains: the two 128-row halves
               const uint32_t acc = (kb > item.k0 || k > 0) ? 1u : 0u;
               tc_mma(tmem, a0 + (uint64_t)(2 * k), bdesc, a.idesc, acc);
@@ -336,8 +351,15 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         __syncwarp();
         if (*abort_flag) break;
       }
-      store_accumulators(&tmD, D, a.M, a.N, tmem, q, lane, stg, a.msub, a.msub == 1, a.acc_stride, a.BN, m0, n0,
-                         adder);
+      if (a.nsplit == 2) {
+        const int hb = a.BN >> 1;
+        store_accumulators(&tmD, D, a.M, a.N, tmem, q, lane, stg, 1, false, a.acc_stride, hb, m0, n0, false);
+        store_accumulators(&tmD, D, a.M, a.N, tmem + a.acc_stride, q, lane, stg, 1, false, a.acc_stride, hb, m0,
+                           n0 + hb, false);
+      } else {
+        store_accumulators(&tmD, D, a.M, a.N, tmem, q, lane, stg, a.msub, a.msub == 1, a.acc_stride, a.BN, m0, n0,
+                           adder);
+      }
       // this item's stores are complete (global writes done) before the tile or flag moves on
       if (lane == 0) {
         asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -429,6 +451,20 @@ bool plan_gemm(int64_t M, int K, int N, int sms, size_t ws_bytes, Plan& P) {
   if (sk && ws_bytes < sk_ws) sk = false;       // no room for the flags: data-parallel
   a.stream_k = sk ? 1 : 0;
   a.BN = sk ? bn_sk : (g_bn_override > 0 ? g_bn_override : pick_bn_dp(a.m_tiles, N, sms));
+  a.nsplit = 1;
+  if (!sk && g_bn_override == 0 && M > 128 && M <= 256) {
+    // split tiles: the narrowest column half (a multiple of 16) that keeps both CTAs of every
+    // column block in one wave; only for wide wkv, where the half is 128..208 columns (three or
+    // more stages of 16 KB + 2 * half * 128 bytes still fit)
+    int hb = 16;
+    while (2 * (int64_t)((N + 2 * hb - 1) / (2 * hb)) > sms) hb += 16;
+    if (hb >= 128 && hb <= 208) {
+      a.nsplit = 2;
+      a.msub = 1;
+      a.m_tiles = (int32_t)((M + 127) / 128);
+      a.BN = 2 * hb;
+    }
+  }
   a.n_tiles = (N + a.BN - 1) / a.BN;
   const int64_t n_tiles_total = (int64_t)a.m_tiles * a.n_tiles;
   if (n_tiles_total > 0x7fffffff) return false;
@@ -438,16 +474,16 @@ bool plan_gemm(int64_t M, int K, int N, int sms, size_t ws_bytes, Plan& P) {
   } else {
     P.grid = n_tiles_total < sms ? (int)n_tiles_total : sms;
   }
-  a.stage_bytes = a.msub * kATileBytes + a.BN * kBK * 2;
+  a.stage_bytes = a.msub * kATileBytes + a.BN * kBK * 2;   // split tiles: both halves
   a.stages = (kSmemBudget - 1024 - kEpiBytes - (int)sizeof(Ctl)) / a.stage_bytes;
   if (a.stages > kMaxStages) a.stages = kMaxStages;
   if (a.stages < 2) return false;
-  a.acc_stride = pow2_at_least((uint32_t)a.BN);
+  a.acc_stride = pow2_at_least((uint32_t)(a.BN / a.nsplit));
   a.tmem_cols = a.acc_stride * 2;              // two accumulators (chains) per item
   if (a.tmem_cols > 512) return false;
   a.idesc = (1u << 4)                          // accumulate in f32
             | (1u << 7) | (1u << 10)           // A and B are bf16
-            | ((uint32_t)(a.BN >> 3) << 17)    // N
+            | ((uint32_t)((a.BN / a.nsplit) >> 3) << 17)    // N (of one MMA)
             | ((uint32_t)(128 >> 4) << 24);    // M = 128; A and B K-major (bits 15, 16 = 0)
   P.smem = 1024 + a.stages * a.stage_bytes + kEpiBytes + (int)sizeof(Ctl);
   P.ws_needed = sk ? sk_ws : 0;
@@ -552,7 +588,7 @@ int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl) {
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
   CUtensorMap mA, mB, mD;
-  if (!make_map_bf16(&mA, p.A, p.M, p.K, 128) || !make_map_bf16(&mB, p.B, p.N, p.K, (uint32_t)a.BN) ||
+  if (!make_map_bf16(&mA, p.A, p.M, p.K, 128) || !make_map_bf16(&mB, p.B, p.N, p.K, (uint32_t)(a.BN / a.nsplit)) ||
       !make_map_f32(&mD, p.D, p.M, p.N)) {
     set_error("engram_project: cuTensorMapEncodeTiled failed (driver entry point missing or bad layout)");
     return ENGRAM_ECUDA;

@@ -215,6 +215,34 @@ def test_project_stream_k_matches_fp64_and_is_deterministic(T, K, N):
     H.check_kv(kv_dp.cpu().numpy()[rows], ref, f"data-parallel T={T} K={K} N={N}")
 
 
+@pytest.mark.parametrize("T,K,N", [
+    (256, 6144, 20480),    # the decode projection: 2 x 72 CTAs of 128 x 288 (halves of 144)
+    (200, 640, 20480),     # ragged second row block
+    (129, 256, 20480),     # a one-row second row block
+    (160, 512, 19008),     # halves of 128; the last column block reaches only into its first half
+])
+def test_project_split_tiles_match_unsplit_and_fp64(T, K, N):
+    # 129..256 tokens with wide wkv run as pairs of 128-row CTAs on 2*BN-column tiles; forcing the
+    # tile width (engram_set_gemm_tile) runs the 256-row tiles instead. Each output element sums
+    # the same k steps in the same order either way.
+    g = torch.Generator(device=DEV).manual_seed(T + K + N)
+    A = (torch.randn(T, K, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    W = (torch.randn(N, K, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    try:
+        E().set_gemm_schedule(1)
+        split = E().engram_project(A, W, err=err)
+        E().set_gemm_tile(144)
+        whole = E().engram_project(A, W, err=err)
+        torch.cuda.synchronize()
+    finally:
+        E().set_gemm_tile(0)
+        E().set_gemm_schedule(0)
+    assert int(err.item()) == 0
+    assert torch.equal(split, whole)
+    H.check_kv(split.cpu().numpy(), O.project(H.bits16(A), H.bits16(W)), f"split T={T} K={K} N={N}")
+
+
 def test_project_integer_exact():
     # small integers: every product and partial sum is exact in fp32
     g = torch.Generator(device=DEV).manual_seed(3)

@@ -3,8 +3,8 @@ memory (an engine whose pool owns all device memory and lends a plugin only its 
 a real-time loop that cannot take cudaMalloc's implicit synchronisation).  It keeps its scratch
 in a static device array instead of a caller workspace.
 
-Checked through the C ABI against engram_forward (caller workspace) on the decode workload, on
-two calls in a row, so leftovers in the shared static array cannot leak into a result.  This
+Checked through the C ABI against engram_forward (caller workspace) on the decode workload (one
+and two layers, each layer's rows in its own slot of the array), on two calls in a row, so leftovers in the shared static array cannot leak into a result.  This
 file is collected last, so a run that stops at the first failure has run every other test.
 """
 import ctypes
@@ -34,8 +34,9 @@ def _plan(w, case, setup, streams, out_ids, err, workspace=None):
                          workspace=workspace, out_ids=out_ids, err=err)
 
 
-def test_noalloc_matches_workspace_entry_point_twice():
-    w, case, setup = H.build("decode_fp8_t256")
+@pytest.mark.parametrize("name", ["decode_fp8_t256", "decode_fp8_t256_2layer"])
+def test_noalloc_matches_workspace_entry_point_twice(name):
+    w, case, setup = H.build(name)
     shape = (w.tokens, w.layers, w.cols)
     ref_streams = [s.clone() for s in case.streams]
     ref_ids = torch.empty(shape, dtype=torch.int32, device=DEV)

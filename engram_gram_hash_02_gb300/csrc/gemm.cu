@@ -18,6 +18,12 @@
 // a 256-row tile, or, for tiles of at most 128 rows, the even and odd k steps of one tile
 // (summed in the epilogue), or the two column halves of a split tile (below).
 //
+// Short token blocks (one block of at most 112 tokens): the token tile holds only the rows that
+// exist, rounded up to 16, so a stage is mostly weight tile and the ring gets deeper. The MMA
+// still reads 128 rows; rows past the tile read whatever shared memory follows (the weight tile,
+// later stages), which only feeds accumulator rows that are never stored (row m of the product
+// depends on row m of A alone), and every such read stays inside the CTA's allocation.
+//
 // Split tiles (129..256 tokens, when wkv is wide): instead of one CTA per 256-row x BN tile, two
 // CTAs per 128-row x 2*BN tile pair up on each column block (consecutive CTAs, so their wkv tiles
 // are read from HBM once and served twice by L2). A stage then holds a 16 KB token tile and a
@@ -70,6 +76,7 @@ struct GemmArgs {
   int32_t M, K, N;
   int32_t BN, msub, stages, num_kb;
   int32_t nsplit;                          // 2: tile = two column halves of BN/2, one MMA each
+  int32_t a_rows, a_bytes;                 // token rows loaded per 128-row half, bytes of the token tile
   int32_t m_tiles, n_tiles, group_m;
   int32_t stage_bytes;
   uint32_t idesc;
@@ -189,9 +196,9 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const uint32_t full = smem_u32(&ctl->full[s]);
         const uint32_t st = tiles + (uint32_t)(s * a.stage_bytes);
         mbar_expect_tx(full, (uint32_t)a.stage_bytes);
-        tma_load_2d(st + a.msub * kATileBytes, &tmB, full, kb * kBK, n0);
+        tma_load_2d(st + a.a_bytes, &tmB, full, kb * kBK, n0);
         if (a.nsplit == 2)
-          tma_load_2d(st + a.msub * kATileBytes + (a.BN >> 1) * (kBK * 2), &tmB, full, kb * kBK, n0 + (a.BN >> 1));
+          tma_load_2d(st + a.a_bytes + (a.BN >> 1) * (kBK * 2), &tmB, full, kb * kBK, n0 + (a.BN >> 1));
       };
       auto load_a = [&](int it, int kb, int m0) {
         const int s = it % a.stages;
@@ -279,7 +286,7 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           // encoded start address, the second 128-row half (16 KB) adds 1024
           const uint32_t st = tiles + (uint32_t)(slot * a.stage_bytes);
           const uint64_t a0 = smem_desc_sw128(st);
-          const uint64_t b0 = smem_desc_sw128(st + (uint32_t)(a.msub * kATileBytes));
+          const uint64_t b0 = smem_desc_sw128(st + (uint32_t)a.a_bytes);
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k) {
             const uint64_t bdesc = b0 + (uint64_t)(2 * k);
@@ -474,7 +481,10 @@ bool plan_gemm(int64_t M, int K, int N, int sms, size_t ws_bytes, Plan& P) {
   } else {
     P.grid = n_tiles_total < sms ? (int)n_tiles_total : sms;
   }
-  a.stage_bytes = a.msub * kATileBytes + a.BN * kBK * 2;   // split tiles: both halves
+  // token rows per half: all 128, or for a single short block only the rows that exist
+  a.a_rows = (!sk && a.msub == 1 && a.m_tiles == 1 && M <= 112) ? (int32_t)((M + 15) / 16 * 16) : 128;
+  a.a_bytes = a.msub * a.a_rows * kBK * 2;
+  a.stage_bytes = a.a_bytes + a.BN * kBK * 2;   // split tiles: both halves
   a.stages = (kSmemBudget - 1024 - kEpiBytes - (int)sizeof(Ctl)) / a.stage_bytes;
   if (a.stages > kMaxStages) a.stages = kMaxStages;
   if (a.stages < 2) return false;
@@ -588,7 +598,7 @@ int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl) {
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
   CUtensorMap mA, mB, mD;
-  if (!make_map_bf16(&mA, p.A, p.M, p.K, 128) || !make_map_bf16(&mB, p.B, p.N, p.K, (uint32_t)(a.BN / a.nsplit)) ||
+  if (!make_map_bf16(&mA, p.A, p.M, p.K, (uint32_t)a.a_rows) || !make_map_bf16(&mB, p.B, p.N, p.K, (uint32_t)(a.BN / a.nsplit)) ||
       !make_map_f32(&mD, p.D, p.M, p.N)) {
     set_error("engram_project: cuTensorMapEncodeTiled failed (driver entry point missing or bad layout)");
     return ENGRAM_ECUDA;

@@ -22,6 +22,9 @@
 //               reads, for accumulator lanes in quarter q, lane 32q + n % 32, column n / 32. So
 //               every quarter holds lane r, column c = scale word of A row r + 32c (per 128-row
 //               half) and of B row r + 32c.
+// A single block of at most 112 tokens loads only the token rows that exist (rounded up to 16), so
+// the ring gets deeper; the MMA's reads of the other rows see whatever shared memory follows and
+// only feed accumulator rows that are never stored (all inside the CTA's allocation).
 // Accumulators: two independent chains (the two 128-row halves of a 256-row tile, or for tiles of
 // at most 128 rows the even and odd k steps, summed in the epilogue) when tensor memory allows,
 // else one. All waits are bounded (~2 s of SM clock cycles); on expiry the CTA reports
@@ -54,6 +57,7 @@ struct MxArgs {
   int32_t M, K, N;
   int32_t BN, msub, chains, stages, num_kb;
   int32_t m_tiles, n_tiles, group_m;
+  int32_t a_rows;                            // token rows loaded per 128-row half (128, or fewer for one short block)
   int32_t a_bytes, b_bytes;
   int32_t stage_bytes;                       // A + W codes + both scale runs, rounded to 1 KB
   int32_t rows_a4, rows_b4;                  // rows of the scale word arrays (M, N rounded up to 4)
@@ -381,7 +385,8 @@ bool plan_mx(int64_t M, int K, int N, int sms, MxPlan& P) {
   a.m_tiles = (int32_t)((M + 128 * a.msub - 1) / (128 * a.msub));
   a.num_kb = K / kStageK;
   a.group_m = 16;
-  a.a_bytes = a.msub * kATileBytes;
+  a.a_rows = (a.msub == 1 && a.m_tiles == 1 && M <= 112) ? (int32_t)((M + 15) / 16 * 16) : 128;
+  a.a_bytes = a.msub * a.a_rows * kStageK;
   a.sf_slot_w = (uint32_t)(4 * a.msub + 8);
   a.sfb_off = (uint32_t)(4 * a.msub);
   const int avail = kSmemBudget - 1024 - kEpiBytes - (int)sizeof(MxCtl);
@@ -454,7 +459,7 @@ int launch_gemm_mx(const GemmMxParams& p, cudaStream_t stream, bool pdl) {
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
   CUtensorMap mA, mB, mD;
-  if (!make_map_u8(&mA, p.A, p.M, p.K, 128) || !make_map_u8(&mB, p.B, p.N, p.K, (uint32_t)a.BN) ||
+  if (!make_map_u8(&mA, p.A, p.M, p.K, (uint32_t)a.a_rows) || !make_map_u8(&mB, p.B, p.N, p.K, (uint32_t)a.BN) ||
       !make_map_f32(&mD, p.D, p.M, p.N)) {
     set_error("engram_project_mxfp8: cuTensorMapEncodeTiled failed (driver entry point missing or bad layout)");
     return ENGRAM_ECUDA;

@@ -38,9 +38,9 @@ L2_FLUSH_BYTES = 512 << 20
 # workload, with the sha256 of the kernel's source at capture time (stale -> traffic null).
 NCU_TRAFFIC: dict = {
     # profiles/wkv_gemm_decode_fp8_t256.md: dram__bytes_read.sum + dram__bytes_write.sum
-    "project0@decode_fp8_t256": {"bytes": 254889472 + 3268864, "src_sha": "42d298574051e71d"},
+    "project0@decode_fp8_t256": {"bytes": 254901760 + 3296000, "src_sha": "ca4a50c28673842a"},
     # profiles/wkv_gemm_mx_decode_fp8_t256.md (FP8 variant, --wkv mxfp8)
-    "project0@decode_fp8_t256@mxfp8": {"bytes": 131441408 + 3196160, "src_sha": "f0631574c6a8fe56",
+    "project0@decode_fp8_t256@mxfp8": {"bytes": 131441408 + 3046400, "src_sha": "6b962bd1336136b1",
                                        "src": "gemm_mx.cu"},
 }
 

@@ -4,8 +4,8 @@
 
 One step is one pass of the whole path over one batch of the workload (default: the decode
 step, 256 sequences x 1 new token, FP8+E8M0 table of ~25M rows, hidden 4096, hc 4).  Inputs
-are resident in HBM; the L2 is flushed (512 MB write) before every timed step; each step is
-timed with CUDA events on the launching stream, per kernel as well.  Under torchrun every
+are resident in HBM; the L2 is flushed (512 MB write, then a 256 MB read) before every timed
+step; each step is timed with CUDA events on the launching stream, per kernel as well.  Under torchrun every
 rank runs its own replica (the path needs no exchange): weak scaling, max time over ranks.
 
 --impl reference times the CPU oracle (oracle/) on a bounded sample of the same workload.
@@ -33,6 +33,7 @@ from engram_synth.case import make_case, to_device  # noqa: E402
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 512 << 20
+L2_FLUSH_READ_BYTES = 256 << 20
 
 # DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by kernel and
 # workload, with the sha256 of the kernel's source at capture time (stale -> traffic null).
@@ -273,6 +274,15 @@ def run_ours(args, rank, world, device):
     stream = torch.cuda.current_stream()
     calls = path.stage_calls(stream)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    flush_read = torch.ones(L2_FLUSH_READ_BYTES // 4, dtype=torch.float32, device=device)
+
+    def flush_l2(k):
+        # write a buffer four times the L2, then read one twice its size: the L2 then holds none of
+        # the step's data and no dirty line of the flush, whose write-back would otherwise land
+        # inside the timed step
+        flush.fill_(float(k))
+        flush_read.sum()
+
 
     def step(evs=None):
         for i, (name, fn) in enumerate(calls):
@@ -288,9 +298,9 @@ def run_ours(args, rank, world, device):
                               cu_seqlens=path.cu, sequence_ids=path.sid, token_mask=path.mask,
                               lookback_ids=path.lookback, out_ids=path.ids, err=path.err)
     for _ in range(args.warmup):
-        flush.fill_(1.0)
+        flush_l2(1)
         plan.run(stream)
-        flush.fill_(1.0)
+        flush_l2(1)
         step()
     torch.cuda.synchronize()
     if path.err.item() != 0:
@@ -311,14 +321,14 @@ def run_ours(args, rank, world, device):
         sampler.mark("t0")
     wall0 = time.perf_counter()
     for k in range(args.steps):
-        flush.fill_(float(k))
+        flush_l2(k)
         fw[k][0].record(stream)
         plan.run(stream)
         fw[k][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     for k in range(args.steps):
-        flush.fill_(float(k))
+        flush_l2(k)
         step(ev[k])
     torch.cuda.synchronize()
     if sampler:
@@ -389,7 +399,8 @@ def run_ours(args, rank, world, device):
                    "head_dim": w.head_dim, "table": w.table_format, "table_rows": int(sum(path.table_rows)),
                    "hidden": w.hidden, "hc": w.hc, "K": w.K, "N": w.N,
                    "wkv": "mxfp8" if mx else "bf16",
-                   "l2": "flushed before every timed step (512 MB write)", "parallelism": f"replicas{world}"},
+                   "l2": "flushed before every timed step (512 MB write, then a 256 MB read)",
+                   "parallelism": f"replicas{world}"},
         "gpu_launches": args.steps * (forward_launches(w) + len(calls)),
         "stages": stages,
         "roofline": {"kernel": dom, "bound": model["bound"], "achieved": round(achieved, 1),

@@ -172,7 +172,9 @@ int engram_project(const uint16_t* A, const uint16_t* wkv, float* kv, int64_t T,
 size_t engram_project_workspace_bytes(int64_t T, int32_t K, int32_t N);
 
 /* Tuning knob for engram_project: force the tile width (columns per CTA, a multiple of 16 in
- * [16, 256]); 0 restores the automatic choice. Process-wide; not thread-safe against calls. */
+ * [16, 256]); 0 restores the automatic choice. A forced width also turns off the split tiles the
+ * automatic choice uses for 129..256 tokens (pairs of 128-row CTAs on twice as many columns).
+ * Process-wide; not thread-safe against calls. */
 void engram_set_gemm_tile(int32_t bn);
 /* Tuning knob for engram_project: 1 forces the data-parallel tile schedule, 2 the stream-K
  * schedule (when the workspace allows), 0 restores the automatic choice. Process-wide. */

@@ -243,6 +243,25 @@ def test_project_split_tiles_match_unsplit_and_fp64(T, K, N):
     H.check_kv(split.cpu().numpy(), O.project(H.bits16(A), H.bits16(W)), f"split T={T} K={K} N={N}")
 
 
+@pytest.mark.parametrize("T,bn", [(40, 64), (1, 16), (112, 128)])
+def test_project_short_token_tiles_over_several_waves(T, bn):
+    # one block of at most 112 tokens loads only its rows (rounded up to 16); with narrow tiles
+    # every CTA runs several tiles in a row over the same ring
+    K, N = 256, 35840
+    g = torch.Generator(device=DEV).manual_seed(T + bn)
+    A = (torch.randn(T, K, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    W = (torch.randn(N, K, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    try:
+        E().set_gemm_tile(bn)
+        kv = E().engram_project(A, W, err=err)
+        torch.cuda.synchronize()
+    finally:
+        E().set_gemm_tile(0)
+    assert int(err.item()) == 0
+    H.check_kv(kv.cpu().numpy(), O.project(H.bits16(A), H.bits16(W)), f"short T={T} bn={bn}")
+
+
 def test_project_integer_exact():
     # small integers: every product and partial sum is exact in fp32
     g = torch.Generator(device=DEV).manual_seed(3)

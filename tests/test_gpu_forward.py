@@ -131,3 +131,28 @@ def test_forward_layer_mixes(base, layer_ids, fmts, mx, sample):
         h = got["streams"][l].index_select(0, sel_t).cpu().numpy()
         H.check_streams(h, lref["streams"], lref["streams_in"], what)
     H.check_kv(got["kv_last"].index_select(0, sel_t).cpu().numpy(), ref["layers"][-1]["kv"], f"{w.name} kv")
+
+
+@pytest.mark.parametrize("name,seq_lens", [
+    ("tiny_bf16", (0, 5, 0, 3, 1)),          # empty sequences between ragged ones
+    ("decode_fp8_t256", (1,) * 129),         # 129 tokens: split tiles whose second row block has one row
+    ("decode_fp8_t256", (1,) * 112),         # the largest short token tile
+    ("q2k_t8192", (7, 0, 120)),              # two Q2_K layers on a ragged batch of 127 tokens
+])
+def test_forward_ragged_and_boundary_sizes(name, seq_lens):
+    w, case, setup = H.build(name, seq_lens=seq_lens)
+    got = H.gpu_forward(w, case, setup)
+    ref = H.oracle_forward(w, case)
+    assert got["err"] == 0
+    assert np.array_equal(got["ids"].cpu().numpy(), ref["ids"].astype(np.int32))
+    for l, lref in enumerate(ref["layers"]):
+        what = f"{name} T={w.tokens} layer {l}"
+        assert np.array_equal(H.bits16(got["A"][l]), lref["a_bits"]), what
+        H.check_streams(got["streams"][l].cpu().numpy(), lref["streams"], lref["streams_in"], what)
+    H.check_kv(got["kv_last"].cpu().numpy(), ref["layers"][-1]["kv"], f"{name} T={w.tokens} kv")
+
+
+def test_forward_zero_tokens_is_a_no_op():
+    w, case, setup = H.build("tiny_bf16", seq_lens=(0,))
+    got = H.gpu_forward(w, case, setup)
+    assert got["err"] == 0 and got["ids"].numel() == 0 and got["streams"][0].numel() == 0

@@ -7,7 +7,7 @@
 //
 // One warp per token. Lane k < max_ngram loads window slot k (issued speculatively, before the
 // token's sequence start is known), then decides whether the slot may be read (its position is
-// alive and in t's document, or a live lookback entry); a ballot turns the per-slot verdicts into
+// alive and in t's document, or a live lookback entry); a ballot turns the per-slot answers into
 // the walk back from t (slot k is open only if slots 0..k all are); shuffles hand every lane the
 // window. Lanes then take the (layer, column) pairs: each mixes its n-gram's slots with XOR of
 // id * multiplier and reduces modulo its head's prime.

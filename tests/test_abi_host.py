@@ -133,3 +133,54 @@ def test_mx_scale_shape():
     assert Bd.mx_scale_shape(256, 6144) == (48, 256, 4)
     assert Bd.mx_scale_shape(1, 6144) == (48, 4, 4)          # rows padded to a multiple of 4
     assert Bd.mx_scale_shape(5, 96) == (1, 8, 4)             # 3 blocks of 32 -> one word per row
+
+
+def test_forward_host_checks_fire_before_any_cuda_call(lib):
+    from engram_gram_hash_02_gb300 import binding as Bd
+    buf = (ctypes.c_uint8 * 8192)()
+    addr = (ctypes.addressof(buf) + 255) & ~255
+    stream = None
+    tables = Bd._HashTables(addr, addr, addr, addr)
+    tok = Bd._Tokens(addr, 256, addr, 256, None, None, None)
+    streams = (ctypes.c_void_p * 2)(addr, addr)
+
+    def layer(fmt, wkv_fmt):
+        return Bd._LayerWeights(Bd.TABLE_FORMATS[fmt], addr, addr, 1000, addr, addr, addr, wkv_fmt,
+                                addr if wkv_fmt == Bd.WKV_MXFP8 else None)
+
+    # more than 256 (layer, column) pairs
+    dims = Bd.EngramDims(11, 4, 8, 256, 4096, 4, 163840, 131072, 0, 1e-6, 1e-6)
+    layers = (Bd._LayerWeights * 11)(*[layer("fp8", Bd.WKV_BF16)] * 11)
+    rc = lib.engram_forward(ctypes.byref(dims), ctypes.byref(tables), layers, ctypes.byref(tok), streams, addr,
+                            1 << 40, None, None, stream)
+    assert rc == -1 and "256" in lib.engram_last_error().decode()
+    # a workspace below engram_forward_workspace_bytes
+    dims = Bd.EngramDims(2, 4, 8, 256, 4096, 4, 163840, 131072, 0, 1e-6, 1e-6)
+    need = lib.engram_forward_workspace_bytes(ctypes.byref(dims), 256)
+    layers = (Bd._LayerWeights * 2)(layer("fp8", Bd.WKV_BF16), layer("q2k", Bd.WKV_MXFP8))
+    rc = lib.engram_forward(ctypes.byref(dims), ctypes.byref(tables), layers, ctypes.byref(tok), streams, addr,
+                            need - 256, None, None, stream)
+    assert rc == -1 and str(need) in lib.engram_last_error().decode()
+    # an MXFP8 wkv needs an FP8 table (its rows are the A operand): rejected before any launch
+    rc = lib.engram_forward(ctypes.byref(dims), ctypes.byref(tables), layers, ctypes.byref(tok), streams, addr,
+                            need, None, None, stream)
+    assert rc == -1 and "MXFP8 wkv needs an FP8" in lib.engram_last_error().decode()
+    # zero tokens: nothing to do
+    tok0 = Bd._Tokens(addr, 0, addr, 1, None, None, None)
+    assert lib.engram_forward(ctypes.byref(dims), ctypes.byref(tables), layers, ctypes.byref(tok0), streams, None,
+                              0, None, None, stream) == 0
+
+
+def test_forward_workspace_holds_one_operand_slot_per_layer(lib):
+    from engram_gram_hash_02_gb300 import binding as Bd
+    r256 = lambda x: (x + 255) // 256 * 256
+    for T in (1, 7, 256, 4096):
+        one = Bd.EngramDims(1, 4, 8, 256, 4096, 4, 163840, 131072, 0, 1e-6, 1e-6)
+        two = Bd.EngramDims(2, 4, 8, 256, 4096, 4, 163840, 131072, 0, 1e-6, 1e-6)
+        C, K, N = 24, 24 * 256, 4096 * 5
+        w1 = lib.engram_forward_workspace_bytes(ctypes.byref(one), T)
+        w2 = lib.engram_forward_workspace_bytes(ctypes.byref(two), T)
+        slot = w2 - w1 - (r256(4 * T * 2 * C) - r256(4 * T * C))
+        # a slot holds the bf16 rows, or the FP8 codes and then their scale words
+        assert slot >= 2 * T * K and slot >= r256(T * K) + (K // 128) * ((T + 3) // 4 * 4) * 4
+        assert w1 == r256(4 * T * C) + slot + r256(4 * T * N)

@@ -395,12 +395,8 @@ def run_ours(args, rank, world, device):
         "vs_baseline": None,
         "dtype": "e4m3 x e4m3 (MXFP8), fp32 accumulate" if mx else "bf16",
         "data": "synthetic (seeded; tables, weights and ids drawn on device)",
-        "config": {"workload": w.name, "tokens": w.tokens, "layers": w.layers, "hash_cols": w.cols,
-                   "head_dim": w.head_dim, "table": w.table_format, "table_rows": int(sum(path.table_rows)),
-                   "hidden": w.hidden, "hc": w.hc, "K": w.K, "N": w.N,
-                   "wkv": "mxfp8" if mx else "bf16",
-                   "l2": "flushed before every timed step (512 MB write, then a 256 MB read)",
-                   "parallelism": f"replicas{world}"},
+        "config": dict(workload_config(w, int(sum(path.table_rows)), "mxfp8" if mx else "bf16", world),
+                       l2="flushed before every timed step (512 MB write, then a 256 MB read)"),
         "gpu_launches": args.steps * (forward_launches(w) + len(calls)),
         "stages": stages,
         "roofline": {"kernel": dom, "bound": model["bound"], "achieved": round(achieved, 1),
@@ -603,6 +599,13 @@ def cpu_baseline(w, case, n_tokens):
                       f"numpy fp64, BLAS threads = host cores"}
 
 
+def workload_config(w, table_rows: int, wkv: str, world: int) -> dict:
+    """The workload keys of the JSON line's config (both arms)."""
+    return {"workload": w.name, "tokens": w.tokens, "layers": w.layers, "hash_cols": w.cols,
+            "head_dim": w.head_dim, "table": w.table_format, "table_rows": table_rows, "hidden": w.hidden,
+            "hc": w.hc, "K": w.K, "N": w.N, "wkv": wkv, "parallelism": f"replicas{world}"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
@@ -633,7 +636,7 @@ def run_reference(args, rank, world):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded)",
-        "config": {"workload": w.name, "tokens": w.tokens, "layers": w.layers},
+        "config": workload_config(w, int(np.asarray(rows).sum()), "bf16", world),
         "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s per layer", "cores": os.cpu_count(),
                          "kind": "oracle",
                          "sample": f"{len(r.sel)} of {w.tokens} tokens per step (hash over all), numpy fp64"},

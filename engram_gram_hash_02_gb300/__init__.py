@@ -8,6 +8,7 @@ from .binding import (  # noqa: F401
     ERR_RAW_ID,
     ERR_ROW_ID,
     TABLE_FORMATS,
+    ProjectPlan,
     EngramDims,
     EngramError,
     ForwardPlan,
@@ -26,9 +27,11 @@ from .binding import (  # noqa: F401
     lib,
     make_dims,
     mx_scale_shape,
+    project_plan,
     project_workspace_bytes,
     quantize_mxfp8,
     set_gemm_mx_tile,
     set_gemm_schedule,
     set_gemm_tile,
+    sync_status,
 )

@@ -53,6 +53,16 @@ class _HashTables(C.Structure):
                 ("offsets", C.c_void_p)]
 
 
+class ProjectPlan(C.Structure):
+    """engram_project_plan's answer (see include/engram.h, EngramProjectPlan)."""
+    _fields_ = [(n, C.c_int32) for n in ("grid", "threads", "smem_bytes", "tile_rows", "tile_cols", "split",
+                                          "token_rows_loaded", "stages", "stage_bytes", "tmem_cols", "stream_k",
+                                          "mma_read_end", "smem_avail")]
+
+    def as_dict(self) -> dict:
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
 class _Tokens(C.Structure):
     _fields_ = [("input_ids", C.c_void_p), ("T", C.c_int64), ("cu_seqlens", C.c_void_p),
                 ("num_seqs", C.c_int32), ("sequence_ids", C.c_void_p), ("token_mask", C.c_void_p),
@@ -93,6 +103,8 @@ def lib() -> C.CDLL:
         L.engram_project_mxfp8.argtypes = [P, P, P, P, P, I64, I32, I32, P, P]
         L.engram_set_gemm_mx_tile.argtypes = [I32]
         L.engram_set_gemm_mx_tile.restype = None
+        L.engram_sync_status.argtypes = [P, P]
+        L.engram_project_plan.argtypes = [I64, I32, I32, I32, I32, P]
         _lib = L
     return _lib
 
@@ -130,6 +142,33 @@ def _stream(stream) -> int | None:
 def _u16(t: torch.Tensor, name: str) -> torch.Tensor:
     """bf16 tensors cross the C boundary as their bit patterns."""
     return _dev(t, torch.bfloat16, name)
+
+
+def _shape(t, shape, name: str):
+    """The kernels index every tensor by the sizes they are given: a tensor of another shape is
+    read or written past its end, so shapes are checked here (before any device check)."""
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if tuple(t.shape) != tuple(int(x) for x in shape):
+        raise ValueError(f"{name} must have shape {tuple(int(x) for x in shape)} (got {tuple(t.shape)})")
+
+
+def _numel_at_least(t, n: int, name: str):
+    if t is not None and t.numel() * t.element_size() < n:
+        raise ValueError(f"{name} holds {t.numel() * t.element_size()} bytes, needs at least {n}")
+
+
+def _table_shape_check(fmt: str, table, scales, num_rows: int, head_dim: int, where: str):
+    if int(num_rows) < 0:
+        raise ValueError(f"{where}: num_rows must be >= 0")
+    row_bytes = {"fp8": head_dim, "q2k": 84, "bf16": 2 * head_dim}[fmt]
+    _numel_at_least(table, int(num_rows) * row_bytes, f"{where}: table")
+    if fmt == "fp8":
+        if scales is None:
+            raise ValueError(f"{where}: an FP8 table needs its scales")
+        _numel_at_least(scales, int(num_rows) * (head_dim // 32), f"{where}: table scales")
 
 
 # ---------------------------------------------------------------------------------------------
@@ -171,8 +210,17 @@ def make_dims(layers, max_ngram, n_heads, head_dim, hidden, hc, raw_vocab, compr
 
 def engram_hash(dims: EngramDims, input_ids, token_map, multipliers, primes, offsets, cu_seqlens=None,
                 sequence_ids=None, token_mask=None, lookback_ids=None, out=None, err=None, stream=None):
-    _dev(input_ids, torch.int32, "input_ids")
     T = input_ids.numel()
+    S = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    _shape(token_map, (dims.raw_vocab,), "token_map")
+    _shape(multipliers, (dims.layers, dims.max_ngram), "multipliers")
+    _shape(primes, (dims.layers, dims.cols), "primes")
+    _shape(offsets, (dims.layers, dims.cols), "offsets")
+    _shape(sequence_ids, (T,), "sequence_ids")
+    _shape(token_mask, (T,), "token_mask")
+    _shape(lookback_ids, (S, dims.max_ngram - 1), "lookback_ids")
+    _shape(out, (T, dims.layers, dims.cols), "out")
+    _dev(input_ids, torch.int32, "input_ids")
     _dev(token_map, torch.int32, "token_map")
     _dev(multipliers, torch.int64, "multipliers")
     _dev(primes, torch.int64, "primes")
@@ -185,7 +233,6 @@ def engram_hash(dims: EngramDims, input_ids, token_map, multipliers, primes, off
     if out is None:
         out = torch.empty((T, dims.layers, dims.cols), dtype=torch.int32, device=input_ids.device)
     _dev(out, torch.int32, "out")
-    S = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
     _check("engram_hash", lib().engram_hash(
         C.byref(dims), _ptr(input_ids), T, _ptr(cu_seqlens), S, _ptr(sequence_ids), _ptr(token_mask),
         _ptr(lookback_ids), _ptr(token_map), _ptr(multipliers), _ptr(primes), _ptr(offsets), _ptr(out),
@@ -196,11 +243,14 @@ def engram_hash(dims: EngramDims, input_ids, token_map, multipliers, primes, off
 def engram_gather_dequant(fmt: str, ids, table, scales, num_rows: int, head_dim: int, out=None, err=None,
                           stream=None):
     """ids: int32 [T, C] (a strided view [T, L, C][:, l] is fine: rows must have unit column stride)."""
-    if not (isinstance(ids, torch.Tensor) and ids.is_cuda and ids.dtype == torch.int32 and ids.dim() == 2
-            and ids.stride(1) == 1):
-        raise ValueError("ids must be a CUDA int32 [T, C] tensor with unit column stride")
+    if not (isinstance(ids, torch.Tensor) and ids.dim() == 2):
+        raise ValueError("ids must be a [T, C] tensor")
     T, Cc = ids.shape
     code = TABLE_FORMATS[fmt]
+    _table_shape_check(fmt, table, scales, num_rows, head_dim, "engram_gather_dequant")
+    _shape(out, (T, Cc * head_dim), "out")
+    if not (ids.is_cuda and ids.dtype == torch.int32 and ids.stride(1) == 1):
+        raise ValueError("ids must be a CUDA int32 [T, C] tensor with unit column stride")
     if not (table.is_cuda and table.is_contiguous()):
         raise ValueError("table must be a contiguous CUDA tensor")
     if scales is not None:
@@ -218,12 +268,15 @@ def engram_gather_dequant(fmt: str, ids, table, scales, num_rows: int, head_dim:
 def engram_project(A, wkv, out=None, err=None, workspace="auto", stream=None):
     """workspace: a uint8 CUDA tensor, None (no workspace), or "auto" (allocated at the size
     engram_project_workspace_bytes asks for)."""
-    _u16(A, "A")
-    _u16(wkv, "wkv")
+    if A.dim() != 2 or wkv.dim() != 2:
+        raise ValueError("A and wkv must be 2-D")
     T, K = A.shape
     N, K2 = wkv.shape
     if K != K2:
         raise ValueError(f"A is [T, {K}] but wkv is [{N}, {K2}]")
+    _shape(out, (T, N), "out")
+    _u16(A, "A")
+    _u16(wkv, "wkv")
     if out is None:
         out = torch.empty((T, N), dtype=torch.float32, device=A.device)
     _dev(out, torch.float32, "out")
@@ -239,13 +292,20 @@ def engram_project(A, wkv, out=None, err=None, workspace="auto", stream=None):
 
 def engram_gate(dims: EngramDims, streams, kv, q_weight, k_weight, token_mask=None, err=None, stream=None):
     """Updates ``streams`` (fp32 [T, hc, H]) in place and returns it."""
+    if not isinstance(streams, torch.Tensor) or streams.dim() != 3:
+        raise ValueError("streams must be a [T, hc, H] tensor")
+    T = streams.shape[0]
+    _shape(streams, (T, dims.hc, dims.hidden), "streams")
+    _shape(kv, (T, dims.hidden * (dims.hc + 1)), "kv")
+    _shape(q_weight, (dims.hc, dims.hidden), "q_weight")
+    _shape(k_weight, (dims.hc, dims.hidden), "k_weight")
+    _shape(token_mask, (T,), "token_mask")
     _dev(streams, torch.float32, "streams")
     _dev(kv, torch.float32, "kv")
     _u16(q_weight, "q_weight")
     _u16(k_weight, "k_weight")
     _opt(token_mask, torch.uint8, "token_mask")
     _opt(err, torch.int32, "err")
-    T = streams.shape[0]
     _check("engram_gate", lib().engram_gate(C.byref(dims), _ptr(streams), _ptr(kv), _ptr(q_weight),
                                              _ptr(k_weight), _ptr(token_mask), T, _ptr(err), _stream(stream)))
     return streams
@@ -271,6 +331,8 @@ def quantize_mxfp8(w: torch.Tensor, codes=None, scales=None, stream=None):
     (engram_quantize_mxfp8)."""
     _u16(w, "w")
     N, K = w.shape
+    _shape(codes, (N, K), "codes")
+    _shape(scales, mx_scale_shape(N, K), "scales")
     codes = torch.empty(N, K, dtype=torch.uint8, device=w.device) if codes is None else _dev(codes, torch.uint8, "codes")
     scales = (torch.empty(mx_scale_shape(N, K), dtype=torch.uint8, device=w.device) if scales is None
               else _dev(scales, torch.uint8, "scales"))
@@ -283,9 +345,14 @@ def engram_gather_fp8_codes(ids, table, table_scales, num_rows: int, head_dim: i
                             err=None, stream=None):
     """FP8 rows by id without dequantisation. ids int32 [T, C] (or a [T, L*C] slice: the row
     stride is ids.stride(0)) -> (codes uint8 [T, C*head_dim], scales ``mx_scale_shape(T, C*head_dim)``)."""
-    if not isinstance(ids, torch.Tensor) or ids.dtype != torch.int32 or not ids.is_cuda or ids.stride(1) != 1:
-        raise ValueError("ids must be a CUDA int32 tensor with unit column stride")
+    if not (isinstance(ids, torch.Tensor) and ids.dim() == 2):
+        raise ValueError("ids must be a [T, C] tensor")
     T, Cc = ids.shape
+    _table_shape_check("fp8", table, table_scales, num_rows, head_dim, "engram_gather_fp8_codes")
+    _shape(codes, (T, Cc * head_dim), "codes")
+    _shape(scales, mx_scale_shape(T, Cc * head_dim), "scales")
+    if ids.dtype != torch.int32 or not ids.is_cuda or ids.stride(1) != 1:
+        raise ValueError("ids must be a CUDA int32 tensor with unit column stride")
     _dev(table, torch.uint8, "table")
     _dev(table_scales, torch.uint8, "table_scales")
     _opt(err, torch.int32, "err")
@@ -305,6 +372,10 @@ def engram_project_mxfp8(a_codes, a_scales, w_codes, w_scales, out=None, err=Non
         _dev(t, torch.uint8, n)
     T, K = a_codes.shape
     N = w_codes.shape[0]
+    _shape(w_codes, (N, K), "w_codes")
+    _shape(a_scales, mx_scale_shape(T, K), "a_scales")
+    _shape(w_scales, mx_scale_shape(N, K), "w_scales")
+    _shape(out, (T, N), "out")
     out = torch.empty(T, N, dtype=torch.float32, device=a_codes.device) if out is None else _dev(out, torch.float32, "out")
     _opt(err, torch.int32, "err")
     _check("engram_project_mxfp8", lib().engram_project_mxfp8(_ptr(a_codes), _ptr(a_scales), _ptr(w_codes),
@@ -319,6 +390,23 @@ def set_gemm_mx_tile(bn: int = 0):
 
 def project_workspace_bytes(T: int, K: int, N: int) -> int:
     return int(lib().engram_project_workspace_bytes(T, K, N))
+
+
+def project_plan(T: int, K: int, N: int, wkv_format: str = "bf16", num_sms: int = 152) -> dict:
+    """The tile plan the projection would launch for this shape (engram_project_plan; host
+    only)."""
+    out = ProjectPlan()
+    fmt = {"bf16": WKV_BF16, "mxfp8": WKV_MXFP8}[wkv_format]
+    _check("engram_project_plan", lib().engram_project_plan(int(T), int(K), int(N), fmt, int(num_sms), C.byref(out)))
+    return out.as_dict()
+
+
+def sync_status(err: torch.Tensor, stream=None) -> int:
+    """engram_sync_status: waits for the stream, then 0 (err word clear), ENGRAM_EDATA (-3, an
+    id out of range was substituted) or ENGRAM_ECUDA (-2).  Returns the code; the message is
+    engram_last_error()."""
+    _dev(err, torch.int32, "err")
+    return int(lib().engram_sync_status(_ptr(err), _stream(stream)))
 
 
 # ---------------------------------------------------------------------------------------------
@@ -351,6 +439,46 @@ def forward_workspace_bytes(dims: EngramDims, T: int) -> int:
     return int(lib().engram_forward_workspace_bytes(C.byref(dims), T))
 
 
+def _check_forward_shapes(dims, tables, layers, input_ids, streams, cu_seqlens, sequence_ids, token_mask,
+                          lookback_ids, workspace, out_ids, err):
+    """Every size engram_forward reads from dims, checked against the tensors (the C side can see
+    only pointers: a short list or an undersized tensor would be read or written past its end)."""
+    L = int(dims.layers)
+    if len(layers) != L or len(streams) != L:
+        raise ValueError(f"dims.layers is {L} but {len(layers)} layer weights and {len(streams)} stream tensors "
+                         "were given")
+    if not isinstance(input_ids, torch.Tensor) or input_ids.dim() != 1:
+        raise ValueError("input_ids must be a 1-D tensor [T]")
+    T = input_ids.numel()
+    H, hc, D, Cc = int(dims.hidden), int(dims.hc), int(dims.head_dim), dims.cols
+    K, N = Cc * D, H * (hc + 1)
+    if cu_seqlens is not None and (cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2):
+        raise ValueError("cu_seqlens must be a 1-D tensor [S + 1] with S >= 1")
+    S = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    _shape(sequence_ids, (T,), "sequence_ids")
+    _shape(token_mask, (T,), "token_mask")
+    _shape(lookback_ids, (S, dims.max_ngram - 1), "lookback_ids")
+    _shape(out_ids, (T, L, Cc), "out_ids")
+    if err is not None and err.numel() < 1:
+        raise ValueError("err must hold one int32")
+    _shape(tables.token_map, (dims.raw_vocab,), "token_map")
+    _shape(tables.multipliers, (L, dims.max_ngram), "multipliers")
+    _shape(tables.primes, (L, Cc), "primes")
+    _shape(tables.offsets, (L, Cc), "offsets")
+    for i, (w, st) in enumerate(zip(layers, streams)):
+        _shape(st, (T, hc, H), f"streams[{i}]")
+        _shape(w.q_weight, (hc, H), f"layers[{i}].q_weight")
+        _shape(w.k_weight, (hc, H), f"layers[{i}].k_weight")
+        _shape(w.wkv, (N, K), f"layers[{i}].wkv")
+        if w.wkv_scales is not None:
+            _shape(w.wkv_scales, mx_scale_shape(N, K), f"layers[{i}].wkv_scales")
+        if w.fmt not in TABLE_FORMATS:
+            raise ValueError(f"layers[{i}]: unknown table format {w.fmt!r}")
+        _table_shape_check(w.fmt, w.table, w.scales, w.num_rows, D, f"layers[{i}]")
+    if workspace is not None:
+        _numel_at_least(workspace, forward_workspace_bytes(dims, T), "workspace")
+
+
 class ForwardPlan:
     """Marshalled arguments of engram_forward for fixed tensors, so a hot loop pays one
     ctypes call per step."""
@@ -360,6 +488,8 @@ class ForwardPlan:
                  out_ids=None, err=None):
         self.dims = dims
         T = input_ids.numel()
+        _check_forward_shapes(dims, tables, layers, input_ids, streams, cu_seqlens, sequence_ids, token_mask,
+                              lookback_ids, workspace, out_ids, err)
         _dev(input_ids, torch.int32, "input_ids")
         for name, t, dt in (("cu_seqlens", cu_seqlens, torch.int32), ("sequence_ids", sequence_ids, torch.int32),
                             ("token_mask", token_mask, torch.uint8), ("lookback_ids", lookback_ids, torch.int32),

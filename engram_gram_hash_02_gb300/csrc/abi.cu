@@ -38,6 +38,22 @@ int num_sms() {
   return cache[dev];
 }
 
+void* PerContextOnce::current_context() {
+  typedef int (*CtxGetCurrentFn)(void**);
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  void* ctx = nullptr;
+  if (fn == nullptr || fn(&ctx) != 0) return nullptr;
+  return ctx;
+}
+
 void set_gemm_bn_override(int bn);
 void set_gemm_mx_bn_override(int bn);
 void set_gemm_schedule_override(int s);
@@ -124,6 +140,49 @@ using namespace engram;
 extern "C" {
 
 const char* engram_last_error(void) { return g_last_error.c_str(); }
+
+int engram_sync_status(const int32_t* err_flag, engram_stream_t stream) {
+  ENGRAM_CHECK_ARG(err_flag != nullptr && aligned(err_flag, 4), "engram_sync_status: err_flag must be a non-NULL, "
+                   "4-byte aligned device word");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, err_flag, sizeof(v), cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return fail_cuda(e, "engram_sync_status: read of err_flag");
+  e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return fail_cuda(e, "engram_sync_status: stream");
+  if (v & ENGRAM_ERR_PIPE_TIMEOUT) {
+    set_error("engram_sync_status: a pipeline wait ran past its time limit (err_flag 0x%x): results invalid", v);
+    return ENGRAM_ECUDA;
+  }
+  if (v != 0) {
+    set_error("engram_sync_status: err_flag 0x%x:%s%s%s", v,
+              (v & ENGRAM_ERR_RAW_ID) ? " raw id outside the token map (hashed as pad_id);" : "",
+              (v & ENGRAM_ERR_ROW_ID) ? " row id outside the table (zero row);" : "",
+              (v & ~(ENGRAM_ERR_RAW_ID | ENGRAM_ERR_ROW_ID)) ? " unknown bits;" : "");
+    return ENGRAM_EDATA;
+  }
+  return ENGRAM_OK;
+}
+
+int engram_project_plan(int64_t T, int32_t K, int32_t N, int32_t wkv_format, int32_t num_sms,
+                        EngramProjectPlan* out) {
+  ENGRAM_CHECK_ARG(out != nullptr, "engram_project_plan: out is NULL");
+  ENGRAM_CHECK_ARG(T >= 1 && T < (int64_t)1 << 31, "engram_project_plan: T must be in [1, 2^31)");
+  ENGRAM_CHECK_ARG(N >= 16 && N % 16 == 0, "engram_project_plan: N must be a positive multiple of 16");
+  ENGRAM_CHECK_ARG(num_sms >= 1 && num_sms <= 1024, "engram_project_plan: num_sms must be in [1, 1024]");
+  bool ok;
+  if (wkv_format == ENGRAM_WKV_BF16) {
+    ENGRAM_CHECK_ARG(K >= 8 && K % 8 == 0, "engram_project_plan: K must be a positive multiple of 8");
+    ok = gemm_plan_info(T, K, N, num_sms, out);
+  } else if (wkv_format == ENGRAM_WKV_MXFP8) {
+    ENGRAM_CHECK_ARG(K >= 128 && K % 128 == 0, "engram_project_plan: MXFP8 K must be a positive multiple of 128");
+    ok = gemm_mx_plan_info(T, K, N, num_sms, out);
+  } else {
+    ENGRAM_CHECK_ARG(false, "engram_project_plan: unknown wkv format %d", wkv_format);
+  }
+  ENGRAM_CHECK_ARG(ok, "engram_project_plan: no tile plan fits (T %lld, K %d, N %d)", (long long)T, K, N);
+  return ENGRAM_OK;
+}
 const char* engram_version(void) { return "libengram 0.1 (sm_103a)"; }
 
 void engram_set_gemm_tile(int32_t bn) {

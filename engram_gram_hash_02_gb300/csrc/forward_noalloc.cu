@@ -9,7 +9,10 @@
 // g_scratch is a file-scope __device__ array: every GPU that loads this library holds it
 // (ENGRAM_NOALLOC_SCRATCH_BYTES) until the process exits. In host code its name is only a
 // host-side stand-in, so its device address is looked up with cudaGetSymbolAddress, once per
-// device, with that device current, on the first call made on that device.
+// device, with that device current, on the first call made on that device. The address is kept
+// together with the context it belongs to: after cudaDeviceReset re-creates the device's
+// context (and reloads the module, so the array may sit elsewhere), the next call looks it up
+// again instead of passing a stale address.
 //
 // Nothing in the scratch has to start at zero: each call overwrites the ids, rows and kv it
 // reads. All calls share the one array, so calls whose work overlaps on the GPU (on different
@@ -25,6 +28,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 void* g_scratch_ptr[kMaxDevices] = {nullptr};
+void* g_scratch_ctx[kMaxDevices] = {nullptr};   // the context g_scratch_ptr[dev] belongs to
 
 // Device address of g_scratch on the current device (looked up on first use).
 int scratch_address(void** out) {
@@ -35,12 +39,14 @@ int scratch_address(void** out) {
     engram::set_error("engram_forward_noalloc: device %d beyond the %d devices supported", dev, kMaxDevices);
     return ENGRAM_EINVAL;
   }
+  void* ctx = engram::PerContextOnce::current_context();
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (g_scratch_ptr[dev] == nullptr || g_scratch_ctx[dev] != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_scratch);
     if (e != cudaSuccess) return engram::fail_cuda(e, "engram_forward_noalloc: cudaGetSymbolAddress");
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = engram::PerContextOnce::current_context();   // current once the module is loaded
   }
   *out = g_scratch_ptr[dev];
   return ENGRAM_OK;

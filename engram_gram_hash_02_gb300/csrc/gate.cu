@@ -240,14 +240,10 @@ cudaError_t launch_gate(const GateParams& p, cudaStream_t stream, bool pdl) {
   if (threads > kMaxThreads) threads = kMaxThreads;
   const size_t smem = (size_t)kBufs * 3 * 4 * (size_t)H;
   if (smem > (size_t)kSmemBudget - 2048) return cudaErrorInvalidValue;
-  static bool configured[64] = {false};     // the attribute is per device
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget - 2048);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) configured[dev] = true;
-  }
+  static PerContextOnce attr;               // the attribute belongs to the context's module
+  cudaError_t ae = attr.run(
+      [] { return cudaFuncSetAttribute(gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget - 2048); });
+  if (ae != cudaSuccess) return ae;
   int per_sm = 0;                           // resident CTAs per SM (registers, shared memory)
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gate_kernel, threads, smem);
   if (e != cudaSuccess) return e;

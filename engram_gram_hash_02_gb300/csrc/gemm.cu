@@ -428,6 +428,13 @@ int pick_bn_dp(int64_t m_tiles, int N, int sms) {
   return best;
 }
 
+// Bytes from the ring's start to the end of the last stage's MMA reads: a full 128-row token tile
+// per half (whatever was loaded), then the weight tile after the loaded token rows.
+int mma_read_end(const GemmArgs& a) {
+  const int a_read = a.msub * kATileBytes;
+  return (a.stages - 1) * a.stage_bytes + (a_read > a.stage_bytes ? a_read : a.stage_bytes);
+}
+
 struct Plan {
   GemmArgs a;
   int grid;
@@ -497,6 +504,10 @@ bool plan_gemm(int64_t M, int K, int N, int sms, size_t ws_bytes, Plan& P) {
             | ((uint32_t)(128 >> 4) << 24);    // M = 128; A and B K-major (bits 15, 16 = 0)
   P.smem = 1024 + a.stages * a.stage_bytes + kEpiBytes + (int)sizeof(Ctl);
   P.ws_needed = sk ? sk_ws : 0;
+  // The MMA reads 128 token rows per half from every stage, also from a short token tile (fewer
+  // rows loaded): the last stage's reads must end inside the allocation (the epilogue's staging
+  // tiles follow the ring). 1024 bytes are kept for aligning the ring.
+  if (mma_read_end(a) > P.smem - 1024 || P.smem > kSmemBudget) return false;
   return true;
 }
 
@@ -576,6 +587,27 @@ size_t gemm_workspace_bytes(int64_t M, int K, int N) {
   return ok ? P.ws_needed : 0;
 }
 
+bool gemm_plan_info(int64_t M, int K, int N, int sms, EngramProjectPlan* out) {
+  Plan P;
+  if (!plan_gemm(M, K, N, sms, (size_t)-1 / 2, P)) return false;
+  const GemmArgs& a = P.a;
+  *out = EngramProjectPlan{};
+  out->grid = P.grid;
+  out->threads = kThreads;
+  out->smem_bytes = P.smem;
+  out->tile_rows = 128 * a.msub;
+  out->tile_cols = a.BN;
+  out->split = a.nsplit;
+  out->token_rows_loaded = a.a_rows;
+  out->stages = a.stages;
+  out->stage_bytes = a.stage_bytes;
+  out->tmem_cols = (int32_t)a.tmem_cols;
+  out->stream_k = a.stream_k;
+  out->mma_read_end = mma_read_end(a);
+  out->smem_avail = P.smem - 1024;
+  return true;
+}
+
 int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl) {
   Plan P;
   if (!plan_gemm(p.M, p.K, p.N, num_sms(), p.workspace != nullptr ? p.ws_bytes : 0, P)) {
@@ -589,14 +621,10 @@ int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl) {
     a.flags = reinterpret_cast<unsigned long long*>(ws);
     a.epoch = g_epoch.fetch_add(1) & 0xffffffffull;
   }
-  static bool configured[64] = {false};     // the attribute is per device
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(wkv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
-    if (e != cudaSuccess) return fail_cuda(e, "engram_project: cudaFuncSetAttribute");
-    if (dev >= 0 && dev < 64) configured[dev] = true;
-  }
+  static PerContextOnce attr;               // the attribute belongs to the context's module
+  cudaError_t ae = attr.run(
+      [] { return cudaFuncSetAttribute(wkv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget); });
+  if (ae != cudaSuccess) return fail_cuda(ae, "engram_project: cudaFuncSetAttribute");
   CUtensorMap mA, mB, mD;
   if (!make_map_bf16(&mA, p.A, p.M, p.K, (uint32_t)a.a_rows) || !make_map_bf16(&mB, p.B, p.N, p.K, (uint32_t)(a.BN / a.nsplit)) ||
       !make_map_f32(&mD, p.D, p.M, p.N)) {

@@ -366,6 +366,14 @@ int mx_stage_bytes(int a_bytes, int msub, int bn) {
   return ((a_bytes + bn * kStageK + 4 * (msub * 128 + bn)) + 1023) & ~1023;
 }
 
+// Bytes from the ring's start to the end of the last stage's MMA reads: a full 128-row token tile
+// per half (whatever was loaded), and the W tile after the loaded token rows.
+int mx_mma_read_end(const MxArgs& a) {
+  const int a_read = a.msub * kATileBytes;
+  const int b_end = a.a_bytes + a.b_bytes;
+  return (a.stages - 1) * a.stage_bytes + (a_read > b_end ? a_read : b_end);
+}
+
 struct MxPlan {
   MxArgs a;
   int grid, smem;
@@ -432,12 +440,36 @@ bool plan_mx(int64_t M, int K, int N, int sms, MxPlan& P) {
             | (1u << 23)                     // scales are UE8M0
             | ((uint32_t)(128 >> 4) << 24);  // M = 128; A and W e4m3 (format 0), K-major
   P.smem = 1024 + a.stages * a.stage_bytes + kEpiBytes + (int)sizeof(MxCtl);
+  // the last stage's MMA reads (a full 128-row token tile per half, whatever was loaded) end
+  // inside the allocation; 1024 bytes are kept for aligning the ring
+  if (mx_mma_read_end(a) > P.smem - 1024 || P.smem > kSmemBudget) return false;
   return true;
 }
 
 }  // namespace
 
 void set_gemm_mx_bn_override(int bn) { g_mx_bn_override = bn; }
+
+bool gemm_mx_plan_info(int64_t M, int K, int N, int sms, EngramProjectPlan* out) {
+  MxPlan P;
+  if (!plan_mx(M, K, N, sms, P)) return false;
+  const MxArgs& a = P.a;
+  *out = EngramProjectPlan{};
+  out->grid = P.grid;
+  out->threads = kThreads;
+  out->smem_bytes = P.smem;
+  out->tile_rows = 128 * a.msub;
+  out->tile_cols = a.BN;
+  out->split = 1;
+  out->token_rows_loaded = a.a_rows;
+  out->stages = a.stages;
+  out->stage_bytes = a.stage_bytes;
+  out->tmem_cols = kTmemCols;
+  out->stream_k = 0;
+  out->mma_read_end = mx_mma_read_end(a);
+  out->smem_avail = P.smem - 1024;
+  return true;
+}
 
 int launch_gemm_mx(const GemmMxParams& p, cudaStream_t stream, bool pdl) {
   MxPlan P;
@@ -449,15 +481,10 @@ int launch_gemm_mx(const GemmMxParams& p, cudaStream_t stream, bool pdl) {
   a.err = p.err;
   a.sfa = reinterpret_cast<const uint32_t*>(p.SA);
   a.sfb = reinterpret_cast<const uint32_t*>(p.SB);
-  static bool configured[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
-    cudaError_t e =
-        cudaFuncSetAttribute(wkv_gemm_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
-    if (e != cudaSuccess) return fail_cuda(e, "engram_project_mxfp8: cudaFuncSetAttribute");
-    if (dev >= 0 && dev < 64) configured[dev] = true;
-  }
+  static PerContextOnce attr;               // the attribute belongs to the context's module
+  cudaError_t ae = attr.run(
+      [] { return cudaFuncSetAttribute(wkv_gemm_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget); });
+  if (ae != cudaSuccess) return fail_cuda(ae, "engram_project_mxfp8: cudaFuncSetAttribute");
   CUtensorMap mA, mB, mD;
   if (!make_map_u8(&mA, p.A, p.M, p.K, (uint32_t)a.a_rows) || !make_map_u8(&mB, p.B, p.N, p.K, (uint32_t)a.BN) ||
       !make_map_f32(&mD, p.D, p.M, p.N)) {

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/engram.h"
 
 namespace engram {
@@ -25,6 +27,36 @@ int fail_cuda(cudaError_t e, const char* what);
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int num_sms();  // of the current device, cached per device
+
+// Once-per-context set-up (kernel attributes, the static scratch address). The key is the current
+// device and its current CUDA context: after cudaDeviceReset the primary context (and with it
+// every module and function attribute) is re-created, so the set-up runs again. Thread-safe.
+class PerContextOnce {
+ public:
+  // Runs fn() unless it already succeeded for the current context; returns its error, if any.
+  template <typename F>
+  cudaError_t run(F fn) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kDevices) return fn();
+    std::lock_guard<std::mutex> g(mutex_);
+    if (done_[dev] && ctx_[dev] == current_context()) return cudaSuccess;
+    e = fn();
+    if (e == cudaSuccess) {
+      done_[dev] = true;
+      ctx_[dev] = current_context();   // current by now (fn made a runtime call)
+    }
+    return e;
+  }
+  static void* current_context();   // the driver's CUcontext of this thread (nullptr if none)
+
+ private:
+  static constexpr int kDevices = 64;
+  void* ctx_[kDevices] = {};
+  bool done_[kDevices] = {};
+  std::mutex mutex_;
+};
 
 // ---- programmatic dependent launch ----------------------------------------------------------
 // Inside engram_forward each kernel is launched so that it may start while its predecessor on
@@ -131,6 +163,9 @@ struct GemmParams {
 // returns ENGRAM_OK or an error code (sets the message)
 int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl = false);
 size_t gemm_workspace_bytes(int64_t M, int K, int N);
+// the plan launch_gemm / launch_gemm_mx would use on `sms` SMs (host only); false if none fits
+bool gemm_plan_info(int64_t M, int K, int N, int sms, EngramProjectPlan* out);
+bool gemm_mx_plan_info(int64_t M, int K, int N, int sms, EngramProjectPlan* out);
 
 // ---- FP8 (MXFP8) operand variant of the projection -----------------------------------------
 struct GatherCodesParams {

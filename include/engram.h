@@ -39,6 +39,7 @@ extern "C" {
 #define ENGRAM_OK 0
 #define ENGRAM_EINVAL (-1) /* bad argument (shape, pointer, alignment, format) */
 #define ENGRAM_ECUDA (-2)  /* a CUDA call or launch failed */
+#define ENGRAM_EDATA (-3)  /* engram_sync_status only: a data-dependent bit is set in err_flag */
 
 /* bits of the device err_flag word */
 #define ENGRAM_ERR_RAW_ID 1        /* raw input id outside [0, raw_vocab): used pad_id */
@@ -82,6 +83,22 @@ typedef struct EngramDims {
 
 const char* engram_last_error(void);
 const char* engram_version(void);
+
+/*
+ * The synchronous form of the err_flag convention: waits for everything enqueued so far on
+ * `stream`, reads the device word err_flag and returns
+ *   ENGRAM_OK     the word is 0;
+ *   ENGRAM_EDATA  (-3) a data-dependent bit is set: ENGRAM_ERR_RAW_ID (a raw input id outside the
+ *                 token map, hashed as pad_id, as [NeMo] DeepseekV41NgramHash.forward pads what it
+ *                 cannot look back at) or ENGRAM_ERR_ROW_ID (a row id outside the table, read as a
+ *                 zero row, as [vLLM] _engram_lookup_kernel reads the rows a rank does not own).
+ *                 The results are defined; the inputs were not what the model expects;
+ *   ENGRAM_ECUDA  (-2) ENGRAM_ERR_PIPE_TIMEOUT is set (the results are invalid), or a CUDA call
+ *                 failed, including an error left by earlier asynchronous work on the stream.
+ * engram_last_error() names the bits. The word is not cleared (the caller owns it).
+ *   err_flag  device int32, non-NULL, 4-byte aligned.
+ */
+int engram_sync_status(const int32_t* err_flag, engram_stream_t stream);
 
 /*
  * Host-side layout ([vLLM] EngramLayout.__init__, find_next_prime, _is_prime).
@@ -166,6 +183,30 @@ int engram_gather_dequant(int32_t fmt, const int32_t* ids, int64_t ids_stride_t,
 int engram_project(const uint16_t* A, const uint16_t* wkv, float* kv, int64_t T, int32_t K,
                    int32_t N, void* workspace, size_t ws_bytes, int32_t* err_flag,
                    engram_stream_t stream);
+
+/*
+ * The tile plan engram_project (wkv_format ENGRAM_WKV_BF16) or engram_project_mxfp8
+ * (ENGRAM_WKV_MXFP8) would launch for a [T, K] x [N, K]^T projection on a GPU with num_sms SMs,
+ * under the current tuning knobs. Host only: no GPU is needed or touched. A diagnostic for
+ * choosing shapes and knobs. Returns ENGRAM_EINVAL if no plan fits (the launch would refuse too).
+ *
+ * The tensor cores read a full 128-row token tile from every stage even when fewer rows were
+ * loaded (a single short block); `mma_read_end` is where the last stage's reads end, counted from
+ * the 1 KB-aligned start of the ring, and a plan is only ever made when it stays within
+ * `smem_avail` (the allocation past the ring start, with the worst-case alignment pad).
+ */
+typedef struct EngramProjectPlan {
+  int32_t grid, threads, smem_bytes;  /* launch: CTAs (persistent, <= num_sms), threads, dynamic smem */
+  int32_t tile_rows, tile_cols;       /* token rows x wkv rows per tile (128 or 256 x 16..256, or a split tile) */
+  int32_t split;                      /* 2: two 128-row CTAs share a 2x-wide column block (bf16 only) */
+  int32_t token_rows_loaded;          /* token rows the TMA loads per 128-row half (128, or fewer) */
+  int32_t stages, stage_bytes;        /* ring depth and bytes per stage */
+  int32_t tmem_cols;                  /* tensor-memory columns allocated */
+  int32_t stream_k;                   /* 1: stream-K schedule */
+  int32_t mma_read_end, smem_avail;   /* see above: mma_read_end <= smem_avail always */
+} EngramProjectPlan;
+int engram_project_plan(int64_t T, int32_t K, int32_t N, int32_t wkv_format, int32_t num_sms,
+                        EngramProjectPlan* out);
 
 /* Workspace bytes that let engram_project run the stream-K schedule for this shape on the current
  * device (0: the shape always runs the data-parallel schedule, or bad sizes). */

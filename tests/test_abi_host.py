@@ -184,3 +184,74 @@ def test_forward_workspace_holds_one_operand_slot_per_layer(lib):
         # a slot holds the bf16 rows, or the FP8 codes and then their scale words
         assert slot >= 2 * T * K and slot >= r256(T * K) + (K // 128) * ((T + 3) // 4 * 4) * 4
         assert w1 == r256(4 * T * C) + slot + r256(4 * T * N)
+
+
+def test_sync_status_rejects_a_null_word(lib):
+    assert lib.engram_sync_status(None, None) == -1
+    assert "err_flag" in lib.engram_last_error().decode()
+
+
+def _plan(lib, T, K, N, fmt, sms):
+    from engram_gram_hash_02_gb300.binding import ProjectPlan
+    out = ProjectPlan()
+    rc = lib.engram_project_plan(T, K, N, fmt, sms, ctypes.byref(out))
+    return rc, out.as_dict()
+
+
+def _check_plan(p, T, fmt, sms, forced=0):
+    where = f"T={T} fmt={fmt} sms={sms} forced={forced}: {p}"
+    # the tensor cores read a full 128-row token tile from the last stage: inside the allocation
+    assert p["mma_read_end"] <= p["smem_avail"], where
+    assert p["smem_avail"] + 1024 == p["smem_bytes"] <= 232448, where
+    assert p["stages"] >= 2, where
+    assert 1 <= p["grid"] <= sms, where
+    assert p["tile_rows"] in (128, 256), where
+    assert p["tile_cols"] % 16 == 0 and 16 <= p["tile_cols"] <= (512 if p["split"] == 2 else 256), where
+    assert p["tmem_cols"] in (32, 64, 128, 256, 512), where
+    rows = p["token_rows_loaded"]
+    assert rows % 16 == 0 and 16 <= rows <= 128, where
+    if rows < 128:                       # short token tiles only for one block of at most 112 tokens
+        assert T <= 112 and p["tile_rows"] == 128 and not p["stream_k"], where
+    if forced and p["split"] == 1:
+        assert p["tile_cols"] == forced, where
+
+
+@pytest.mark.parametrize("K,N", [(6144, 20480), (6144, 35840), (512, 1280), (2048, 1280), (128, 16), (6144, 112)])
+def test_projection_plans_keep_the_mma_reads_inside_shared_memory(lib, K, N):
+    """Every plan the two projection planners make (T 1..512 and a few large T, automatic and
+    forced tile widths) keeps the last stage's 128-row token-tile reads inside the CTA's shared
+    memory, and its other sizes within what the kernels assume."""
+    Ts = list(range(1, 513)) + [1000, 4096, 32768]
+    try:
+        for fmt in (0, 1):
+            if fmt == 1 and K % 128:
+                continue
+            setter = lib.engram_set_gemm_tile if fmt == 0 else lib.engram_set_gemm_mx_tile
+            for forced in (0, 16, 48, 112, 128, 144, 224, 256):
+                setter(forced)
+                for T in Ts:
+                    for sms in (148, 152):
+                        rc, p = _plan(lib, T, K, N, fmt, sms)
+                        if rc != 0:
+                            # only a forced width the MXFP8 tensor memory cannot hold may be refused
+                            assert fmt == 1 and forced >= 224 and T > 128, (T, K, N, forced,
+                                                                            lib.engram_last_error().decode())
+                            continue
+                        _check_plan(p, T, fmt, sms, forced)
+    finally:
+        lib.engram_set_gemm_tile(0)
+        lib.engram_set_gemm_mx_tile(0)
+
+
+def test_projection_plan_rejects_bad_shapes(lib):
+    assert _plan(lib, 0, 6144, 20480, 0, 152)[0] == -1
+    assert _plan(lib, 256, 6144, 20481, 0, 152)[0] == -1
+    assert _plan(lib, 256, 6100, 20480, 1, 152)[0] == -1      # MXFP8 needs K % 128 == 0
+    assert _plan(lib, 256, 6144, 20480, 7, 152)[0] == -1
+
+
+def test_decode_plan_is_the_split_tile():
+    """The decode shape (256 tokens, wide wkv) runs split tiles: pairs of 128-row CTAs."""
+    import engram_gram_hash_02_gb300 as E
+    p = E.project_plan(256, 6144, 20480, "bf16", 148)
+    assert p["split"] == 2 and p["tile_rows"] == 128 and p["grid"] <= 148

@@ -338,7 +338,44 @@ def test_bad_arguments_return_einval():
     h = torch.zeros(2, 4, 256, device=DEV)
     kv = torch.zeros(2, 5 * 256, device=DEV)
     q = torch.zeros(4, 256, device=DEV, dtype=torch.bfloat16)
-    bad = E().make_dims(1, 3, 4, 64, 256, 9, 10, 10, 0)          # hc > 8
-    with pytest.raises(E().EngramError):
-        E().engram_gate(bad, h, kv, q, q)
+    bad = E().make_dims(1, 3, 4, 64, 256, 9, 10, 10, 0)          # hc > 8: refused by the library
+    h9 = torch.zeros(2, 9, 256, device=DEV)
+    kv9 = torch.zeros(2, 10 * 256, device=DEV)
+    q9 = torch.zeros(9, 256, device=DEV, dtype=torch.bfloat16)
+    with pytest.raises(E().EngramError) as ei:
+        E().engram_gate(bad, h9, kv9, q9, q9)
+    assert ei.value.code == -1
+    with pytest.raises(ValueError):                              # streams shape disagrees with dims
+        E().engram_gate(dims, h9, kv9, q9, q9)
     E().engram_gate(dims, h[:0], kv[:0], q, q)                   # T = 0: no-op
+
+
+def test_sync_status_reports_substituted_ids():
+    """engram_sync_status (through the C ABI): 0 on clean inputs; ENGRAM_EDATA (-3) once a row id
+    outside the table was read as a zero row, or a raw id outside the token map hashed as pad_id.
+    The ids are set on the host; nothing faults."""
+    rows, T, C, D = 3000, 40, 24, 256
+    table, scales, ids = _gather_case("fp8", rows, T, C, D, seed=11)
+    ok_ids = ids.clamp(0, rows - 1).to(DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    E().engram_gather_dequant("fp8", ok_ids, table, scales, rows, D, err=err)
+    assert E().sync_status(err) == 0
+    E().engram_gather_dequant("fp8", ids.to(DEV), table, scales, rows, D, err=err)   # ids[0, 0] == rows
+    assert E().sync_status(err) == -3
+    assert "row id" in E().lib().engram_last_error().decode()
+
+    w = get_workload("decode_fp8_t256")
+    batch = gen.batch_inputs(w)
+    primes, offsets, _, mult = H.product_setup(w)
+    dims = H.dims_for(w, H.pad_id_of(w, batch["token_map"]))
+    args = (to_device(batch["token_map"], DEV), to_device(mult, DEV), to_device(primes, DEV), to_device(offsets, DEV))
+    err.zero_()
+    E().engram_hash(dims, to_device(batch["input_ids"], DEV), *args, cu_seqlens=to_device(batch["cu_seqlens"], DEV),
+                    lookback_ids=to_device(batch["lookback_ids"], DEV), err=err)
+    assert E().sync_status(err) == 0
+    bad = batch["input_ids"].copy()
+    bad[17] = w.raw_vocab                          # outside the token map
+    E().engram_hash(dims, to_device(bad, DEV), *args, cu_seqlens=to_device(batch["cu_seqlens"], DEV),
+                    lookback_ids=to_device(batch["lookback_ids"], DEV), err=err)
+    assert E().sync_status(err) == -3
+    assert "raw id" in E().lib().engram_last_error().decode()

@@ -2,11 +2,12 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
-One step is one pass of the whole path over one batch of the workload (default: the decode
-step, 256 sequences x 1 new token, FP8+E8M0 table of ~25M rows, hidden 4096, hc 4).  Inputs
-are resident in HBM; the L2 is flushed (512 MB write, then a 256 MB read) before every timed
-step; each step is timed with CUDA events on the launching stream, per kernel as well.  Under torchrun every
-rank runs its own replica (the path needs no exchange): weak scaling, max time over ranks.
+One step is one pass of the whole path over one batch of the workload (default: the large
+configuration, 16384 tokens of uniform ids over an FP8+E8M0 table of 201M rows (53 GB),
+24 hash columns of 256, hidden 7168, hc 4).  Inputs are resident in HBM; the L2 is flushed
+(512 MB write, then a 256 MB read) before every timed step; each step is timed with CUDA events
+on the launching stream, per kernel as well.  Under torchrun every rank runs its own replica (the
+path needs no exchange): weak scaling, max time over ranks.
 
 --impl reference times the CPU oracle (oracle/) on a bounded sample of the same workload.
 """
@@ -32,15 +33,15 @@ from engram_synth import get_workload  # noqa: E402
 from engram_synth.case import make_case, to_device  # noqa: E402
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NOMINAL_HBM_GBS = 7900.0          # HBM3e nominal; HBM fractions are also given against it
+DEFAULT_WORKLOAD = "large_fp8_t16384"
 L2_FLUSH_BYTES = 512 << 20
 L2_FLUSH_READ_BYTES = 256 << 20
 
 # DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by kernel and
 # workload, with the sha256 of the kernel's source at capture time (stale -> traffic null).
 NCU_TRAFFIC: dict = {
-    # profiles/wkv_gemm_decode_fp8_t256.md: dram__bytes_read.sum + dram__bytes_write.sum
     "project0@decode_fp8_t256": {"bytes": 254901760 + 3296000, "src_sha": "ca4a50c28673842a"},
-    # profiles/wkv_gemm_mx_decode_fp8_t256.md (FP8 variant, --wkv mxfp8)
     "project0@decode_fp8_t256@mxfp8": {"bytes": 131441408 + 3046400, "src_sha": "6b962bd1336136b1",
                                        "src": "gemm_mx.cu"},
 }
@@ -233,22 +234,27 @@ def tensor_peak(peaks_d, mx: bool) -> float:
 
 def stage_model(w, name, peaks_d, mx: bool = False):
     """Algorithmic bytes / flops of one launch of a stage at workload w (``mx``: the FP8 variant,
-    MXFP8 codes plus one scale byte per 32 values for both projection operands)."""
+    MXFP8 codes plus one scale byte per 32 values for both projection operands).
+
+    ``bytes`` is what the method must move with kv in the model's dtype (bf16, 2 bytes per
+    element); this library keeps kv in fp32, and the 2 extra bytes per kv element written by the
+    projection and read by the gate are ``extra_bytes`` (not counted in ``bytes``)."""
     T, L, Cc, D, K, N, H, hc = w.tokens, w.layers, w.cols, w.head_dim, w.K, w.N, w.hidden, w.hc
     row = {"fp8": D + D // 32, "q2k": 84, "bf16": 2 * D}[w.table_format]
     op = (K + K // 32) if mx else 2 * K              # bytes of one operand row
     if name == "hash":
-        return {"bytes": 8 * T + 4 * T * L * Cc, "flops": 0, "bound": "alu"}
+        return {"bytes": 8 * T + 4 * T * L * Cc, "flops": 0, "bound": "alu", "extra_bytes": 0}
     if name.startswith("gather"):
-        return {"bytes": T * Cc * (row + 4) + T * op, "flops": 0, "bound": "hbm"}
+        return {"bytes": T * Cc * (row + 4) + T * op, "flops": 0, "bound": "hbm", "extra_bytes": 0}
     if name.startswith("project"):
-        by = N * op + T * op + 4 * T * N
+        by = N * op + T * op + 2 * T * N
         fl = 2 * T * N * K
         t_hbm = by / (peaks_d["hbm_gbs"] * 1e9)
         t_tc = fl / (tensor_peak(peaks_d, mx) * 1e12)
-        return {"bytes": by, "flops": fl, "bound": "hbm" if t_hbm >= t_tc else "tensor"}
+        return {"bytes": by, "flops": fl, "bound": "hbm" if t_hbm >= t_tc else "tensor", "extra_bytes": 2 * T * N}
     if name.startswith("gate"):
-        return {"bytes": 8 * hc * H * T + 4 * N * T + 4 * hc * H, "flops": 8 * hc * H * T, "bound": "hbm"}
+        return {"bytes": 8 * hc * H * T + 2 * N * T + 4 * hc * H, "flops": 8 * hc * H * T, "bound": "hbm",
+                "extra_bytes": 2 * T * N}
     raise ValueError(name)
 
 
@@ -374,6 +380,8 @@ def run_ours(args, rank, world, device):
         m = stage_model(w, name, pk, mx)
         gbs = m["bytes"] / (t / 1e3) / 1e9
         stages[name] = {"us": round(t * 1e3, 2), "GB/s": round(gbs, 1), "bound": m["bound"]}
+        if m["extra_bytes"]:
+            stages[name]["GB/s_with_fp32_kv"] = round((m["bytes"] + m["extra_bytes"]) / (t / 1e3) / 1e9, 1)
         if m["flops"] and name.startswith("project"):
             tfs = m["flops"] / (t / 1e3) / 1e12
             stages[name]["TFLOP/s"] = round(tfs, 1)
@@ -381,6 +389,7 @@ def run_ours(args, rank, world, device):
                 stages[name]["frac"] = round(tfs / tensor_peak(pk, mx), 4)
         if m["bound"] == "hbm":
             stages[name]["frac"] = round(gbs / pk["hbm_gbs"], 4)
+            stages[name]["frac_nominal"] = round(gbs / NOMINAL_HBM_GBS, 4)
     line = {
         "metric": "engram_tokens_per_s_per_layer",
         "value": round(value, 1),
@@ -399,12 +408,7 @@ def run_ours(args, rank, world, device):
                        l2="flushed before every timed step (512 MB write, then a 256 MB read)"),
         "gpu_launches": args.steps * (forward_launches(w) + len(calls)),
         "stages": stages,
-        "roofline": {"kernel": dom, "bound": model["bound"], "achieved": round(achieved, 1),
-                     "peak": peak, "unit": unit, "frac": None if peak is None else round(achieved / peak, 4),
-                     "peak_source": f"{pk_kind} ({'hbm_gbs' if unit == 'GB/s' else 'bf16_tflops'}, burst)"
-                                    + (" x 2 (nominal fp8 / bf16)" if unit != 'GB/s' and mx else ""),
-                     "algorithmic_bytes": model["bytes"], "algorithmic_flops": model["flops"],
-                     "traffic": traffic},
+        "roofline": roofline_entry(dom, model, achieved, peak, unit, pk, pk_kind, mx, traffic),
         "clocks": clocks,
         "wall_s_timed": round(wall, 4),
     }
@@ -416,6 +420,24 @@ def run_ours(args, rank, world, device):
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, path.case, args.cpu_tokens)
     return line
+
+
+def roofline_entry(dom, model, achieved, peak, unit, pk, pk_kind, mx, traffic) -> dict:
+    """The JSON line's roofline object for the dominant kernel: achieved against the measured peak
+    (burst), plus the sustained tensor peak or the nominal HBM bandwidth for context."""
+    r = {"kernel": dom, "bound": model["bound"], "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+         "frac": None if peak is None else round(achieved / peak, 4),
+         "peak_source": f"{pk_kind} ({'hbm_gbs' if unit == 'GB/s' else 'bf16_tflops'}, burst)"
+                        + (" x 2 (nominal fp8 / bf16)" if unit != "GB/s" and mx else ""),
+         "algorithmic_bytes": model["bytes"], "algorithmic_flops": model["flops"],
+         "extra_bytes_fp32_kv": model["extra_bytes"], "traffic": traffic}
+    if unit == "TFLOP/s" and "bf16_tflops_sustained" in pk:
+        sus = pk["bf16_tflops_sustained"] * (FP8_OVER_BF16 if mx else 1.0)
+        r["peak_sustained"] = sus
+        r["frac_sustained"] = round(achieved / sus, 4)
+    if unit == "GB/s":
+        r["frac_nominal"] = round(achieved / NOMINAL_HBM_GBS, 4)
+    return r
 
 
 def run_only(args, device):
@@ -541,6 +563,42 @@ class OracleRunner:
     """The oracle on host copies of the workload: rows of the table are fetched once for the
     tokens in the sample, so each timed step runs the oracle's full path on them."""
 
+    _BATCH_KEYS = ("input_ids", "token_map", "cu_seqlens", "sequence_ids", "token_mask", "lookback_ids")
+    _LAYER_KEYS = ("need", "table", "scales", "wkv", "q", "k", "h")
+
+    def save(self, path):
+        """Write everything step() reads to an .npz (for a child process that times it)."""
+        arrs = {"sel": self.sel}
+        for k in self._BATCH_KEYS:
+            if self.b.get(k) is not None:
+                arrs["b_" + k] = self.b[k]
+        for l, lay in enumerate(self.layers):
+            arrs[f"fmt_{l}_{lay['fmt']}"] = np.zeros(0)
+            for k in self._LAYER_KEYS:
+                if lay[k] is not None:
+                    arrs[f"l{l}_{k}"] = lay[k]
+        np.savez(path, **arrs)
+
+    @classmethod
+    def load(cls, w, path):
+        from oracle import engram_oracle as O
+        r = cls.__new__(cls)
+        r.O, r.w = O, w
+        z = np.load(path)
+        r.sel = z["sel"]
+        r.b = {k: (z["b_" + k] if "b_" + k in z.files else None) for k in cls._BATCH_KEYS}
+        r.pad = int(r.b["token_map"][w.pad_token_id])
+        r.primes, r.offsets, _ = O.layout(w.vocab_size, w.layers, w.max_ngram, w.n_heads)
+        r.mult = O.hash_multipliers(w.layer_ids, w.max_ngram, w.compressed_vocab)
+        r.layers = []
+        for l in range(w.layers):
+            fmt = next(f.split("_", 2)[2] for f in z.files if f.startswith(f"fmt_{l}_"))
+            lay = {"fmt": fmt}
+            for k in cls._LAYER_KEYS:
+                lay[k] = z[f"l{l}_{k}"] if f"l{l}_{k}" in z.files else None
+            r.layers.append(lay)
+        return r
+
     def __init__(self, w, case, n_tokens):
         from oracle import engram_oracle as O
         self.O, self.w = O, w
@@ -582,21 +640,60 @@ class OracleRunner:
             O.gate(lay["h"], kv, lay["q"], lay["k"], w.eps, w.clamp, None if mask is None else mask[self.sel])
 
 
-def cpu_baseline(w, case, n_tokens):
-    r = OracleRunner(w, case, n_tokens)
-    r.step()                                  # warm (page in the fp64 weights once)
+def time_oracle(r, seconds: float = 10.0, max_reps: int = 20):
+    """Mean seconds per oracle pass: one warm pass (pages in the fp64 weights), then passes until
+    `seconds` have gone by or `max_reps` passes ran."""
+    r.step()
     t0 = time.perf_counter()
     reps = 0
     while True:
         r.step()
         reps += 1
-        if time.perf_counter() - t0 > 10.0 or reps >= 20:
+        if time.perf_counter() - t0 > seconds or reps >= max_reps:
             break
-    dt = (time.perf_counter() - t0) / reps
-    return {"value": round(len(r.sel) * w.layers / dt, 2), "unit": "tokens/s per layer",
-            "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{len(r.sel)} of {w.tokens} tokens per pass (hash over all {w.tokens}), {reps} passes, "
-                      f"numpy fp64, BLAS threads = host cores"}
+    return (time.perf_counter() - t0) / reps, reps
+
+
+BLAS_THREAD_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
+                    "NUMEXPR_NUM_THREADS")
+
+
+def cpu_child(args):
+    """Child process of cpu_baseline: times the oracle state in args.cpu_child with the BLAS thread
+    count its environment sets; prints one JSON line."""
+    w = get_workload(args.workload)
+    r = OracleRunner.load(w, args.cpu_child)
+    dt, reps = time_oracle(r, args.cpu_seconds)
+    print(json.dumps({"s_per_pass": dt, "reps": reps, "tokens": int(len(r.sel)), "layers": w.layers}))
+
+
+def cpu_baseline(w, case, n_tokens, seconds: float = 10.0):
+    """The oracle as it stands, on the host's cores: one run with one BLAS thread, one with a
+    thread per core, each in a child process of its own (the thread count of numpy's BLAS is
+    fixed when it loads). The same bounded token sample in both."""
+    import tempfile
+    r = OracleRunner(w, case, n_tokens)
+    ncores = os.cpu_count() or 1
+    runs = {}
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "oracle_state.npz")
+        r.save(path)
+        for label, threads in (("1_core", 1), ("all_cores", ncores)):
+            env = dict(os.environ, **{k: str(threads) for k in BLAS_THREAD_VARS})
+            env["CUDA_VISIBLE_DEVICES"] = ""          # the child never touches a GPU
+            cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--workload", w.name,
+                   "--cpu-child", path, "--cpu-seconds", str(seconds)]
+            out = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+            if out.returncode != 0:
+                raise RuntimeError(f"oracle timing child failed: {out.stderr[-2000:]}")
+            res = json.loads(out.stdout.strip().splitlines()[-1])
+            runs[label] = {"value": round(res["tokens"] * res["layers"] / res["s_per_pass"], 2), "cores": threads,
+                           "passes": res["reps"]}
+    best = runs["all_cores"]
+    return {"value": best["value"], "unit": "tokens/s per layer", "cores": best["cores"], "kind": "oracle",
+            "one_core": runs["1_core"], "all_cores": runs["all_cores"],
+            "sample": f"{len(r.sel)} of {w.tokens} tokens per pass (hash over all {w.tokens} tokens), "
+                      f"numpy fp64; one child process with 1 BLAS thread and one with {ncores}"}
 
 
 def workload_config(w, table_rows: int, wkv: str, world: int) -> dict:
@@ -615,7 +712,7 @@ def run_reference(args, rank, world):
     _, _, rows = O.layout(w.vocab_size, w.layers, w.max_ngram, w.n_heads)
     case = make_case(w, [int(r) for r in np.asarray(rows).reshape(-1)], device)
     r = OracleRunner(w, case, args.cpu_tokens)
-    for _ in range(args.warmup):
+    for _ in range(min(args.warmup, 3)):
         r.step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
@@ -651,7 +748,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode_fp8_t256")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--wkv", choices=["bf16", "mxfp8"], default="bf16",
                     help="wkv format: bf16 (the workloads' own), or MXFP8 (the FP8 operand variant)")
     ap.add_argument("--cpu-tokens", type=int, default=32)
@@ -661,7 +758,12 @@ def main():
                     help="profiling: run one stage alone")
     ap.add_argument("--table-rows", type=int, default=0,
                     help="profiling: shrink the table to about this many rows per layer")
+    ap.add_argument("--cpu-child", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.cpu_child:
+        cpu_child(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
 

@@ -137,7 +137,8 @@ class ClockSampler:
 class Path:
     """Device-resident workload plus pre-marshalled C-ABI calls for each stage."""
 
-    def __init__(self, w, device, table_rows=None, wkv="bf16"):
+    def __init__(self, w, device, table_rows=None, wkv="bf16", light=False):
+        """light: only what the hash and the gather read and write (profiling one of them)."""
         import ctypes as C
 
         import engram_gram_hash_02_gb300 as E
@@ -151,7 +152,8 @@ class Path:
             w = replace(w, vocab_size=max(1024, int(table_rows) // w.cols))
             self.w = w
         primes, offsets, rows, mult = self._layout(E, w)
-        self.case = case = make_case(w, rows, device)
+        self.light = light
+        self.case = case = make_case(w, rows, device, with_weights=not light)
         b = case.batch
         self.pad = int(b["token_map"][w.pad_token_id])
         self.dims = E.make_dims(w.layers, w.max_ngram, w.n_heads, w.head_dim, w.hidden, w.hc, w.raw_vocab,
@@ -169,6 +171,10 @@ class Path:
             raise SystemExit("--wkv mxfp8 needs an FP8+E8M0 table (its rows are the projection's A operand)")
         self.layers = []
         for l, t in enumerate(case.tables):
+            if light:
+                self.layers.append(E.LayerWeights(t["fmt"], t["table"], t["scales"], t["num_rows"], None, None,
+                                                  None))
+                continue
             wkv_l, wsc = case.wkv[l], None
             if self.mx:                   # weight preparation, once, outside every timed region
                 wkv_l, wsc = E.quantize_mxfp8(case.wkv[l])
@@ -181,9 +187,10 @@ class Path:
         if self.mx:                       # FP8 variant: codes [T, K] and scales [T, K/32] of the rows
             self.A_codes = torch.empty((T, K), dtype=torch.uint8, device=d)
             self.A_scales = torch.empty(E.mx_scale_shape(T, K), dtype=torch.uint8, device=d)
-        self.kv = torch.empty((T, N), dtype=torch.float32, device=d)
+        self.kv = None if light else torch.empty((T, N), dtype=torch.float32, device=d)
         self.err = torch.zeros(1, dtype=torch.int32, device=d)
-        self.gemm_ws = torch.empty(max(256, E.project_workspace_bytes(T, K, N)), dtype=torch.uint8, device=d)
+        self.gemm_ws = torch.empty(256 if light else max(256, E.project_workspace_bytes(T, K, N)),
+                                   dtype=torch.uint8, device=d)
         self.table_rows = rows
 
     @staticmethod
@@ -205,6 +212,16 @@ class Path:
                      p(self.tables.primes), p(self.tables.offsets), p(self.ids), p(self.err), s)
         calls = [("hash", lambda: lib.engram_hash(*hash_args))]
         for l, lw in enumerate(self.layers):
+            if self.light:                # the hash and the gathers only
+                if self.mx:
+                    gc_args = (self.ids.data_ptr() + 4 * l * Cc, L * Cc, T, Cc, w.head_dim, p(lw.table),
+                               p(lw.scales), int(lw.num_rows), p(self.A_codes), p(self.A_scales), p(self.err), s)
+                    calls.append((f"gather{l}", lambda a=gc_args: lib.engram_gather_fp8_codes(*a)))
+                else:
+                    g_args = (B.TABLE_FORMATS[lw.fmt], self.ids.data_ptr() + 4 * l * Cc, L * Cc, T, Cc, w.head_dim,
+                              p(lw.table), p(lw.scales), int(lw.num_rows), p(self.A), p(self.err), s)
+                    calls.append((f"gather{l}", lambda a=g_args: lib.engram_gather_dequant(*a)))
+                continue
             g_args = (B.TABLE_FORMATS[lw.fmt], self.ids.data_ptr() + 4 * l * Cc, L * Cc, T, Cc, w.head_dim,
                       p(lw.table), p(lw.scales), int(lw.num_rows), p(self.A), p(self.err), s)
             pr_args = (p(self.A), p(lw.wkv), p(self.kv), T, K, N, p(self.gemm_ws), self.gemm_ws.numel(), p(self.err), s)
@@ -441,11 +458,20 @@ def roofline_entry(dom, model, achieved, peak, unit, pk, pk_kind, mx, traffic) -
 
 
 def run_only(args, device):
-    """Run one stage alone (for short profiler captures); prints its mean time."""
-    path = Path(get_workload(args.workload), device, args.table_rows, wkv=args.wkv)
+    """Run one stage alone (for short profiler captures); prints its mean time. ``forward`` runs
+    engram_forward as a whole (its own kernels: the hash fused with the FP8 layers' gathers)."""
+    w = get_workload(args.workload)
+    if args.tokens:
+        w = w.with_tokens((args.tokens,))
+    path = Path(w, device, args.table_rows, wkv=args.wkv, light=args.only in ("hash", "gather"))
     w = path.w
     stream = torch.cuda.current_stream()
     all_calls = path.stage_calls(stream)
+    if args.only == "forward":
+        plan = path.E.ForwardPlan(path.dims, path.tables, path.layers, path.input_ids, path.streams,
+                                  cu_seqlens=path.cu, sequence_ids=path.sid, token_mask=path.mask,
+                                  lookback_ids=path.lookback, out_ids=path.ids, err=path.err)
+        all_calls = [("forward", lambda: plan.run(stream) or 0)]
     calls = [(n, f) for n, f in all_calls if n.startswith(args.only)]
     for n, f in all_calls:                      # produce the stage's inputs once
         if n.startswith(args.only):
@@ -754,8 +780,10 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=32)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["hash", "gather", "project", "gate"],
-                    help="profiling: run one stage alone")
+    ap.add_argument("--only", choices=["hash", "gather", "project", "gate", "forward"],
+                    help="profiling: run one stage alone (forward: engram_forward as a whole)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="profiling (--only): one sequence of this many tokens instead of the workload's")
     ap.add_argument("--table-rows", type=int, default=0,
                     help="profiling: shrink the table to about this many rows per layer")
     ap.add_argument("--cpu-child", default=None, help=argparse.SUPPRESS)

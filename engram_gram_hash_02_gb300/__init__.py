@@ -30,6 +30,7 @@ from .binding import (  # noqa: F401
     project_plan,
     project_workspace_bytes,
     quantize_mxfp8,
+    set_gate_form,
     set_gemm_mx_tile,
     set_gemm_schedule,
     set_gemm_tile,

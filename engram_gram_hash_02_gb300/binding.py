@@ -104,6 +104,8 @@ def lib() -> C.CDLL:
         L.engram_set_gemm_mx_tile.argtypes = [I32]
         L.engram_set_gemm_mx_tile.restype = None
         L.engram_sync_status.argtypes = [P, P]
+        L.engram_set_gate_form.argtypes = [I32]
+        L.engram_set_gate_form.restype = None
         L.engram_project_plan.argtypes = [I64, I32, I32, I32, I32, P]
         _lib = L
     return _lib
@@ -384,6 +386,11 @@ def engram_project_mxfp8(a_codes, a_scales, w_codes, w_scales, out=None, err=Non
     return out
 
 
+def set_gate_form(form: int = 0):
+    """0 automatic, 1 persistent gate kernel, 2 one CTA per (token, stream) item."""
+    lib().engram_set_gate_form(int(form))
+
+
 def set_gemm_mx_tile(bn: int = 0):
     lib().engram_set_gemm_mx_tile(int(bn))
 
@@ -475,8 +482,7 @@ def _check_forward_shapes(dims, tables, layers, input_ids, streams, cu_seqlens, 
         if w.fmt not in TABLE_FORMATS:
             raise ValueError(f"layers[{i}]: unknown table format {w.fmt!r}")
         _table_shape_check(w.fmt, w.table, w.scales, w.num_rows, D, f"layers[{i}]")
-    if workspace is not None:
-        _numel_at_least(workspace, forward_workspace_bytes(dims, T), "workspace")
+    # the workspace's size reaches the library with its pointer, which refuses one that is too small
 
 
 class ForwardPlan:

@@ -374,6 +374,8 @@ int engram_project_mxfp8(const uint8_t* A, const uint8_t* A_scales, const uint8_
   return project_mx_impl(A, A_scales, W, W_scales, kv, T, K, N, err_flag, stream, false);
 }
 
+void engram_set_gate_form(int32_t form) { set_gate_form_override((form == 1 || form == 2) ? form : 0); }
+
 void engram_set_gemm_mx_tile(int32_t bn) { set_gemm_mx_bn_override((bn >= 16 && bn <= 256 && bn % 16 == 0) ? bn : 0); }
 
 // One layer's gathered operand in the engram_forward workspace: bf16 rows [T, K], or for the

@@ -231,9 +231,143 @@ gate_kernel(const GateParams p) {
   }
 }
 
+// ---- small-T form: one CTA per (token, stream) item --------------------------------------------
+// When there are too few items to keep a persistent grid busy (the decode step: 256 tokens x 4
+// streams over 148 SMs), each item gets a CTA of its own and every load goes straight to registers:
+// each thread holds kVec float4 chunks of h_j, key_j and the value (chunk c = tid + m * threads), all
+// requested before any is used (the stream row even before waiting for the projection). One block
+// barrier: the warps' partial sums meet in shared memory and every thread forms the gate from
+// them (the same arithmetic in every thread), then writes its chunks of h + g * v. No waits, so no
+// time limit is needed.
+constexpr int kItemThreads = 256;
+
+template <int kVec>
+__global__ void __launch_bounds__(kItemThreads)
+gate_item_kernel(const GateParams p) {
+  __shared__ float red[kItemThreads / 32][3];
+  const int H = p.H, H4 = H >> 2;
+  const int tid = threadIdx.x;
+  const int64_t item = blockIdx.x;
+  const int64_t t = item / p.hc;
+  const int j = (int)(item - t * p.hc);
+  if (p.token_mask != nullptr && __ldg(p.token_mask + t) == 0) {   // masked: not read or written
+    pdl_wait();
+    return;
+  }
+  const int64_t N = (int64_t)(p.hc + 1) * H;
+  float4* hrow = reinterpret_cast<float4*>(p.streams + item * (int64_t)H);
+  const float4* krow = reinterpret_cast<const float4*>(p.kv + t * N + (int64_t)j * H);
+  const float4* vrow = reinterpret_cast<const float4*>(p.kv + t * N + (int64_t)p.hc * H);
+  const uint2* qrow = reinterpret_cast<const uint2*>(p.q_weight + (int64_t)j * H);
+  const uint2* kwrow = reinterpret_cast<const uint2*>(p.k_weight + (int64_t)j * H);
+  float4 x[kVec], y[kVec], v[kVec];
+  uint2 qr[kVec], kr[kVec];
+#pragma unroll
+  for (int m = 0; m < kVec; ++m) {                 // not written by the projection: before the wait
+    const int c = tid + m * kItemThreads;
+    if (c < H4) {
+      x[m] = hrow[c];
+      qr[m] = __ldg(qrow + c);
+      kr[m] = __ldg(kwrow + c);
+    }
+  }
+  pdl_wait();                                      // kv comes from the projection
+  pdl_trigger();
+#pragma unroll
+  for (int m = 0; m < kVec; ++m) {
+    const int c = tid + m * kItemThreads;
+    if (c < H4) {
+      y[m] = krow[c];
+      v[m] = vrow[c];
+    }
+  }
+  float ssh = 0.f, ssk = 0.f, dot = 0.f;
+#pragma unroll
+  for (int m = 0; m < kVec; ++m) {
+    const int c = tid + m * kItemThreads;
+    if (c < H4) {
+      ssh = fmaf(x[m].x, x[m].x, ssh); ssh = fmaf(x[m].y, x[m].y, ssh);
+      ssh = fmaf(x[m].z, x[m].z, ssh); ssh = fmaf(x[m].w, x[m].w, ssh);
+      ssk = fmaf(y[m].x, y[m].x, ssk); ssk = fmaf(y[m].y, y[m].y, ssk);
+      ssk = fmaf(y[m].z, y[m].z, ssk); ssk = fmaf(y[m].w, y[m].w, ssk);
+      dot = fmaf(x[m].x * bf16lo(qr[m].x), y[m].x * bf16lo(kr[m].x), dot);
+      dot = fmaf(x[m].y * bf16hi(qr[m].x), y[m].y * bf16hi(kr[m].x), dot);
+      dot = fmaf(x[m].z * bf16lo(qr[m].y), y[m].z * bf16lo(kr[m].y), dot);
+      dot = fmaf(x[m].w * bf16hi(qr[m].y), y[m].w * bf16hi(kr[m].y), dot);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    ssh += __shfl_xor_sync(0xffffffffu, ssh, off);
+    ssk += __shfl_xor_sync(0xffffffffu, ssk, off);
+    dot += __shfl_xor_sync(0xffffffffu, dot, off);
+  }
+  const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  if (lane == 0) {
+    red[warp][0] = ssh;
+    red[warp][1] = ssk;
+    red[warp][2] = dot;
+  }
+  __syncthreads();
+  float a = 0.f, b = 0.f, cdot = 0.f;
+  for (int w = 0; w < nwarps; ++w) {               // the same order in every thread
+    a += red[w][0];
+    b += red[w][1];
+    cdot += red[w][2];
+  }
+  const float invH = 1.0f / (float)H;
+  const float s = cdot * rsqrtf(a * invH + p.eps) * rsqrtf(b * invH + p.eps) / sqrtf((float)H);
+  float ss = 0.f;                                  // sign(0) = 0
+  if (s > 0.f) ss = sqrtf(fmaxf(s, p.clamp));
+  else if (s < 0.f) ss = -sqrtf(fmaxf(-s, p.clamp));
+  const float g = 1.0f / (1.0f + expf(-ss));
+#pragma unroll
+  for (int m = 0; m < kVec; ++m) {
+    const int c = tid + m * kItemThreads;
+    if (c < H4)
+      hrow[c] = make_float4(fmaf(g, v[m].x, x[m].x), fmaf(g, v[m].y, x[m].y), fmaf(g, v[m].z, x[m].z),
+                            fmaf(g, v[m].w, x[m].w));
+  }
+}
+
+template <int kVec>
+cudaError_t launch_gate_items(const GateParams& p, cudaStream_t stream, bool pdl) {
+  const int H4 = p.H / 4;
+  const int threads = H4 >= kItemThreads ? kItemThreads : ((H4 + 31) / 32) * 32;
+  return launch_k(gate_item_kernel<kVec>, dim3((unsigned)(p.T * p.hc)), dim3(threads), 0, stream, pdl, p);
+}
+
+int g_gate_form = 0;   // engram_set_gate_form: 0 automatic, 1 persistent, 2 one CTA per item
+
 }  // namespace
 
+void set_gate_form_override(int f) { g_gate_form = f; }
+
+// Items (token x stream) up to which the one-CTA-per-item form is used: about a wave and a half of
+// small CTAs (below that a persistent grid leaves most of its CTAs with one or two serial items).
+int64_t gate_item_threshold() { return (int64_t)num_sms() * 8; }
+
 cudaError_t launch_gate(const GateParams& p, cudaStream_t stream, bool pdl) {
+  const int64_t items = p.T * p.hc;
+  const bool item_form = g_gate_form == 2 || (g_gate_form == 0 && items <= gate_item_threshold());
+  if (item_form && items <= 0x7fffffff) {
+    switch ((p.H / 4 + kItemThreads - 1) / kItemThreads) {     // float4 chunks per thread and row
+      case 0:
+      case 1: return launch_gate_items<1>(p, stream, pdl);
+      case 2: return launch_gate_items<2>(p, stream, pdl);
+      case 3: return launch_gate_items<3>(p, stream, pdl);
+      case 4: return launch_gate_items<4>(p, stream, pdl);
+      case 5: return launch_gate_items<5>(p, stream, pdl);
+      case 6: return launch_gate_items<6>(p, stream, pdl);
+      case 7: return launch_gate_items<7>(p, stream, pdl);
+      case 8: return launch_gate_items<8>(p, stream, pdl);
+      default: break;                                          // H > 8192: not reached (checked)
+    }
+  }
+  return launch_gate_persistent(p, stream, pdl);
+}
+
+cudaError_t launch_gate_persistent(const GateParams& p, cudaStream_t stream, bool pdl) {
   const int H = p.H;
   int threads = ((H / (4 * kChunks) + 31) / 32) * 32;   // every thread covers at most kChunks chunks
   if (threads < 64) threads = 64;

@@ -43,11 +43,13 @@ __device__ __forceinline__ bool stage_cu(const HashParams& p, int32_t* s_cu) {
 }
 
 // What one lane of a token's warp loads before the token's sequence is known (issued early so it
-// overlaps the block's staging of cu_seqlens).
+// overlaps the block's staging of cu_seqlens). The dependent loads (token_map[raw], and the
+// lookback entry, which needs the sequence) are issued together afterwards, so a token costs two
+// dependent round trips to memory before its ids are known.
 struct TokenLoads {
   uint64_t prime[8], off[8];                 // per (layer, column) idx = lane + 32u
   int64_t pos;                               // t - lane: this lane's window slot
-  int32_t raw, sid, sid_next, mapped;
+  int32_t raw, sid, sid_next;
   bool slot, alive, raw_ok;
 };
 
@@ -74,7 +76,6 @@ __device__ __forceinline__ TokenLoads hash_token_loads(const HashParams& p, int6
     }
   }
   L.raw_ok = L.raw >= 0 && L.raw < p.raw_vocab;
-  L.mapped = (L.slot && L.raw_ok) ? __ldg(p.token_map + L.raw) : p.pad_id;
   return L;
 }
 
@@ -96,11 +97,12 @@ __device__ __forceinline__ void hash_token_finish(const HashParams& p, int64_t t
   }
 
   // ---- slot k = lane: may it be read, and what does it hold --------------------------------
+  // (the token_map and lookback loads of the lanes are in flight together)
   bool ok = false;
   int64_t val = p.pad_id;
   if (lane < p.max_ngram) {
     if (L.pos >= start) {
-      val = L.mapped;                                 // pad_id for a raw id outside the map
+      val = (L.slot && L.raw_ok) ? __ldg(p.token_map + L.raw) : p.pad_id;   // pad_id outside the map
       if (lane == 0 && !L.raw_ok && p.err != nullptr) atomicOr(p.err, ENGRAM_ERR_RAW_ID);
       ok = L.alive && L.sid != 0 && (lane == 0 || L.sid == L.sid_next);
     } else if (p.lookback_ids != nullptr) {

@@ -218,5 +218,7 @@ struct GateParams {
   int32_t* err;
 };
 cudaError_t launch_gate(const GateParams& p, cudaStream_t stream, bool pdl = false);
+cudaError_t launch_gate_persistent(const GateParams& p, cudaStream_t stream, bool pdl = false);
+void set_gate_form_override(int f);
 
 }  // namespace engram

@@ -50,13 +50,16 @@ def make_tables(w, rows_per_layer, device, seed: int):
     return out
 
 
-def make_case(w, rows_per_layer, device="cpu", seed: int | None = None, with_tables: bool = True) -> Case:
+def make_case(w, rows_per_layer, device="cpu", seed: int | None = None, with_tables: bool = True,
+              with_weights: bool = True) -> Case:
+    """with_weights False leaves out wkv, the gate weights and the streams (for looking at the
+    hash or the gather alone)."""
     seed = w.seed if seed is None else seed
     batch = gen.batch_inputs(w, seed)
     T = w.tokens
     tables = make_tables(w, rows_per_layer, device, seed) if with_tables else []
     wkv, qs, ks, st = [], [], [], []
-    for layer in range(w.layers):
+    for layer in range(w.layers if with_weights else 0):
         s = seed * 100 + layer
         wkv.append(gen.wkv_weight(w.N, w.K, w.wkv_std, s, device))
         q, k = gen.gate_weights(w.hc, w.hidden, w.qk_std, s, device)

@@ -285,6 +285,13 @@ int engram_gate(const EngramDims* dims, float* streams, const float* kv,
                 const uint16_t* q_weight, const uint16_t* k_weight, const uint8_t* token_mask,
                 int64_t T, int32_t* err_flag, engram_stream_t stream);
 
+/* Tuning knob for engram_gate (and the gate inside engram_forward): 1 forces the persistent kernel
+ * (a few CTAs per SM streaming (token, stream) rows through shared memory), 2 the one-CTA-per-item
+ * kernel (every load of a (token, stream) item in registers at once, for few items), 0 restores the
+ * automatic choice (one CTA per item up to 8 items per SM). Process-wide; not thread-safe against
+ * calls. Both give the same results up to fp32 summation order. */
+void engram_set_gate_form(int32_t form);
+
 /* Per-layer resident weights ([Atlas] EngramLayerWeights; [vLLM] Engram parameters). */
 typedef struct EngramLayerWeights {
   int32_t table_format;        /* EngramTableFmt */

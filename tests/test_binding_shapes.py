@@ -81,7 +81,6 @@ def _mutations(E):
         "token map": m(lambda a: setattr(a[1], "token_map", torch.zeros(RAW - 1, dtype=torch.int32))),
         "multipliers": m(lambda a: setattr(a[1], "multipliers", torch.ones(L_, NG - 1, dtype=torch.int64))),
         "primes": m(lambda a: setattr(a[1], "primes", torch.ones(1, C_, dtype=torch.int64))),
-        "workspace too small": m(lambda a: a[5].__setitem__("workspace", torch.zeros(1024, dtype=torch.uint8))),
         "empty err": m(lambda a: a[5].__setitem__("err", torch.zeros(0, dtype=torch.int32))),
         "2-D input ids": m(lambda a: a.__setitem__(3, torch.zeros(T, 1, dtype=torch.int32))),
     }

@@ -280,7 +280,17 @@ def test_project_integer_exact():
                                             (9, 2, 1000, False), (3, 1, 8, True), (16, 8, 512, False),
                                             (700, 4, 4096, True), (120, 4, 8192, False), (90, 4, 7168, True),
                                             (3000, 8, 64, True)])
-def test_gate_vs_oracle(T, hc, H_, masked):
+@pytest.mark.parametrize("form", [1, 2])
+def test_gate_vs_oracle(T, hc, H_, masked, form):
+    """Both gate kernels (1 persistent, 2 one CTA per item) at every shape."""
+    E().set_gate_form(form)
+    try:
+        _gate_vs_oracle(T, hc, H_, masked)
+    finally:
+        E().set_gate_form(0)
+
+
+def _gate_vs_oracle(T, hc, H_, masked):
     g = torch.Generator(device=DEV).manual_seed(T + hc + H_)
     h = torch.randn(T, hc, H_, generator=g, device=DEV)
     kv = torch.randn(T, (hc + 1) * H_, generator=g, device=DEV) * 0.03
@@ -301,7 +311,14 @@ def test_gate_vs_oracle(T, hc, H_, masked):
     H.check_streams(got, ref, h0, f"gate T={T} hc={hc} H={H_}")
 
 
-def test_gate_all_masked_leaves_streams_bit_unchanged():
+@pytest.fixture(params=[1, 2], ids=["persistent", "per_item"])
+def gate_form(request):
+    E().set_gate_form(request.param)
+    yield request.param
+    E().set_gate_form(0)
+
+
+def test_gate_all_masked_leaves_streams_bit_unchanged(gate_form):
     T, hc, H_ = 500, 4, 4096
     h = torch.randn(T, hc, H_, device=DEV)
     before = h.clone()
@@ -314,7 +331,7 @@ def test_gate_all_masked_leaves_streams_bit_unchanged():
     assert torch.equal(h, before) and int(err.item()) == 0
 
 
-def test_gate_zero_value_bit_unchanged():
+def test_gate_zero_value_bit_unchanged(gate_form):
     T, hc, H_ = 8, 4, 512
     h = torch.randn(T, hc, H_, device=DEV)
     before = h.clone()

@@ -422,7 +422,9 @@ def run_ours(args, rank, world, device):
         "dtype": "e4m3 x e4m3 (MXFP8), fp32 accumulate" if mx else "bf16",
         "data": "synthetic (seeded; tables, weights and ids drawn on device)",
         "config": dict(workload_config(w, int(sum(path.table_rows)), "mxfp8" if mx else "bf16", world),
-                       l2="flushed before every timed step (512 MB write, then a 256 MB read)"),
+                       l2="flushed before every timed step (512 MB write, then a 256 MB read)",
+                       **({"gate_fusion": True} if args.gate_fusion else {}),
+                       **({"gate_form": args.gate_form} if args.gate_form else {})),
         "gpu_launches": args.steps * (forward_launches(w) + len(calls)),
         "stages": stages,
         "roofline": roofline_entry(dom, model, achieved, peak, unit, pk, pk_kind, mx, traffic),
@@ -777,6 +779,10 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--wkv", choices=["bf16", "mxfp8"], default="bf16",
                     help="wkv format: bf16 (the workloads' own), or MXFP8 (the FP8 operand variant)")
+    ap.add_argument("--gate-fusion", action="store_true",
+                    help="engram_forward with the gate's key sums fused into the projection's epilogue")
+    ap.add_argument("--gate-form", type=int, choices=[0, 1, 2], default=0,
+                    help="gate kernel: 0 automatic, 1 persistent, 2 one CTA per (token, stream) item")
     ap.add_argument("--cpu-tokens", type=int, default=32)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -807,6 +813,11 @@ def main():
         if not torch.cuda.is_available():
             raise SystemExit("bench.py needs a CUDA device for --impl ours")
         torch.cuda.set_device(local)
+        import engram_gram_hash_02_gb300 as E
+        if args.gate_form:
+            E.set_gate_form(args.gate_form)
+        if args.gate_fusion:
+            E.set_gate_fusion(True)
         if args.only:
             run_only(args, torch.device("cuda", local))
             return

@@ -31,6 +31,7 @@ from .binding import (  # noqa: F401
     project_workspace_bytes,
     quantize_mxfp8,
     set_gate_form,
+    set_gate_fusion,
     set_gemm_mx_tile,
     set_gemm_schedule,
     set_gemm_tile,

@@ -106,6 +106,8 @@ def lib() -> C.CDLL:
         L.engram_sync_status.argtypes = [P, P]
         L.engram_set_gate_form.argtypes = [I32]
         L.engram_set_gate_form.restype = None
+        L.engram_set_gate_fusion.argtypes = [I32]
+        L.engram_set_gate_fusion.restype = None
         L.engram_project_plan.argtypes = [I64, I32, I32, I32, I32, P]
         _lib = L
     return _lib
@@ -389,6 +391,11 @@ def engram_project_mxfp8(a_codes, a_scales, w_codes, w_scales, out=None, err=Non
 def set_gate_form(form: int = 0):
     """0 automatic, 1 persistent gate kernel, 2 one CTA per (token, stream) item."""
     lib().engram_set_gate_form(int(form))
+
+
+def set_gate_fusion(on: bool = False):
+    """engram_forward with the gate's key reductions fused into the projection's epilogue."""
+    lib().engram_set_gate_fusion(1 if on else 0)
 
 
 def set_gemm_mx_tile(bn: int = 0):

@@ -274,12 +274,14 @@ int engram_gather_dequant(int32_t fmt, const int32_t* ids, int64_t ids_stride_t,
 }
 
 static int project_impl(const uint16_t* A, const uint16_t* wkv, float* kv, int64_t T, int32_t K, int32_t N,
-                        void* workspace, size_t ws_bytes, int32_t* err_flag, engram_stream_t stream, bool pdl) {
+                        void* workspace, size_t ws_bytes, int32_t* err_flag, engram_stream_t stream, bool pdl,
+                        const GateFuse* gf = nullptr) {
   if (T == 0) return ENGRAM_OK;
   int rc = check_project(A, wkv, kv, T, K, N);
   if (rc) return rc;
   ENGRAM_CHECK_ARG(workspace == nullptr || aligned(workspace, 256), "engram_project: workspace must be 256-byte aligned");
   GemmParams p{A, wkv, kv, T, K, N, err_flag, workspace, workspace != nullptr ? ws_bytes : 0};
+  if (gf != nullptr) p.gf = *gf;
   return launch_gemm(p, static_cast<cudaStream_t>(stream), pdl);
 }
 
@@ -290,12 +292,12 @@ int engram_project(const uint16_t* A, const uint16_t* wkv, float* kv, int64_t T,
 
 static int gate_impl(const EngramDims* dims, float* streams, const float* kv, const uint16_t* q_weight,
                      const uint16_t* k_weight, const uint8_t* token_mask, int64_t T, int32_t* err_flag,
-                     engram_stream_t stream, bool pdl) {
+                     engram_stream_t stream, bool pdl, int32_t part_cols = 0) {
   if (T == 0) return check_dims(dims, false, true);
   int rc = check_gate(dims, streams, kv, q_weight, k_weight, T);
   if (rc) return rc;
   GateParams p{streams, kv, q_weight, k_weight, token_mask, T, dims->hidden, dims->hc, dims->eps, dims->clamp,
-               err_flag};
+               err_flag, part_cols};
   cudaError_t e = launch_gate(p, static_cast<cudaStream_t>(stream), pdl);
   return e == cudaSuccess ? ENGRAM_OK : fail_cuda(e, "engram_gate: launch");
 }
@@ -361,11 +363,13 @@ static int check_project_mx(const uint8_t* A, const uint8_t* SA, const uint8_t* 
 }
 
 static int project_mx_impl(const uint8_t* A, const uint8_t* SA, const uint8_t* W, const uint8_t* SW, float* kv,
-                           int64_t T, int32_t K, int32_t N, int32_t* err_flag, engram_stream_t stream, bool pdl) {
+                           int64_t T, int32_t K, int32_t N, int32_t* err_flag, engram_stream_t stream, bool pdl,
+                           const GateFuse* gf = nullptr) {
   if (T == 0) return ENGRAM_OK;
   int rc = check_project_mx(A, SA, W, SW, kv, T, K, N);
   if (rc) return rc;
   GemmMxParams p{A, SA, W, SW, kv, T, K, N, err_flag};
+  if (gf != nullptr) p.gf = *gf;
   return launch_gemm_mx(p, static_cast<cudaStream_t>(stream), pdl);
 }
 
@@ -373,6 +377,10 @@ int engram_project_mxfp8(const uint8_t* A, const uint8_t* A_scales, const uint8_
                          float* kv, int64_t T, int32_t K, int32_t N, int32_t* err_flag, engram_stream_t stream) {
   return project_mx_impl(A, A_scales, W, W_scales, kv, T, K, N, err_flag, stream, false);
 }
+
+static int g_gate_fusion = 0;   // engram_set_gate_fusion
+
+void engram_set_gate_fusion(int32_t on) { g_gate_fusion = on ? 1 : 0; }
 
 void engram_set_gate_form(int32_t form) { set_gate_form_override((form == 1 || form == 2) ? form : 0); }
 
@@ -513,16 +521,27 @@ int engram_forward(const EngramDims* dims, const EngramHashTables* tables, const
   }
   for (int l = 0; l < L; ++l) {
     const EngramLayerWeights& w = layers[l];
-    if (w.wkv_format == ENGRAM_WKV_MXFP8) {
+    const bool mx = w.wkv_format == ENGRAM_WKV_MXFP8;
+    // the gate fused into the projection's epilogue (engram_set_gate_fusion): the keys are reduced to
+    // per-tile partial sums there; needs H % 32 == 0 and tiles no wider than one stream
+    GateFuse gf{};
+    if (g_gate_fusion && dims->hidden % 32 == 0) {
+      const int tile_cols = gemm_tile_cols(T, (int)K, (int)N, mx);
+      if (tile_cols > 0 && tile_cols <= dims->hidden)
+        gf = GateFuse{streams[l], w.q_weight, w.k_weight, dims->hidden, dims->hc, dims->hidden * dims->hc, tile_cols};
+    }
+    const GateFuse* gfp = gf.keys > 0 ? &gf : nullptr;
+    if (mx) {
       // FP8 variant: the rows' codes and scales are the A operand as they are
       rc = project_mx_impl(rows_of(l), scales_of(l), reinterpret_cast<const uint8_t*>(w.wkv), w.wkv_scales, kv, T,
-                           (int32_t)K, (int32_t)N, err_flag, stream, true);
+                           (int32_t)K, (int32_t)N, err_flag, stream, true, gfp);
     } else {
       rc = project_impl(reinterpret_cast<const uint16_t*>(rows_of(l)), w.wkv, kv, T, (int32_t)K, (int32_t)N, gemm_ws,
-                        gemm_ws_bytes, err_flag, stream, true);
+                        gemm_ws_bytes, err_flag, stream, true, gfp);
     }
     if (rc) return rc;
-    rc = gate_impl(dims, streams[l], kv, w.q_weight, w.k_weight, tok->token_mask, T, err_flag, stream, true);
+    rc = gate_impl(dims, streams[l], kv, w.q_weight, w.k_weight, tok->token_mask, T, err_flag, stream, true,
+                   gf.tile_cols);
     if (rc) return rc;
   }
   return ENGRAM_OK;

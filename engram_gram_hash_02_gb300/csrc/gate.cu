@@ -80,11 +80,44 @@ struct Items {
   }
 };
 
+// The partial sums the fused projection left for item (t, j): one 16-byte slot (ssk, dot of the
+// tile's first stream, ssk, dot of its second) per tile covering stream j, tiles first .. last.
+struct PartRange {
+  int first, count;
+};
+__device__ __forceinline__ PartRange part_range(const GateParams& p, int j) {
+  const int first = (j * p.H) / p.part_cols;
+  const int last = ((j + 1) * p.H - 1) / p.part_cols;
+  return {first, last - first + 1};
+}
+// Sum over the partial slots of one item, in tile order (lane i takes tiles i, i + 32, ...; then a
+// fixed shuffle tree): the same order for every call. Warp-collective.
+__device__ __forceinline__ void sum_partials(const GateParams& p, const float* slots, PartRange pr, int j, int lane,
+                                             float& ssk, float& dot) {
+  ssk = 0.f;
+  dot = 0.f;
+  for (int i = lane; i < pr.count; i += 32) {
+    const int tt = pr.first + i;
+    const int o = (((tt * p.part_cols) / p.H) == j) ? 0 : 2;   // j is the tile's first or second stream
+    ssk += slots[4 * i + o];
+    dot += slots[4 * i + o + 1];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    ssk += __shfl_xor_sync(0xffffffffu, ssk, off);
+    dot += __shfl_xor_sync(0xffffffffu, dot, off);
+  }
+}
+
+// kFused: the projection fused the key sums (GateParams::part_cols > 0): the key slot of a buffer
+// receives the item's partial slots instead of the key row.
+template <bool kFused>
 __global__ void __launch_bounds__(kMaxThreads, 1)
 gate_kernel(const GateParams p) {
-  extern __shared__ __align__(128) float buf[];          // kBufs x [h | key | value], H floats each
+  extern __shared__ __align__(128) float buf[];          // kBufs x [h | key (or partials) | value], H floats each
   __shared__ __align__(8) uint64_t full[kBufs];
   __shared__ float red[kMaxThreads / 32][3];
+  __shared__ float fused_sums[2];
   __shared__ float gate_s;
   __shared__ int abort_s;
 
@@ -108,15 +141,21 @@ gate_kernel(const GateParams p) {
   auto buffer = [&](int n) { return smem_u32(buf) + (uint32_t)((n % kBufs) * 3) * row_bytes; };
   auto issue_h = [&](int64_t i, int n) {                 // stream row: not written by the projection
     const uint32_t bar = smem_u32(&full[n % kBufs]);
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(3u * row_bytes)
-                 : "memory");
+    uint32_t bytes = 3u * row_bytes;
+    if (kFused) bytes = 2u * row_bytes + 16u * (uint32_t)part_range(p, (int)(i % p.hc)).count;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
     bulk_copy(buffer(n), p.streams + i * (int64_t)H, row_bytes, bar);
   };
-  auto issue_kv = [&](int64_t i, int n) {                // key and value: the projection's output
+  auto issue_kv = [&](int64_t i, int n) {                // key (or partials) and value: the projection's output
     const uint32_t bar = smem_u32(&full[n % kBufs]);
     const int64_t t = i / p.hc;
     const int j = (int)(i - t * p.hc);
-    bulk_copy(buffer(n) + row_bytes, p.kv + t * N + (int64_t)j * H, row_bytes, bar);
+    if (kFused) {
+      const PartRange pr = part_range(p, j);
+      bulk_copy(buffer(n) + row_bytes, p.kv + t * N + 4 * pr.first, 16u * (uint32_t)pr.count, bar);
+    } else {
+      bulk_copy(buffer(n) + row_bytes, p.kv + t * N + (int64_t)j * H, row_bytes, bar);
+    }
     bulk_copy(buffer(n) + 2u * row_bytes, p.kv + t * N + (int64_t)p.hc * H, row_bytes, bar);
   };
   int64_t first_items[kBufs];
@@ -162,14 +201,25 @@ gate_kernel(const GateParams p) {
     for (int m = 0; m < kChunks; ++m) {
       const int c = tid + m * (int)blockDim.x;
       if (c >= H4) break;
-      const float4 x = hs[c], y = ks[c];
-      const uint2 qr = qreg[m], kr = kreg[m];
+      const float4 x = hs[c];
       ssh = fmaf(x.x, x.x, ssh); ssh = fmaf(x.y, x.y, ssh); ssh = fmaf(x.z, x.z, ssh); ssh = fmaf(x.w, x.w, ssh);
-      ssk = fmaf(y.x, y.x, ssk); ssk = fmaf(y.y, y.y, ssk); ssk = fmaf(y.z, y.z, ssk); ssk = fmaf(y.w, y.w, ssk);
-      dot = fmaf(x.x * bf16lo(qr.x), y.x * bf16lo(kr.x), dot);
-      dot = fmaf(x.y * bf16hi(qr.x), y.y * bf16hi(kr.x), dot);
-      dot = fmaf(x.z * bf16lo(qr.y), y.z * bf16lo(kr.y), dot);
-      dot = fmaf(x.w * bf16hi(qr.y), y.w * bf16hi(kr.y), dot);
+      if (!kFused) {
+        const float4 y = ks[c];
+        const uint2 qr = qreg[m], kr = kreg[m];
+        ssk = fmaf(y.x, y.x, ssk); ssk = fmaf(y.y, y.y, ssk); ssk = fmaf(y.z, y.z, ssk); ssk = fmaf(y.w, y.w, ssk);
+        dot = fmaf(x.x * bf16lo(qr.x), y.x * bf16lo(kr.x), dot);
+        dot = fmaf(x.y * bf16hi(qr.x), y.y * bf16hi(kr.x), dot);
+        dot = fmaf(x.z * bf16lo(qr.y), y.z * bf16lo(kr.y), dot);
+        dot = fmaf(x.w * bf16hi(qr.y), y.w * bf16hi(kr.y), dot);
+      }
+    }
+    if (kFused && warp == 0) {                           // the key sums: the item's partial slots
+      float fs, fd;
+      sum_partials(p, reinterpret_cast<const float*>(ks), part_range(p, jc), jc, lane, fs, fd);
+      if (lane == 0) {
+        fused_sums[0] = fs;
+        fused_sums[1] = fd;
+      }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -190,6 +240,10 @@ gate_kernel(const GateParams p) {
         a += red[w][0];
         b += red[w][1];
         c += red[w][2];
+      }
+      if (kFused) {
+        b = fused_sums[0];
+        c = fused_sums[1];
       }
       const float invH = 1.0f / (float)H;
       const float rh = rsqrtf(a * invH + p.eps);
@@ -241,10 +295,11 @@ gate_kernel(const GateParams p) {
 // time limit is needed.
 constexpr int kItemThreads = 256;
 
-template <int kVec>
+template <int kVec, bool kFused>
 __global__ void __launch_bounds__(kItemThreads)
 gate_item_kernel(const GateParams p) {
   __shared__ float red[kItemThreads / 32][3];
+  __shared__ float fused_sums[2];
   const int H = p.H, H4 = H >> 2;
   const int tid = threadIdx.x;
   const int64_t item = blockIdx.x;
@@ -277,8 +332,18 @@ gate_item_kernel(const GateParams p) {
   for (int m = 0; m < kVec; ++m) {
     const int c = tid + m * kItemThreads;
     if (c < H4) {
-      y[m] = krow[c];
+      if (!kFused) y[m] = krow[c];
       v[m] = vrow[c];
+    }
+  }
+  const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  if (kFused && warp == 0) {                       // the key sums: the item's partial slots
+    const PartRange pr = part_range(p, j);
+    float fs, fd;
+    sum_partials(p, p.kv + t * N + 4 * pr.first, pr, j, lane, fs, fd);
+    if (lane == 0) {
+      fused_sums[0] = fs;
+      fused_sums[1] = fd;
     }
   }
   float ssh = 0.f, ssk = 0.f, dot = 0.f;
@@ -288,6 +353,8 @@ gate_item_kernel(const GateParams p) {
     if (c < H4) {
       ssh = fmaf(x[m].x, x[m].x, ssh); ssh = fmaf(x[m].y, x[m].y, ssh);
       ssh = fmaf(x[m].z, x[m].z, ssh); ssh = fmaf(x[m].w, x[m].w, ssh);
+    }
+    if (!kFused && c < H4) {
       ssk = fmaf(y[m].x, y[m].x, ssk); ssk = fmaf(y[m].y, y[m].y, ssk);
       ssk = fmaf(y[m].z, y[m].z, ssk); ssk = fmaf(y[m].w, y[m].w, ssk);
       dot = fmaf(x[m].x * bf16lo(qr[m].x), y[m].x * bf16lo(kr[m].x), dot);
@@ -302,7 +369,6 @@ gate_item_kernel(const GateParams p) {
     ssk += __shfl_xor_sync(0xffffffffu, ssk, off);
     dot += __shfl_xor_sync(0xffffffffu, dot, off);
   }
-  const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   if (lane == 0) {
     red[warp][0] = ssh;
     red[warp][1] = ssk;
@@ -314,6 +380,10 @@ gate_item_kernel(const GateParams p) {
     a += red[w][0];
     b += red[w][1];
     cdot += red[w][2];
+  }
+  if (kFused) {
+    b = fused_sums[0];
+    cdot = fused_sums[1];
   }
   const float invH = 1.0f / (float)H;
   const float s = cdot * rsqrtf(a * invH + p.eps) * rsqrtf(b * invH + p.eps) / sqrtf((float)H);
@@ -334,7 +404,9 @@ template <int kVec>
 cudaError_t launch_gate_items(const GateParams& p, cudaStream_t stream, bool pdl) {
   const int H4 = p.H / 4;
   const int threads = H4 >= kItemThreads ? kItemThreads : ((H4 + 31) / 32) * 32;
-  return launch_k(gate_item_kernel<kVec>, dim3((unsigned)(p.T * p.hc)), dim3(threads), 0, stream, pdl, p);
+  if (p.part_cols > 0)
+    return launch_k(gate_item_kernel<kVec, true>, dim3((unsigned)(p.T * p.hc)), dim3(threads), 0, stream, pdl, p);
+  return launch_k(gate_item_kernel<kVec, false>, dim3((unsigned)(p.T * p.hc)), dim3(threads), 0, stream, pdl, p);
 }
 
 int g_gate_form = 0;   // engram_set_gate_form: 0 automatic, 1 persistent, 2 one CTA per item
@@ -374,12 +446,18 @@ cudaError_t launch_gate_persistent(const GateParams& p, cudaStream_t stream, boo
   if (threads > kMaxThreads) threads = kMaxThreads;
   const size_t smem = (size_t)kBufs * 3 * 4 * (size_t)H;
   if (smem > (size_t)kSmemBudget - 2048) return cudaErrorInvalidValue;
+  const bool fused = p.part_cols > 0;
+  void (*kernel)(const GateParams) = fused ? gate_kernel<true> : gate_kernel<false>;
   static PerContextOnce attr;               // the attribute belongs to the context's module
-  cudaError_t ae = attr.run(
-      [] { return cudaFuncSetAttribute(gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget - 2048); });
+  cudaError_t ae = attr.run([] {
+    cudaError_t e1 = cudaFuncSetAttribute(gate_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          kSmemBudget - 2048);
+    if (e1 != cudaSuccess) return e1;
+    return cudaFuncSetAttribute(gate_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget - 2048);
+  });
   if (ae != cudaSuccess) return ae;
   int per_sm = 0;                           // resident CTAs per SM (registers, shared memory)
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gate_kernel, threads, smem);
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm > kMaxCtasPerSm) per_sm = kMaxCtasPerSm;
   if (per_sm < 1) per_sm = 1;
@@ -388,7 +466,7 @@ cudaError_t launch_gate_persistent(const GateParams& p, cudaStream_t stream, boo
   int64_t grid = ((int64_t)num_sms() * per_sm / p.hc) * p.hc;
   if (grid < p.hc) grid = p.hc;
   if (grid > items) grid = items;                       // items = T * hc: still a multiple of hc
-  return launch_k(gate_kernel, dim3((unsigned)grid), dim3(threads), smem, stream, pdl, p);
+  return launch_k(kernel, dim3((unsigned)grid), dim3(threads), smem, stream, pdl, p);
 }
 
 }  // namespace engram

@@ -86,6 +86,7 @@ struct GemmArgs {
   unsigned long long* flags;               // [grid] (stream-K)
   unsigned long long epoch;
   int32_t* err;
+  GateFuse gf;                             // gf.keys > 0: the gate's key sums instead of the keys
 };
 
 struct Item {
@@ -141,6 +142,9 @@ __device__ __forceinline__ void epi_bar() {  // the 128 epilogue threads only
   asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
 }
 
+// kFused: the gate's key sums in the epilogue (GemmArgs::gf); a separate instantiation, so the
+// plain projection keeps its own register allocation.
+template <bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
 wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmD,
@@ -332,6 +336,16 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     // i ^ (r % 8): conflict-free), and one lane stores the tile with a TMA bulk tensor store. A
     // 16-column tail (tile widths that are odd multiples of 16) is stored by the threads.
     const uint32_t stg = epi_stage + (uint32_t)(q * kEpiWarpBytes);
+    constexpr bool fused = kFused;
+    if (fused) {                               // the first tile's stream rows, while the ring fills
+      Schedule peek = sch;
+      Item nx;
+      if (peek.next(nx)) {
+        int pm0, pn0;
+        tile_origin(a, nx.tile, pm0, pn0);
+        if (pn0 < a.gf.keys) gate_prefetch_rows(a.gf, a.M, a.msub, q, lane, pm0, pn0, a.BN);
+      }
+    }
     while (sch.next(item)) {
       const bool ok = mbar_wait(smem_u32(&ctl->acc_full), (uint32_t)(n_items & 1), abort_flag, a.err,
                                 kWaitLimitCycles);
@@ -358,7 +372,10 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         __syncwarp();
         if (*abort_flag) break;
       }
-      if (a.nsplit == 2) {
+      if (fused) {
+        fused_gate_epilogue(a.gf, &tmD, D, a.M, a.N, tmem, q, lane, stg, a.msub, a.nsplit == 1 && a.msub == 1,
+                            a.acc_stride, a.BN, a.nsplit, m0, n0);
+      } else if (a.nsplit == 2) {
         const int hb = a.BN >> 1;
         store_accumulators(&tmD, D, a.M, a.N, tmem, q, lane, stg, 1, false, a.acc_stride, hb, m0, n0, false);
         store_accumulators(&tmD, D, a.M, a.N, tmem + a.acc_stride, q, lane, stg, 1, false, a.acc_stride, hb, m0,
@@ -382,6 +399,15 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       tc_fence_before();
       mbar_arrive(smem_u32(&ctl->acc_empty));  // tensor memory may take the next item
       ++n_items;
+      if (fused) {                             // the next tile's stream rows into L2 during its main loop
+        Schedule peek = sch;
+        Item nx;
+        if (peek.next(nx)) {
+          int pm0, pn0;
+          tile_origin(a, nx.tile, pm0, pn0);
+          if (pn0 < a.gf.keys) gate_prefetch_rows(a.gf, a.M, a.msub, q, lane, pm0, pn0, a.BN);
+        }
+      }
     }
   }
 
@@ -446,7 +472,7 @@ size_t sk_workspace(int sms) { return ((size_t)sms * 8 + 255) & ~(size_t)255; } 
 
 // Data-parallel by default; stream-K (256-wide tiles) when asked for, the data-parallel schedule
 // would leave SMs idle, and the caller's workspace holds the flags.
-bool plan_gemm(int64_t M, int K, int N, int sms, size_t ws_bytes, Plan& P) {
+bool plan_gemm(int64_t M, int K, int N, int sms, size_t ws_bytes, Plan& P, bool allow_sk = true) {
   GemmArgs& a = P.a;
   a = GemmArgs{};
   a.M = (int32_t)M;
@@ -460,7 +486,7 @@ bool plan_gemm(int64_t M, int K, int N, int sms, size_t ws_bytes, Plan& P) {
   const int64_t tiles_sk = (int64_t)a.m_tiles * ((N + bn_sk - 1) / bn_sk);
   const size_t sk_ws = sk_workspace(sms);
   // stream-K is opt-in (engram_set_gemm_schedule(2)): measured slower than data-parallel so far
-  bool sk = g_sched_override == 2 && a.num_kb >= 2 && tiles_sk < 2 * (int64_t)sms;
+  bool sk = allow_sk && g_sched_override == 2 && a.num_kb >= 2 && tiles_sk < 2 * (int64_t)sms;
   if (g_bn_override > 0 && g_bn_override != bn_sk) sk = false;
   if (sk && ws_bytes < sk_ws) sk = false;       // no room for the flags: data-parallel
   a.stream_k = sk ? 1 : 0;
@@ -608,22 +634,42 @@ bool gemm_plan_info(int64_t M, int K, int N, int sms, EngramProjectPlan* out) {
   return true;
 }
 
+int gemm_tile_cols(int64_t M, int K, int N, bool mx) {
+  if (mx) {
+    EngramProjectPlan info;
+    return gemm_mx_plan_info(M, K, N, num_sms(), &info) ? info.tile_cols : 0;
+  }
+  Plan P;
+  return plan_gemm(M, K, N, num_sms(), 0, P, false) ? P.a.BN : 0;
+}
+
 int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl) {
   Plan P;
-  if (!plan_gemm(p.M, p.K, p.N, num_sms(), p.workspace != nullptr ? p.ws_bytes : 0, P)) {
+  const bool fused = p.gf.keys > 0;             // the gate's key sums need whole tiles: no stream-K
+  if (!plan_gemm(p.M, p.K, p.N, num_sms(), p.workspace != nullptr ? p.ws_bytes : 0, P, !fused)) {
     set_error("engram_project: no tile plan fits (T %lld, K %d, N %d)", (long long)p.M, p.K, p.N);
     return ENGRAM_EINVAL;
   }
   GemmArgs a = P.a;
   a.err = p.err;
+  a.gf = p.gf;
+  if (fused && a.gf.tile_cols != a.BN) {
+    set_error("engram_project: fused gate planned for tiles of %d columns, the projection runs %d", a.gf.tile_cols,
+              a.BN);
+    return ENGRAM_EINVAL;
+  }
   if (a.stream_k) {
     uint8_t* ws = static_cast<uint8_t*>(p.workspace);
     a.flags = reinterpret_cast<unsigned long long*>(ws);
     a.epoch = g_epoch.fetch_add(1) & 0xffffffffull;
   }
   static PerContextOnce attr;               // the attribute belongs to the context's module
-  cudaError_t ae = attr.run(
-      [] { return cudaFuncSetAttribute(wkv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget); });
+  cudaError_t ae = attr.run([] {
+    cudaError_t e1 =
+        cudaFuncSetAttribute(wkv_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+    if (e1 != cudaSuccess) return e1;
+    return cudaFuncSetAttribute(wkv_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+  });
   if (ae != cudaSuccess) return fail_cuda(ae, "engram_project: cudaFuncSetAttribute");
   CUtensorMap mA, mB, mD;
   if (!make_map_bf16(&mA, p.A, p.M, p.K, (uint32_t)a.a_rows) || !make_map_bf16(&mB, p.B, p.N, p.K, (uint32_t)(a.BN / a.nsplit)) ||
@@ -631,8 +677,8 @@ int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl) {
     set_error("engram_project: cuTensorMapEncodeTiled failed (driver entry point missing or bad layout)");
     return ENGRAM_ECUDA;
   }
-  cudaError_t e = launch_k(wkv_gemm_kernel, dim3((unsigned)P.grid), dim3(kThreads), (size_t)P.smem, stream, pdl, mA,
-                           mB, mD, p.D, a);
+  cudaError_t e = launch_k(fused ? wkv_gemm_kernel<true> : wkv_gemm_kernel<false>, dim3((unsigned)P.grid),
+                           dim3(kThreads), (size_t)P.smem, stream, pdl, mA, mB, mD, p.D, a);
   if (e != cudaSuccess) return fail_cuda(e, "engram_project: launch");
   return ENGRAM_OK;
 }

@@ -67,6 +67,7 @@ struct MxArgs {
   const uint32_t* sfa;                       // [M, K/128] scale words (bytes of 4 consecutive blocks)
   const uint32_t* sfb;                       // [N, K/128]
   int32_t* err;
+  GateFuse gf;                               // gf.keys > 0: the gate's key sums instead of the keys
 };
 
 __device__ __forceinline__ void mx_tile_origin(const MxArgs& a, int tile, int& m0, int& n0) {
@@ -105,6 +106,9 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* v) {
                : "memory");
 }
 
+// kFused: the gate's key sums in the epilogue (MxArgs::gf); a separate instantiation, so the plain
+// projection keeps its own register allocation.
+template <bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
 wkv_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, float* __restrict__ D, const MxArgs a) {
@@ -273,6 +277,14 @@ wkv_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     const int q = warp & 3;
     pdl_wait();                                // kv may still be read by an earlier kernel
     const uint32_t stg = epi_stage + (uint32_t)(q * kEpiWarpBytes);
+    constexpr bool fused = kFused;
+    auto prefetch_tile = [&](int tile) {       // a tile's stream rows into L2 during its main loop
+      if (!fused || tile >= n_tiles_total) return;
+      int pm0, pn0;
+      mx_tile_origin(a, tile, pm0, pn0);
+      if (pn0 < a.gf.keys) gate_prefetch_rows(a.gf, a.M, a.msub, q, lane, pm0, pn0, a.BN);
+    };
+    prefetch_tile(blockIdx.x);
     int n_items = 0;
     for (int tile = blockIdx.x; tile < n_tiles_total; tile += gridDim.x) {
       const bool ok = mbar_wait(smem_u32(&ctl->acc_full), (uint32_t)(n_items & 1), abort_flag, a.err,
@@ -281,8 +293,12 @@ wkv_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
       if (!ok || *abort_flag) break;
       int m0, n0;
       mx_tile_origin(a, tile, m0, n0);
-      store_accumulators(&tmD, D, a.M, a.N, tmem, q, lane, stg, a.msub, a.msub == 1 && a.chains == 2, a.acc_stride,
-                         a.BN, m0, n0, false);
+      if (fused)
+        fused_gate_epilogue(a.gf, &tmD, D, a.M, a.N, tmem, q, lane, stg, a.msub, a.msub == 1 && a.chains == 2,
+                            a.acc_stride, a.BN, 1, m0, n0);
+      else
+        store_accumulators(&tmD, D, a.M, a.N, tmem, q, lane, stg, a.msub, a.msub == 1 && a.chains == 2,
+                           a.acc_stride, a.BN, m0, n0, false);
       if (lane == 0) {
         asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // staging tile reusable
       }
@@ -290,6 +306,7 @@ wkv_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
       tc_fence_before();
       mbar_arrive(smem_u32(&ctl->acc_empty));  // tensor memory may take the next tile
       ++n_items;
+      prefetch_tile(tile + (int)gridDim.x);
     }
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     __syncwarp();
@@ -479,11 +496,21 @@ int launch_gemm_mx(const GemmMxParams& p, cudaStream_t stream, bool pdl) {
   }
   MxArgs a = P.a;
   a.err = p.err;
+  a.gf = p.gf;
+  if (a.gf.keys > 0 && a.gf.tile_cols != a.BN) {
+    set_error("engram_project_mxfp8: fused gate planned for tiles of %d columns, the projection runs %d",
+              a.gf.tile_cols, a.BN);
+    return ENGRAM_EINVAL;
+  }
   a.sfa = reinterpret_cast<const uint32_t*>(p.SA);
   a.sfb = reinterpret_cast<const uint32_t*>(p.SB);
   static PerContextOnce attr;               // the attribute belongs to the context's module
-  cudaError_t ae = attr.run(
-      [] { return cudaFuncSetAttribute(wkv_gemm_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget); });
+  cudaError_t ae = attr.run([] {
+    cudaError_t e1 =
+        cudaFuncSetAttribute(wkv_gemm_mx_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+    if (e1 != cudaSuccess) return e1;
+    return cudaFuncSetAttribute(wkv_gemm_mx_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+  });
   if (ae != cudaSuccess) return fail_cuda(ae, "engram_project_mxfp8: cudaFuncSetAttribute");
   CUtensorMap mA, mB, mD;
   if (!make_map_u8(&mA, p.A, p.M, p.K, (uint32_t)a.a_rows) || !make_map_u8(&mB, p.B, p.N, p.K, (uint32_t)a.BN) ||
@@ -491,8 +518,8 @@ int launch_gemm_mx(const GemmMxParams& p, cudaStream_t stream, bool pdl) {
     set_error("engram_project_mxfp8: cuTensorMapEncodeTiled failed (driver entry point missing or bad layout)");
     return ENGRAM_ECUDA;
   }
-  cudaError_t e = launch_k(wkv_gemm_mx_kernel, dim3((unsigned)P.grid), dim3(kThreads), (size_t)P.smem, stream, pdl,
-                           mA, mB, mD, p.D, a);
+  cudaError_t e = launch_k(a.gf.keys > 0 ? wkv_gemm_mx_kernel<true> : wkv_gemm_mx_kernel<false>,
+                           dim3((unsigned)P.grid), dim3(kThreads), (size_t)P.smem, stream, pdl, mA, mB, mD, p.D, a);
   if (e != cudaSuccess) return fail_cuda(e, "engram_project_mxfp8: launch");
   return ENGRAM_OK;
 }

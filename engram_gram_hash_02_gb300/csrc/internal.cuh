@@ -150,6 +150,17 @@ inline cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, boo
   return launch_gather(m, stream, pdl);
 }
 
+// The gate fused into the projection's epilogue (see tc_common.cuh): the key columns of kv are
+// reduced to per-tile partial sums instead of being stored. keys == 0: the fusion is off.
+struct GateFuse {
+  const float* h;            // streams [M, hc, H] fp32
+  const uint16_t* qw;        // q_weight [hc, H] bf16
+  const uint16_t* kw;        // k_weight [hc, H] bf16
+  int32_t H, hc;
+  int32_t keys;              // hc * H: the key columns (0: the fusion is off)
+  int32_t tile_cols;         // columns per partial slot: the tile width (set by the projection's plan)
+};
+
 struct GemmParams {
   const uint16_t* A;
   const uint16_t* B;
@@ -159,6 +170,7 @@ struct GemmParams {
   int32_t* err;
   void* workspace;      // stream-K flags (may be NULL)
   size_t ws_bytes;
+  GateFuse gf;          // gf.keys > 0: gate partials instead of the key columns (data-parallel only)
 };
 // returns ENGRAM_OK or an error code (sets the message)
 int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl = false);
@@ -203,8 +215,12 @@ struct GemmMxParams {
   int64_t M;
   int32_t K, N;
   int32_t* err;
+  GateFuse gf;                // as GemmParams::gf
 };
 int launch_gemm_mx(const GemmMxParams& p, cudaStream_t stream, bool pdl = false);
+// tile width the projection of this shape runs with (the partial slot width of the fused gate);
+// 0 if no plan fits
+int gemm_tile_cols(int64_t M, int K, int N, bool mx);
 
 struct GateParams {
   float* streams;
@@ -216,6 +232,8 @@ struct GateParams {
   int32_t H, hc;
   float eps, clamp;
   int32_t* err;
+  int32_t part_cols;          // > 0: the projection fused the gate's key sums (GateFuse, tile width
+                              // part_cols): the key columns of kv hold per-tile partials
 };
 cudaError_t launch_gate(const GateParams& p, cudaStream_t stream, bool pdl = false);
 cudaError_t launch_gate_persistent(const GateParams& p, cudaStream_t stream, bool pdl = false);

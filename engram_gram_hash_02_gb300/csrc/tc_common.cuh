@@ -140,14 +140,16 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
 // or a bulk reduce-add when `adder`. A 16-column tail (tile widths that are odd multiples of 16)
 // is stored by the threads. With `sum_chains` (a single 128-row half), the accumulator at
 // column offset acc_stride holds a second partial sum of the same tile and is added first.
+// Columns before c_begin (a multiple of 16) are not stored.
 __device__ __forceinline__ void store_accumulators(const CUtensorMap* tmD, float* D, int64_t M, int N, uint32_t tmem,
                                                    int q, int lane, uint32_t stg, int msub, bool sum_chains,
-                                                   uint32_t acc_stride, int BN, int m0, int n0, bool adder) {
+                                                   uint32_t acc_stride, int BN, int m0, int n0, bool adder,
+                                                   int c_begin = 0) {
   for (int ms = 0; ms < msub; ++ms) {
     const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ms * acc_stride);
     const int row0 = ms * 128 + q * 32;    // first row of this warp (within the item)
     const int lrow = row0 + lane;          // this thread's row (within the item)
-    for (int c0 = 0; c0 < BN; c0 += kEpiChunk) {
+    for (int c0 = c_begin; c0 < BN; c0 += kEpiChunk) {
       const bool two = c0 + 16 < BN;     // BN is a multiple of 16
       uint32_t r[32];
       tmem_ld16(tbase + c0, &r[0]);
@@ -204,6 +206,169 @@ __device__ __forceinline__ void store_accumulators(const CUtensorMap* tmD, float
               : "memory");
         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
       }
+    }
+  }
+}
+
+// ---- the gate fused into the projection's epilogue ----------------------------------------------
+// With the fusion on, the key columns [0, hc*H) of kv are never stored. For every token row of a
+// tile, the epilogue thread that drains the row accumulates the two sums the gate needs from the
+// keys, per stream j the tile covers (at most two, as the tile is at most H wide):
+//     ssk_j = sum key^2          dot_j = sum (h * q_weight[j]) * (key * k_weight[j])
+// over the tile's key columns of stream j, reading the stream row h from global memory (the
+// epilogue warps prefetch the next tile's rows into L2 while the tensor cores run). It writes them
+// as one 16-byte partial (ssk_first, dot_first, ssk_second, dot_second) at kv[t, 4 * tile_n] (the
+// key columns are free). The value columns are stored as before. A finishing pass sums, for each
+// (token, stream), the partials of the tiles covering the stream in tile order, adds sum h^2 and
+// applies the gate.
+struct RowPartials {
+  float ssk[2], dot[2];
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// One 32-column chunk of a row's key columns: the stream row h at columns x .. x+31 (loaded one
+// chunk ahead of its use) and the chunk's own stream index per 16-column half (a stream boundary is
+// a multiple of 32, so no half straddles one).
+struct HChunk {
+  float4 h[8];
+};
+__device__ __forceinline__ void load_hchunk(const GateFuse& gf, int64_t row, int x, bool two, HChunk& c) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    if (half == 1 && !two) break;
+    const int xx = x + 16 * half;
+    const int j = xx / gf.H;
+    const float4* hp = reinterpret_cast<const float4*>(gf.h + (row * gf.hc + j) * (int64_t)gf.H + (xx - j * gf.H));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c.h[4 * half + i] = hp[i];
+  }
+}
+
+// 16 key values r[0..15] of this thread's row at global columns x .. x+15 (one stream's), with the
+// matching 16 stream values hv, into P.
+__device__ __forceinline__ void gate_partial16(const GateFuse& gf, const uint32_t* r, const float* hv, int x, int j0,
+                                               RowPartials& P) {
+  const int j = x / gf.H;
+  const int xi = x - j * gf.H;
+  const uint4* qp = reinterpret_cast<const uint4*>(gf.qw + (int64_t)j * gf.H + xi);
+  const uint4* kp = reinterpret_cast<const uint4*>(gf.kw + (int64_t)j * gf.H + xi);
+  uint4 q4[2], k4[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    q4[i] = __ldg(qp + i);
+    k4[i] = __ldg(kp + i);
+  }
+  const uint32_t* qv = reinterpret_cast<const uint32_t*>(q4);
+  const uint32_t* kv = reinterpret_cast<const uint32_t*>(k4);
+  float ssk = 0.f, dot = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    const float y0 = __uint_as_float(r[i]), y1 = __uint_as_float(r[i + 1]);
+    ssk = fmaf(y0, y0, ssk);
+    ssk = fmaf(y1, y1, ssk);
+    dot = fmaf(hv[i] * bf16_lo(qv[i >> 1]), y0 * bf16_lo(kv[i >> 1]), dot);
+    dot = fmaf(hv[i + 1] * bf16_hi(qv[i >> 1]), y1 * bf16_hi(kv[i >> 1]), dot);
+  }
+  if (j == j0) {                             // the tile's first stream, or its second
+    P.ssk[0] += ssk;
+    P.dot[0] += dot;
+  } else {
+    P.ssk[1] += ssk;
+    P.dot[1] += dot;
+  }
+}
+
+// Partials of this thread's row over the key columns of one accumulator region (columns n0 ..
+// n0+cols-1 of the tile). Warp-collective (the tensor-memory loads): every lane runs it; rows past M
+// only skip their global reads. The stream values of the next chunk are requested before the
+// current chunk is reduced.
+__device__ __forceinline__ void gate_partials_region(const GateFuse& gf, uint32_t tbase, bool sum_chains,
+                                                     uint32_t acc_stride, int cols, int n0, int j0, int64_t row,
+                                                     bool row_ok, RowPartials& P) {
+  const int kend = min(cols, gf.keys - n0);  // key columns of this region: [0, kend)
+  if (kend <= 0) return;
+  HChunk cur, nxt;
+  if (row_ok) load_hchunk(gf, row, n0, 16 < kend, cur);
+  for (int c0 = 0; c0 < kend; c0 += kEpiChunk) {
+    const int x = n0 + c0;
+    const bool two = c0 + 16 < kend;
+    uint32_t r[32];
+    tmem_ld16(tbase + c0, &r[0]);
+    if (two) tmem_ld16(tbase + c0 + 16, &r[16]);
+    const int c1 = c0 + kEpiChunk;
+    if (row_ok && c1 < kend) load_hchunk(gf, row, n0 + c1, c1 + 16 < kend, nxt);
+    if (sum_chains) {
+      uint32_t r2[32];
+      tmem_ld16(tbase + acc_stride + c0, &r2[0]);
+      if (two) tmem_ld16(tbase + acc_stride + c0 + 16, &r2[16]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
+    } else {
+      tmem_ld_wait();
+    }
+    if (row_ok) {
+      const float* hv = reinterpret_cast<const float*>(cur.h);
+      gate_partial16(gf, &r[0], hv, x, j0, P);
+      if (two) gate_partial16(gf, &r[16], hv + 16, x + 16, j0, P);
+    }
+    cur = nxt;
+  }
+}
+
+// Prefetch into L2 the stream rows a tile's key columns will need (this thread's rows).
+__device__ __forceinline__ void gate_prefetch_rows(const GateFuse& gf, int64_t M, int msub, int q, int lane, int m0,
+                                                   int n0, int BN) {
+  const int x1 = min(n0 + BN, gf.keys);
+  for (int ms = 0; ms < msub; ++ms) {
+    const int64_t row = (int64_t)m0 + ms * 128 + q * 32 + lane;
+    if (row >= M) continue;
+    for (int x = n0; x < x1; x += 32) {      // 128-byte lines (a stream boundary is a multiple of 32)
+      const int j = x / gf.H;
+      const float* p = gf.h + (row * gf.hc + j) * (int64_t)gf.H + (x - j * gf.H);
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+    }
+  }
+}
+
+// The epilogue of one tile with the gate fused: partials of the key columns, store of the value
+// columns. Arguments as store_accumulators; `nsplit` 2 (two column halves of BN/2 in the two
+// accumulators) or 1. BN is the tile width.
+__device__ __forceinline__ void fused_gate_epilogue(const GateFuse& gf, const CUtensorMap* tmD, float* D, int64_t M,
+                                                    int N, uint32_t tmem, int q, int lane, uint32_t stg, int msub,
+                                                    bool sum_chains, uint32_t acc_stride, int BN, int nsplit, int m0,
+                                                    int n0) {
+  const int tile_n = n0 / gf.tile_cols;
+  const int j0 = n0 / gf.H;                  // the first stream the tile covers
+  if (n0 < gf.keys) {
+    for (int ms = 0; ms < msub; ++ms) {
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ms * acc_stride);
+      const int64_t row = (int64_t)m0 + ms * 128 + q * 32 + lane;
+      const bool row_ok = row < M;
+      RowPartials P = {{0.f, 0.f}, {0.f, 0.f}};
+      if (nsplit == 2) {
+        const int hb = BN >> 1;
+        gate_partials_region(gf, tbase, false, acc_stride, hb, n0, j0, row, row_ok, P);
+        gate_partials_region(gf, tbase + acc_stride, false, acc_stride, hb, n0 + hb, j0, row, row_ok, P);
+      } else {
+        gate_partials_region(gf, tbase, sum_chains, acc_stride, BN, n0, j0, row, row_ok, P);
+      }
+      if (row_ok)
+        *reinterpret_cast<float4*>(D + row * N + 4 * tile_n) = make_float4(P.ssk[0], P.dot[0], P.ssk[1], P.dot[1]);
+    }
+  }
+  if (n0 + BN > gf.keys) {                   // value columns of this tile: stored as they are
+    const int c_begin = n0 < gf.keys ? gf.keys - n0 : 0;
+    if (nsplit == 2) {
+      const int hb = BN >> 1;
+      if (c_begin < hb)
+        store_accumulators(tmD, D, M, N, tmem, q, lane, stg, 1, false, acc_stride, hb, m0, n0, false, c_begin);
+      store_accumulators(tmD, D, M, N, tmem + acc_stride, q, lane, stg, 1, false, acc_stride, hb, m0, n0 + hb, false,
+                         c_begin > hb ? c_begin - hb : 0);
+    } else {
+      store_accumulators(tmD, D, M, N, tmem, q, lane, stg, msub, sum_chains, acc_stride, BN, m0, n0, false, c_begin);
     }
   }
 }

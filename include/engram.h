@@ -292,6 +292,20 @@ int engram_gate(const EngramDims* dims, float* streams, const float* kv,
  * calls. Both give the same results up to fp32 summation order. */
 void engram_set_gate_form(int32_t form);
 
+/*
+ * Tuning knob for engram_forward (and engram_forward_noalloc): 1 fuses the gate's key reductions
+ * into the projection's epilogue ([NeMo] compile_engram_gate fuses the gate's reductions; [vLLM]
+ * Engram.forward runs the gate right after the wkv projection). The epilogue then never stores the
+ * key columns of kv: for every token row of a tile it forms, per stream the tile covers,
+ * sum key^2 and sum (h * q_weight) * (key * k_weight) from the stream row and the accumulators,
+ * and a finishing pass adds sum h^2, forms the gate and adds g * value. Same results as the
+ * unfused path up to fp32 summation order. Applies to layers with hidden % 32 == 0 whose
+ * projection tiles are at most `hidden` columns wide (the others run unfused); the projection then
+ * runs its data-parallel schedule. 0 (the default) turns it off. Process-wide; not thread-safe
+ * against calls.
+ */
+void engram_set_gate_fusion(int32_t on);
+
 /* Per-layer resident weights ([Atlas] EngramLayerWeights; [vLLM] Engram parameters). */
 typedef struct EngramLayerWeights {
   int32_t table_format;        /* EngramTableFmt */

@@ -320,9 +320,10 @@ def run_ours(args, rank, world, device):
     plan = path.E.ForwardPlan(path.dims, path.tables, path.layers, path.input_ids, path.streams,
                               cu_seqlens=path.cu, sequence_ids=path.sid, token_mask=path.mask,
                               lookback_ids=path.lookback, out_ids=path.ids, err=path.err)
+    side = torch.cuda.Stream(device) if args.side_stream else None    # engram_forward2
     for _ in range(args.warmup):
         flush_l2(1)
-        plan.run(stream)
+        plan.run(stream, side)
         flush_l2(1)
         step()
     torch.cuda.synchronize()
@@ -346,7 +347,7 @@ def run_ours(args, rank, world, device):
     for k in range(args.steps):
         flush_l2(k)
         fw[k][0].record(stream)
-        plan.run(stream)
+        plan.run(stream, side)
         fw[k][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -424,6 +425,7 @@ def run_ours(args, rank, world, device):
         "config": dict(workload_config(w, int(sum(path.table_rows)), "mxfp8" if mx else "bf16", world),
                        l2="flushed before every timed step (512 MB write, then a 256 MB read)",
                        **({"gate_fusion": True} if args.gate_fusion else {}),
+                       **({"side_stream": True} if args.side_stream else {}),
                        **({"gate_form": args.gate_form} if args.gate_form else {})),
         "gpu_launches": args.steps * (forward_launches(w) + len(calls)),
         "stages": stages,
@@ -779,6 +781,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--wkv", choices=["bf16", "mxfp8"], default="bf16",
                     help="wkv format: bf16 (the workloads' own), or MXFP8 (the FP8 operand variant)")
+    ap.add_argument("--side-stream", action="store_true",
+                    help="engram_forward2: the later layers' gathers on a second stream")
     ap.add_argument("--gate-fusion", action="store_true",
                     help="engram_forward with the gate's key sums fused into the projection's epilogue")
     ap.add_argument("--gate-form", type=int, choices=[0, 1, 2], default=0,

@@ -92,6 +92,7 @@ def lib() -> C.CDLL:
         L.engram_forward_workspace_bytes.restype = SZ
         L.engram_forward.argtypes = [P, P, P, P, P, P, SZ, P, P, P]
         L.engram_forward_noalloc.argtypes = [P, P, P, P, P, P, P, P]
+        L.engram_forward2.argtypes = [P, P, P, P, P, P, SZ, P, P, P, P]
         L.engram_set_gemm_tile.argtypes = [I32]
         L.engram_set_gemm_tile.restype = None
         L.engram_set_gemm_schedule.argtypes = [I32]
@@ -537,7 +538,15 @@ class ForwardPlan:
         self._err = err
         self._keep = (tables, layers, input_ids, streams, cu_seqlens, sequence_ids, token_mask, lookback_ids)
 
-    def run(self, stream=None):
+    def run(self, stream=None, side_stream=None):
+        """engram_forward on `stream` (default: the current stream); with `side_stream`,
+        engram_forward2 (the later layers' gathers on the side stream)."""
+        if side_stream is not None:
+            _check("engram_forward2", lib().engram_forward2(
+                C.byref(self.dims), C.byref(self._tables), self._layers, C.byref(self._tokens), self._streams,
+                _ptr(self.workspace), self._ws_bytes, _ptr(self._out_ids), _ptr(self._err), _stream(stream),
+                side_stream.cuda_stream))
+            return
         _check("engram_forward", lib().engram_forward(
             C.byref(self.dims), C.byref(self._tables), self._layers, C.byref(self._tokens), self._streams,
             _ptr(self.workspace), self._ws_bytes, _ptr(self._out_ids), _ptr(self._err), _stream(stream)))

@@ -403,9 +403,43 @@ size_t engram_forward_workspace_bytes(const EngramDims* d, int64_t T) {
          round256((size_t)(T * N * 4));
 }
 
-int engram_forward(const EngramDims* dims, const EngramHashTables* tables, const EngramLayerWeights* layers,
-                   const EngramTokens* tok, float* const* streams, void* workspace, size_t ws_bytes,
-                   int32_t* out_ids, int32_t* err_flag, engram_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Events that order the side stream of engram_forward2 with the caller's stream: created once per
+// device and context (no timing), and used under g_side_mutex, so one call's records and waits are
+// enqueued as one sequence (a concurrent call cannot re-record an event between another call's
+// record and its wait).
+constexpr int kSideEvents = 33;           // the hash, then up to 32 gather launches on the side stream
+constexpr int kSideDevices = 64;
+std::mutex g_side_mutex;
+cudaEvent_t g_side_ev[kSideDevices][kSideEvents];
+
+int side_events(cudaEvent_t** out) {
+  static PerContextOnce once;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "engram_forward2: cudaGetDevice");
+  ENGRAM_CHECK_ARG(dev >= 0 && dev < kSideDevices, "engram_forward2: device %d beyond the %d supported", dev,
+                   kSideDevices);
+  e = once.run([dev] {
+    for (int i = 0; i < kSideEvents; ++i) {
+      cudaError_t e1 = cudaEventCreateWithFlags(&g_side_ev[dev][i], cudaEventDisableTiming);
+      if (e1 != cudaSuccess) return e1;
+    }
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return fail_cuda(e, "engram_forward2: cudaEventCreateWithFlags");
+  *out = g_side_ev[dev];
+  return ENGRAM_OK;
+}
+
+// The whole path on `st`; with `side` (not NULL, not st) the gathers of the layers after the first
+// run on the side stream (see engram_forward2).
+int forward_core(const EngramDims* dims, const EngramHashTables* tables, const EngramLayerWeights* layers,
+                 const EngramTokens* tok, float* const* streams, void* workspace, size_t ws_bytes, int32_t* out_ids,
+                 int32_t* err_flag, engram_stream_t stream, cudaStream_t side) {
   int rc = check_dims(dims, true, true);
   if (rc) return rc;
   ENGRAM_CHECK_ARG(tables && layers && tok && streams, "tables, layers, tokens and streams must be non-NULL");
@@ -489,15 +523,38 @@ int engram_forward(const EngramDims* dims, const EngramHashTables* tables, const
     cudaError_t e = launch_hash(hp, st, true);
     if (e != cudaSuccess) return fail_cuda(e, "engram_hash: launch");
   }
+  // With a side stream, the layers after the first run are gathered there (layer 0's rows, if the
+  // hash did not fetch them, on `st`: they are needed first); each waits for the hash, and each
+  // projection on `st` waits for its run's rows.
+  const bool use_side = side != nullptr && side != st && L > (fused > 0 ? fused : 1);
+  std::unique_lock<std::mutex> side_lock;
+  cudaEvent_t* ev = nullptr;
+  int n_ev = 0;
+  int side_from = L;                          // first layer gathered on the side stream
+  int wait_ev[256];                           // per layer: event its projection waits for (-1: none)
+  for (int l = 0; l < L; ++l) wait_ev[l] = -1;
+  if (use_side) {
+    rc = side_events(&ev);
+    if (rc) return rc;
+    side_lock = std::unique_lock<std::mutex>(g_side_mutex);
+    cudaError_t ce = cudaEventRecord(ev[n_ev++], st);          // the ids are written
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(side, ev[0], 0);
+    if (ce != cudaSuccess) return fail_cuda(ce, "engram_forward2: event");
+    side_from = fused > 0 ? fused : 1;
+  }
   // the other layers' rows: one launch per run of consecutive layers with the same table format
   // and operand kind (bf16 rows or FP8 codes), before the first projection
   for (int l = fused; l < L;) {
     const int fmt = layers[l].table_format;
     const bool mx = layers[l].wkv_format == ENGRAM_WKV_MXFP8;
     int e = l + 1;
-    while (e < L && e - l < kMaxGatherLayers && layers[e].table_format == fmt &&
+    const int run_end = l < side_from ? side_from : L;          // a run never crosses onto the side stream
+    while (e < run_end && e - l < kMaxGatherLayers && layers[e].table_format == fmt &&
            (layers[e].wkv_format == ENGRAM_WKV_MXFP8) == mx)
       ++e;
+    const bool on_side = l >= side_from && n_ev < kSideEvents;
+    cudaStream_t gst = on_side ? side : st;
+    const bool gpdl = !on_side;
     cudaError_t ce;
     if (mx) {
       GatherCodesLayers m{};
@@ -506,7 +563,7 @@ int engram_forward(const EngramDims* dims, const EngramHashTables* tables, const
         m.l[j - l] = GatherCodesParams{ids + (int64_t)j * C, (int64_t)L * C, T, C, dims->head_dim, layers[j].table,
                                        layers[j].table_scales, layers[j].table_rows, rows_of(j), scales_of(j),
                                        err_flag};
-      ce = launch_gather_codes(m, st, true);
+      ce = launch_gather_codes(m, gst, gpdl);
     } else {
       GatherLayers m{};
       m.n = e - l;
@@ -514,9 +571,14 @@ int engram_forward(const EngramDims* dims, const EngramHashTables* tables, const
         m.l[j - l] = GatherParams{fmt, ids + (int64_t)j * C, (int64_t)L * C, T, C, dims->head_dim, layers[j].table,
                                   layers[j].table_scales, layers[j].table_rows,
                                   reinterpret_cast<uint16_t*>(rows_of(j)), err_flag};
-      ce = launch_gather(m, st, true);
+      ce = launch_gather(m, gst, gpdl);
     }
     if (ce != cudaSuccess) return fail_cuda(ce, "engram_forward: gather launch");
+    if (on_side) {                             // this run's rows are ready for its projections
+      ce = cudaEventRecord(ev[n_ev], side);
+      if (ce != cudaSuccess) return fail_cuda(ce, "engram_forward2: event");
+      wait_ev[l] = n_ev++;
+    }
     l = e;
   }
   for (int l = 0; l < L; ++l) {
@@ -531,6 +593,10 @@ int engram_forward(const EngramDims* dims, const EngramHashTables* tables, const
         gf = GateFuse{streams[l], w.q_weight, w.k_weight, dims->hidden, dims->hc, dims->hidden * dims->hc, tile_cols};
     }
     const GateFuse* gfp = gf.keys > 0 ? &gf : nullptr;
+    if (wait_ev[l] >= 0) {
+      cudaError_t ce = cudaStreamWaitEvent(st, ev[wait_ev[l]], 0);
+      if (ce != cudaSuccess) return fail_cuda(ce, "engram_forward2: event wait");
+    }
     if (mx) {
       // FP8 variant: the rows' codes and scales are the A operand as they are
       rc = project_mx_impl(rows_of(l), scales_of(l), reinterpret_cast<const uint8_t*>(w.wkv), w.wkv_scales, kv, T,
@@ -545,6 +611,23 @@ int engram_forward(const EngramDims* dims, const EngramHashTables* tables, const
     if (rc) return rc;
   }
   return ENGRAM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int engram_forward(const EngramDims* dims, const EngramHashTables* tables, const EngramLayerWeights* layers,
+                   const EngramTokens* tok, float* const* streams, void* workspace, size_t ws_bytes,
+                   int32_t* out_ids, int32_t* err_flag, engram_stream_t stream) {
+  return forward_core(dims, tables, layers, tok, streams, workspace, ws_bytes, out_ids, err_flag, stream, nullptr);
+}
+
+int engram_forward2(const EngramDims* dims, const EngramHashTables* tables, const EngramLayerWeights* layers,
+                    const EngramTokens* tok, float* const* streams, void* workspace, size_t ws_bytes,
+                    int32_t* out_ids, int32_t* err_flag, engram_stream_t stream, engram_stream_t side_stream) {
+  return forward_core(dims, tables, layers, tok, streams, workspace, ws_bytes, out_ids, err_flag, stream,
+                      static_cast<cudaStream_t>(side_stream));
 }
 
 }  // extern "C"

@@ -366,6 +366,24 @@ int engram_forward(const EngramDims* dims, const EngramHashTables* tables,
                    float* const* streams, void* workspace, size_t ws_bytes, int32_t* out_ids,
                    int32_t* err_flag, engram_stream_t stream);
 
+/*
+ * engram_forward with a second caller stream for the row gathers of the later layers ([vLLM]
+ * Engram._start_prefetch / _ready_rows: the next engram layers' rows are staged on a side stream
+ * while the current layer computes). The hash (with the leading FP8 layers' rows) and layer 0's
+ * rows run on `stream`; the gathers of the other layers run on side_stream once the hash is done,
+ * and each layer's projection on `stream` waits for its rows. The ordering uses CUDA events the
+ * library creates once per device (no device memory, no device-side waits); a call's records and
+ * waits are enqueued under a lock, so calls from several host threads stay correct. Every piece of
+ * work the call puts on side_stream is waited for by `stream` before its last projection, so work
+ * ordered after the call on `stream` alone sees all of it.
+ *   side_stream  a cudaStream_t; NULL or equal to `stream`: exactly engram_forward.
+ * Other arguments and results as engram_forward (bit-identical streams).
+ */
+int engram_forward2(const EngramDims* dims, const EngramHashTables* tables,
+                    const EngramLayerWeights* layers, const EngramTokens* tokens,
+                    float* const* streams, void* workspace, size_t ws_bytes, int32_t* out_ids,
+                    int32_t* err_flag, engram_stream_t stream, engram_stream_t side_stream);
+
 /* Size of the static device scratch of engram_forward_noalloc: 32 MiB, held by every GPU that
  * loads the library until the process exits. */
 #define ENGRAM_NOALLOC_SCRATCH_BYTES (32u << 20)

@@ -69,7 +69,7 @@ def a_slot_bytes(T: int, K: int) -> int:
     return r256(max(T * K * 2, r256(T * K) + (K + 127) // 128 * ((T + 3) // 4 * 4) * 4))
 
 
-def gpu_forward(w, case, setup, device="cuda", with_err=True, mx=False):
+def gpu_forward(w, case, setup, device="cuda", with_err=True, mx=False, side=False):
     """Run engram_forward on the device; returns ids, per-layer streams, the workspace views.
     With ``mx`` (a bool, or one per layer) the layers carry MXFP8 wkv (quantised on the device)
     and the FP8 variant runs for them."""
@@ -91,11 +91,13 @@ def gpu_forward(w, case, setup, device="cuda", with_err=True, mx=False):
     streams = [s.clone() for s in case.streams]
     err = torch.zeros(1, dtype=torch.int32, device=device) if with_err else None
     out_ids = torch.empty((w.tokens, w.layers, w.cols), dtype=torch.int32, device=device)
-    plan = E.engram_forward(dims, tables, layers, to_device(b["input_ids"], device), streams,
-                            cu_seqlens=to_device(b["cu_seqlens"], device),
-                            sequence_ids=to_device(b["sequence_ids"], device),
-                            token_mask=to_device(b["token_mask"], device),
-                            lookback_ids=to_device(b["lookback_ids"], device), out_ids=out_ids, err=err)
+    plan = E.ForwardPlan(dims, tables, layers, to_device(b["input_ids"], device), streams,
+                         cu_seqlens=to_device(b["cu_seqlens"], device),
+                         sequence_ids=to_device(b["sequence_ids"], device),
+                         token_mask=to_device(b["token_mask"], device),
+                         lookback_ids=to_device(b["lookback_ids"], device), out_ids=out_ids, err=err)
+    # with `side`, engram_forward2: the later layers' gathers on a second stream
+    plan.run(side_stream=torch.cuda.Stream(device) if side else None)
     torch.cuda.synchronize()
     ws = plan.workspace
     T, K, N, L = w.tokens, w.K, w.N, w.layers

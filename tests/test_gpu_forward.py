@@ -156,3 +156,52 @@ def test_forward_zero_tokens_is_a_no_op():
     w, case, setup = H.build("tiny_bf16", seq_lens=(0,))
     got = H.gpu_forward(w, case, setup)
     assert got["err"] == 0 and got["ids"].numel() == 0 and got["streams"][0].numel() == 0
+
+
+# engram_forward2: the gathers of the layers after the first run on a caller side stream, joined
+# back by events before each projection. The streams must be bit-identical to engram_forward's (the
+# same kernels on the same data), over the plans of the layer mixes above.
+@pytest.mark.parametrize("base,layer_ids,fmts,mx", [
+    ("q2k_t8192", None, None, False),                            # layer 0 gathered on the main stream
+    ("q2k_t8192", None, ("q2k", "fp8"), False),
+    ("decode_fp8_t256_2layer", None, ("fp8", "q2k"), False),      # FP8 rows from the hash, Q2_K on the side
+    ("decode_fp8_t256_2layer", None, None, (False, True)),
+    ("tiny_fp8", tuple(range(1, 11)), ("q2k",) * 10, False),     # runs of 8 and 1 on the side stream
+    ("tiny_fp8", tuple(range(1, 11)), tuple(("q2k", "bf16")[l % 2] for l in range(10)), False),
+    ("tiny_bf16", None, None, False),                            # one layer: nothing to move
+])
+def test_forward2_side_stream_matches_forward(base, layer_ids, fmts, mx):
+    w = get_workload(base)
+    kw = {"name": f"{base}_side"}
+    if layer_ids is not None:
+        kw["layer_ids"] = layer_ids
+    if fmts is not None:
+        kw["extra"] = {"layer_formats": fmts}
+    w = replace(w, **kw)
+    if fmts is not None and "bf16" in fmts:
+        w = replace(w, head_dim=256)
+    w, case, setup = H.build(w)
+    ref = H.gpu_forward(w, case, setup, mx=mx)
+    for _ in range(2):                                           # twice: the events are reused
+        got = H.gpu_forward(w, case, setup, mx=mx, side=True)
+        assert got["err"] == 0
+        assert torch.equal(got["ids"], ref["ids"])
+        for l in range(w.layers):
+            assert torch.equal(got["streams"][l], ref["streams"][l]), f"{w.name} layer {l}"
+    del case
+    torch.cuda.empty_cache()
+
+
+def test_forward2_q2k_matches_oracle():
+    w, case, setup = H.build("q2k_t8192")
+    got = H.gpu_forward(w, case, setup, side=True)
+    toks = _sample(w, case, 256)
+    ref = H.oracle_forward(w, case, toks)
+    assert got["err"] == 0
+    sel_t = torch.from_numpy(ref["tokens"]).to(got["ids"].device)
+    for l, lref in enumerate(ref["layers"]):
+        assert np.array_equal(H.bits16(got["A"][l].index_select(0, sel_t)), lref["a_bits"])
+        h = got["streams"][l].index_select(0, sel_t).cpu().numpy()
+        H.check_streams(h, lref["streams"], lref["streams_in"], f"q2k side stream layer {l}")
+    del case
+    torch.cuda.empty_cache()

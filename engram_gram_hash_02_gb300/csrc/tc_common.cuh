@@ -228,49 +228,45 @@ struct RowPartials {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// One 32-column chunk of a row's key columns: the stream row h at columns x .. x+31 (loaded one
-// chunk ahead of its use) and the chunk's own stream index per 16-column half (a stream boundary is
-// a multiple of 32, so no half straddles one).
-struct HChunk {
-  float4 h[8];
-};
-__device__ __forceinline__ void load_hchunk(const GateFuse& gf, int64_t row, int x, bool two, HChunk& c) {
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    if (half == 1 && !two) break;
-    const int xx = x + 16 * half;
-    const int j = xx / gf.H;
-    const float4* hp = reinterpret_cast<const float4*>(gf.h + (row * gf.hc + j) * (int64_t)gf.H + (xx - j * gf.H));
-#pragma unroll
-    for (int i = 0; i < 4; ++i) c.h[4 * half + i] = hp[i];
-  }
+// Four key values (y0..y3, raw fp32 bits) with their stream values, q_weight and k_weight pairs.
+__device__ __forceinline__ void gate_acc4(uint32_t y0, uint32_t y1, uint32_t y2, uint32_t y3, float4 h, uint32_t q01,
+                                          uint32_t q23, uint32_t k01, uint32_t k23, float& ssk, float& dot) {
+  const float a = __uint_as_float(y0), b = __uint_as_float(y1), c = __uint_as_float(y2), d = __uint_as_float(y3);
+  ssk = fmaf(a, a, ssk);
+  ssk = fmaf(b, b, ssk);
+  ssk = fmaf(c, c, ssk);
+  ssk = fmaf(d, d, ssk);
+  dot = fmaf(h.x * bf16_lo(q01), a * bf16_lo(k01), dot);
+  dot = fmaf(h.y * bf16_hi(q01), b * bf16_hi(k01), dot);
+  dot = fmaf(h.z * bf16_lo(q23), c * bf16_lo(k23), dot);
+  dot = fmaf(h.w * bf16_hi(q23), d * bf16_hi(k23), dot);
 }
 
-// 16 key values r[0..15] of this thread's row at global columns x .. x+15 (one stream's), with the
-// matching 16 stream values hv, into P.
-__device__ __forceinline__ void gate_partial16(const GateFuse& gf, const uint32_t* r, const float* hv, int x, int j0,
+// The stream values of 16 columns x .. x+15 of this thread's row (one stream's: a stream boundary is
+// a multiple of 32, and x a multiple of 16).
+struct H16 {
+  float4 a, b, c, d;
+};
+__device__ __forceinline__ H16 load_h16(const GateFuse& gf, int64_t row, int x) {
+  const int j = x / gf.H;
+  const float4* hp = reinterpret_cast<const float4*>(gf.h + (row * gf.hc + j) * (int64_t)gf.H + (x - j * gf.H));
+  return H16{hp[0], hp[1], hp[2], hp[3]};
+}
+
+// 16 key values r[0..15] of this thread's row at global columns x .. x+15, with their stream
+// values, into P.
+__device__ __forceinline__ void gate_partial16(const GateFuse& gf, const uint32_t* r, const H16& h, int x, int j0,
                                                RowPartials& P) {
   const int j = x / gf.H;
   const int xi = x - j * gf.H;
   const uint4* qp = reinterpret_cast<const uint4*>(gf.qw + (int64_t)j * gf.H + xi);
   const uint4* kp = reinterpret_cast<const uint4*>(gf.kw + (int64_t)j * gf.H + xi);
-  uint4 q4[2], k4[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    q4[i] = __ldg(qp + i);
-    k4[i] = __ldg(kp + i);
-  }
-  const uint32_t* qv = reinterpret_cast<const uint32_t*>(q4);
-  const uint32_t* kv = reinterpret_cast<const uint32_t*>(k4);
+  const uint4 q0 = __ldg(qp), q1 = __ldg(qp + 1), k0 = __ldg(kp), k1 = __ldg(kp + 1);
   float ssk = 0.f, dot = 0.f;
-#pragma unroll
-  for (int i = 0; i < 16; i += 2) {
-    const float y0 = __uint_as_float(r[i]), y1 = __uint_as_float(r[i + 1]);
-    ssk = fmaf(y0, y0, ssk);
-    ssk = fmaf(y1, y1, ssk);
-    dot = fmaf(hv[i] * bf16_lo(qv[i >> 1]), y0 * bf16_lo(kv[i >> 1]), dot);
-    dot = fmaf(hv[i + 1] * bf16_hi(qv[i >> 1]), y1 * bf16_hi(kv[i >> 1]), dot);
-  }
+  gate_acc4(r[0], r[1], r[2], r[3], h.a, q0.x, q0.y, k0.x, k0.y, ssk, dot);
+  gate_acc4(r[4], r[5], r[6], r[7], h.b, q0.z, q0.w, k0.z, k0.w, ssk, dot);
+  gate_acc4(r[8], r[9], r[10], r[11], h.c, q1.x, q1.y, k1.x, k1.y, ssk, dot);
+  gate_acc4(r[12], r[13], r[14], r[15], h.d, q1.z, q1.w, k1.z, k1.w, ssk, dot);
   if (j == j0) {                             // the tile's first stream, or its second
     P.ssk[0] += ssk;
     P.dot[0] += dot;
@@ -289,16 +285,24 @@ __device__ __forceinline__ void gate_partials_region(const GateFuse& gf, uint32_
                                                      bool row_ok, RowPartials& P) {
   const int kend = min(cols, gf.keys - n0);  // key columns of this region: [0, kend)
   if (kend <= 0) return;
-  HChunk cur, nxt;
-  if (row_ok) load_hchunk(gf, row, n0, 16 < kend, cur);
+  H16 h0 = {}, h1 = {};
+  if (row_ok) {
+    h0 = load_h16(gf, row, n0);
+    if (16 < kend) h1 = load_h16(gf, row, n0 + 16);
+  }
   for (int c0 = 0; c0 < kend; c0 += kEpiChunk) {
     const int x = n0 + c0;
     const bool two = c0 + 16 < kend;
     uint32_t r[32];
     tmem_ld16(tbase + c0, &r[0]);
     if (two) tmem_ld16(tbase + c0 + 16, &r[16]);
+    // the next chunk's stream values, in flight while this chunk is reduced
     const int c1 = c0 + kEpiChunk;
-    if (row_ok && c1 < kend) load_hchunk(gf, row, n0 + c1, c1 + 16 < kend, nxt);
+    H16 n0v = {}, n1v = {};
+    if (row_ok && c1 < kend) {
+      n0v = load_h16(gf, row, n0 + c1);
+      if (c1 + 16 < kend) n1v = load_h16(gf, row, n0 + c1 + 16);
+    }
     if (sum_chains) {
       uint32_t r2[32];
       tmem_ld16(tbase + acc_stride + c0, &r2[0]);
@@ -310,11 +314,11 @@ __device__ __forceinline__ void gate_partials_region(const GateFuse& gf, uint32_
       tmem_ld_wait();
     }
     if (row_ok) {
-      const float* hv = reinterpret_cast<const float*>(cur.h);
-      gate_partial16(gf, &r[0], hv, x, j0, P);
-      if (two) gate_partial16(gf, &r[16], hv + 16, x + 16, j0, P);
+      gate_partial16(gf, &r[0], h0, x, j0, P);
+      if (two) gate_partial16(gf, &r[16], h1, x + 16, j0, P);
     }
-    cur = nxt;
+    h0 = n0v;
+    h1 = n1v;
   }
 }
 

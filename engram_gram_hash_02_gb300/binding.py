@@ -109,6 +109,8 @@ def lib() -> C.CDLL:
         L.engram_set_gate_form.restype = None
         L.engram_set_gate_fusion.argtypes = [I32]
         L.engram_set_gate_fusion.restype = None
+        L.engram_set_operand_gather.argtypes = [I32]
+        L.engram_set_operand_gather.restype = None
         L.engram_project_plan.argtypes = [I64, I32, I32, I32, I32, P]
         _lib = L
     return _lib
@@ -397,6 +399,11 @@ def set_gate_form(form: int = 0):
 def set_gate_fusion(on: bool = False):
     """engram_forward with the gate's key reductions fused into the projection's epilogue."""
     lib().engram_set_gate_fusion(1 if on else 0)
+
+
+def set_operand_gather(on: bool = False):
+    """engram_forward with the FP8 variant's projection gathering its token rows from the table."""
+    lib().engram_set_operand_gather(1 if on else 0)
 
 
 def set_gemm_mx_tile(bn: int = 0):

@@ -362,14 +362,30 @@ static int check_project_mx(const uint8_t* A, const uint8_t* SA, const uint8_t* 
   return ENGRAM_OK;
 }
 
+// The operand gather of the FP8 variant: the projection reads its token rows from the table itself.
+struct OperandGather {
+  const int32_t* ids;
+  int64_t ids_stride;
+  const void* table;
+  int64_t table_rows;
+  int32_t D;
+};
+
 static int project_mx_impl(const uint8_t* A, const uint8_t* SA, const uint8_t* W, const uint8_t* SW, float* kv,
                            int64_t T, int32_t K, int32_t N, int32_t* err_flag, engram_stream_t stream, bool pdl,
-                           const GateFuse* gf = nullptr) {
+                           const GateFuse* gf = nullptr, const OperandGather* og = nullptr) {
   if (T == 0) return ENGRAM_OK;
   int rc = check_project_mx(A, SA, W, SW, kv, T, K, N);
   if (rc) return rc;
   GemmMxParams p{A, SA, W, SW, kv, T, K, N, err_flag};
   if (gf != nullptr) p.gf = *gf;
+  if (og != nullptr) {
+    p.ids = og->ids;
+    p.ids_stride = og->ids_stride;
+    p.table = static_cast<const uint8_t*>(og->table);
+    p.table_rows = og->table_rows;
+    p.D = og->D;
+  }
   return launch_gemm_mx(p, static_cast<cudaStream_t>(stream), pdl);
 }
 
@@ -379,6 +395,9 @@ int engram_project_mxfp8(const uint8_t* A, const uint8_t* A_scales, const uint8_
 }
 
 static int g_gate_fusion = 0;   // engram_set_gate_fusion
+static int g_operand_gather = 0;   // engram_set_operand_gather
+
+void engram_set_operand_gather(int32_t on) { g_operand_gather = on ? 1 : 0; }
 
 void engram_set_gate_fusion(int32_t on) { g_gate_fusion = on ? 1 : 0; }
 
@@ -498,6 +517,12 @@ int forward_core(const EngramDims* dims, const EngramHashTables* tables, const E
                    tok->lookback_ids, tables->token_map, tables->multipliers, tables->primes, tables->offsets, ids,
                    err_flag, hp);
   if (rc) return rc;
+  // FP8-variant layers whose projection gathers its own token rows (engram_set_operand_gather):
+  // the gathers before it write only the rows' scale words
+  auto operand_gather = [&](int l) {
+    return g_operand_gather && layers[l].wkv_format == ENGRAM_WKV_MXFP8 && dims->head_dim % 128 == 0 &&
+           layers[l].table_rows < ((int64_t)1 << 31);
+  };
   // the hash kernel also fetches the rows of the leading run of FP8 layers
   int fused = 0;
   while (fused < L && fused < kMaxGatherLayers && layers[fused].table_format == ENGRAM_TABLE_FP8_E8M0) ++fused;
@@ -511,7 +536,7 @@ int forward_core(const EngramDims* dims, const EngramHashTables* tables, const E
       g.scales[l] = layers[l].table_scales;
       g.num_rows[l] = layers[l].table_rows;
       if (layers[l].wkv_format == ENGRAM_WKV_MXFP8) {
-        g.out_codes[l] = rows_of(l);
+        g.out_codes[l] = operand_gather(l) ? nullptr : rows_of(l);
         g.out_scales[l] = scales_of(l);
       } else {
         g.out_bf16[l] = reinterpret_cast<uint16_t*>(rows_of(l));
@@ -561,8 +586,8 @@ int forward_core(const EngramDims* dims, const EngramHashTables* tables, const E
       m.n = e - l;
       for (int j = l; j < e; ++j)
         m.l[j - l] = GatherCodesParams{ids + (int64_t)j * C, (int64_t)L * C, T, C, dims->head_dim, layers[j].table,
-                                       layers[j].table_scales, layers[j].table_rows, rows_of(j), scales_of(j),
-                                       err_flag};
+                                       layers[j].table_scales, layers[j].table_rows,
+                                       operand_gather(j) ? nullptr : rows_of(j), scales_of(j), err_flag};
       ce = launch_gather_codes(m, gst, gpdl);
     } else {
       GatherLayers m{};
@@ -599,8 +624,9 @@ int forward_core(const EngramDims* dims, const EngramHashTables* tables, const E
     }
     if (mx) {
       // FP8 variant: the rows' codes and scales are the A operand as they are
+      const OperandGather og{ids + (int64_t)l * C, (int64_t)L * C, w.table, w.table_rows, dims->head_dim};
       rc = project_mx_impl(rows_of(l), scales_of(l), reinterpret_cast<const uint8_t*>(w.wkv), w.wkv_scales, kv, T,
-                           (int32_t)K, (int32_t)N, err_flag, stream, true, gfp);
+                           (int32_t)K, (int32_t)N, err_flag, stream, true, gfp, operand_gather(l) ? &og : nullptr);
     } else {
       rc = project_impl(reinterpret_cast<const uint16_t*>(rows_of(l)), w.wkv, kv, T, (int32_t)K, (int32_t)N, gemm_ws,
                         gemm_ws_bytes, err_flag, stream, true, gfp);

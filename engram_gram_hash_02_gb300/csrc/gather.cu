@@ -276,10 +276,12 @@ hash_gather_fp8_kernel(const HashGatherParams p) {
         const int64_t id = s_ids[l * C + col];   // ids of token t in (layer, column) order
         if (id >= 0 && id < p.num_rows[l]) {
           rid[u] = id;
-          v[u] = ld_stream_v4(static_cast<const uint8_t*>(p.table[l]) + id * p.D + (j << 4));
-          // the scale byte the chunk needs (bf16 out: its own block, j / 2) or hands on (codes out:
-          // chunk j copies the byte of block j, for j < sblocks)
+          // the codes (not for a scales-only layer, whose codes the projection gathers itself)
           const bool bf16_out = p.out_bf16[l] != nullptr;
+          if (bf16_out || p.out_codes[l] != nullptr)
+            v[u] = ld_stream_v4(static_cast<const uint8_t*>(p.table[l]) + id * p.D + (j << 4));
+          // the scale byte the chunk needs (bf16 out: its own block, j / 2) or hands on (codes or
+          // scales out: chunk j copies the byte of block j, for j < sblocks)
           if (bf16_out || j < sblocks) sb[u] = __ldg(p.scales[l] + id * sblocks + (bf16_out ? (j >> 1) : j));
         } else if (j == 0) {
           flag(p.h.err, ENGRAM_ERR_ROW_ID);
@@ -313,7 +315,7 @@ hash_gather_fp8_kernel(const HashGatherParams p) {
         dst[0] = lo;
         dst[1] = hi;
       } else {
-        *reinterpret_cast<uint4*>(p.out_codes[l] + e0) = v[u];
+        if (p.out_codes[l] != nullptr) *reinterpret_cast<uint4*>(p.out_codes[l] + e0) = v[u];
         if (j < sblocks) {
           const int b = col * sblocks + j;          // block of 32 along K
           p.out_scales[l][((int64_t)(b >> 2) * rows4 + t) * 4 + (b & 3)] = ok ? (uint8_t)sb[u] : (uint8_t)127;

@@ -38,6 +38,9 @@ namespace {
 
 constexpr int kStageK = 128;                 // k per stage: one 128-byte swizzle row of codes
 constexpr int kThreads = 320;
+constexpr int kGatherWarps = 4;              // operand gather: warps 10..13
+constexpr int64_t kNoRow = -(1ll << 62);     // operand gather: a tile row past the matrix
+constexpr int kThreadsGather = kThreads + 32 * kGatherWarps;
 constexpr int kEpiThreads = 128;
 constexpr int kMaxStages = 8;
 constexpr int kATileBytes = 128 * kStageK;   // 16 KB: 128 rows x 128 codes
@@ -68,6 +71,12 @@ struct MxArgs {
   const uint32_t* sfb;                       // [N, K/128]
   int32_t* err;
   GateFuse gf;                               // gf.keys > 0: the gate's key sums instead of the keys
+  // operand gather (gather warps): the token tile's FP8 rows straight from the table
+  const int32_t* ids;                        // ids of token m at ids + m * ids_stride, one per column
+  int64_t ids_stride;
+  const uint8_t* table;                      // e4m3 codes [table_rows, D]
+  int64_t table_rows;
+  int32_t D;                                 // table row width, a multiple of 128
 };
 
 __device__ __forceinline__ void mx_tile_origin(const MxArgs& a, int tile, int& m0, int& n0) {
@@ -106,10 +115,16 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* v) {
                : "memory");
 }
 
-// kFused: the gate's key sums in the epilogue (MxArgs::gf); a separate instantiation, so the plain
-// projection keeps its own register allocation.
-template <bool kFused>
-__global__ void __launch_bounds__(kThreads, 1)
+// kFused: the gate's key sums in the epilogue (MxArgs::gf). kGatherA: the token tiles are gathered
+// from the table by four more warps (MxArgs::ids): warp 10 + w takes the stages of iterations
+// w, w + 4, ...: for each row of the tile it reads the row's id, copies the row's 128 codes of the
+// stage from the table with cp.async (16 bytes a lane, 8 lanes a row) into the 128B-swizzled
+// position the MMA reads (16-byte piece i of row r at piece i ^ (r % 8)), waits for its copies,
+// makes them visible to the tensor cores (proxy fence) and arrives on the stage's barrier (which
+// then expects the producer's copies and this arrival). Invalid ids read a zero row. Separate
+// instantiations, so the plain projection keeps its own register allocation.
+template <bool kFused, bool kGatherA>
+__global__ void __launch_bounds__(kGatherA ? kThreadsGather : kThreads, 1)
 wkv_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, float* __restrict__ D, const MxArgs a) {
   if (a.err != nullptr && (*reinterpret_cast<volatile int32_t*>(a.err) & ENGRAM_ERR_PIPE_TIMEOUT)) {
@@ -131,7 +146,7 @@ wkv_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
-      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->full[s]), kGatherA ? 2 : 1);   // producer (+ the stage's gather warp)
       mbar_init(smem_u32(&ctl->empty[s]), 1);
       mbar_init(smem_u32(&ctl->sf_full[s]), 4);
     }
@@ -142,7 +157,7 @@ wkv_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tmA);
+    if (!kGatherA) prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmD);
   }
@@ -169,7 +184,8 @@ wkv_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         const uint32_t st = tiles + (uint32_t)s * stage_bytes;
         const int rows_a = min(a.msub * 128, a.rows_a4 - m0);
         const int rows_b = min(a.BN, a.rows_b4 - n0);
-        mbar_expect_tx(full, (uint32_t)(a.a_bytes + a.b_bytes + 4 * rows_a + 4 * rows_b));
+        const int a_code_bytes = kGatherA ? 0 : a.a_bytes;          // gathered: cp.async, not counted
+        mbar_expect_tx(full, (uint32_t)(a_code_bytes + a.b_bytes + 4 * rows_a + 4 * rows_b));
         tma_load_2d(st + (uint32_t)a.a_bytes, &tmB, full, kb * kStageK, n0);
         bulk_load(st + sf_off + sfb_words_off, a.sfb + (int64_t)kb * a.rows_b4 + n0, 4u * (uint32_t)rows_b, full);
       };
@@ -177,7 +193,8 @@ wkv_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         const int s = it % a.stages;
         const uint32_t full = smem_u32(&ctl->full[s]);
         const uint32_t st = tiles + (uint32_t)s * stage_bytes;
-        for (int ms = 0; ms < a.msub; ++ms) tma_load_2d(st + ms * kATileBytes, &tmA, full, kb * kStageK, m0 + ms * 128);
+        if (!kGatherA)
+          for (int ms = 0; ms < a.msub; ++ms) tma_load_2d(st + ms * kATileBytes, &tmA, full, kb * kStageK, m0 + ms * 128);
         const int rows_a = min(a.msub * 128, a.rows_a4 - m0);
         bulk_load(st + sf_off, a.sfa + (int64_t)kb * a.rows_a4 + m0, 4u * (uint32_t)rows_a, full);
       };
@@ -310,7 +327,61 @@ wkv_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     }
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     __syncwarp();
-  } else {
+  } else if (kGatherA && warp >= 10) {
+    // ---------------- operand gather: token rows from the table ----------------
+    pdl_wait();                                // the ids come from the hash kernel
+    const int gw = warp - 10;
+    const int lr = lane >> 3;                  // row of a group of four
+    const int k16 = lane & 7;                  // 16-byte piece of the row's 128 codes
+    int it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < n_tiles_total; tile += gridDim.x) {
+      int m0, n0;
+      mx_tile_origin(a, tile, m0, n0);
+      for (int kb = 0; kb < a.num_kb; ++kb, ++it) {
+        if ((it & (kGatherWarps - 1)) != gw) continue;
+        const int s = it % a.stages;
+        const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+        if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, a.err, kWaitLimitCycles)) {
+          ok = false;
+          break;
+        }
+        const uint32_t st = tiles + (uint32_t)s * stage_bytes;
+        const int kcode = kb * kStageK;         // the stage's first code in the token row
+        const int col = kcode / a.D;
+        const int x = kcode - col * a.D + 16 * k16;
+        for (int ms = 0; ms < a.msub; ++ms) {
+          for (int rb = 0; rb < a.a_rows; rb += 32) {
+            int64_t idv[8];
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {        // the ids of 8 groups of 4 rows first
+              const int r = rb + 4 * g + lr;
+              const int64_t m = (int64_t)m0 + ms * 128 + r;
+              idv[g] = (r < a.a_rows && m < a.M) ? (int64_t)__ldg(a.ids + m * a.ids_stride + col) : kNoRow;
+            }
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              if (idv[g] == kNoRow) continue;  // rows past the matrix: not stored, not loaded
+              const int r = rb + 4 * g + lr;
+              const uint32_t dst = st + (uint32_t)(ms * kATileBytes + r * 128 + ((k16 ^ (r & 7)) << 4));
+              const bool valid = idv[g] >= 0 && idv[g] < a.table_rows;
+              const uint8_t* src = a.table + (valid ? idv[g] * a.D + x : 0);
+              // 16 bytes, or (an id outside the table) 16 zero bytes: source size 0
+              asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                           "r"(valid ? 16 : 0)
+                           : "memory");
+              if (!valid && k16 == 0 && a.err != nullptr) atomicOr(a.err, ENGRAM_ERR_ROW_ID);
+            }
+          }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the tensor cores
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->full[s]));
+      }
+    }
+  } else if (warp < 10) {
     // ---------------- scale writers ----------------
     const int q = warp & 3;                    // TMEM lane quarter of this warp
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
@@ -497,6 +568,18 @@ int launch_gemm_mx(const GemmMxParams& p, cudaStream_t stream, bool pdl) {
   MxArgs a = P.a;
   a.err = p.err;
   a.gf = p.gf;
+  const bool gather = p.ids != nullptr;
+  if (gather) {
+    if (p.D < 128 || p.D % 128 != 0 || p.table == nullptr) {
+      set_error("engram_project_mxfp8: the operand gather needs table rows a multiple of 128 wide (got %d)", p.D);
+      return ENGRAM_EINVAL;
+    }
+    a.ids = p.ids;
+    a.ids_stride = p.ids_stride;
+    a.table = p.table;
+    a.table_rows = p.table_rows;
+    a.D = p.D;
+  }
   if (a.gf.keys > 0 && a.gf.tile_cols != a.BN) {
     set_error("engram_project_mxfp8: fused gate planned for tiles of %d columns, the projection runs %d",
               a.gf.tile_cols, a.BN);
@@ -506,20 +589,26 @@ int launch_gemm_mx(const GemmMxParams& p, cudaStream_t stream, bool pdl) {
   a.sfb = reinterpret_cast<const uint32_t*>(p.SB);
   static PerContextOnce attr;               // the attribute belongs to the context's module
   cudaError_t ae = attr.run([] {
-    cudaError_t e1 =
-        cudaFuncSetAttribute(wkv_gemm_mx_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
-    if (e1 != cudaSuccess) return e1;
-    return cudaFuncSetAttribute(wkv_gemm_mx_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+    for (auto k : {wkv_gemm_mx_kernel<false, false>, wkv_gemm_mx_kernel<true, false>, wkv_gemm_mx_kernel<false, true>,
+                   wkv_gemm_mx_kernel<true, true>}) {
+      cudaError_t e1 = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+      if (e1 != cudaSuccess) return e1;
+    }
+    return cudaSuccess;
   });
   if (ae != cudaSuccess) return fail_cuda(ae, "engram_project_mxfp8: cudaFuncSetAttribute");
   CUtensorMap mA, mB, mD;
-  if (!make_map_u8(&mA, p.A, p.M, p.K, (uint32_t)a.a_rows) || !make_map_u8(&mB, p.B, p.N, p.K, (uint32_t)a.BN) ||
-      !make_map_f32(&mD, p.D, p.M, p.N)) {
+  // (with the operand gather the A map is not used; it is made over the table so that it is valid)
+  const bool map_a = gather ? make_map_u8(&mA, p.table, p.table_rows, p.D, 1)
+                            : make_map_u8(&mA, p.A, p.M, p.K, (uint32_t)a.a_rows);
+  if (!map_a || !make_map_u8(&mB, p.B, p.N, p.K, (uint32_t)a.BN) || !make_map_f32(&mD, p.Dout, p.M, p.N)) {
     set_error("engram_project_mxfp8: cuTensorMapEncodeTiled failed (driver entry point missing or bad layout)");
     return ENGRAM_ECUDA;
   }
-  cudaError_t e = launch_k(a.gf.keys > 0 ? wkv_gemm_mx_kernel<true> : wkv_gemm_mx_kernel<false>,
-                           dim3((unsigned)P.grid), dim3(kThreads), (size_t)P.smem, stream, pdl, mA, mB, mD, p.D, a);
+  auto kernel = a.gf.keys > 0 ? (gather ? wkv_gemm_mx_kernel<true, true> : wkv_gemm_mx_kernel<true, false>)
+                               : (gather ? wkv_gemm_mx_kernel<false, true> : wkv_gemm_mx_kernel<false, false>);
+  cudaError_t e = launch_k(kernel, dim3((unsigned)P.grid), dim3(gather ? kThreadsGather : kThreads), (size_t)P.smem,
+                           stream, pdl, mA, mB, mD, p.Dout, a);
   if (e != cudaSuccess) return fail_cuda(e, "engram_project_mxfp8: launch");
   return ENGRAM_OK;
 }

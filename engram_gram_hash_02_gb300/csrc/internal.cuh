@@ -120,7 +120,7 @@ struct HashGatherParams {
   const uint8_t* scales[kMaxGatherLayers];         // [num_rows, D/32]
   int64_t num_rows[kMaxGatherLayers];
   uint16_t* out_bf16[kMaxGatherLayers];            // [T, C*D] or NULL
-  uint8_t* out_codes[kMaxGatherLayers];            // [T, C*D] or NULL
+  uint8_t* out_codes[kMaxGatherLayers];            // [T, C*D] or NULL (with out_scales: scale words only)
   uint8_t* out_scales[kMaxGatherLayers];           // [ceil(C*D/128)][T4][4] or NULL
 };
 cudaError_t launch_hash_gather(const HashGatherParams& p, cudaStream_t stream, bool pdl = false);
@@ -188,7 +188,7 @@ struct GatherCodesParams {
   const void* table;          // e4m3 codes [rows, D]
   const uint8_t* scales;      // [rows, D/32]
   int64_t num_rows;
-  uint8_t* codes;             // [T, C*D]
+  uint8_t* codes;             // [T, C*D], or NULL: only the scale words (the projection gathers the codes)
   uint8_t* out_scales;        // [T, C*D/32]
   int32_t* err;
 };
@@ -207,15 +207,22 @@ cudaError_t launch_quantize_mxfp8(const uint16_t* w, int64_t N, int32_t K, uint8
                                   cudaStream_t stream);
 
 struct GemmMxParams {
-  const uint8_t* A;           // e4m3 codes [M, K]
+  const uint8_t* A;           // e4m3 codes [M, K] (unused with the operand gather)
   const uint8_t* SA;          // scale bytes [M, K/32]
   const uint8_t* B;           // e4m3 codes [N, K]
   const uint8_t* SB;          // scale bytes [N, K/32]
-  float* D;                   // [M, N]
+  float* Dout;                // [M, N]
   int64_t M;
   int32_t K, N;
   int32_t* err;
   GateFuse gf;                // as GemmParams::gf
+  // operand gather (ids != NULL): A row m is the concatenation of table rows ids[m * ids_stride + c],
+  // c = 0 .. K/D - 1, read from the table by the projection itself (SA still holds their scales)
+  const int32_t* ids;
+  int64_t ids_stride;
+  const uint8_t* table;       // e4m3 codes [table_rows, D]
+  int64_t table_rows;
+  int32_t D;
 };
 int launch_gemm_mx(const GemmMxParams& p, cudaStream_t stream, bool pdl = false);
 // tile width the projection of this shape runs with (the partial slot width of the fused gate);

@@ -88,10 +88,12 @@ gather_fp8_codes_kernel(const GatherCodesLayers m) {
     const int col = (int)(r - t * p.C);
     const int64_t id = __ldg(p.ids + t * p.ids_stride_t + col);
     const bool ok = id >= 0 && id < p.num_rows;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (ok) v = ld_stream_v4(weight + id * p.D + (j << 4));
-    else if (j == 0 && p.err != nullptr) atomicOr(p.err, ENGRAM_ERR_ROW_ID);
-    *reinterpret_cast<uint4*>(p.codes + (i << 4)) = v;
+    if (!ok && j == 0 && p.err != nullptr) atomicOr(p.err, ENGRAM_ERR_ROW_ID);
+    if (p.codes != nullptr) {                    // NULL: scale words only (the projection gathers the codes)
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (ok) v = ld_stream_v4(weight + id * p.D + (j << 4));
+      *reinterpret_cast<uint4*>(p.codes + (i << 4)) = v;
+    }
     // scale bytes: the row's D/32 bytes, copied by the threads of the first D/32 chunks into the
     // projection's word layout (block b of token t at byte 4 * ((b / 4) * rows4 + t) + b % 4)
     if (j < sblocks) {

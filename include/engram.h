@@ -306,6 +306,17 @@ void engram_set_gate_form(int32_t form);
  */
 void engram_set_gate_fusion(int32_t on);
 
+/*
+ * Tuning knob for engram_forward (and engram_forward2 / engram_forward_noalloc): 1 lets the FP8
+ * variant's projection gather its token rows from the table itself ([vLLM] _engram_lookup_kernel
+ * stages the rows the wkv projection consumes; here they go straight into the projection's operand
+ * tiles in shared memory, never through a gathered copy in HBM). The gathers before it then write
+ * only the rows' scale words. Applies to layers with an MXFP8 wkv, head_dim % 128 == 0 and fewer
+ * than 2^31 table rows. Same results as with the gathered copy (bit-identical kv). 0 (the default)
+ * turns it off. Process-wide; not thread-safe against calls.
+ */
+void engram_set_operand_gather(int32_t on);
+
 /* Per-layer resident weights ([Atlas] EngramLayerWeights; [vLLM] Engram parameters). */
 typedef struct EngramLayerWeights {
   int32_t table_format;        /* EngramTableFmt */

@@ -426,6 +426,7 @@ def run_ours(args, rank, world, device):
                        l2="flushed before every timed step (512 MB write, then a 256 MB read)",
                        **({"gate_fusion": True} if args.gate_fusion else {}),
                        **({"side_stream": True} if args.side_stream else {}),
+                       **({"operand_gather": True} if args.operand_gather else {}),
                        **({"gate_form": args.gate_form} if args.gate_form else {})),
         "gpu_launches": args.steps * (forward_launches(w) + len(calls)),
         "stages": stages,
@@ -781,6 +782,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--wkv", choices=["bf16", "mxfp8"], default="bf16",
                     help="wkv format: bf16 (the workloads' own), or MXFP8 (the FP8 operand variant)")
+    ap.add_argument("--operand-gather", action="store_true",
+                    help="FP8 variant: the projection gathers its token rows from the table itself")
     ap.add_argument("--side-stream", action="store_true",
                     help="engram_forward2: the later layers' gathers on a second stream")
     ap.add_argument("--gate-fusion", action="store_true",
@@ -822,6 +825,8 @@ def main():
             E.set_gate_form(args.gate_form)
         if args.gate_fusion:
             E.set_gate_fusion(True)
+        if args.operand_gather:
+            E.set_operand_gather(True)
         if args.only:
             run_only(args, torch.device("cuda", local))
             return

@@ -396,9 +396,11 @@ def set_gate_form(form: int = 0):
     lib().engram_set_gate_form(int(form))
 
 
-def set_gate_fusion(on: bool = False):
-    """engram_forward with the gate's key reductions fused into the projection's epilogue."""
-    lib().engram_set_gate_fusion(1 if on else 0)
+def set_gate_fusion(mode=0):
+    """How engram_forward joins the gate to the projection: 0 (or False) a separate gate kernel,
+    1 (or True) the key reductions in the projection's epilogue, 2 the gate inside the projection
+    kernel, overlapped with it."""
+    lib().engram_set_gate_fusion(int(mode))
 
 
 def set_operand_gather(on: bool = False):

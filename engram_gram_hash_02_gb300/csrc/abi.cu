@@ -275,13 +275,14 @@ int engram_gather_dequant(int32_t fmt, const int32_t* ids, int64_t ids_stride_t,
 
 static int project_impl(const uint16_t* A, const uint16_t* wkv, float* kv, int64_t T, int32_t K, int32_t N,
                         void* workspace, size_t ws_bytes, int32_t* err_flag, engram_stream_t stream, bool pdl,
-                        const GateFuse* gf = nullptr) {
+                        const GateFuse* gf = nullptr, const GateOverlap* go = nullptr) {
   if (T == 0) return ENGRAM_OK;
   int rc = check_project(A, wkv, kv, T, K, N);
   if (rc) return rc;
   ENGRAM_CHECK_ARG(workspace == nullptr || aligned(workspace, 256), "engram_project: workspace must be 256-byte aligned");
   GemmParams p{A, wkv, kv, T, K, N, err_flag, workspace, workspace != nullptr ? ws_bytes : 0};
   if (gf != nullptr) p.gf = *gf;
+  if (go != nullptr) p.go = *go;
   return launch_gemm(p, static_cast<cudaStream_t>(stream), pdl);
 }
 
@@ -399,7 +400,7 @@ static int g_operand_gather = 0;   // engram_set_operand_gather
 
 void engram_set_operand_gather(int32_t on) { g_operand_gather = on ? 1 : 0; }
 
-void engram_set_gate_fusion(int32_t on) { g_gate_fusion = on ? 1 : 0; }
+void engram_set_gate_fusion(int32_t mode) { g_gate_fusion = (mode == 1 || mode == 2) ? mode : 0; }
 
 void engram_set_gate_form(int32_t form) { set_gate_form_override((form == 1 || form == 2) ? form : 0); }
 
@@ -413,13 +414,16 @@ static size_t a_slot_bytes(int64_t T, int64_t K) {
   return round256(rows > codes ? rows : codes);
 }
 
+// Row-block counters of the overlapped gate: one word per 128 tokens and layer.
+static size_t done_bytes(int64_t T, int layers) { return round256((size_t)((T + 127) / 128) * layers * 4); }
+
 size_t engram_forward_workspace_bytes(const EngramDims* d, int64_t T) {
   if (d == nullptr || T < 0 || d->layers < 1) return 0;
   const int64_t C = (int64_t)(d->max_ngram - 1) * d->n_heads;
   const int64_t K = C * d->head_dim;
   const int64_t N = (int64_t)d->hidden * (d->hc + 1);
   return round256((size_t)(T * d->layers * C * 4)) + (size_t)d->layers * a_slot_bytes(T, K) +
-         round256((size_t)(T * N * 4));
+         round256((size_t)(T * N * 4)) + done_bytes(T, d->layers);
 }
 
 }  // extern "C"
@@ -506,6 +510,12 @@ int forward_core(const EngramDims* dims, const EngramHashTables* tables, const E
   auto rows_of = [&](int l) { return A0 + (size_t)l * a_slot; };                 // bf16 rows or codes
   auto scales_of = [&](int l) { return rows_of(l) + round256((size_t)(T * K)); };  // FP8 variant
   float* kv = reinterpret_cast<float*>(A0 + (size_t)L * a_slot);
+  // the overlapped gate's row-block counters (after kv), cleared by the hash launch
+  const int64_t nblk = (T + 127) / 128;
+  uint32_t* done = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(kv) + round256((size_t)(T * N * 4)));
+  auto overlap_gate = [&](int l) { return g_gate_fusion == 2 && layers[l].wkv_format == ENGRAM_WKV_BF16; };
+  bool any_overlap = false;
+  for (int l = 0; l < L; ++l) any_overlap = any_overlap || overlap_gate(l);
   // workspace beyond the minimum goes to the projection (stream-K partials)
   void* gemm_ws = ws_bytes > need ? static_cast<void*>(ws + need) : nullptr;
   const size_t gemm_ws_bytes = ws_bytes > need ? ws_bytes - need : 0;
@@ -517,6 +527,10 @@ int forward_core(const EngramDims* dims, const EngramHashTables* tables, const E
                    tok->lookback_ids, tables->token_map, tables->multipliers, tables->primes, tables->offsets, ids,
                    err_flag, hp);
   if (rc) return rc;
+  if (any_overlap) {
+    hp.zero = done;
+    hp.zero_n = (int32_t)(nblk * L);
+  }
   // FP8-variant layers whose projection gathers its own token rows (engram_set_operand_gather):
   // the gathers before it write only the rows' scale words
   auto operand_gather = [&](int l) {
@@ -612,7 +626,7 @@ int forward_core(const EngramDims* dims, const EngramHashTables* tables, const E
     // the gate fused into the projection's epilogue (engram_set_gate_fusion): the keys are reduced to
     // per-tile partial sums there; needs H % 32 == 0 and tiles no wider than one stream
     GateFuse gf{};
-    if (g_gate_fusion && dims->hidden % 32 == 0) {
+    if (g_gate_fusion == 1 && dims->hidden % 32 == 0) {
       const int tile_cols = gemm_tile_cols(T, (int)K, (int)N, mx);
       if (tile_cols > 0 && tile_cols <= dims->hidden)
         gf = GateFuse{streams[l], w.q_weight, w.k_weight, dims->hidden, dims->hc, dims->hidden * dims->hc, tile_cols};
@@ -628,8 +642,17 @@ int forward_core(const EngramDims* dims, const EngramHashTables* tables, const E
       rc = project_mx_impl(rows_of(l), scales_of(l), reinterpret_cast<const uint8_t*>(w.wkv), w.wkv_scales, kv, T,
                            (int32_t)K, (int32_t)N, err_flag, stream, true, gfp, operand_gather(l) ? &og : nullptr);
     } else {
+      GateOverlap go{};
+      if (overlap_gate(l)) {
+        rc = check_gate(dims, streams[l], kv, w.q_weight, w.k_weight, T);
+        if (rc) return rc;
+        go = GateOverlap{streams[l], w.q_weight, w.k_weight, tok->token_mask, dims->hidden, dims->hc, dims->eps,
+                         dims->clamp, done + (int64_t)l * nblk};
+      }
       rc = project_impl(reinterpret_cast<const uint16_t*>(rows_of(l)), w.wkv, kv, T, (int32_t)K, (int32_t)N, gemm_ws,
-                        gemm_ws_bytes, err_flag, stream, true, gfp);
+                        gemm_ws_bytes, err_flag, stream, true, gfp, overlap_gate(l) ? &go : nullptr);
+      if (rc) return rc;
+      if (overlap_gate(l)) continue;           // the projection kernel applied the gate
     }
     if (rc) return rc;
     rc = gate_impl(dims, streams[l], kv, w.q_weight, w.k_weight, tok->token_mask, T, err_flag, stream, true,

@@ -227,13 +227,12 @@ unsigned grid_for(int64_t work_items, int64_t per_block) {
 
 // ---- hash fused with the leading FP8 layers' gathers (engram_forward) ---------------------------
 // One CTA per token: warp 0 hashes the token (its window loads in flight while the block stages
-// cu_seqlens; then its token_map and lookback loads together), the ids go to the global id buffer
-// and to shared memory, then all threads fetch the token's rows of layers 0 .. layers-1. The
-// (layer, column, 16-byte chunk) items of the token are one flat index space; each thread issues
-// the loads of up to kHgChunks items (codes and scale byte) before it consumes any, so a token's
-// rows cost one round trip to memory: about three dependent round trips per token in all.
-constexpr int kHgThreads = 256;
-constexpr int kHgChunks = 4;
+// cu_seqlens), the ids go to the global id buffer and to shared memory, then all threads fetch
+// the token's rows of layers 0 .. layers-1, 16 bytes per thread and step, dequantised to bf16 or
+// copied as codes, or (a layer whose projection gathers its own rows) only the scale words.
+// (A form that issued every chunk load of the token at once, with 128 or 256 threads, ran faster
+// alone but made the chained decode step 2 us longer; this one is kept.)
+constexpr int kHgThreads = 128;
 
 __global__ void __launch_bounds__(kHgThreads)
 hash_gather_fp8_kernel(const HashGatherParams p) {
@@ -241,6 +240,7 @@ hash_gather_fp8_kernel(const HashGatherParams p) {
   __shared__ int32_t s_ids[256];
   pdl_wait();                                    // inputs may come from the preceding kernel
   pdl_trigger();
+  clear_words(p.h);
   const int64_t t = blockIdx.x;
   const int lane = threadIdx.x & 31;
   const bool hasher = threadIdx.x < 32;
@@ -253,72 +253,48 @@ hash_gather_fp8_kernel(const HashGatherParams p) {
   const int C = p.h.cols;
   const int cpr = p.D >> 4;                     // 16-byte chunks per row
   const int sblocks = p.D >> 5;
-  const int per_layer = C * cpr;
-  const int total = p.layers * per_layer;       // <= 256 * cpr
   const int64_t K = (int64_t)C * p.D;
   const int64_t rows4 = (p.h.T + 3) & ~(int64_t)3;
 #pragma unroll 1
-  for (int base = threadIdx.x; base < total; base += kHgThreads * kHgChunks) {
-    uint4 v[kHgChunks];
-    uint32_t sb[kHgChunks];
-    int64_t rid[kHgChunks];
-#pragma unroll
-    for (int u = 0; u < kHgChunks; ++u) {        // every load of the batch first
-      const int i = base + u * kHgThreads;
-      v[u] = make_uint4(0, 0, 0, 0);
-      sb[u] = 0;
-      rid[u] = -1;
-      if (i < total) {
-        const int l = i / per_layer;
-        const int rem = i - l * per_layer;
-        const int col = rem / cpr;
-        const int j = rem - col * cpr;
-        const int64_t id = s_ids[l * C + col];   // ids of token t in (layer, column) order
-        if (id >= 0 && id < p.num_rows[l]) {
-          rid[u] = id;
-          // the codes (not for a scales-only layer, whose codes the projection gathers itself)
-          const bool bf16_out = p.out_bf16[l] != nullptr;
-          if (bf16_out || p.out_codes[l] != nullptr)
-            v[u] = ld_stream_v4(static_cast<const uint8_t*>(p.table[l]) + id * p.D + (j << 4));
-          // the scale byte the chunk needs (bf16 out: its own block, j / 2) or hands on (codes or
-          // scales out: chunk j copies the byte of block j, for j < sblocks)
-          if (bf16_out || j < sblocks) sb[u] = __ldg(p.scales[l] + id * sblocks + (bf16_out ? (j >> 1) : j));
-        } else if (j == 0) {
-          flag(p.h.err, ENGRAM_ERR_ROW_ID);
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kHgChunks; ++u) {
-      const int i = base + u * kHgThreads;
-      if (i >= total) continue;
-      const int l = i / per_layer;
-      const int rem = i - l * per_layer;
-      const int col = rem / cpr;
-      const int j = rem - col * cpr;
-      const bool ok = rid[u] >= 0;
+  for (int l = 0; l < p.layers; ++l) {
+    const uint8_t* __restrict__ weight = static_cast<const uint8_t*>(p.table[l]);
+    const uint8_t* __restrict__ scales = p.scales[l];
+    const int64_t num_rows = p.num_rows[l];
+    uint16_t* const out_bf16 = p.out_bf16[l];
+    uint8_t* const out_codes = p.out_codes[l];
+    uint8_t* const out_scales = p.out_scales[l];
+    const bool scales_only = out_bf16 == nullptr && out_codes == nullptr;
+    for (int i = threadIdx.x; i < C * cpr; i += kHgThreads) {
+      const int col = i / cpr;
+      const int j = i - col * cpr;
+      if (scales_only && j >= sblocks) continue;
+      const int64_t id = s_ids[l * C + col];      // ids of token t in (layer, column) order
+      const bool ok = id >= 0 && id < num_rows;
+      if (!ok && j == 0) flag(p.h.err, ENGRAM_ERR_ROW_ID);
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (ok && !scales_only) v = ld_stream_v4(weight + id * p.D + (j << 4));
       const int64_t e0 = t * K + (int64_t)col * p.D + (j << 4);   // first element of this chunk
-      if (p.out_bf16[l] != nullptr) {
+      if (out_bf16 != nullptr) {
         uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
         if (ok) {
-          const float scale = __uint_as_float(sb[u] << 23);   // E8M0 byte: the fp32 exponent field
-          lo.x = dequant_pair(v[u].x, scale);
-          lo.y = dequant_pair(v[u].x >> 16, scale);
-          lo.z = dequant_pair(v[u].y, scale);
-          lo.w = dequant_pair(v[u].y >> 16, scale);
-          hi.x = dequant_pair(v[u].z, scale);
-          hi.y = dequant_pair(v[u].z >> 16, scale);
-          hi.z = dequant_pair(v[u].w, scale);
-          hi.w = dequant_pair(v[u].w >> 16, scale);
+          const float scale = __uint_as_float((uint32_t)__ldg(scales + id * sblocks + (j >> 1)) << 23);
+          lo.x = dequant_pair(v.x, scale);
+          lo.y = dequant_pair(v.x >> 16, scale);
+          lo.z = dequant_pair(v.y, scale);
+          lo.w = dequant_pair(v.y >> 16, scale);
+          hi.x = dequant_pair(v.z, scale);
+          hi.y = dequant_pair(v.z >> 16, scale);
+          hi.z = dequant_pair(v.w, scale);
+          hi.w = dequant_pair(v.w >> 16, scale);
         }
-        uint4* dst = reinterpret_cast<uint4*>(p.out_bf16[l] + e0);
+        uint4* dst = reinterpret_cast<uint4*>(out_bf16 + e0);
         dst[0] = lo;
         dst[1] = hi;
       } else {
-        if (p.out_codes[l] != nullptr) *reinterpret_cast<uint4*>(p.out_codes[l] + e0) = v[u];
+        if (out_codes != nullptr) *reinterpret_cast<uint4*>(out_codes + e0) = v;
         if (j < sblocks) {
           const int b = col * sblocks + j;          // block of 32 along K
-          p.out_scales[l][((int64_t)(b >> 2) * rows4 + t) * 4 + (b & 3)] = ok ? (uint8_t)sb[u] : (uint8_t)127;
+          out_scales[((int64_t)(b >> 2) * rows4 + t) * 4 + (b & 3)] = ok ? __ldg(scales + id * sblocks + j) : (uint8_t)127;
         }
       }
     }

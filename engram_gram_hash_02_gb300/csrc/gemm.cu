@@ -63,14 +63,6 @@ constexpr int kMaxStages = 8;
 constexpr int kATileBytes = 128 * kBK * 2;  // 16 KB
 constexpr unsigned long long kFlagMagic = 0x5EA5C0DEull;
 
-struct Ctl {
-  uint64_t full[kMaxStages];
-  uint64_t empty[kMaxStages];
-  uint64_t acc_full;                       // MMA -> epilogue: the item's accumulators are final
-  uint64_t acc_empty;                      // epilogue -> MMA: tensor memory drained
-  uint32_t tmem_base;
-  int32_t abort_flag;
-};
 
 struct GemmArgs {
   int32_t M, K, N;
@@ -87,6 +79,7 @@ struct GemmArgs {
   unsigned long long epoch;
   int32_t* err;
   GateFuse gf;                             // gf.keys > 0: the gate's key sums instead of the keys
+  GateOverlap go;                          // the gate overlapped with the projection (kOverlap)
 };
 
 struct Item {
@@ -138,14 +131,157 @@ __device__ __forceinline__ void tile_origin(const GemmArgs& a, int tile, int& m0
   n0 = (in_group / gsize) * a.BN;
 }
 
-__device__ __forceinline__ void epi_bar() {  // the 128 epilogue threads only
-  asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+constexpr int kGateThreads = 256;            // gate warps of the overlapped gate (warps 6..13)
+constexpr int kThreadsOverlap = kThreads + kGateThreads;
+constexpr int kGateVec = 8;                  // float4 chunks of a row per gate thread (H <= 8192)
+__device__ __forceinline__ void gate_bar() {  // the 256 gate threads only
+  asm volatile("bar.sync 2, %0;" ::"n"(kGateThreads) : "memory");
+}
+__device__ __forceinline__ float gbf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float gbf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Shared state of the gate warps: the warps' partial sums (two buffers: item parity) and the
+// go/stop decision of thread 0, so that every gate thread leaves the loop at the same item.
+struct GateShared {
+  float red[2][kGateThreads / 32][3];
+  int go[2];                                 // by the parity of the row-block waits
+};
+
+struct Ctl {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t acc_full;                       // MMA -> epilogue: the item's accumulators are final
+  uint64_t acc_empty;                      // epilogue -> MMA: tensor memory drained
+  uint32_t tmem_base;
+  int32_t abort_flag;
+  uint32_t published;                      // stream-K: epilogue warps done with the current segment
+  GateShared gate;                         // the overlapped gate's warps
+};
+
+// The gate warps of the overlapped gate: (token, stream) items round-robin over the CTAs in token
+// order; before the items of a row block, thread 0 waits (bounded) until every tile of that block
+// has been stored (the epilogues count them in a.go.done), then the 256 threads load the stream
+// row, the key and the value into registers, reduce, and write h + g * v in place.
+__device__ __forceinline__ void overlapped_gate(const GemmArgs& a, const float* kv, GateShared* gs,
+                                                volatile int32_t* abort_flag) {
+  const GateOverlap& g = a.go;
+  const int gt = threadIdx.x - kThreads;     // 0 .. 255
+  const int gl = gt & 31, gw = gt >> 5;
+  const int H = g.H, H4 = H >> 2, hc = g.hc;
+  const int64_t N = a.N;
+  const int rows_blk = 128 * a.msub;
+  const int64_t items = (int64_t)a.M * hc;
+  int ready = -1;
+  int n = 0;                                 // items processed: parity of the partial-sum buffer
+  int waits = 0;                             // row-block waits: parity of the go word
+  // Both buffers are double: a thread writes buffer p for the next use only after a gate barrier
+  // that every gate thread reached after its last read of buffer p.
+  for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
+    const int64_t t = item / hc;
+    const int j = (int)(item - t * hc);
+    if (g.mask != nullptr && __ldg(g.mask + t) == 0) continue;   // masked: not read or written
+    const int blk = (int)(t / rows_blk);
+    if (blk > ready) {                       // the row block's kv must be complete
+      if (gt == 0) {
+        int ok = 1;
+        const uint64_t t0 = clock64();
+        for (uint32_t it = 0;; ++it) {
+          uint32_t v;
+          asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(g.done + blk) : "memory");
+          if (v >= (uint32_t)(a.n_tiles * (kEpiThreads / 32))) break;   // every epilogue warp of every tile
+          __nanosleep(128);
+          if ((it & 15u) == 15u && (*abort_flag || (uint64_t)clock64() - t0 > kWaitLimitCycles)) {
+            if (!*abort_flag && a.err != nullptr) atomicOr(a.err, ENGRAM_ERR_PIPE_TIMEOUT);
+            *abort_flag = 1;
+            ok = 0;
+            break;
+          }
+        }
+        __threadfence();
+        gs->go[waits & 1] = ok;
+      }
+      gate_bar();
+      const int go = gs->go[waits & 1];
+      ++waits;
+      if (!go) break;                        // the same answer in every gate thread
+      ready = blk;
+    }
+    float4* hrow = reinterpret_cast<float4*>(g.streams + item * (int64_t)H);
+    const float* kvrow = kv + t * N;
+    const float4* krow = reinterpret_cast<const float4*>(kvrow + (int64_t)j * H);
+    const float4* vrow = reinterpret_cast<const float4*>(kvrow + (int64_t)hc * H);
+    const uint2* qrow = reinterpret_cast<const uint2*>(g.qw + (int64_t)j * H);
+    const uint2* krw = reinterpret_cast<const uint2*>(g.kw + (int64_t)j * H);
+    float4 x[kGateVec], v[kGateVec];
+    float ssh = 0.f, ssk = 0.f, dot = 0.f;
+    {
+      float4 y[kGateVec];
+#pragma unroll
+      for (int m = 0; m < kGateVec; ++m) {
+        const int c = gt + m * kGateThreads;
+        if (c < H4) {
+          x[m] = __ldcg(hrow + c);             // L2 only: kv was stored by other SMs in this kernel
+          y[m] = __ldcg(krow + c);
+          v[m] = __ldcg(vrow + c);
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < kGateVec; ++m) {
+        const int c = gt + m * kGateThreads;
+        if (c < H4) {
+          const uint2 qr = __ldg(qrow + c), kr = __ldg(krw + c);
+          ssh = fmaf(x[m].x, x[m].x, ssh); ssh = fmaf(x[m].y, x[m].y, ssh);
+          ssh = fmaf(x[m].z, x[m].z, ssh); ssh = fmaf(x[m].w, x[m].w, ssh);
+          ssk = fmaf(y[m].x, y[m].x, ssk); ssk = fmaf(y[m].y, y[m].y, ssk);
+          ssk = fmaf(y[m].z, y[m].z, ssk); ssk = fmaf(y[m].w, y[m].w, ssk);
+          dot = fmaf(x[m].x * gbf16lo(qr.x), y[m].x * gbf16lo(kr.x), dot);
+          dot = fmaf(x[m].y * gbf16hi(qr.x), y[m].y * gbf16hi(kr.x), dot);
+          dot = fmaf(x[m].z * gbf16lo(qr.y), y[m].z * gbf16lo(kr.y), dot);
+          dot = fmaf(x[m].w * gbf16hi(qr.y), y[m].w * gbf16hi(kr.y), dot);
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      ssh += __shfl_xor_sync(0xffffffffu, ssh, off);
+      ssk += __shfl_xor_sync(0xffffffffu, ssk, off);
+      dot += __shfl_xor_sync(0xffffffffu, dot, off);
+    }
+    if (gl == 0) {
+      gs->red[n & 1][gw][0] = ssh;
+      gs->red[n & 1][gw][1] = ssk;
+      gs->red[n & 1][gw][2] = dot;
+    }
+    gate_bar();
+    float sa = 0.f, sb = 0.f, sc = 0.f;
+    for (int w = 0; w < kGateThreads / 32; ++w) {   // the same order in every thread
+      sa += gs->red[n & 1][w][0];
+      sb += gs->red[n & 1][w][1];
+      sc += gs->red[n & 1][w][2];
+    }
+    const float invH = 1.0f / (float)H;
+    const float sv = sc * rsqrtf(sa * invH + g.eps) * rsqrtf(sb * invH + g.eps) / sqrtf((float)H);
+    float ss = 0.f;                                  // sign(0) = 0
+    if (sv > 0.f) ss = sqrtf(fmaxf(sv, g.clamp));
+    else if (sv < 0.f) ss = -sqrtf(fmaxf(-sv, g.clamp));
+    const float gate = 1.0f / (1.0f + expf(-ss));
+#pragma unroll
+    for (int m = 0; m < kGateVec; ++m) {
+      const int c = gt + m * kGateThreads;
+      if (c < H4)
+        hrow[c] = make_float4(fmaf(gate, v[m].x, x[m].x), fmaf(gate, v[m].y, x[m].y), fmaf(gate, v[m].z, x[m].z),
+                              fmaf(gate, v[m].w, x[m].w));
+    }
+    ++n;
+  }
 }
 
 // kFused: the gate's key sums in the epilogue (GemmArgs::gf); a separate instantiation, so the
 // plain projection keeps its own register allocation.
-template <bool kFused>
-__global__ void __launch_bounds__(kThreads, 1)
+// kOverlap: eight more warps apply the gate to the tokens of finished row blocks while the tensor
+// cores work on later tiles (GemmArgs::go).
+template <bool kFused, bool kOverlap>
+__global__ void __launch_bounds__(kOverlap ? kThreadsOverlap : kThreads, 1)
 wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmD,
                 float* __restrict__ D, const GemmArgs a) {
@@ -172,6 +308,7 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     mbar_init(smem_u32(&ctl->acc_full), 1);
     mbar_init(smem_u32(&ctl->acc_empty), kEpiThreads);
     ctl->abort_flag = 0;
+    ctl->published = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -322,6 +459,12 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       }
       if (!ok) tc_commit(smem_u32(&ctl->acc_full));
     }
+  } else if (warp >= 6) {
+    // ---------------- the overlapped gate (kOverlap) ----------------
+    if constexpr (kOverlap) {
+      pdl_wait();                              // the streams may be written by an earlier kernel
+      overlapped_gate(a, D, &ctl->gate, abort_flag);
+    }
   } else {
     // ---------------- epilogue: TMEM -> registers -> shared tile -> fp32 kv --------------------
     const int q = warp & 3;                    // TMEM lane quarter this warp may access
@@ -391,10 +534,24 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       }
       __syncwarp();
       if (publish) {
-        // this segment is in kv (every warp's stores complete): let the next segment's CTA add
+        // this segment is in kv once every epilogue warp's stores are complete: the last of the
+        // four warps to get here lets the next segment's CTA add (a count, not a barrier, so an
+        // abort that only some warps see cannot leave the others waiting)
         __threadfence();
-        epi_bar();
-        if (et == 0) st_release(a.flags + blockIdx.x, want);
+        __syncwarp();
+        if (lane == 0 && (atomicAdd(&ctl->published, 1u) & 3u) == 3u) {
+          __threadfence();
+          st_release(a.flags + blockIdx.x, want);
+        }
+      }
+      if (kOverlap) {
+        // this warp's quarter of the tile is in kv (its stores are complete): count it for the row
+        // block, four counts a tile (no barrier across the epilogue warps, so an abort that only
+        // some of them see cannot leave the others waiting)
+        __threadfence();
+        __syncwarp();
+        if (lane == 0)
+          asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.go.done + m0 / (128 * a.msub)) : "memory");
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&ctl->acc_empty));  // tensor memory may take the next item
@@ -646,13 +803,23 @@ int gemm_tile_cols(int64_t M, int K, int N, bool mx) {
 int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl) {
   Plan P;
   const bool fused = p.gf.keys > 0;             // the gate's key sums need whole tiles: no stream-K
-  if (!plan_gemm(p.M, p.K, p.N, num_sms(), p.workspace != nullptr ? p.ws_bytes : 0, P, !fused)) {
+  const bool overlap = p.go.streams != nullptr;  // the gate waits for whole row blocks: no stream-K
+  if (fused && overlap) {
+    set_error("engram_project: the fused key sums and the overlapped gate exclude each other");
+    return ENGRAM_EINVAL;
+  }
+  if (!plan_gemm(p.M, p.K, p.N, num_sms(), p.workspace != nullptr ? p.ws_bytes : 0, P, !fused && !overlap)) {
     set_error("engram_project: no tile plan fits (T %lld, K %d, N %d)", (long long)p.M, p.K, p.N);
     return ENGRAM_EINVAL;
   }
   GemmArgs a = P.a;
   a.err = p.err;
   a.gf = p.gf;
+  a.go = p.go;
+  if (overlap && (p.go.done == nullptr || p.go.H % 4 != 0 || p.go.H > 4 * kGateThreads * kGateVec)) {
+    set_error("engram_project: overlapped gate needs its row-block counters and H <= %d", 4 * kGateThreads * kGateVec);
+    return ENGRAM_EINVAL;
+  }
   if (fused && a.gf.tile_cols != a.BN) {
     set_error("engram_project: fused gate planned for tiles of %d columns, the projection runs %d", a.gf.tile_cols,
               a.BN);
@@ -665,10 +832,11 @@ int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl) {
   }
   static PerContextOnce attr;               // the attribute belongs to the context's module
   cudaError_t ae = attr.run([] {
-    cudaError_t e1 =
-        cudaFuncSetAttribute(wkv_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
-    if (e1 != cudaSuccess) return e1;
-    return cudaFuncSetAttribute(wkv_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+    for (auto k : {wkv_gemm_kernel<false, false>, wkv_gemm_kernel<true, false>, wkv_gemm_kernel<false, true>}) {
+      cudaError_t e1 = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+      if (e1 != cudaSuccess) return e1;
+    }
+    return cudaSuccess;
   });
   if (ae != cudaSuccess) return fail_cuda(ae, "engram_project: cudaFuncSetAttribute");
   CUtensorMap mA, mB, mD;
@@ -677,8 +845,9 @@ int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl) {
     set_error("engram_project: cuTensorMapEncodeTiled failed (driver entry point missing or bad layout)");
     return ENGRAM_ECUDA;
   }
-  cudaError_t e = launch_k(fused ? wkv_gemm_kernel<true> : wkv_gemm_kernel<false>, dim3((unsigned)P.grid),
-                           dim3(kThreads), (size_t)P.smem, stream, pdl, mA, mB, mD, p.D, a);
+  auto kernel = fused ? wkv_gemm_kernel<true, false> : overlap ? wkv_gemm_kernel<false, true> : wkv_gemm_kernel<false, false>;
+  cudaError_t e = launch_k(kernel, dim3((unsigned)P.grid), dim3(overlap ? kThreadsOverlap : kThreads), (size_t)P.smem,
+                           stream, pdl, mA, mB, mD, p.D, a);
   if (e != cudaSuccess) return fail_cuda(e, "engram_project: launch");
   return ENGRAM_OK;
 }

@@ -39,7 +39,6 @@ namespace {
 constexpr int kStageK = 128;                 // k per stage: one 128-byte swizzle row of codes
 constexpr int kThreads = 320;
 constexpr int kGatherWarps = 4;              // operand gather: warps 10..13
-constexpr int64_t kNoRow = -(1ll << 62);     // operand gather: a tile row past the matrix
 constexpr int kThreadsGather = kThreads + 32 * kGatherWarps;
 constexpr int kEpiThreads = 128;
 constexpr int kMaxStages = 8;
@@ -116,8 +115,8 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* v) {
 }
 
 // kFused: the gate's key sums in the epilogue (MxArgs::gf). kGatherA: the token tiles are gathered
-// from the table by four more warps (MxArgs::ids): warp 10 + w takes the stages of iterations
-// w, w + 4, ...: for each row of the tile it reads the row's id, copies the row's 128 codes of the
+// from the table by four more warps (MxArgs::ids): warp 10 + w serves the ring stages s with
+// s % 4 == w: for each row of the tile it reads the row's id, copies the row's 128 codes of the
 // stage from the table with cp.async (16 bytes a lane, 8 lanes a row) into the 128B-swizzled
 // position the MMA reads (16-byte piece i of row r at piece i ^ (r % 8)), waits for its copies,
 // makes them visible to the tensor cores (proxy fence) and arrives on the stage's barrier (which
@@ -329,18 +328,21 @@ wkv_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     __syncwarp();
   } else if (kGatherA && warp >= 10) {
     // ---------------- operand gather: token rows from the table ----------------
+    // Stage s is always served by warp 10 + s % 4, so a warp waits only for the consumption of
+    // its own previous copy into that stage (a barrier phase never more than one ahead).
     pdl_wait();                                // the ids come from the hash kernel
     const int gw = warp - 10;
     const int lr = lane >> 3;                  // row of a group of four
     const int k16 = lane & 7;                  // 16-byte piece of the row's 128 codes
+    const int rows = a.msub * 128;             // tile rows: lane L holds the ids of rows L + 32 i
     int it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < n_tiles_total; tile += gridDim.x) {
       int m0, n0;
       mx_tile_origin(a, tile, m0, n0);
       for (int kb = 0; kb < a.num_kb; ++kb, ++it) {
-        if ((it & (kGatherWarps - 1)) != gw) continue;
         const int s = it % a.stages;
+        if (s % kGatherWarps != gw) continue;
         const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
         if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, a.err, kWaitLimitCycles)) {
           ok = false;
@@ -350,29 +352,28 @@ wkv_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         const int kcode = kb * kStageK;         // the stage's first code in the token row
         const int col = kcode / a.D;
         const int x = kcode - col * a.D + 16 * k16;
-        for (int ms = 0; ms < a.msub; ++ms) {
-          for (int rb = 0; rb < a.a_rows; rb += 32) {
-            int64_t idv[8];
+        int32_t idl[8];                         // this lane's rows' ids, all requested at once
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {        // the ids of 8 groups of 4 rows first
-              const int r = rb + 4 * g + lr;
-              const int64_t m = (int64_t)m0 + ms * 128 + r;
-              idv[g] = (r < a.a_rows && m < a.M) ? (int64_t)__ldg(a.ids + m * a.ids_stride + col) : kNoRow;
-            }
+        for (int i = 0; i < 8; ++i) {
+          const int R = lane + 32 * i;          // row within the tile
+          const int r = R & 127;
+          const int64_t m = (int64_t)m0 + R;
+          idl[i] = (R < rows && r < a.a_rows && m < a.M) ? __ldg(a.ids + m * a.ids_stride + col) : 0;
+        }
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
-              if (idv[g] == kNoRow) continue;  // rows past the matrix: not stored, not loaded
-              const int r = rb + 4 * g + lr;
-              const uint32_t dst = st + (uint32_t)(ms * kATileBytes + r * 128 + ((k16 ^ (r & 7)) << 4));
-              const bool valid = idv[g] >= 0 && idv[g] < a.table_rows;
-              const uint8_t* src = a.table + (valid ? idv[g] * a.D + x : 0);
-              // 16 bytes, or (an id outside the table) 16 zero bytes: source size 0
-              asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                           "r"(valid ? 16 : 0)
-                           : "memory");
-              if (!valid && k16 == 0 && a.err != nullptr) atomicOr(a.err, ENGRAM_ERR_ROW_ID);
-            }
-          }
+        for (int g = 0; g < 64; ++g) {          // rows 4g .. 4g + 3, 8 lanes a row
+          const int R = 4 * g + lr;
+          const int32_t id = __shfl_sync(0xffffffffu, idl[g >> 3], R & 31);   // every lane takes part
+          const int ms = R >> 7, r = R & 127;
+          // rows past the tile's loaded rows or past the matrix: not loaded (never stored)
+          if (R >= rows || r >= a.a_rows || (int64_t)m0 + R >= a.M) continue;
+          const uint32_t dst = st + (uint32_t)(ms * kATileBytes + r * 128 + ((k16 ^ (r & 7)) << 4));
+          const bool valid = id >= 0 && (int64_t)id < a.table_rows;
+          const uint8_t* src = a.table + (valid ? (int64_t)id * a.D + x : 0);
+          // 16 bytes, or (an id outside the table) 16 zero bytes: source size 0
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                       : "memory");
+          if (!valid && k16 == 0 && a.err != nullptr) atomicOr(a.err, ENGRAM_ERR_ROW_ID);
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
         asm volatile("cp.async.wait_group 0;" ::: "memory");

@@ -13,6 +13,7 @@ hash_kernel(const HashParams p) {
   __shared__ int32_t s_cu[kSmemCu];
   pdl_wait();                                    // inputs may come from the preceding kernel
   pdl_trigger();
+  clear_words(p);
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const bool live = t < p.T;

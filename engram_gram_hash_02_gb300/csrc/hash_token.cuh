@@ -20,6 +20,12 @@ namespace {
 
 constexpr int kSmemCu = 2048;   // cu_seqlens entries staged in shared memory (else searched in global)
 
+// The words engram_forward asks the hash launch to clear (block 0, after the dependency wait).
+__device__ __forceinline__ void clear_words(const HashParams& p) {
+  if (blockIdx.x == 0 && p.zero != nullptr)
+    for (int i = threadIdx.x; i < p.zero_n; i += blockDim.x) p.zero[i] = 0u;
+}
+
 // largest s in [0, S) with cu[s] <= t (empty sequences before t are skipped)
 template <typename Load>
 __device__ __forceinline__ int32_t find_sequence(Load cu, int32_t S, int64_t t) {
@@ -43,13 +49,11 @@ __device__ __forceinline__ bool stage_cu(const HashParams& p, int32_t* s_cu) {
 }
 
 // What one lane of a token's warp loads before the token's sequence is known (issued early so it
-// overlaps the block's staging of cu_seqlens). The dependent loads (token_map[raw], and the
-// lookback entry, which needs the sequence) are issued together afterwards, so a token costs two
-// dependent round trips to memory before its ids are known.
+// overlaps the block's staging of cu_seqlens).
 struct TokenLoads {
   uint64_t prime[8], off[8];                 // per (layer, column) idx = lane + 32u
   int64_t pos;                               // t - lane: this lane's window slot
-  int32_t raw, sid, sid_next;
+  int32_t raw, sid, sid_next, mapped;
   bool slot, alive, raw_ok;
 };
 
@@ -76,6 +80,7 @@ __device__ __forceinline__ TokenLoads hash_token_loads(const HashParams& p, int6
     }
   }
   L.raw_ok = L.raw >= 0 && L.raw < p.raw_vocab;
+  L.mapped = (L.slot && L.raw_ok) ? __ldg(p.token_map + L.raw) : p.pad_id;
   return L;
 }
 
@@ -97,12 +102,11 @@ __device__ __forceinline__ void hash_token_finish(const HashParams& p, int64_t t
   }
 
   // ---- slot k = lane: may it be read, and what does it hold --------------------------------
-  // (the token_map and lookback loads of the lanes are in flight together)
   bool ok = false;
   int64_t val = p.pad_id;
   if (lane < p.max_ngram) {
     if (L.pos >= start) {
-      val = (L.slot && L.raw_ok) ? __ldg(p.token_map + L.raw) : p.pad_id;   // pad_id outside the map
+      val = L.mapped;                                 // pad_id for a raw id outside the map
       if (lane == 0 && !L.raw_ok && p.err != nullptr) atomicOr(p.err, ENGRAM_ERR_RAW_ID);
       ok = L.alive && L.sid != 0 && (lane == 0 || L.sid == L.sid_next);
     } else if (p.lookback_ids != nullptr) {

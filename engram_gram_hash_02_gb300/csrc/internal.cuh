@@ -101,6 +101,8 @@ struct HashParams {
   int32_t S;
   int32_t layers, max_ngram, n_heads, cols;
   int32_t raw_vocab, pad_id;
+  uint32_t* zero;             // engram_forward: words the first block clears (the overlapped gate's
+  int32_t zero_n;             // row-block counters), after waiting for the preceding kernel
 };
 cudaError_t launch_hash(const HashParams& p, cudaStream_t stream, bool pdl = false);
 
@@ -161,6 +163,19 @@ struct GateFuse {
   int32_t tile_cols;         // columns per partial slot: the tile width (set by the projection's plan)
 };
 
+// The gate run by extra warps of the projection kernel, overlapped with its tensor-core work: the
+// gate of a token starts once every tile of its row block is stored (counted in `done`, one
+// counter per 128-row block, zero when the projection starts).
+struct GateOverlap {
+  float* streams;            // [M, hc, H] fp32, updated in place (NULL: off)
+  const uint16_t* qw;        // q_weight [hc, H] bf16
+  const uint16_t* kw;        // k_weight [hc, H] bf16
+  const uint8_t* mask;       // [M] or NULL
+  int32_t H, hc;
+  float eps, clamp;
+  uint32_t* done;            // [ceil(M / 128)]
+};
+
 struct GemmParams {
   const uint16_t* A;
   const uint16_t* B;
@@ -171,6 +186,7 @@ struct GemmParams {
   void* workspace;      // stream-K flags (may be NULL)
   size_t ws_bytes;
   GateFuse gf;          // gf.keys > 0: gate partials instead of the key columns (data-parallel only)
+  GateOverlap go;       // go.streams != NULL: the gate inside the projection (data-parallel only)
 };
 // returns ENGRAM_OK or an error code (sets the message)
 int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl = false);

@@ -293,18 +293,23 @@ int engram_gate(const EngramDims* dims, float* streams, const float* kv,
 void engram_set_gate_form(int32_t form);
 
 /*
- * Tuning knob for engram_forward (and engram_forward_noalloc): 1 fuses the gate's key reductions
- * into the projection's epilogue ([NeMo] compile_engram_gate fuses the gate's reductions; [vLLM]
- * Engram.forward runs the gate right after the wkv projection). The epilogue then never stores the
- * key columns of kv: for every token row of a tile it forms, per stream the tile covers,
- * sum key^2 and sum (h * q_weight) * (key * k_weight) from the stream row and the accumulators,
- * and a finishing pass adds sum h^2, forms the gate and adds g * value. Same results as the
- * unfused path up to fp32 summation order. Applies to layers with hidden % 32 == 0 whose
- * projection tiles are at most `hidden` columns wide (the others run unfused); the projection then
- * runs its data-parallel schedule. 0 (the default) turns it off. Process-wide; not thread-safe
- * against calls.
+ * Tuning knob for engram_forward (and engram_forward2 / engram_forward_noalloc): how the gate
+ * joins the projection ([NeMo] compile_engram_gate fuses the gate's reductions; [vLLM]
+ * Engram.forward runs the gate right after the wkv projection). Same results as the separate
+ * gate up to fp32 summation order; the projection then runs its data-parallel schedule.
+ *   0  (the default) the gate is its own kernel after the projection.
+ *   1  key reductions in the projection's epilogue: the key columns of kv are never stored; for
+ *      every token row of a tile the epilogue forms, per stream the tile covers, sum key^2 and
+ *      sum (h * q_weight) * (key * k_weight) from the stream row and the accumulators, and a
+ *      finishing pass adds sum h^2, forms the gate and adds g * value. Layers with
+ *      hidden % 32 == 0 whose projection tiles are at most `hidden` columns wide (others run
+ *      mode 0).
+ *   2  the gate inside the projection kernel, overlapped with it: eight more warps per CTA apply
+ *      the gate to the tokens of each 128- or 256-row block as soon as every tile of that block
+ *      is stored, while the tensor cores work on later tiles (bf16 wkv layers; others run mode 0).
+ * Process-wide; not thread-safe against calls.
  */
-void engram_set_gate_fusion(int32_t on);
+void engram_set_gate_fusion(int32_t mode);
 
 /*
  * Tuning knob for engram_forward (and engram_forward2 / engram_forward_noalloc): 1 lets the FP8

@@ -180,10 +180,11 @@ def test_forward_workspace_holds_one_operand_slot_per_layer(lib):
         C, K, N = 24, 24 * 256, 4096 * 5
         w1 = lib.engram_forward_workspace_bytes(ctypes.byref(one), T)
         w2 = lib.engram_forward_workspace_bytes(ctypes.byref(two), T)
-        slot = w2 - w1 - (r256(4 * T * 2 * C) - r256(4 * T * C))
+        done = lambda L: r256((T + 127) // 128 * L * 4)       # the overlapped gate's row-block counters
+        slot = w2 - w1 - (r256(4 * T * 2 * C) - r256(4 * T * C)) - (done(2) - done(1))
         # a slot holds the bf16 rows, or the FP8 codes and then their scale words
         assert slot >= 2 * T * K and slot >= r256(T * K) + (K // 128) * ((T + 3) // 4 * 4) * 4
-        assert w1 == r256(4 * T * C) + slot + r256(4 * T * N)
+        assert w1 == r256(4 * T * C) + slot + r256(4 * T * N) + done(1)
 
 
 def test_sync_status_rejects_a_null_word(lib):

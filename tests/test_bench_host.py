@@ -63,3 +63,9 @@ def test_cpu_baseline_times_the_oracle_on_one_and_all_cores():
     assert out["kind"] == "oracle" and out["unit"] == "tokens/s per layer"
     assert out["one_core"]["cores"] == 1 and out["all_cores"]["cores"] == (os.cpu_count() or 1)
     assert out["one_core"]["value"] > 0 and out["value"] == out["all_cores"]["value"]
+
+
+def test_mxfp8_peak_is_the_measured_one():
+    assert bench.tensor_peak(PEAKS, True) == bench.MXFP8_PEAK_TFLOPS["burst"]
+    assert bench.tensor_peak(PEAKS, False) == PEAKS["bf16_tflops"]
+    assert bench.tensor_peak(PEAKS, False, "sustained") == PEAKS["bf16_tflops_sustained"]

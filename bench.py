@@ -376,6 +376,13 @@ def run_ours(args, rank, world, device):
     tokens = w.tokens * w.layers
     value = replica_throughput(world, tokens, ms)
 
+    # ---- the FP8 operand variant on the same workload (wkv encoded as MXFP8 once) ------------
+    variant = None
+    if not mx and not args.no_variant and all(t["fmt"] == "fp8" for t in path.case.tables):
+        variant = time_fp8_variant(args, path, stream, flush_l2, device)
+        variant["ms"] = max_over_ranks(variant["ms"], device)
+        variant["ms_per_step"] = round(variant["ms"], 5)
+
     # ---- end to end through the public API with host buffers -------------------------------
     e2e = run_e2e(args, path, stream, device) if not args.no_e2e else None
     if e2e is not None:
@@ -444,9 +451,42 @@ def run_ours(args, rank, world, device):
                        "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                        "ms_per_step": round(e2e["ms"], 5),
                        "pipelining": f"{e2e['slots']} buffer slots; copies in (token inputs packed in one pinned buffer, then the streams) / forward / copies out on 3 streams"}
+    if variant is not None:
+        line["variants"] = {"mxfp8_wkv": dict(variant, value=round(replica_throughput(world, tokens, variant["ms"]), 1),
+                                              unit="tokens/s per layer")}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, path.case, args.cpu_tokens)
     return line
+
+
+def time_fp8_variant(args, path, stream, flush_l2, device) -> dict:
+    """engram_forward with every layer's wkv encoded as MXFP8 (engram_quantize_mxfp8, once, outside
+    the timed region) and the FP8 table rows fed to the block-scaled projection: the same steps,
+    L2 flush and events as the headline."""
+    E = path.E
+    layers = []
+    for l, lw in enumerate(path.layers):
+        codes, scales = E.quantize_mxfp8(path.case.wkv[l])
+        layers.append(E.LayerWeights(lw.fmt, lw.table, lw.scales, lw.num_rows, codes, lw.q_weight, lw.k_weight,
+                                     wkv_scales=scales))
+    plan = E.ForwardPlan(path.dims, path.tables, layers, path.input_ids, path.streams, cu_seqlens=path.cu,
+                         sequence_ids=path.sid, token_mask=path.mask, lookback_ids=path.lookback, err=path.err)
+    for _ in range(args.warmup):
+        flush_l2(1)
+        plan.run(stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        flush_l2(k)
+        ev[k][0].record(stream)
+        plan.run(stream)
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    if path.err.item() != 0:
+        raise RuntimeError(f"device error flag {path.err.item()} in the FP8 variant")
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    return {"ms": ms, "ms_per_step": round(ms, 5), "dtype": "e4m3 x e4m3 (MXFP8), fp32 accumulate",
+            "note": "wkv encoded once as MXFP8 (E8M0 scale per 32); the FP8 table rows are the projection's A operand"}
 
 
 def roofline_entry(dom, model, achieved, peak, unit, pk, pk_kind, mx, traffic) -> dict:
@@ -799,6 +839,7 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=32)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-variant", action="store_true", help="skip the FP8 operand variant's line")
     ap.add_argument("--only", choices=["hash", "gather", "project", "gate", "forward"],
                     help="profiling: run one stage alone (forward: engram_forward as a whole)")
     ap.add_argument("--tokens", type=int, default=0,

@@ -440,6 +440,8 @@ def run_ours(args, rank, world, device):
                        **({"gate_fusion": args.gate_fusion} if args.gate_fusion else {}),
                        **({"side_stream": True} if args.side_stream else {}),
                        **({"operand_gather": True} if args.operand_gather else {}),
+                       **({"gemm_tile": args.gemm_tile} if args.gemm_tile else {}),
+                       **({"mx_tile": args.mx_tile} if args.mx_tile else {}),
                        **({"gate_form": args.gate_form} if args.gate_form else {})),
         "gpu_launches": args.steps * (forward_launches(w) + len(calls)),
         "stages": stages,
@@ -830,6 +832,8 @@ def main():
                     help="wkv format: bf16 (the workloads' own), or MXFP8 (the FP8 operand variant)")
     ap.add_argument("--operand-gather", action="store_true",
                     help="FP8 variant: the projection gathers its token rows from the table itself")
+    ap.add_argument("--gemm-tile", type=int, default=0, help="tuning: force the bf16 projection's tile width")
+    ap.add_argument("--mx-tile", type=int, default=0, help="tuning: force the MXFP8 projection's tile width")
     ap.add_argument("--side-stream", action="store_true",
                     help="engram_forward2: the later layers' gathers on a second stream")
     ap.add_argument("--gate-fusion", type=int, nargs="?", const=1, default=0, choices=[0, 1, 2],
@@ -875,6 +879,10 @@ def main():
             E.set_gate_fusion(args.gate_fusion)
         if args.operand_gather:
             E.set_operand_gather(True)
+        if args.gemm_tile:
+            E.set_gemm_tile(args.gemm_tile)
+        if args.mx_tile:
+            E.set_gemm_mx_tile(args.mx_tile)
         if args.only:
             run_only(args, torch.device("cuda", local))
             return

@@ -73,6 +73,8 @@ struct GemmArgs {
   int32_t stage_bytes;
   uint32_t idesc;
   uint32_t tmem_cols, acc_stride;
+  int32_t acc_sets;                        // 2: two accumulator sets, items alternate (epilogue overlaps MMAs)
+  uint32_t set_stride;                     // tensor-memory columns between the sets
   int32_t stream_k;                        // 0: data-parallel tiles, 1: stream-K
   int64_t total_units;                     // tiles * num_kb
   unsigned long long* flags;               // [grid] (stream-K)
@@ -150,8 +152,8 @@ struct GateShared {
 struct Ctl {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  uint64_t acc_full;                       // MMA -> epilogue: the item's accumulators are final
-  uint64_t acc_empty;                      // epilogue -> MMA: tensor memory drained
+  uint64_t acc_full[2];                    // MMA -> epilogue: an accumulator set's item is final
+  uint64_t acc_empty[2];                   // epilogue -> MMA: the set is drained
   uint32_t tmem_base;
   int32_t abort_flag;
   uint32_t published;                      // stream-K: epilogue warps done with the current segment
@@ -305,8 +307,10 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       mbar_init(smem_u32(&ctl->full[s]), 1);
       mbar_init(smem_u32(&ctl->empty[s]), 1);
     }
-    mbar_init(smem_u32(&ctl->acc_full), 1);
-    mbar_init(smem_u32(&ctl->acc_empty), kEpiThreads);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&ctl->acc_full[b]), 1);
+      mbar_init(smem_u32(&ctl->acc_empty[b]), kEpiThreads);
+    }
     ctl->abort_flag = 0;
     ctl->published = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -409,14 +413,18 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       int slot = 0;                            // iteration mod stages
       uint32_t round = 0;                      // (iteration / stages) & 1
       bool ok = true;
+      int set = 0;
       while (ok && sch.next(item)) {
-        // the epilogue has drained the previous item's accumulators
-        if (!mbar_wait(smem_u32(&ctl->acc_empty), (uint32_t)(n_items & 1) ^ 1u, abort_flag, a.err,
-                       kWaitLimitCycles)) {
+        // the epilogue has drained this accumulator set's previous item (with two sets, the item
+        // before last: its drain overlaps this item's MMAs)
+        set = n_items & (a.acc_sets - 1);
+        const uint32_t use = (uint32_t)(n_items >> (a.acc_sets - 1));
+        if (!mbar_wait(smem_u32(&ctl->acc_empty[set]), (use & 1u) ^ 1u, abort_flag, a.err, kWaitLimitCycles)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const uint32_t tacc = tmem + (uint32_t)set * a.set_stride;
         for (int kb = item.k0; kb < item.k1; ++kb) {
           if (!mbar_wait(smem_u32(&ctl->full[slot]), round, abort_flag, a.err, kWaitLimitCycles)) {
             ok = false;
@@ -434,17 +442,17 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             if (a.nsplit == 2) {
               // two chains: the two column halves (the second half's rows start BN/2 rows on)
               const uint32_t acc = (kb > item.k0 || k > 0) ? 1u : 0u;
-              tc_mma(tmem, a0 + (uint64_t)(2 * k), bdesc, a.idesc, acc);
-              tc_mma(tmem + a.acc_stride, a0 + (uint64_t)(2 * k), bdesc + (uint64_t)(((a.BN >> 1) * kBK * 2) >> 4),
+              tc_mma(tacc, a0 + (uint64_t)(2 * k), bdesc, a.idesc, acc);
+              tc_mma(tacc + a.acc_stride, a0 + (uint64_t)(2 * k), bdesc + (uint64_t)(((a.BN >> 1) * kBK * 2) >> 4),
                      a.idesc, acc);
             } else if (a.msub == 2) {
               // two chains: the two 128-row halves
               const uint32_t acc = (kb > item.k0 || k > 0) ? 1u : 0u;
-              tc_mma(tmem, a0 + (uint64_t)(2 * k), bdesc, a.idesc, acc);
-              tc_mma(tmem + a.acc_stride, a0 + (uint64_t)(2 * k + (kATileBytes >> 4)), bdesc, a.idesc, acc);
+              tc_mma(tacc, a0 + (uint64_t)(2 * k), bdesc, a.idesc, acc);
+              tc_mma(tacc + a.acc_stride, a0 + (uint64_t)(2 * k + (kATileBytes >> 4)), bdesc, a.idesc, acc);
             } else {
               // two chains: even and odd k steps of the same tile
-              tc_mma(tmem + (k & 1) * a.acc_stride, a0 + (uint64_t)(2 * k), bdesc, a.idesc,
+              tc_mma(tacc + (k & 1) * a.acc_stride, a0 + (uint64_t)(2 * k), bdesc, a.idesc,
                      (kb > item.k0 || k > 1) ? 1u : 0u);
             }
           }
@@ -454,10 +462,10 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             round ^= 1u;
           }
         }
-        tc_commit(smem_u32(&ctl->acc_full));     // this item's accumulators final (or drained)
+        tc_commit(smem_u32(&ctl->acc_full[set]));   // this item's accumulators final (or drained)
         ++n_items;
       }
-      if (!ok) tc_commit(smem_u32(&ctl->acc_full));
+      if (!ok) tc_commit(smem_u32(&ctl->acc_full[set]));
     }
   } else if (warp >= 6) {
     // ---------------- the overlapped gate (kOverlap) ----------------
@@ -490,10 +498,12 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       }
     }
     while (sch.next(item)) {
-      const bool ok = mbar_wait(smem_u32(&ctl->acc_full), (uint32_t)(n_items & 1), abort_flag, a.err,
-                                kWaitLimitCycles);
+      const int set = n_items & (a.acc_sets - 1);
+      const uint32_t use = (uint32_t)(n_items >> (a.acc_sets - 1));
+      const bool ok = mbar_wait(smem_u32(&ctl->acc_full[set]), use & 1u, abort_flag, a.err, kWaitLimitCycles);
       tc_fence_after();
       if (!ok || *abort_flag) break;
+      const uint32_t tacc = tmem + (uint32_t)set * a.set_stride;
       int m0, n0;
       tile_origin(a, item.tile, m0, n0);
       // A tile cut between CTAs is summed into kv in unit order: the CTA holding its first
@@ -516,15 +526,15 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         if (*abort_flag) break;
       }
       if (fused) {
-        fused_gate_epilogue(a.gf, &tmD, D, a.M, a.N, tmem, q, lane, stg, a.msub, a.nsplit == 1 && a.msub == 1,
+        fused_gate_epilogue(a.gf, &tmD, D, a.M, a.N, tacc, q, lane, stg, a.msub, a.nsplit == 1 && a.msub == 1,
                             a.acc_stride, a.BN, a.nsplit, m0, n0);
       } else if (a.nsplit == 2) {
         const int hb = a.BN >> 1;
-        store_accumulators(&tmD, D, a.M, a.N, tmem, q, lane, stg, 1, false, a.acc_stride, hb, m0, n0, false);
-        store_accumulators(&tmD, D, a.M, a.N, tmem + a.acc_stride, q, lane, stg, 1, false, a.acc_stride, hb, m0,
+        store_accumulators(&tmD, D, a.M, a.N, tacc, q, lane, stg, 1, false, a.acc_stride, hb, m0, n0, false);
+        store_accumulators(&tmD, D, a.M, a.N, tacc + a.acc_stride, q, lane, stg, 1, false, a.acc_stride, hb, m0,
                            n0 + hb, false);
       } else {
-        store_accumulators(&tmD, D, a.M, a.N, tmem, q, lane, stg, a.msub, a.msub == 1, a.acc_stride, a.BN, m0, n0,
+        store_accumulators(&tmD, D, a.M, a.N, tacc, q, lane, stg, a.msub, a.msub == 1, a.acc_stride, a.BN, m0, n0,
                            adder);
       }
       // this item's stores are complete (global writes done) before the tile or flag moves on
@@ -554,7 +564,7 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.go.done + m0 / (128 * a.msub)) : "memory");
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&ctl->acc_empty));  // tensor memory may take the next item
+      mbar_arrive(smem_u32(&ctl->acc_empty[set]));   // the set may take its next item
       ++n_items;
       if (fused) {                             // the next tile's stream rows into L2 during its main loop
         Schedule peek = sch;
@@ -575,8 +585,9 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (*abort_flag) {
       // make sure no MMA is still writing the accumulators we are about to free
       volatile int32_t never = 0;
-      for (int ph = 0; ph < 2; ++ph)
-        mbar_wait(smem_u32(&ctl->acc_full), (uint32_t)ph, &never, nullptr, kWaitLimitCycles / 8);
+      for (int b = 0; b < a.acc_sets; ++b)
+        for (int ph = 0; ph < 2; ++ph)
+          mbar_wait(smem_u32(&ctl->acc_full[b]), (uint32_t)ph, &never, nullptr, kWaitLimitCycles / 8);
     }
     __syncwarp();
     tc_fence_after();
@@ -681,6 +692,15 @@ bool plan_gemm(int64_t M, int K, int N, int sms, size_t ws_bytes, Plan& P, bool 
   a.acc_stride = pow2_at_least((uint32_t)(a.BN / a.nsplit));
   a.tmem_cols = a.acc_stride * 2;              // two accumulators (chains) per item
   if (a.tmem_cols > 512) return false;
+  // Two accumulator sets when they fit (tiles of at most 128 columns): items alternate between
+  // them, so the epilogue drains one while the tensor cores fill the other.
+  a.acc_sets = 1;
+  a.set_stride = 0;
+  if (!sk && a.nsplit == 1 && 2 * a.tmem_cols <= 512) {
+    a.acc_sets = 2;
+    a.set_stride = a.tmem_cols;
+    a.tmem_cols *= 2;
+  }
   a.idesc = (1u << 4)                          // accumulate in f32
             | (1u << 7) | (1u << 10)           // A and B are bf16
             | ((uint32_t)((a.BN / a.nsplit) >> 3) << 17)    // N (of one MMA)

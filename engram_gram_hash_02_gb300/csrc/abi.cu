@@ -275,8 +275,7 @@ int engram_gather_dequant(int32_t fmt, const int32_t* ids, int64_t ids_stride_t,
 
 static int project_impl(const uint16_t* A, const uint16_t* wkv, float* kv, int64_t T, int32_t K, int32_t N,
                         void* workspace, size_t ws_bytes, int32_t* err_flag, engram_stream_t stream, bool pdl,
-                        const GateFuse* gf = nullptr, const GateOverlap* go = nullptr,
-                        const KvSplit* split = nullptr) {
+                        const GateFuse* gf = nullptr, const GateOverlap* go = nullptr) {
   if (T == 0) return ENGRAM_OK;
   int rc = check_project(A, wkv, kv, T, K, N);
   if (rc) return rc;
@@ -284,7 +283,6 @@ static int project_impl(const uint16_t* A, const uint16_t* wkv, float* kv, int64
   GemmParams p{A, wkv, kv, T, K, N, err_flag, workspace, workspace != nullptr ? ws_bytes : 0};
   if (gf != nullptr) p.gf = *gf;
   if (go != nullptr) p.go = *go;
-  if (split != nullptr) p.split = *split;
   return launch_gemm(p, static_cast<cudaStream_t>(stream), pdl);
 }
 
@@ -293,34 +291,14 @@ int engram_project(const uint16_t* A, const uint16_t* wkv, float* kv, int64_t T,
   return project_impl(A, wkv, kv, T, K, N, workspace, ws_bytes, err_flag, stream, false);
 }
 
-// Where the gate reads an item's key and value (and, fused, its partial sums).
-struct GateSource {
-  const void* keys;
-  int64_t key_stride;
-  int32_t key_bf16;
-  const float* values;
-  int64_t value_stride;
-  int32_t part_cols;
-  const float* part;
-  int64_t part_stride;
-};
-
-// kv fp32 [T, (hc+1) H]: the keys then the value in each row
-static GateSource full_kv_source(const EngramDims* dims, const float* kv) {
-  const int64_t N = (int64_t)dims->hidden * (dims->hc + 1);
-  return GateSource{kv, N, 0, kv + (int64_t)dims->hc * dims->hidden, N, 0, nullptr, 0};
-}
-
-static int gate_impl(const EngramDims* dims, float* streams, const GateSource& src, const uint16_t* q_weight,
+static int gate_impl(const EngramDims* dims, float* streams, const float* kv, const uint16_t* q_weight,
                      const uint16_t* k_weight, const uint8_t* token_mask, int64_t T, int32_t* err_flag,
-                     engram_stream_t stream, bool pdl) {
+                     engram_stream_t stream, bool pdl, int32_t part_cols = 0) {
   if (T == 0) return check_dims(dims, false, true);
-  int rc = check_gate(dims, streams, src.values, q_weight, k_weight, T);
+  int rc = check_gate(dims, streams, kv, q_weight, k_weight, T);
   if (rc) return rc;
-  ENGRAM_CHECK_ARG(src.part_cols > 0 || (src.keys != nullptr && aligned(src.keys, 16)), "gate: keys missing");
-  GateParams p{streams, src.keys, src.key_stride, src.key_bf16, src.values, src.value_stride, q_weight, k_weight,
-               token_mask, T, dims->hidden, dims->hc, dims->eps, dims->clamp, err_flag, src.part_cols, src.part,
-               src.part_stride};
+  GateParams p{streams, kv, q_weight, k_weight, token_mask, T, dims->hidden, dims->hc, dims->eps, dims->clamp,
+               err_flag, part_cols};
   cudaError_t e = launch_gate(p, static_cast<cudaStream_t>(stream), pdl);
   return e == cudaSuccess ? ENGRAM_OK : fail_cuda(e, "engram_gate: launch");
 }
@@ -328,8 +306,7 @@ static int gate_impl(const EngramDims* dims, float* streams, const GateSource& s
 int engram_gate(const EngramDims* dims, float* streams, const float* kv, const uint16_t* q_weight,
                 const uint16_t* k_weight, const uint8_t* token_mask, int64_t T, int32_t* err_flag,
                 engram_stream_t stream) {
-  if (dims == nullptr) return check_dims(dims, false, true);
-  return gate_impl(dims, streams, full_kv_source(dims, kv), q_weight, k_weight, token_mask, T, err_flag, stream, false);
+  return gate_impl(dims, streams, kv, q_weight, k_weight, token_mask, T, err_flag, stream, false);
 }
 
 // ---- FP8 (MXFP8) operand variant ------------------------------------------------------------
@@ -397,14 +374,12 @@ struct OperandGather {
 
 static int project_mx_impl(const uint8_t* A, const uint8_t* SA, const uint8_t* W, const uint8_t* SW, float* kv,
                            int64_t T, int32_t K, int32_t N, int32_t* err_flag, engram_stream_t stream, bool pdl,
-                           const GateFuse* gf = nullptr, const OperandGather* og = nullptr,
-                           const KvSplit* split = nullptr) {
+                           const GateFuse* gf = nullptr, const OperandGather* og = nullptr) {
   if (T == 0) return ENGRAM_OK;
   int rc = check_project_mx(A, SA, W, SW, kv, T, K, N);
   if (rc) return rc;
   GemmMxParams p{A, SA, W, SW, kv, T, K, N, err_flag};
   if (gf != nullptr) p.gf = *gf;
-  if (split != nullptr) p.split = *split;
   if (og != nullptr) {
     p.ids = og->ids;
     p.ids_stride = og->ids_stride;
@@ -538,21 +513,6 @@ int forward_core(const EngramDims* dims, const EngramHashTables* tables, const E
   // the overlapped gate's row-block counters (after kv), cleared by the hash launch
   const int64_t nblk = (T + 127) / 128;
   uint32_t* done = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(kv) + round256((size_t)(T * N * 4)));
-  // kv's region in the split layout: the keys in bf16 [T, hc H], then (256-byte aligned) the value
-  // in fp32 [T, H]. The gate reads half the key bytes; the value keeps fp32 (with a bf16 value the
-  // Q2_K layers' streams came out 2.1e-3 from the oracle). Used when it fits the region, the key
-  // width is a multiple of 16 and the gate's key sums are not fused (their partial slots sit in
-  // the full layout's key columns).
-  const int64_t keys_cols = (int64_t)dims->hc * dims->hidden;
-  const size_t split_bytes = round256((size_t)(T * keys_cols * 2)) + (size_t)(T * dims->hidden * 4);
-  const bool split = g_gate_fusion != 1 && keys_cols % 16 == 0 && split_bytes <= round256((size_t)(T * N * 4));
-  KvSplit kvs{};
-  if (split)
-    kvs = KvSplit{reinterpret_cast<uint16_t*>(kv),
-                  reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(kv) + round256((size_t)(T * keys_cols * 2))),
-                  (int32_t)keys_cols};
-  const GateSource src = split ? GateSource{kvs.keys, keys_cols, 1, kvs.values, dims->hidden, 0, nullptr, 0}
-                               : full_kv_source(dims, kv);
   auto overlap_gate = [&](int l) { return g_gate_fusion == 2 && layers[l].wkv_format == ENGRAM_WKV_BF16; };
   bool any_overlap = false;
   for (int l = 0; l < L; ++l) any_overlap = any_overlap || overlap_gate(l);
@@ -669,8 +629,7 @@ int forward_core(const EngramDims* dims, const EngramHashTables* tables, const E
     if (g_gate_fusion == 1 && dims->hidden % 32 == 0) {
       const int tile_cols = gemm_tile_cols(T, (int)K, (int)N, mx);
       if (tile_cols > 0 && tile_cols <= dims->hidden)
-        gf = GateFuse{streams[l], w.q_weight, w.k_weight, dims->hidden, dims->hc, dims->hidden * dims->hc, tile_cols,
-                      kv, N};
+        gf = GateFuse{streams[l], w.q_weight, w.k_weight, dims->hidden, dims->hc, dims->hidden * dims->hc, tile_cols};
     }
     const GateFuse* gfp = gf.keys > 0 ? &gf : nullptr;
     if (wait_ev[l] >= 0) {
@@ -681,26 +640,23 @@ int forward_core(const EngramDims* dims, const EngramHashTables* tables, const E
       // FP8 variant: the rows' codes and scales are the A operand as they are
       const OperandGather og{ids + (int64_t)l * C, (int64_t)L * C, w.table, w.table_rows, dims->head_dim};
       rc = project_mx_impl(rows_of(l), scales_of(l), reinterpret_cast<const uint8_t*>(w.wkv), w.wkv_scales, kv, T,
-                           (int32_t)K, (int32_t)N, err_flag, stream, true, gfp, operand_gather(l) ? &og : nullptr,
-                           split ? &kvs : nullptr);
+                           (int32_t)K, (int32_t)N, err_flag, stream, true, gfp, operand_gather(l) ? &og : nullptr);
     } else {
       GateOverlap go{};
       if (overlap_gate(l)) {
-        rc = check_gate(dims, streams[l], src.values, w.q_weight, w.k_weight, T);
+        rc = check_gate(dims, streams[l], kv, w.q_weight, w.k_weight, T);
         if (rc) return rc;
         go = GateOverlap{streams[l], w.q_weight, w.k_weight, tok->token_mask, dims->hidden, dims->hc, dims->eps,
                          dims->clamp, done + (int64_t)l * nblk};
       }
       rc = project_impl(reinterpret_cast<const uint16_t*>(rows_of(l)), w.wkv, kv, T, (int32_t)K, (int32_t)N, gemm_ws,
-                        gemm_ws_bytes, err_flag, stream, true, gfp, overlap_gate(l) ? &go : nullptr,
-                        split ? &kvs : nullptr);
+                        gemm_ws_bytes, err_flag, stream, true, gfp, overlap_gate(l) ? &go : nullptr);
       if (rc) return rc;
       if (overlap_gate(l)) continue;           // the projection kernel applied the gate
     }
     if (rc) return rc;
-    GateSource gsrc = src;
-    if (gf.tile_cols > 0) gsrc = GateSource{nullptr, 0, 0, src.values, src.value_stride, gf.tile_cols, kv, N};
-    rc = gate_impl(dims, streams[l], gsrc, w.q_weight, w.k_weight, tok->token_mask, T, err_flag, stream, true);
+    rc = gate_impl(dims, streams[l], kv, w.q_weight, w.k_weight, tok->token_mask, T, err_flag, stream, true,
+                   gf.tile_cols);
     if (rc) return rc;
   }
   return ENGRAM_OK;

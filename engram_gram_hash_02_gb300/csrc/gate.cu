@@ -109,20 +109,11 @@ __device__ __forceinline__ void sum_partials(const GateParams& p, const float* s
   }
 }
 
-// Where an item's key comes from: fp32 keys, bf16 keys (engram_forward's split layout), or the
-// partial sums the projection fused (GateParams::part_cols > 0: no key is read).
-enum KeyMode { kKeyF32 = 0, kKeyBf16 = 1, kKeyFused = 2 };
-
-__device__ __forceinline__ float4 bf16x4_to_float4(uint2 w) {
-  return make_float4(bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y));
-}
-
-// kMode: the key source (KeyMode). With kKeyFused the key slot of a buffer receives the item's
-// partial slots; with kKeyBf16 it receives the bf16 key row (half a row of bytes).
-template <int kMode>
+// kFused: the projection fused the key sums (GateParams::part_cols > 0): the key slot of a buffer
+// receives the item's partial slots instead of the key row.
+template <bool kFused>
 __global__ void __launch_bounds__(kMaxThreads, 1)
 gate_kernel(const GateParams p) {
-  constexpr bool kFused = kMode == kKeyFused;
   extern __shared__ __align__(128) float buf[];          // kBufs x [h | key (or partials) | value], H floats each
   __shared__ __align__(8) uint64_t full[kBufs];
   __shared__ float red[kMaxThreads / 32][3];
@@ -133,7 +124,7 @@ gate_kernel(const GateParams p) {
   const int H = p.H;
   const int tid = threadIdx.x;
   const uint32_t row_bytes = 4u * (uint32_t)H;
-  const uint32_t key_bytes = kMode == kKeyBf16 ? 2u * (uint32_t)H : row_bytes;
+  const int64_t N = (int64_t)(p.hc + 1) * H;
   const Items items(p, gridDim.x);
 
   if (tid == 0) {
@@ -150,7 +141,7 @@ gate_kernel(const GateParams p) {
   auto buffer = [&](int n) { return smem_u32(buf) + (uint32_t)((n % kBufs) * 3) * row_bytes; };
   auto issue_h = [&](int64_t i, int n) {                 // stream row: not written by the projection
     const uint32_t bar = smem_u32(&full[n % kBufs]);
-    uint32_t bytes = 2u * row_bytes + key_bytes;
+    uint32_t bytes = 3u * row_bytes;
     if (kFused) bytes = 2u * row_bytes + 16u * (uint32_t)part_range(p, (int)(i % p.hc)).count;
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
     bulk_copy(buffer(n), p.streams + i * (int64_t)H, row_bytes, bar);
@@ -161,13 +152,11 @@ gate_kernel(const GateParams p) {
     const int j = (int)(i - t * p.hc);
     if (kFused) {
       const PartRange pr = part_range(p, j);
-      bulk_copy(buffer(n) + row_bytes, p.part + t * p.part_stride + 4 * pr.first, 16u * (uint32_t)pr.count, bar);
+      bulk_copy(buffer(n) + row_bytes, p.kv + t * N + 4 * pr.first, 16u * (uint32_t)pr.count, bar);
     } else {
-      const size_t esz = kMode == kKeyBf16 ? 2 : 4;
-      bulk_copy(buffer(n) + row_bytes,
-                static_cast<const uint8_t*>(p.keys) + (size_t)(t * p.key_stride + (int64_t)j * H) * esz, key_bytes, bar);
+      bulk_copy(buffer(n) + row_bytes, p.kv + t * N + (int64_t)j * H, row_bytes, bar);
     }
-    bulk_copy(buffer(n) + 2u * row_bytes, p.values + t * p.value_stride, row_bytes, bar);
+    bulk_copy(buffer(n) + 2u * row_bytes, p.kv + t * N + (int64_t)p.hc * H, row_bytes, bar);
   };
   int64_t first_items[kBufs];
   if (tid == 0) {
@@ -215,7 +204,7 @@ gate_kernel(const GateParams p) {
       const float4 x = hs[c];
       ssh = fmaf(x.x, x.x, ssh); ssh = fmaf(x.y, x.y, ssh); ssh = fmaf(x.z, x.z, ssh); ssh = fmaf(x.w, x.w, ssh);
       if (!kFused) {
-        const float4 y = kMode == kKeyBf16 ? bf16x4_to_float4(reinterpret_cast<const uint2*>(ks)[c]) : ks[c];
+        const float4 y = ks[c];
         const uint2 qr = qreg[m], kr = kreg[m];
         ssk = fmaf(y.x, y.x, ssk); ssk = fmaf(y.y, y.y, ssk); ssk = fmaf(y.z, y.z, ssk); ssk = fmaf(y.w, y.w, ssk);
         dot = fmaf(x.x * bf16lo(qr.x), y.x * bf16lo(kr.x), dot);
@@ -306,10 +295,9 @@ gate_kernel(const GateParams p) {
 // time limit is needed.
 constexpr int kItemThreads = 256;
 
-template <int kVec, int kMode>
+template <int kVec, bool kFused>
 __global__ void __launch_bounds__(kItemThreads)
 gate_item_kernel(const GateParams p) {
-  constexpr bool kFused = kMode == kKeyFused;
   __shared__ float red[kItemThreads / 32][3];
   __shared__ float fused_sums[2];
   const int H = p.H, H4 = H >> 2;
@@ -321,11 +309,10 @@ gate_item_kernel(const GateParams p) {
     pdl_wait();
     return;
   }
+  const int64_t N = (int64_t)(p.hc + 1) * H;
   float4* hrow = reinterpret_cast<float4*>(p.streams + item * (int64_t)H);
-  const int64_t key0 = t * p.key_stride + (int64_t)j * H;          // first key element of the item
-  const float4* krow = reinterpret_cast<const float4*>(static_cast<const float*>(p.keys) + key0);
-  const uint2* krow16 = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.keys) + key0);
-  const float4* vrow = reinterpret_cast<const float4*>(p.values + t * p.value_stride);
+  const float4* krow = reinterpret_cast<const float4*>(p.kv + t * N + (int64_t)j * H);
+  const float4* vrow = reinterpret_cast<const float4*>(p.kv + t * N + (int64_t)p.hc * H);
   const uint2* qrow = reinterpret_cast<const uint2*>(p.q_weight + (int64_t)j * H);
   const uint2* kwrow = reinterpret_cast<const uint2*>(p.k_weight + (int64_t)j * H);
   float4 x[kVec], y[kVec], v[kVec];
@@ -345,8 +332,7 @@ gate_item_kernel(const GateParams p) {
   for (int m = 0; m < kVec; ++m) {
     const int c = tid + m * kItemThreads;
     if (c < H4) {
-      if (kMode == kKeyF32) y[m] = krow[c];
-      if (kMode == kKeyBf16) y[m] = bf16x4_to_float4(krow16[c]);
+      if (!kFused) y[m] = krow[c];
       v[m] = vrow[c];
     }
   }
@@ -354,7 +340,7 @@ gate_item_kernel(const GateParams p) {
   if (kFused && warp == 0) {                       // the key sums: the item's partial slots
     const PartRange pr = part_range(p, j);
     float fs, fd;
-    sum_partials(p, p.part + t * p.part_stride + 4 * pr.first, pr, j, lane, fs, fd);
+    sum_partials(p, p.kv + t * N + 4 * pr.first, pr, j, lane, fs, fd);
     if (lane == 0) {
       fused_sums[0] = fs;
       fused_sums[1] = fd;
@@ -418,10 +404,9 @@ template <int kVec>
 cudaError_t launch_gate_items(const GateParams& p, cudaStream_t stream, bool pdl) {
   const int H4 = p.H / 4;
   const int threads = H4 >= kItemThreads ? kItemThreads : ((H4 + 31) / 32) * 32;
-  const dim3 grid((unsigned)(p.T * p.hc));
-  if (p.part_cols > 0) return launch_k(gate_item_kernel<kVec, kKeyFused>, grid, dim3(threads), 0, stream, pdl, p);
-  if (p.key_bf16) return launch_k(gate_item_kernel<kVec, kKeyBf16>, grid, dim3(threads), 0, stream, pdl, p);
-  return launch_k(gate_item_kernel<kVec, kKeyF32>, grid, dim3(threads), 0, stream, pdl, p);
+  if (p.part_cols > 0)
+    return launch_k(gate_item_kernel<kVec, true>, dim3((unsigned)(p.T * p.hc)), dim3(threads), 0, stream, pdl, p);
+  return launch_k(gate_item_kernel<kVec, false>, dim3((unsigned)(p.T * p.hc)), dim3(threads), 0, stream, pdl, p);
 }
 
 int g_gate_form = 0;   // engram_set_gate_form: 0 automatic, 1 persistent, 2 one CTA per item
@@ -461,15 +446,14 @@ cudaError_t launch_gate_persistent(const GateParams& p, cudaStream_t stream, boo
   if (threads > kMaxThreads) threads = kMaxThreads;
   const size_t smem = (size_t)kBufs * 3 * 4 * (size_t)H;
   if (smem > (size_t)kSmemBudget - 2048) return cudaErrorInvalidValue;
-  void (*kernel)(const GateParams) =
-      p.part_cols > 0 ? gate_kernel<kKeyFused> : p.key_bf16 ? gate_kernel<kKeyBf16> : gate_kernel<kKeyF32>;
+  const bool fused = p.part_cols > 0;
+  void (*kernel)(const GateParams) = fused ? gate_kernel<true> : gate_kernel<false>;
   static PerContextOnce attr;               // the attribute belongs to the context's module
   cudaError_t ae = attr.run([] {
-    for (auto k : {gate_kernel<kKeyF32>, gate_kernel<kKeyBf16>, gate_kernel<kKeyFused>}) {
-      cudaError_t e1 = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget - 2048);
-      if (e1 != cudaSuccess) return e1;
-    }
-    return cudaSuccess;
+    cudaError_t e1 = cudaFuncSetAttribute(gate_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          kSmemBudget - 2048);
+    if (e1 != cudaSuccess) return e1;
+    return cudaFuncSetAttribute(gate_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget - 2048);
   });
   if (ae != cudaSuccess) return ae;
   int per_sm = 0;                           // resident CTAs per SM (registers, shared memory)

@@ -82,7 +82,6 @@ struct GemmArgs {
   int32_t* err;
   GateFuse gf;                             // gf.keys > 0: the gate's key sums instead of the keys
   GateOverlap go;                          // the gate overlapped with the projection (kOverlap)
-  KvSplit split;                           // split.keys != NULL: bf16 keys + fp32 value, not kv fp32
 };
 
 struct Item {
@@ -210,12 +209,9 @@ __device__ __forceinline__ void overlapped_gate(const GemmArgs& a, const float* 
       ready = blk;
     }
     float4* hrow = reinterpret_cast<float4*>(g.streams + item * (int64_t)H);
-    // the key and value: kv fp32 [M, N], or the split layout (bf16 keys [M, hc H], fp32 value [M, H])
-    const bool split = a.split.keys != nullptr;
-    const float4* krow = reinterpret_cast<const float4*>(kv + t * N + (int64_t)j * H);
-    const uint2* krow16 = reinterpret_cast<const uint2*>(a.split.keys + t * a.split.keys_cols + (int64_t)j * H);
-    const float4* vrow = split ? reinterpret_cast<const float4*>(a.split.values + t * (N - a.split.keys_cols))
-                               : reinterpret_cast<const float4*>(kv + t * N + (int64_t)hc * H);
+    const float* kvrow = kv + t * N;
+    const float4* krow = reinterpret_cast<const float4*>(kvrow + (int64_t)j * H);
+    const float4* vrow = reinterpret_cast<const float4*>(kvrow + (int64_t)hc * H);
     const uint2* qrow = reinterpret_cast<const uint2*>(g.qw + (int64_t)j * H);
     const uint2* krw = reinterpret_cast<const uint2*>(g.kw + (int64_t)j * H);
     float4 x[kGateVec], v[kGateVec];
@@ -227,12 +223,7 @@ __device__ __forceinline__ void overlapped_gate(const GemmArgs& a, const float* 
         const int c = gt + m * kGateThreads;
         if (c < H4) {
           x[m] = __ldcg(hrow + c);             // L2 only: kv was stored by other SMs in this kernel
-          if (split) {
-            const uint2 w = __ldcg(krow16 + c);
-            y[m] = make_float4(gbf16lo(w.x), gbf16hi(w.x), gbf16lo(w.y), gbf16hi(w.y));
-          } else {
-            y[m] = __ldcg(krow + c);
-          }
+          y[m] = __ldcg(krow + c);
           v[m] = __ldcg(vrow + c);
         }
       }
@@ -294,8 +285,8 @@ __device__ __forceinline__ void overlapped_gate(const GemmArgs& a, const float* 
 template <bool kFused, bool kOverlap>
 __global__ void __launch_bounds__(kOverlap ? kThreadsOverlap : kThreads, 1)
 wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmK,
-                const __grid_constant__ CUtensorMap tmV, float* __restrict__ D, const GemmArgs a) {
+                const __grid_constant__ CUtensorMap tmD,
+                float* __restrict__ D, const GemmArgs a) {
   // A timeout anywhere in an earlier launch sharing the flag word voids the result: skip the
   // work instead of waiting out the time limits again.
   if (a.err != nullptr && (*reinterpret_cast<volatile int32_t*>(a.err) & ENGRAM_ERR_PIPE_TIMEOUT)) {
@@ -534,20 +525,17 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         __syncwarp();
         if (*abort_flag) break;
       }
-      const KvOut out{&tmD, D, a.N, &tmK, a.split.keys, &tmV, a.split.values,
-                      a.split.keys != nullptr ? a.split.keys_cols : 0};
       if (fused) {
-        fused_gate_epilogue(a.gf, out, a.M, tacc, q, lane, stg, a.msub, a.nsplit == 1 && a.msub == 1, a.acc_stride,
-                            a.BN, a.nsplit, m0, n0);
+        fused_gate_epilogue(a.gf, &tmD, D, a.M, a.N, tacc, q, lane, stg, a.msub, a.nsplit == 1 && a.msub == 1,
+                            a.acc_stride, a.BN, a.nsplit, m0, n0);
       } else if (a.nsplit == 2) {
         const int hb = a.BN >> 1;
-        store_tile(out, a.M, tacc, q, lane, stg, 1, false, a.acc_stride, hb, m0, n0);
-        store_tile(out, a.M, tacc + a.acc_stride, q, lane, stg, 1, false, a.acc_stride, hb, m0, n0 + hb);
-      } else if (adder) {                      // stream-K: the full layout only
-        store_accumulators(&tmD, D, a.M, a.N, tacc, q, lane, stg, a.msub, a.msub == 1, a.acc_stride, a.BN, m0, n0,
-                           true);
+        store_accumulators(&tmD, D, a.M, a.N, tacc, q, lane, stg, 1, false, a.acc_stride, hb, m0, n0, false);
+        store_accumulators(&tmD, D, a.M, a.N, tacc + a.acc_stride, q, lane, stg, 1, false, a.acc_stride, hb, m0,
+                           n0 + hb, false);
       } else {
-        store_tile(out, a.M, tacc, q, lane, stg, a.msub, a.msub == 1, a.acc_stride, a.BN, m0, n0);
+        store_accumulators(&tmD, D, a.M, a.N, tacc, q, lane, stg, a.msub, a.msub == 1, a.acc_stride, a.BN, m0, n0,
+                           adder);
       }
       // this item's stores are complete (global writes done) before the tile or flag moves on
       if (lane == 0) {
@@ -762,20 +750,6 @@ bool make_map_f32(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D bf16 map over the split layout's keys [rows, cols]; box = 32 x 32 with the 64B swizzle (the
-// epilogue's bf16 staging tiles)
-bool make_map_keys_bf16(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols) {
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kEpiChunk, 32};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // 2-D bf16 map over a row-major [rows, K] matrix; box = 64 k x box_rows rows, 128B swizzle
 bool make_map_bf16(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
@@ -850,12 +824,11 @@ int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl) {
   Plan P;
   const bool fused = p.gf.keys > 0;             // the gate's key sums need whole tiles: no stream-K
   const bool overlap = p.go.streams != nullptr;  // the gate waits for whole row blocks: no stream-K
-  const bool split = p.split.keys != nullptr;    // split output: data-parallel tiles only
   if (fused && overlap) {
     set_error("engram_project: the fused key sums and the overlapped gate exclude each other");
     return ENGRAM_EINVAL;
   }
-  if (!plan_gemm(p.M, p.K, p.N, num_sms(), p.workspace != nullptr ? p.ws_bytes : 0, P, !fused && !overlap && !split)) {
+  if (!plan_gemm(p.M, p.K, p.N, num_sms(), p.workspace != nullptr ? p.ws_bytes : 0, P, !fused && !overlap)) {
     set_error("engram_project: no tile plan fits (T %lld, K %d, N %d)", (long long)p.M, p.K, p.N);
     return ENGRAM_EINVAL;
   }
@@ -863,11 +836,6 @@ int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl) {
   a.err = p.err;
   a.gf = p.gf;
   a.go = p.go;
-  a.split = p.split;
-  if (split && (p.split.keys_cols % 16 != 0 || p.split.keys_cols <= 0 || p.split.keys_cols >= p.N)) {
-    set_error("engram_project: split output needs a key width that is a multiple of 16 inside N");
-    return ENGRAM_EINVAL;
-  }
   if (overlap && (p.go.done == nullptr || p.go.H % 4 != 0 || p.go.H > 4 * kGateThreads * kGateVec)) {
     set_error("engram_project: overlapped gate needs its row-block counters and H <= %d", 4 * kGateThreads * kGateVec);
     return ENGRAM_EINVAL;
@@ -891,25 +859,15 @@ int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl) {
     return cudaSuccess;
   });
   if (ae != cudaSuccess) return fail_cuda(ae, "engram_project: cudaFuncSetAttribute");
-  CUtensorMap mA, mB, mD, mK, mV;
-  bool maps = make_map_bf16(&mA, p.A, p.M, p.K, (uint32_t)a.a_rows) &&
-              make_map_bf16(&mB, p.B, p.N, p.K, (uint32_t)(a.BN / a.nsplit));
-  if (split) {       // the value map stands in for the unused full map
-    maps = maps && make_map_keys_bf16(&mK, p.split.keys, p.M, p.split.keys_cols) &&
-           make_map_f32(&mV, p.split.values, p.M, p.N - p.split.keys_cols) &&
-           make_map_f32(&mD, p.split.values, p.M, p.N - p.split.keys_cols);
-  } else {
-    maps = maps && make_map_f32(&mD, p.D, p.M, p.N);
-    mK = mD;
-    mV = mD;
-  }
-  if (!maps) {
+  CUtensorMap mA, mB, mD;
+  if (!make_map_bf16(&mA, p.A, p.M, p.K, (uint32_t)a.a_rows) || !make_map_bf16(&mB, p.B, p.N, p.K, (uint32_t)(a.BN / a.nsplit)) ||
+      !make_map_f32(&mD, p.D, p.M, p.N)) {
     set_error("engram_project: cuTensorMapEncodeTiled failed (driver entry point missing or bad layout)");
     return ENGRAM_ECUDA;
   }
   auto kernel = fused ? wkv_gemm_kernel<true, false> : overlap ? wkv_gemm_kernel<false, true> : wkv_gemm_kernel<false, false>;
   cudaError_t e = launch_k(kernel, dim3((unsigned)P.grid), dim3(overlap ? kThreadsOverlap : kThreads), (size_t)P.smem,
-                           stream, pdl, mA, mB, mD, mK, mV, p.D, a);
+                           stream, pdl, mA, mB, mD, p.D, a);
   if (e != cudaSuccess) return fail_cuda(e, "engram_project: launch");
   return ENGRAM_OK;
 }

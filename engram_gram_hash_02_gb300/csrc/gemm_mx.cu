@@ -70,7 +70,6 @@ struct MxArgs {
   const uint32_t* sfb;                       // [N, K/128]
   int32_t* err;
   GateFuse gf;                               // gf.keys > 0: the gate's key sums instead of the keys
-  KvSplit split;                             // split.keys != NULL: bf16 keys + fp32 value, not kv fp32
   // operand gather (gather warps): the token tile's FP8 rows straight from the table
   const int32_t* ids;                        // ids of token m at ids + m * ids_stride, one per column
   int64_t ids_stride;
@@ -126,8 +125,7 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* v) {
 template <bool kFused, bool kGatherA>
 __global__ void __launch_bounds__(kGatherA ? kThreadsGather : kThreads, 1)
 wkv_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, float* __restrict__ D, const MxArgs a) {
+                   const __grid_constant__ CUtensorMap tmD, float* __restrict__ D, const MxArgs a) {
   if (a.err != nullptr && (*reinterpret_cast<volatile int32_t*>(a.err) & ENGRAM_ERR_PIPE_TIMEOUT)) {
     pdl_wait();
     return;
@@ -311,13 +309,12 @@ wkv_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
       if (!ok || *abort_flag) break;
       int m0, n0;
       mx_tile_origin(a, tile, m0, n0);
-      const KvOut out{&tmD, D, a.N, &tmK, a.split.keys, &tmV, a.split.values,
-                      a.split.keys != nullptr ? a.split.keys_cols : 0};
       if (fused)
-        fused_gate_epilogue(a.gf, out, a.M, tmem, q, lane, stg, a.msub, a.msub == 1 && a.chains == 2, a.acc_stride,
-                            a.BN, 1, m0, n0);
+        fused_gate_epilogue(a.gf, &tmD, D, a.M, a.N, tmem, q, lane, stg, a.msub, a.msub == 1 && a.chains == 2,
+                            a.acc_stride, a.BN, 1, m0, n0);
       else
-        store_tile(out, a.M, tmem, q, lane, stg, a.msub, a.msub == 1 && a.chains == 2, a.acc_stride, a.BN, m0, n0);
+        store_accumulators(&tmD, D, a.M, a.N, tmem, q, lane, stg, a.msub, a.msub == 1 && a.chains == 2,
+                           a.acc_stride, a.BN, m0, n0, false);
       if (lane == 0) {
         asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // staging tile reusable
       }
@@ -572,12 +569,6 @@ int launch_gemm_mx(const GemmMxParams& p, cudaStream_t stream, bool pdl) {
   MxArgs a = P.a;
   a.err = p.err;
   a.gf = p.gf;
-  a.split = p.split;
-  const bool split = p.split.keys != nullptr;
-  if (split && (p.split.keys_cols % 16 != 0 || p.split.keys_cols <= 0 || p.split.keys_cols >= p.N)) {
-    set_error("engram_project_mxfp8: split output needs a key width that is a multiple of 16 inside N");
-    return ENGRAM_EINVAL;
-  }
   const bool gather = p.ids != nullptr;
   if (gather) {
     if (p.D < 128 || p.D % 128 != 0 || p.table == nullptr) {
@@ -607,28 +598,18 @@ int launch_gemm_mx(const GemmMxParams& p, cudaStream_t stream, bool pdl) {
     return cudaSuccess;
   });
   if (ae != cudaSuccess) return fail_cuda(ae, "engram_project_mxfp8: cudaFuncSetAttribute");
-  CUtensorMap mA, mB, mD, mK, mV;
+  CUtensorMap mA, mB, mD;
   // (with the operand gather the A map is not used; it is made over the table so that it is valid)
   const bool map_a = gather ? make_map_u8(&mA, p.table, p.table_rows, p.D, 1)
                             : make_map_u8(&mA, p.A, p.M, p.K, (uint32_t)a.a_rows);
-  bool maps = map_a && make_map_u8(&mB, p.B, p.N, p.K, (uint32_t)a.BN);
-  if (split) {       // the value map stands in for the unused full map
-    maps = maps && make_map_keys_bf16(&mK, p.split.keys, p.M, p.split.keys_cols) &&
-           make_map_f32(&mV, p.split.values, p.M, p.N - p.split.keys_cols) &&
-           make_map_f32(&mD, p.split.values, p.M, p.N - p.split.keys_cols);
-  } else {
-    maps = maps && make_map_f32(&mD, p.Dout, p.M, p.N);
-    mK = mD;
-    mV = mD;
-  }
-  if (!maps) {
+  if (!map_a || !make_map_u8(&mB, p.B, p.N, p.K, (uint32_t)a.BN) || !make_map_f32(&mD, p.Dout, p.M, p.N)) {
     set_error("engram_project_mxfp8: cuTensorMapEncodeTiled failed (driver entry point missing or bad layout)");
     return ENGRAM_ECUDA;
   }
   auto kernel = a.gf.keys > 0 ? (gather ? wkv_gemm_mx_kernel<true, true> : wkv_gemm_mx_kernel<true, false>)
                                : (gather ? wkv_gemm_mx_kernel<false, true> : wkv_gemm_mx_kernel<false, false>);
   cudaError_t e = launch_k(kernel, dim3((unsigned)P.grid), dim3(gather ? kThreadsGather : kThreads), (size_t)P.smem,
-                           stream, pdl, mA, mB, mD, mK, mV, p.Dout, a);
+                           stream, pdl, mA, mB, mD, p.Dout, a);
   if (e != cudaSuccess) return fail_cuda(e, "engram_project_mxfp8: launch");
   return ENGRAM_OK;
 }

@@ -161,8 +161,6 @@ struct GateFuse {
   int32_t H, hc;
   int32_t keys;              // hc * H: the key columns (0: the fusion is off)
   int32_t tile_cols;         // columns per partial slot: the tile width (set by the projection's plan)
-  float* part;               // partial slots of token t at part + t * part_stride (4 floats a tile)
-  int64_t part_stride;
 };
 
 // The gate run by extra warps of the projection kernel, overlapped with its tensor-core work: the
@@ -178,14 +176,6 @@ struct GateOverlap {
   uint32_t* done;            // [ceil(M / 128)]
 };
 
-// The projection's output in engram_forward's split layout: the keys in bf16 [M, keys_cols], the
-// value in fp32 [M, N - keys_cols] (the full layout is kv fp32 [M, N]).
-struct KvSplit {
-  uint16_t* keys;            // NULL: the full layout
-  float* values;
-  int32_t keys_cols;         // hc * H
-};
-
 struct GemmParams {
   const uint16_t* A;
   const uint16_t* B;
@@ -197,7 +187,6 @@ struct GemmParams {
   size_t ws_bytes;
   GateFuse gf;          // gf.keys > 0: gate partials instead of the key columns (data-parallel only)
   GateOverlap go;       // go.streams != NULL: the gate inside the projection (data-parallel only)
-  KvSplit split;        // split.keys != NULL: bf16 keys and fp32 value instead of kv fp32 (D unused)
 };
 // returns ENGRAM_OK or an error code (sets the message)
 int launch_gemm(const GemmParams& p, cudaStream_t stream, bool pdl = false);
@@ -243,7 +232,6 @@ struct GemmMxParams {
   int32_t K, N;
   int32_t* err;
   GateFuse gf;                // as GemmParams::gf
-  KvSplit split;              // as GemmParams::split
   // operand gather (ids != NULL): A row m is the concatenation of table rows ids[m * ids_stride + c],
   // c = 0 .. K/D - 1, read from the table by the projection itself (SA still holds their scales)
   const int32_t* ids;
@@ -259,11 +247,7 @@ int gemm_tile_cols(int64_t M, int K, int N, bool mx);
 
 struct GateParams {
   float* streams;
-  const void* keys;           // key of (t, j) at keys + t * key_stride + j * H elements (fp32 or bf16)
-  int64_t key_stride;
-  int32_t key_bf16;           // 1: bf16 keys (engram_forward's split layout), 0: fp32
-  const float* values;        // value of token t at values + t * value_stride
-  int64_t value_stride;
+  const float* kv;
   const uint16_t* q_weight;
   const uint16_t* k_weight;
   const uint8_t* token_mask;
@@ -272,9 +256,7 @@ struct GateParams {
   float eps, clamp;
   int32_t* err;
   int32_t part_cols;          // > 0: the projection fused the gate's key sums (GateFuse, tile width
-                              // part_cols): no keys, the partial slots of token t at part + t * part_stride
-  const float* part;
-  int64_t part_stride;
+                              // part_cols): the key columns of kv hold per-tile partials
 };
 cudaError_t launch_gate(const GateParams& p, cudaStream_t stream, bool pdl = false);
 cudaError_t launch_gate_persistent(const GateParams& p, cudaStream_t stream, bool pdl = false);

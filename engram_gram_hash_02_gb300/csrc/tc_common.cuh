@@ -13,7 +13,6 @@ namespace engram {
 bool make_map_bf16(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, uint32_t box_rows);
 bool make_map_u8(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, uint32_t box_rows);
 bool make_map_f32(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols);
-bool make_map_keys_bf16(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols);
 
 namespace {
 
@@ -211,123 +210,6 @@ __device__ __forceinline__ void store_accumulators(const CUtensorMap* tmD, float
   }
 }
 
-// ---- the split output layout (engram_forward): bf16 keys, fp32 value ------------------------------
-// The projection's output destinations: the full layout (kv fp32 [M, N] through tmD) or the split
-// layout (keys bf16 [M, keys] through tmK, value fp32 [M, N - keys] through tmV).
-struct KvOut {
-  const CUtensorMap* tmD;
-  float* D;
-  int N;
-  const CUtensorMap* tmK;
-  uint16_t* K;
-  const CUtensorMap* tmV;
-  float* V;
-  int keys;                                  // split layout: the key columns; 0: the full layout
-};
-
-__device__ __forceinline__ uint32_t pack_bf16x2_rn(uint32_t lo, uint32_t hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));   // round to nearest even
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// store_accumulators for the split layout. A 32-column chunk of keys is rounded to bf16 and stored
-// with TMA from a 32 x 64-byte staging tile in the 64B-swizzled order (16-byte piece i of row r at
-// piece i ^ ((r / 2) % 4): conflict-free); a 32-column chunk of the value as fp32 with TMA, as in
-// store_accumulators; 16-column pieces (a tail, or a chunk across the key/value boundary) are
-// stored by the threads. Columns before c_begin (a multiple of 16) are not stored.
-__device__ __forceinline__ void store_accumulators_split(const KvOut& o, int64_t M, uint32_t tmem, int q, int lane,
-                                                         uint32_t stg, int msub, bool sum_chains, uint32_t acc_stride,
-                                                         int BN, int m0, int n0, int c_begin) {
-  const int vcols = o.N - o.keys;
-  for (int ms = 0; ms < msub; ++ms) {
-    const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ms * acc_stride);
-    const int row0 = ms * 128 + q * 32;      // first row of this warp (within the item)
-    const int64_t row = (int64_t)m0 + row0 + lane;
-    for (int c0 = c_begin; c0 < BN; c0 += kEpiChunk) {
-      const int x = n0 + c0;
-      const bool two = c0 + 16 < BN;         // BN is a multiple of 16
-      uint32_t r[32];
-      tmem_ld16(tbase + c0, &r[0]);
-      if (two) tmem_ld16(tbase + c0 + 16, &r[16]);
-      if (sum_chains) {
-        uint32_t r2[32];
-        tmem_ld16(tbase + acc_stride + c0, &r2[0]);
-        if (two) tmem_ld16(tbase + acc_stride + c0 + 16, &r2[16]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
-      } else {
-        tmem_ld_wait();
-      }
-      const bool keys32 = two && x + 32 <= o.keys;
-      const bool vals32 = two && x >= o.keys;
-      if (keys32 || vals32) {
-        // the previous TMA store from this staging tile has read it
-        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-        __syncwarp();
-        if (keys32) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t addr = stg + (uint32_t)(lane * 64 + ((i ^ ((lane >> 1) & 3)) * 16));
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                         "r"(pack_bf16x2_rn(r[8 * i], r[8 * i + 1])), "r"(pack_bf16x2_rn(r[8 * i + 2], r[8 * i + 3])),
-                         "r"(pack_bf16x2_rn(r[8 * i + 4], r[8 * i + 5])), "r"(pack_bf16x2_rn(r[8 * i + 6], r[8 * i + 7]))
-                         : "memory");
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint32_t addr = stg + (uint32_t)(lane * 128 + ((i ^ (lane & 7)) * 16));
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r[4 * i]), "r"(r[4 * i + 1]),
-                         "r"(r[4 * i + 2]), "r"(r[4 * i + 3])
-                         : "memory");
-          }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the TMA unit
-        __syncwarp();
-        if (lane == 0) {
-          const uint64_t map = reinterpret_cast<uint64_t>(keys32 ? o.tmK : o.tmV);
-          const int cx = keys32 ? x : x - o.keys;
-          asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map),
-                       "r"(cx), "r"(m0 + row0), "r"(stg)
-                       : "memory");
-          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        }
-        continue;
-      }
-      // 16-column pieces: this thread's row by plain stores
-      for (int h = 0; h < (two ? 32 : 16); h += 16) {
-        const int xx = x + h;
-        if (row >= M || xx >= o.N) continue;
-        if (xx < o.keys) {
-          uint4* dst = reinterpret_cast<uint4*>(o.K + row * o.keys + xx);
-          dst[0] = make_uint4(pack_bf16x2_rn(r[h + 0], r[h + 1]), pack_bf16x2_rn(r[h + 2], r[h + 3]),
-                              pack_bf16x2_rn(r[h + 4], r[h + 5]), pack_bf16x2_rn(r[h + 6], r[h + 7]));
-          dst[1] = make_uint4(pack_bf16x2_rn(r[h + 8], r[h + 9]), pack_bf16x2_rn(r[h + 10], r[h + 11]),
-                              pack_bf16x2_rn(r[h + 12], r[h + 13]), pack_bf16x2_rn(r[h + 14], r[h + 15]));
-        } else {
-          float4* dst = reinterpret_cast<float4*>(o.V + row * vcols + (xx - o.keys));
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_float4(__uint_as_float(r[h + 4 * i]), __uint_as_float(r[h + 4 * i + 1]),
-                                 __uint_as_float(r[h + 4 * i + 2]), __uint_as_float(r[h + 4 * i + 3]));
-        }
-      }
-    }
-  }
-}
-
-// One tile's store in either layout (full: store_accumulators).
-__device__ __forceinline__ void store_tile(const KvOut& o, int64_t M, uint32_t tmem, int q, int lane, uint32_t stg,
-                                           int msub, bool sum_chains, uint32_t acc_stride, int BN, int m0, int n0,
-                                           int c_begin = 0) {
-  if (o.keys > 0)
-    store_accumulators_split(o, M, tmem, q, lane, stg, msub, sum_chains, acc_stride, BN, m0, n0, c_begin);
-  else
-    store_accumulators(o.tmD, o.D, M, o.N, tmem, q, lane, stg, msub, sum_chains, acc_stride, BN, m0, n0, false,
-                       c_begin);
-}
-
 // ---- the gate fused into the projection's epilogue ----------------------------------------------
 // With the fusion on, the key columns [0, hc*H) of kv are never stored. For every token row of a
 // tile, the epilogue thread that drains the row accumulates the two sums the gate needs from the
@@ -458,9 +340,10 @@ __device__ __forceinline__ void gate_prefetch_rows(const GateFuse& gf, int64_t M
 // The epilogue of one tile with the gate fused: partials of the key columns, store of the value
 // columns. Arguments as store_accumulators; `nsplit` 2 (two column halves of BN/2 in the two
 // accumulators) or 1. BN is the tile width.
-__device__ __forceinline__ void fused_gate_epilogue(const GateFuse& gf, const KvOut& o, int64_t M, uint32_t tmem,
-                                                    int q, int lane, uint32_t stg, int msub, bool sum_chains,
-                                                    uint32_t acc_stride, int BN, int nsplit, int m0, int n0) {
+__device__ __forceinline__ void fused_gate_epilogue(const GateFuse& gf, const CUtensorMap* tmD, float* D, int64_t M,
+                                                    int N, uint32_t tmem, int q, int lane, uint32_t stg, int msub,
+                                                    bool sum_chains, uint32_t acc_stride, int BN, int nsplit, int m0,
+                                                    int n0) {
   const int tile_n = n0 / gf.tile_cols;
   const int j0 = n0 / gf.H;                  // the first stream the tile covers
   if (n0 < gf.keys) {
@@ -477,19 +360,19 @@ __device__ __forceinline__ void fused_gate_epilogue(const GateFuse& gf, const Kv
         gate_partials_region(gf, tbase, sum_chains, acc_stride, BN, n0, j0, row, row_ok, P);
       }
       if (row_ok)
-        *reinterpret_cast<float4*>(gf.part + row * gf.part_stride + 4 * tile_n) =
-            make_float4(P.ssk[0], P.dot[0], P.ssk[1], P.dot[1]);
+        *reinterpret_cast<float4*>(D + row * N + 4 * tile_n) = make_float4(P.ssk[0], P.dot[0], P.ssk[1], P.dot[1]);
     }
   }
   if (n0 + BN > gf.keys) {                   // value columns of this tile: stored as they are
     const int c_begin = n0 < gf.keys ? gf.keys - n0 : 0;
     if (nsplit == 2) {
       const int hb = BN >> 1;
-      if (c_begin < hb) store_tile(o, M, tmem, q, lane, stg, 1, false, acc_stride, hb, m0, n0, c_begin);
-      store_tile(o, M, tmem + acc_stride, q, lane, stg, 1, false, acc_stride, hb, m0, n0 + hb,
-                 c_begin > hb ? c_begin - hb : 0);
+      if (c_begin < hb)
+        store_accumulators(tmD, D, M, N, tmem, q, lane, stg, 1, false, acc_stride, hb, m0, n0, false, c_begin);
+      store_accumulators(tmD, D, M, N, tmem + acc_stride, q, lane, stg, 1, false, acc_stride, hb, m0, n0 + hb, false,
+                         c_begin > hb ? c_begin - hb : 0);
     } else {
-      store_tile(o, M, tmem, q, lane, stg, msub, sum_chains, acc_stride, BN, m0, n0, c_begin);
+      store_accumulators(tmD, D, M, N, tmem, q, lane, stg, msub, sum_chains, acc_stride, BN, m0, n0, false, c_begin);
     }
   }
 }

@@ -32,7 +32,7 @@ def _forward(w, case, setup, mode, mx=False, tile=0):
     E().set_gate_fusion(mode)
     (E().set_gemm_mx_tile if mx else E().set_gemm_tile)(tile)
     try:
-        return H.gpu_forward(w, case, setup, mx=mx, full_kv=(mode == 1))
+        return H.gpu_forward(w, case, setup, mx=mx)
     finally:
         E().set_gate_fusion(0)
         E().set_gemm_tile(0)

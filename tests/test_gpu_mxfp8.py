@@ -144,7 +144,7 @@ def test_forward_mxfp8_matches_oracle(name, sample):
     last = ref["layers"][-1]
     assert np.array_equal(got["A_codes_last"].index_select(0, sel_t).cpu().numpy(), last["a_bits"][0])
     assert np.array_equal(got["A_scales_last"][sel], last["a_bits"][1])
-    H.check_kv(got["kv_last"].index_select(0, sel_t).cpu().numpy(), last["kv"], f"{name} mx kv", got["kv_bf16_cols"])
+    H.check_kv(got["kv_last"].index_select(0, sel_t).cpu().numpy(), last["kv"], f"{name} mx kv")
     for l, lref in enumerate(ref["layers"]):
         h = got["streams"][l].index_select(0, sel_t).cpu().numpy()
         H.check_streams(h, lref["streams"], lref["streams_in"], f"{name} mx layer {l}")

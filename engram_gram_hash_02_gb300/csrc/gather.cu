@@ -49,7 +49,19 @@ __device__ __forceinline__ void flag(int32_t* err, int32_t bit) {
   if (err != nullptr) atomicOr(err, bit);
 }
 
+// Flat chunk index i -> (row r = t * C + col, chunk j), in I: uint32_t when every index of the
+// launch fits in 31 bits (one short integer division each instead of a 64-bit one), else int64_t.
+template <typename I>
+__device__ __forceinline__ void split_chunk(int64_t i, int chunks_per_row, int C, I& t, int& col, int& j) {
+  const I ii = (I)i;
+  const I r = ii / (I)chunks_per_row;
+  j = (int)(ii - r * (I)chunks_per_row);
+  t = r / (I)C;
+  col = (int)(r - t * (I)C);
+}
+
 // ---- FP8-E4M3 + E8M0 ------------------------------------------------------------------
+template <typename I>
 __global__ void __launch_bounds__(kThreads)
 gather_fp8_kernel(const GatherLayers m) {
   const GatherParams& p = m.l[blockIdx.y];
@@ -73,11 +85,10 @@ gather_fp8_kernel(const GatherLayers m) {
       v[u] = make_uint4(0, 0, 0, 0);
       sb[u] = 0;
       if (i < total) {
-        const int64_t r = i / chunks_per_row;
-        const int j = (int)(i - r * chunks_per_row);
-        const int64_t t = r / p.C;
-        const int col = (int)(r - t * p.C);
-        const int64_t id = __ldg(p.ids + t * p.ids_stride_t + col);
+        I t;
+        int col, j;
+        split_chunk<I>(i, chunks_per_row, p.C, t, col, j);
+        const int64_t id = __ldg(p.ids + (int64_t)t * p.ids_stride_t + col);
         if (id >= 0 && id < p.num_rows) {
           ok[u] = true;
           v[u] = ld_stream_v4(weight + id * p.D + (j << 4));
@@ -111,6 +122,7 @@ gather_fp8_kernel(const GatherLayers m) {
 }
 
 // ---- bf16 rows: copy ----------------------------------------------------------------------
+template <typename I>
 __global__ void __launch_bounds__(kThreads)
 gather_bf16_kernel(const GatherLayers m) {
   const GatherParams& p = m.l[blockIdx.y];
@@ -128,11 +140,10 @@ gather_bf16_kernel(const GatherLayers m) {
       const int64_t i = base + u * stride;
       v[u] = make_uint4(0, 0, 0, 0);
       if (i < total) {
-        const int64_t r = i / chunks_per_row;
-        const int j = (int)(i - r * chunks_per_row);
-        const int64_t t = r / p.C;
-        const int col = (int)(r - t * p.C);
-        const int64_t id = __ldg(p.ids + t * p.ids_stride_t + col);
+        I t;
+        int col, j;
+        split_chunk<I>(i, chunks_per_row, p.C, t, col, j);
+        const int64_t id = __ldg(p.ids + (int64_t)t * p.ids_stride_t + col);
         if (id >= 0 && id < p.num_rows) {
           v[u] = ld_stream_v4(table + id * p.D + (j << 3));
         } else if (j == 0) {
@@ -152,6 +163,7 @@ gather_bf16_kernel(const GatherLayers m) {
 // Element e: sub-block b = e/16 (scale = low nibble, min = high nibble of byte b),
 // quant = (qs[32*(e/128) + e%32] >> 2*((e%128)/32)) & 3, then d*scale*q - dmin*min.
 // Lane L writes elements 8L..8L+7: half = L/16, bit pair j = (L/4)%4, l0 = 8*(L%4), b = L/2.
+template <typename I>
 __global__ void __launch_bounds__(kThreads)
 gather_q2k_kernel(const GatherLayers m) {
   const GatherParams& p = m.l[blockIdx.y];
@@ -178,9 +190,9 @@ gather_q2k_kernel(const GatherLayers m) {
       ok[u] = false;
       word[u] = 0;
       if (r < rows) {
-        const int64_t t = r / p.C;
-        const int col = (int)(r - t * p.C);
-        const int64_t id = __ldg(p.ids + t * p.ids_stride_t + col);
+        const I t = (I)r / (I)p.C;
+        const int col = (int)((I)r - t * (I)p.C);
+        const int64_t id = __ldg(p.ids + (int64_t)t * p.ids_stride_t + col);
         ok[u] = id >= 0 && id < p.num_rows;
         if (ok[u] && lane < 21) word[u] = __ldg(table + id * 21 + lane);
         if (!ok[u] && lane == 0) flag(p.err, ENGRAM_ERR_ROW_ID);
@@ -312,16 +324,22 @@ cudaError_t launch_gather(const GatherLayers& m, cudaStream_t stream, bool pdl) 
   if (m.n < 1 || m.n > kMaxGatherLayers) return cudaErrorInvalidValue;
   const GatherParams& p = m.l[0];                // every layer has p's format, T, C and D
   const int64_t rows = p.T * p.C;
+  // flat indices below 2^31 (with a stride's overshoot): 32-bit index arithmetic
+  const int64_t span = rows * (p.D / 8) + 2 * (int64_t)num_sms() * 64 * kThreads * kChunksPerThread;
+  const bool narrow = span < ((int64_t)1 << 31);
   switch (p.fmt) {
     case ENGRAM_TABLE_FP8_E8M0:
-      return launch_k(gather_fp8_kernel, dim3(grid_for(rows * (p.D / 16), kThreads * kChunksPerThread), m.n),
-                      dim3(kThreads), 0, stream, pdl, m);
+      return launch_k(narrow ? gather_fp8_kernel<uint32_t> : gather_fp8_kernel<int64_t>,
+                      dim3(grid_for(rows * (p.D / 16), kThreads * kChunksPerThread), m.n), dim3(kThreads), 0, stream,
+                      pdl, m);
     case ENGRAM_TABLE_BF16:
-      return launch_k(gather_bf16_kernel, dim3(grid_for(rows * (p.D / 8), kThreads * kChunksPerThread), m.n),
-                      dim3(kThreads), 0, stream, pdl, m);
+      return launch_k(narrow ? gather_bf16_kernel<uint32_t> : gather_bf16_kernel<int64_t>,
+                      dim3(grid_for(rows * (p.D / 8), kThreads * kChunksPerThread), m.n), dim3(kThreads), 0, stream,
+                      pdl, m);
     case ENGRAM_TABLE_Q2K:
-      return launch_k(gather_q2k_kernel, dim3(grid_for(rows, (kThreads / 32) * kQ2kRowsPerWarp), m.n),
-                      dim3(kThreads), 0, stream, pdl, m);
+      return launch_k(narrow ? gather_q2k_kernel<uint32_t> : gather_q2k_kernel<int64_t>,
+                      dim3(grid_for(rows, (kThreads / 32) * kQ2kRowsPerWarp), m.n), dim3(kThreads), 0, stream, pdl,
+                      m);
     default:
       return cudaErrorInvalidValue;
   }

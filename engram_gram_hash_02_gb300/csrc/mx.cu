@@ -71,6 +71,7 @@ quantize_mxfp8_kernel(const uint16_t* __restrict__ w, int64_t N, int32_t K, uint
 // FP8 rows by id, copied without dequantisation: 16 threads per 256-byte row (16-byte chunks);
 // the chunk-0 thread also copies the row's scale bytes. Rows outside the table: codes 0, scale
 // byte 127 (a zero row).
+template <typename I>
 __global__ void __launch_bounds__(kThreads)
 gather_fp8_codes_kernel(const GatherCodesLayers m) {
   const GatherCodesParams& p = m.l[blockIdx.y];
@@ -82,10 +83,13 @@ gather_fp8_codes_kernel(const GatherCodesLayers m) {
   const int64_t rows4 = (p.T + 3) & ~(int64_t)3;
   const uint8_t* __restrict__ weight = static_cast<const uint8_t*>(p.table);
   for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < total; i += (int64_t)gridDim.x * kThreads) {
-    const int64_t r = i / chunks_per_row;
-    const int j = (int)(i - r * chunks_per_row);
-    const int64_t t = r / p.C;
-    const int col = (int)(r - t * p.C);
+    // index split in I: uint32_t when the launch's indices fit in 31 bits, else int64_t
+    const I ii = (I)i;
+    const I r = ii / (I)chunks_per_row;
+    const int j = (int)(ii - r * (I)chunks_per_row);
+    const I tt = r / (I)p.C;
+    const int64_t t = (int64_t)tt;
+    const int col = (int)(r - tt * (I)p.C);
     const int64_t id = __ldg(p.ids + t * p.ids_stride_t + col);
     const bool ok = id >= 0 && id < p.num_rows;
     if (!ok && j == 0 && p.err != nullptr) atomicOr(p.err, ENGRAM_ERR_ROW_ID);
@@ -124,7 +128,9 @@ cudaError_t launch_gather_codes(const GatherCodesLayers& m, cudaStream_t stream,
   const int64_t cap = (int64_t)num_sms() * 32;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  return launch_k(gather_fp8_codes_kernel, dim3((unsigned)blocks, (unsigned)m.n), dim3(kThreads), 0, stream, pdl, m);
+  const bool narrow = total + blocks * kThreads < ((int64_t)1 << 31);
+  return launch_k(narrow ? gather_fp8_codes_kernel<uint32_t> : gather_fp8_codes_kernel<int64_t>,
+                  dim3((unsigned)blocks, (unsigned)m.n), dim3(kThreads), 0, stream, pdl, m);
 }
 
 }  // namespace engram

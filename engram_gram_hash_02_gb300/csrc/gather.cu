@@ -12,6 +12,8 @@
 // the quants, scale nibbles and d/dmin of its 8 outputs.
 #include <cuda_fp8.h>
 
+#include <type_traits>
+
 #include "hash_token.cuh"
 
 namespace engram {
@@ -50,7 +52,9 @@ __device__ __forceinline__ void flag(int32_t* err, int32_t bit) {
 }
 
 // Flat chunk index i -> (row r = t * C + col, chunk j), in I: uint32_t when every index of the
-// launch fits in 31 bits (one short integer division each instead of a 64-bit one), else int64_t.
+// launch fits in 31 bits (a 32-bit division by a loop-invariant divisor, whose reciprocal the
+// compiler keeps out of the loop), else int64_t. (The multiply-and-shift of fastdiv.h measured
+// slower here at large T, though faster in the Q2_K and code gathers, which use it.)
 template <typename I>
 __device__ __forceinline__ void split_chunk(int64_t i, int chunks_per_row, int C, I& t, int& col, int& j) {
   const I ii = (I)i;
@@ -190,7 +194,9 @@ gather_q2k_kernel(const GatherLayers m) {
       ok[u] = false;
       word[u] = 0;
       if (r < rows) {
-        const I t = (I)r / (I)p.C;
+        I t;
+        if constexpr (std::is_same<I, uint32_t>::value) t = fast_div((uint32_t)r, m.div_c);
+        else t = r / p.C;
         const int col = (int)((I)r - t * (I)p.C);
         const int64_t id = __ldg(p.ids + (int64_t)t * p.ids_stride_t + col);
         ok[u] = id >= 0 && id < p.num_rows;
@@ -320,9 +326,12 @@ cudaError_t launch_hash_gather(const HashGatherParams& p, cudaStream_t stream, b
   return launch_k(hash_gather_fp8_kernel, dim3((unsigned)p.h.T), dim3(kHgThreads), 0, stream, pdl, p);
 }
 
-cudaError_t launch_gather(const GatherLayers& m, cudaStream_t stream, bool pdl) {
-  if (m.n < 1 || m.n > kMaxGatherLayers) return cudaErrorInvalidValue;
+cudaError_t launch_gather(const GatherLayers& layers, cudaStream_t stream, bool pdl) {
+  if (layers.n < 1 || layers.n > kMaxGatherLayers) return cudaErrorInvalidValue;
+  GatherLayers m = layers;
   const GatherParams& p = m.l[0];                // every layer has p's format, T, C and D
+  if (p.C < 1 || p.D < 16) return cudaErrorInvalidValue;
+  m.div_c = make_fastdiv((uint32_t)p.C);
   const int64_t rows = p.T * p.C;
   // flat indices below 2^31 (with a stride's overshoot): 32-bit index arithmetic
   const int64_t span = rows * (p.D / 8) + 2 * (int64_t)num_sms() * 64 * kThreads * kChunksPerThread;

@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "../../include/engram.h"
+#include "fastdiv.h"
 
 namespace engram {
 
@@ -139,10 +140,12 @@ struct GatherParams {
   uint16_t* out;
   int32_t* err;
 };
-// n layers of the same format, T, C and D in one launch (grid y = layer)
+// n layers of the same format, T, C and D in one launch (grid y = layer); the launcher fills the
+// division by C (the Q2_K gather's)
 struct GatherLayers {
   int32_t n;
   GatherParams l[kMaxGatherLayers];
+  FastDiv div_c;
 };
 cudaError_t launch_gather(const GatherLayers& p, cudaStream_t stream, bool pdl = false);
 inline cudaError_t launch_gather(const GatherParams& p, cudaStream_t stream, bool pdl = false) {
@@ -211,6 +214,7 @@ struct GatherCodesParams {
 struct GatherCodesLayers {
   int32_t n;
   GatherCodesParams l[kMaxGatherLayers];
+  FastDiv div_cpr, div_c;     // the divisions by the chunks per row and by C (filled by the launcher)
 };
 cudaError_t launch_gather_codes(const GatherCodesLayers& p, cudaStream_t stream, bool pdl = false);
 inline cudaError_t launch_gather_codes(const GatherCodesParams& p, cudaStream_t stream, bool pdl = false) {

@@ -14,6 +14,8 @@
 // Scale layout of both operands (the projection's own, so a stage's scales are one contiguous
 // run it can bulk-copy): 32-bit words [K/128][rows4], rows4 = rows rounded up to a multiple of 4;
 // word (kb, r) holds the bytes of row r's blocks 4kb .. 4kb+3, lowest byte first.
+#include <type_traits>
+
 #include "internal.cuh"
 
 namespace engram {
@@ -83,13 +85,23 @@ gather_fp8_codes_kernel(const GatherCodesLayers m) {
   const int64_t rows4 = (p.T + 3) & ~(int64_t)3;
   const uint8_t* __restrict__ weight = static_cast<const uint8_t*>(p.table);
   for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < total; i += (int64_t)gridDim.x * kThreads) {
-    // index split in I: uint32_t when the launch's indices fit in 31 bits, else int64_t
-    const I ii = (I)i;
-    const I r = ii / (I)chunks_per_row;
-    const int j = (int)(ii - r * (I)chunks_per_row);
-    const I tt = r / (I)p.C;
-    const int64_t t = (int64_t)tt;
-    const int col = (int)(r - tt * (I)p.C);
+    // index split: multiply-and-shift by the launch's constants when its indices fit in 31 bits
+    // (I = uint32_t), else int64_t divisions
+    int64_t t;
+    int j, col;
+    if constexpr (std::is_same<I, uint32_t>::value) {
+      const uint32_t ii = (uint32_t)i;
+      const uint32_t r = fast_div(ii, m.div_cpr);
+      j = (int)(ii - r * (uint32_t)chunks_per_row);
+      const uint32_t tt = fast_div(r, m.div_c);
+      t = tt;
+      col = (int)(r - tt * (uint32_t)p.C);
+    } else {
+      const int64_t r = i / chunks_per_row;
+      j = (int)(i - r * chunks_per_row);
+      t = r / p.C;
+      col = (int)(r - t * p.C);
+    }
     const int64_t id = __ldg(p.ids + t * p.ids_stride_t + col);
     const bool ok = id >= 0 && id < p.num_rows;
     if (!ok && j == 0 && p.err != nullptr) atomicOr(p.err, ENGRAM_ERR_ROW_ID);
@@ -120,9 +132,13 @@ cudaError_t launch_quantize_mxfp8(const uint16_t* w, int64_t N, int32_t K, uint8
                   scales);
 }
 
-cudaError_t launch_gather_codes(const GatherCodesLayers& m, cudaStream_t stream, bool pdl) {
-  if (m.n < 1 || m.n > kMaxGatherLayers) return cudaErrorInvalidValue;
+cudaError_t launch_gather_codes(const GatherCodesLayers& layers, cudaStream_t stream, bool pdl) {
+  if (layers.n < 1 || layers.n > kMaxGatherLayers) return cudaErrorInvalidValue;
+  GatherCodesLayers m = layers;
   const GatherCodesParams& p = m.l[0];           // every layer has p's T, C and D
+  if (p.C < 1 || p.D < 16) return cudaErrorInvalidValue;
+  m.div_cpr = make_fastdiv((uint32_t)(p.D >> 4));
+  m.div_c = make_fastdiv((uint32_t)p.C);
   const int64_t total = p.T * p.C * (p.D >> 4);
   int64_t blocks = (total + kThreads - 1) / kThreads;
   const int64_t cap = (int64_t)num_sms() * 32;

@@ -41,9 +41,9 @@ L2_FLUSH_READ_BYTES = 256 << 20
 # DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by kernel and
 # workload, with the sha256 of the kernel's source at capture time (stale -> traffic null).
 NCU_TRAFFIC: dict = {
-    "project0@large_fp8_t16384": {"bytes": 4940026368 + 2314579456, "src_sha": "63d915fbf837e181"},
-    "project0@decode_fp8_t256": {"bytes": 254901760 + 3296000, "src_sha": "ca4a50c28673842a"},
-    "project0@decode_fp8_t256@mxfp8": {"bytes": 131441408 + 3046400, "src_sha": "6b962bd1336136b1",
+    "project0@large_fp8_t16384": {"bytes": 4940148480 + 2313792256, "src_sha": "ac30053ebb5e5758"},
+    "project0@decode_fp8_t256": {"bytes": 254888448 + 3236608, "src_sha": "ac30053ebb5e5758"},
+    "project0@decode_fp8_t256@mxfp8": {"bytes": 131440384 + 3169024, "src_sha": "5e41d2dd6af5de4d",
                                        "src": "gemm_mx.cu"},
 }
 

@@ -72,6 +72,7 @@ def _check(w, case, got, ref_unfused, sample, mx, mode=1):
     ("decode_fp8_t256", (1,) * 112, False, 0, 0),      # a single short token tile
     ("decode_fp8_t256", (1,) * 129, False, 0, 0),      # a second row block of one token
     ("prefill_fp8_t32768", (700, 324), False, 0, 0),   # documents and masked tokens, 256-row tiles
+    ("prefill_fp8_t32768", (1500, 548), True, 0, 256),  # FP8 variant, several 256-row blocks
     ("q2k_t8192", (300,), False, 0, 0),
     ("tiny_fp8", None, False, 0, 0),                   # H 256 with 256-wide tiles: one stream each
 ])

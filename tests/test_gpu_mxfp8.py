@@ -87,7 +87,8 @@ def _words(sc_rows: torch.Tensor) -> torch.Tensor:
 
 @pytest.mark.parametrize("T,K,N,bn", [(200, 512, 1280, 0), (64, 1024, 2048, 0), (300, 2048, 3072, 0),
                                       (1, 6144, 35840, 0), (64, 6144, 35840, 0), (256, 6144, 20480, 0),
-                                      (129, 768, 400, 0), (256, 1024, 2048, 128), (100, 1024, 2048, 208)])
+                                      (129, 768, 400, 0), (256, 1024, 2048, 128), (100, 1024, 2048, 208),
+                                      (2200, 1024, 2048, 0)])     # several row blocks, a ragged last one
 def test_project_mxfp8_vs_oracle(T, K, N, bn):
     a, sa, b, sb = _random_mx(T, K, N, T + K + N)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)

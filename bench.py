@@ -242,7 +242,7 @@ class Path:
         return calls
 
 
-# MXFP8 dense tensor peak, measured on this part (the driver's peaks file has none): cuBLAS
+# MXFP8 dense tensor peak, measured on this part (MEASURED_PEAKS.json holds no FP8 figure): cuBLAS
 # through torch._scaled_mm, e4m3 x e4m3 with one E8M0 scale per 32 values, 8192^3, best of 10
 # (burst) and back to back for 4 s (sustained). The nominal fp8 / bf16 ratio (4.5 / 2.25) times the
 # measured bf16 peak would be 3847 TFLOP/s.

@@ -476,7 +476,6 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   } else {
     // ---------------- epilogue: TMEM -> registers -> shared tile -> fp32 kv --------------------
     const int q = warp & 3;                    // TMEM lane quarter this warp may access
-    const int et = threadIdx.x - 64;           // 0..127
     pdl_wait();                                // kv may still be read by an earlier kernel
     Schedule sch(a, blockIdx.x, gridDim.x);
     Item item;

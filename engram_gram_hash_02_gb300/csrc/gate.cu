@@ -287,19 +287,22 @@ gate_kernel(const GateParams p) {
 
 // ---- small-T form: one CTA per (token, stream) item --------------------------------------------
 // When there are too few items to keep a persistent grid busy (the decode step: 256 tokens x 4
-// streams over 148 SMs), each item gets a CTA of its own and every load goes straight to registers:
-// each thread holds kVec float4 chunks of h_j, key_j and the value (chunk c = tid + m * threads), all
-// requested before any is used (the stream row even before waiting for the projection). One block
-// barrier: the warps' partial sums meet in shared memory and every thread forms the gate from
-// them (the same arithmetic in every thread), then writes its chunks of h + g * v. No waits, so no
-// time limit is needed.
+// streams over 148 SMs), each item gets a CTA of its own. Each thread owns kVec float4 chunks of the
+// row (chunk c = tid + m * threads): its chunks of h_j are copied into shared memory with cp.async
+// before waiting for the projection (no registers held), its chunks of key_j and the value go to
+// registers, all requested before any is used. A thread reads back only the chunks it copied
+// itself, so the copies need no block barrier. One block barrier: the warps' partial sums meet in
+// shared memory and every thread forms the gate from them (the same arithmetic in every thread),
+// then writes its chunks of h + g * v. No waits on other threads' progress, so no time limit is
+// needed. Registers stay within four CTAs per SM up to 4 chunks a thread (H <= 4096).
 constexpr int kItemThreads = 256;
 
 template <int kVec, bool kFused>
-__global__ void __launch_bounds__(kItemThreads)
+__global__ void __launch_bounds__(kItemThreads, kVec <= 4 ? 4 : 1)
 gate_item_kernel(const GateParams p) {
   __shared__ float red[kItemThreads / 32][3];
   __shared__ float fused_sums[2];
+  __shared__ __align__(16) float4 xs[kVec * kItemThreads];   // this CTA's stream row h_j
   const int H = p.H, H4 = H >> 2;
   const int tid = threadIdx.x;
   const int64_t item = blockIdx.x;
@@ -315,17 +318,18 @@ gate_item_kernel(const GateParams p) {
   const float4* vrow = reinterpret_cast<const float4*>(p.kv + t * N + (int64_t)p.hc * H);
   const uint2* qrow = reinterpret_cast<const uint2*>(p.q_weight + (int64_t)j * H);
   const uint2* kwrow = reinterpret_cast<const uint2*>(p.k_weight + (int64_t)j * H);
-  float4 x[kVec], y[kVec], v[kVec];
+  float4 y[kVec], v[kVec];
   uint2 qr[kVec], kr[kVec];
 #pragma unroll
   for (int m = 0; m < kVec; ++m) {                 // not written by the projection: before the wait
     const int c = tid + m * kItemThreads;
     if (c < H4) {
-      x[m] = hrow[c];
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(&xs[c])), "l"(hrow + c) : "memory");
       qr[m] = __ldg(qrow + c);
       kr[m] = __ldg(kwrow + c);
     }
   }
+  asm volatile("cp.async.commit_group;" ::: "memory");
   pdl_wait();                                      // kv comes from the projection
   pdl_trigger();
 #pragma unroll
@@ -346,21 +350,23 @@ gate_item_kernel(const GateParams p) {
       fused_sums[1] = fd;
     }
   }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");   // this thread's chunks of h_j have landed
   float ssh = 0.f, ssk = 0.f, dot = 0.f;
 #pragma unroll
   for (int m = 0; m < kVec; ++m) {
     const int c = tid + m * kItemThreads;
     if (c < H4) {
-      ssh = fmaf(x[m].x, x[m].x, ssh); ssh = fmaf(x[m].y, x[m].y, ssh);
-      ssh = fmaf(x[m].z, x[m].z, ssh); ssh = fmaf(x[m].w, x[m].w, ssh);
-    }
-    if (!kFused && c < H4) {
-      ssk = fmaf(y[m].x, y[m].x, ssk); ssk = fmaf(y[m].y, y[m].y, ssk);
-      ssk = fmaf(y[m].z, y[m].z, ssk); ssk = fmaf(y[m].w, y[m].w, ssk);
-      dot = fmaf(x[m].x * bf16lo(qr[m].x), y[m].x * bf16lo(kr[m].x), dot);
-      dot = fmaf(x[m].y * bf16hi(qr[m].x), y[m].y * bf16hi(kr[m].x), dot);
-      dot = fmaf(x[m].z * bf16lo(qr[m].y), y[m].z * bf16lo(kr[m].y), dot);
-      dot = fmaf(x[m].w * bf16hi(qr[m].y), y[m].w * bf16hi(kr[m].y), dot);
+      const float4 x = xs[c];
+      ssh = fmaf(x.x, x.x, ssh); ssh = fmaf(x.y, x.y, ssh);
+      ssh = fmaf(x.z, x.z, ssh); ssh = fmaf(x.w, x.w, ssh);
+      if (!kFused) {
+        ssk = fmaf(y[m].x, y[m].x, ssk); ssk = fmaf(y[m].y, y[m].y, ssk);
+        ssk = fmaf(y[m].z, y[m].z, ssk); ssk = fmaf(y[m].w, y[m].w, ssk);
+        dot = fmaf(x.x * bf16lo(qr[m].x), y[m].x * bf16lo(kr[m].x), dot);
+        dot = fmaf(x.y * bf16hi(qr[m].x), y[m].y * bf16hi(kr[m].x), dot);
+        dot = fmaf(x.z * bf16lo(qr[m].y), y[m].z * bf16lo(kr[m].y), dot);
+        dot = fmaf(x.w * bf16hi(qr[m].y), y[m].w * bf16hi(kr[m].y), dot);
+      }
     }
   }
 #pragma unroll
@@ -394,9 +400,10 @@ gate_item_kernel(const GateParams p) {
 #pragma unroll
   for (int m = 0; m < kVec; ++m) {
     const int c = tid + m * kItemThreads;
-    if (c < H4)
-      hrow[c] = make_float4(fmaf(g, v[m].x, x[m].x), fmaf(g, v[m].y, x[m].y), fmaf(g, v[m].z, x[m].z),
-                            fmaf(g, v[m].w, x[m].w));
+    if (c < H4) {
+      const float4 x = xs[c];
+      hrow[c] = make_float4(fmaf(g, v[m].x, x.x), fmaf(g, v[m].y, x.y), fmaf(g, v[m].z, x.z), fmaf(g, v[m].w, x.w));
+    }
   }
 }
 

@@ -205,3 +205,67 @@ def test_forward2_q2k_matches_oracle():
         H.check_streams(h, lref["streams"], lref["streams_in"], f"q2k side stream layer {l}")
     del case
     torch.cuda.empty_cache()
+
+
+def _forward_plan(w, case, setup):
+    """An engram_forward plan over its own copies of the streams (and its own workspace)."""
+    import engram_gram_hash_02_gb300 as E
+    from engram_synth.case import to_device
+    primes, offsets, rows, mult = setup
+    b = case.batch
+    dims = H.dims_for(w, H.pad_id_of(w, b["token_map"]))
+    tables = E.HashTables(to_device(b["token_map"], "cuda"), to_device(mult, "cuda"), to_device(primes, "cuda"),
+                          to_device(offsets, "cuda"))
+    layers = [E.LayerWeights(t["fmt"], t["table"], t["scales"], t["num_rows"], case.wkv[l], case.q_weight[l],
+                             case.k_weight[l]) for l, t in enumerate(case.tables)]
+    streams = [s.clone() for s in case.streams]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    plan = E.ForwardPlan(dims, tables, layers, to_device(b["input_ids"], "cuda"), streams,
+                         cu_seqlens=to_device(b["cu_seqlens"], "cuda"),
+                         sequence_ids=to_device(b["sequence_ids"], "cuda"),
+                         token_mask=to_device(b["token_mask"], "cuda"),
+                         lookback_ids=to_device(b["lookback_ids"], "cuda"), err=err)
+    return plan, streams, err
+
+
+def test_forward2_from_two_host_threads():
+    """engram_forward2 called from two host threads at once, each with its own main and side
+    streams and its own buffers (ctypes releases the interpreter lock during the call, so the calls
+    overlap on the host): two Q2_K layers, so the second layer's rows are gathered on the side
+    stream and joined back by the library's events. After n in-place updates each thread's streams
+    equal those of n updates on one thread, bit for bit."""
+    import threading
+    w, case, setup = H.build("q2k_t8192", seq_lens=(300, 212))
+    n = 8
+    ref_plan, ref_streams, ref_err = _forward_plan(w, case, setup)
+    side = torch.cuda.Stream()
+    for _ in range(n):
+        ref_plan.run(side_stream=side)
+    torch.cuda.synchronize()
+    plans = [_forward_plan(w, case, setup) for _ in range(2)]
+    errors = []
+
+    def worker(i):
+        try:
+            plan = plans[i][0]
+            main, side_i = torch.cuda.Stream(), torch.cuda.Stream()
+            for _ in range(n):
+                plan.run(stream=main, side_stream=side_i)
+            main.synchronize()
+        except Exception as e:                                   # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=300)
+    torch.cuda.synchronize()
+    assert not errors, errors
+    assert int(ref_err.item()) == 0
+    for i, (_, streams, err) in enumerate(plans):
+        assert int(err.item()) == 0
+        for l in range(w.layers):
+            assert torch.equal(streams[l], ref_streams[l]), f"thread {i} layer {l}"
+    del case
+    torch.cuda.empty_cache()

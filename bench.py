@@ -41,9 +41,9 @@ L2_FLUSH_READ_BYTES = 256 << 20
 # DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by kernel and
 # workload, with the sha256 of the kernel's source at capture time (stale -> traffic null).
 NCU_TRAFFIC: dict = {
-    "project0@large_fp8_t16384": {"bytes": 4940208640 + 2314119168, "src_sha": "5a4addc94773dbcc"},
-    "project0@decode_fp8_t256": {"bytes": 254888704 + 3313408, "src_sha": "5a4addc94773dbcc"},
-    "project0@decode_fp8_t256@mxfp8": {"bytes": 131440384 + 3169024, "src_sha": "5e41d2dd6af5de4d",
+    "project0@large_fp8_t16384": {"bytes": 4938854656 + 2314286592, "src_sha": "00fef9d6c5ea4026"},
+    "project0@decode_fp8_t256": {"bytes": 254897920 + 3391232, "src_sha": "00fef9d6c5ea4026"},
+    "project0@decode_fp8_t256@mxfp8": {"bytes": 131441664 + 3283200, "src_sha": "eb50e0f2c991739b",
                                        "src": "gemm_mx.cu"},
 }
 

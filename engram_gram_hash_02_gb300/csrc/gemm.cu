@@ -536,12 +536,19 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         store_accumulators(&tmD, D, a.M, a.N, tacc, q, lane, stg, a.msub, a.msub == 1, a.acc_stride, a.BN, m0, n0,
                            adder);
       }
-      // this item's stores are complete (global writes done) before the tile or flag moves on
-      if (lane == 0) {
-        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-        asm volatile("fence.proxy.async.global;" ::: "memory");
+      // The accumulators are read (every tcgen05.ld of the item has completed): the set may take
+      // its next item now, while this item's stores are still in flight. (Waiting for the stores
+      // first kept the tensor cores idle for the whole drain of the tile to HBM.)
+      tc_fence_before();
+      mbar_arrive(smem_u32(&ctl->acc_empty[set]));
+      if (publish || kOverlap) {
+        // the stores are complete (global writes done) before a flag or a count says so
+        if (lane == 0) {
+          asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        __syncwarp();
       }
-      __syncwarp();
       if (publish) {
         // this segment is in kv once every epilogue warp's stores are complete: the last of the
         // four warps to get here lets the next segment's CTA add (a count, not a barrier, so an
@@ -562,8 +569,6 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         if (lane == 0)
           asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.go.done + m0 / (128 * a.msub)) : "memory");
       }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&ctl->acc_empty[set]));   // the set may take its next item
       ++n_items;
       if (fused) {                             // the next tile's stream rows into L2 during its main loop
         Schedule peek = sch;
@@ -575,6 +580,9 @@ wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
       }
     }
+    // the last stores have read their staging tiles (and are complete) before shared memory goes
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
   }
 
   tc_fence_before();

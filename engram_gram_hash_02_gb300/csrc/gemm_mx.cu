@@ -315,12 +315,11 @@ wkv_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
       else
         store_accumulators(&tmD, D, a.M, a.N, tmem, q, lane, stg, a.msub, a.msub == 1 && a.chains == 2,
                            a.acc_stride, a.BN, m0, n0, false);
-      if (lane == 0) {
-        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // staging tile reusable
-      }
-      __syncwarp();
+      // the accumulators are read (every tcgen05.ld has completed): tensor memory may take the next
+      // tile while this one's stores are in flight (a staging tile is reused only after its store
+      // has read it)
       tc_fence_before();
-      mbar_arrive(smem_u32(&ctl->acc_empty));  // tensor memory may take the next tile
+      mbar_arrive(smem_u32(&ctl->acc_empty));
       ++n_items;
       prefetch_tile(tile + (int)gridDim.x);
     }

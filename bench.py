@@ -281,12 +281,13 @@ def stage_model(w, name, peaks_d, mx: bool = False):
     raise ValueError(name)
 
 
-def forward_launches(w) -> int:
+def forward_launches(w, table_order: bool = False) -> int:
     """Kernels one engram_forward call launches: the hash (which also gathers the rows of up to 8
     leading FP8 layers), one gather launch per 8 remaining layers of the workload's one format,
-    then per layer the projection and the gate."""
-    fused = min(w.layers, 8) if w.table_format == "fp8" else 0
-    return 1 + -(-(w.layers - fused) // 8) + 2 * w.layers
+    then per layer the projection and the gate. Table-order gathers: no rows from the hash, and four
+    more launches per layer (clear, count, scan, scatter)."""
+    fused = min(w.layers, 8) if w.table_format == "fp8" and not table_order else 0
+    return 1 + -(-(w.layers - fused) // 8) + 2 * w.layers + (4 * w.layers if table_order else 0)
 
 
 def kernel_src(name):
@@ -440,10 +441,11 @@ def run_ours(args, rank, world, device):
                        **({"gate_fusion": args.gate_fusion} if args.gate_fusion else {}),
                        **({"side_stream": True} if args.side_stream else {}),
                        **({"operand_gather": True} if args.operand_gather else {}),
+                       **({"gather_order": "table"} if args.gather_order else {}),
                        **({"gemm_tile": args.gemm_tile} if args.gemm_tile else {}),
                        **({"mx_tile": args.mx_tile} if args.mx_tile else {}),
                        **({"gate_form": args.gate_form} if args.gate_form else {})),
-        "gpu_launches": args.steps * (forward_launches(w) + len(calls)),
+        "gpu_launches": args.steps * (forward_launches(w, bool(args.gather_order)) + len(calls)),
         "stages": stages,
         "roofline": roofline_entry(dom, model, achieved, peak, unit, pk, pk_kind, mx, traffic),
         "clocks": clocks,
@@ -834,6 +836,8 @@ def main():
                     help="FP8 variant: the projection gathers its token rows from the table itself")
     ap.add_argument("--gemm-tile", type=int, default=0, help="tuning: force the bf16 projection's tile width")
     ap.add_argument("--mx-tile", type=int, default=0, help="tuning: force the MXFP8 projection's tile width")
+    ap.add_argument("--gather-order", type=int, default=0, choices=[0, 1],
+                    help="engram_forward's gathers: 0 token order, 1 table order (rows grouped by table region)")
     ap.add_argument("--side-stream", action="store_true",
                     help="engram_forward2: the later layers' gathers on a second stream")
     ap.add_argument("--gate-fusion", type=int, nargs="?", const=1, default=0, choices=[0, 1, 2],
@@ -879,6 +883,8 @@ def main():
             E.set_gate_fusion(args.gate_fusion)
         if args.operand_gather:
             E.set_operand_gather(True)
+        if args.gather_order:
+            E.set_gather_order(args.gather_order)
         if args.gemm_tile:
             E.set_gemm_tile(args.gemm_tile)
         if args.mx_tile:

@@ -111,6 +111,8 @@ def lib() -> C.CDLL:
         L.engram_set_gate_fusion.restype = None
         L.engram_set_operand_gather.argtypes = [I32]
         L.engram_set_operand_gather.restype = None
+        L.engram_set_gather_order.argtypes = [I32]
+        L.engram_set_gather_order.restype = None
         L.engram_project_plan.argtypes = [I64, I32, I32, I32, I32, P]
         _lib = L
     return _lib
@@ -406,6 +408,11 @@ def set_gate_fusion(mode=0):
 def set_operand_gather(on: bool = False):
     """engram_forward with the FP8 variant's projection gathering its token rows from the table."""
     lib().engram_set_operand_gather(1 if on else 0)
+
+
+def set_gather_order(mode: int = 0):
+    """engram_forward's gathers: 0 token order, 1 table order (rows grouped by table region)."""
+    lib().engram_set_gather_order(int(mode))
 
 
 def set_gemm_mx_tile(bn: int = 0):

@@ -16,7 +16,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libengram.so")
 
-SOURCES = ["abi.cu", "hash.cu", "gather.cu", "gemm.cu", "gemm_mx.cu", "mx.cu", "gate.cu", "layout.cpp",
+SOURCES = ["abi.cu", "hash.cu", "gather.cu", "gemm.cu", "gemm_mx.cu", "mx.cu", "gate.cu", "order.cu", "layout.cpp",
            "forward_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -398,8 +398,11 @@ int engram_project_mxfp8(const uint8_t* A, const uint8_t* A_scales, const uint8_
 
 static int g_gate_fusion = 0;   // engram_set_gate_fusion
 static int g_operand_gather = 0;   // engram_set_operand_gather
+static int g_gather_order = 0;     // engram_set_gather_order
 
 void engram_set_operand_gather(int32_t on) { g_operand_gather = on ? 1 : 0; }
+
+void engram_set_gather_order(int32_t mode) { g_gather_order = mode == 1 ? 1 : 0; }
 
 void engram_set_gate_fusion(int32_t mode) { g_gate_fusion = (mode == 1 || mode == 2) ? mode : 0; }
 
@@ -418,13 +421,16 @@ static size_t a_slot_bytes(int64_t T, int64_t K) {
 // Row-block counters of the overlapped gate: one word per 128 tokens and layer.
 static size_t done_bytes(int64_t T, int layers) { return round256((size_t)((T + 127) / 128) * layers * 4); }
 
+// Per layer, the table-order gathers' permutation and region counters (engram_set_gather_order).
+static size_t order_bytes(int64_t T, int64_t C) { return round256((size_t)(T * C * 4)) + (size_t)kOrderBuckets * 4; }
+
 size_t engram_forward_workspace_bytes(const EngramDims* d, int64_t T) {
   if (d == nullptr || T < 0 || d->layers < 1) return 0;
   const int64_t C = (int64_t)(d->max_ngram - 1) * d->n_heads;
   const int64_t K = C * d->head_dim;
   const int64_t N = (int64_t)d->hidden * (d->hc + 1);
   return round256((size_t)(T * d->layers * C * 4)) + (size_t)d->layers * a_slot_bytes(T, K) +
-         round256((size_t)(T * N * 4)) + done_bytes(T, d->layers);
+         round256((size_t)(T * N * 4)) + done_bytes(T, d->layers) + (size_t)d->layers * order_bytes(T, C);
 }
 
 }  // extern "C"
@@ -514,6 +520,13 @@ int forward_core(const EngramDims* dims, const EngramHashTables* tables, const E
   // the overlapped gate's row-block counters (after kv), cleared by the hash launch
   const int64_t nblk = (T + 127) / 128;
   uint32_t* done = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(kv) + round256((size_t)(T * N * 4)));
+  // after them, per layer: the table-order permutation and its region counters
+  uint8_t* const order0 = reinterpret_cast<uint8_t*>(done) + done_bytes(T, L);
+  auto perm_of = [&](int l) { return reinterpret_cast<int32_t*>(order0 + (size_t)l * order_bytes(T, C)); };
+  auto hist_of = [&](int l) {
+    return reinterpret_cast<uint32_t*>(order0 + (size_t)l * order_bytes(T, C) + round256((size_t)(T * C * 4)));
+  };
+  const bool table_order = g_gather_order == 1;
   auto overlap_gate = [&](int l) { return g_gate_fusion == 2 && layers[l].wkv_format == ENGRAM_WKV_BF16; };
   bool any_overlap = false;
   for (int l = 0; l < L; ++l) any_overlap = any_overlap || overlap_gate(l);
@@ -538,9 +551,12 @@ int forward_core(const EngramDims* dims, const EngramHashTables* tables, const E
     return g_operand_gather && layers[l].wkv_format == ENGRAM_WKV_MXFP8 && dims->head_dim % 128 == 0 &&
            layers[l].table_rows < ((int64_t)1 << 31);
   };
-  // the hash kernel also fetches the rows of the leading run of FP8 layers
+  // the hash kernel also fetches the rows of the leading run of FP8 layers (in token order; with
+  // table-order gathers every layer is gathered by a launch of its own format)
   int fused = 0;
-  while (fused < L && fused < kMaxGatherLayers && layers[fused].table_format == ENGRAM_TABLE_FP8_E8M0) ++fused;
+  while (!table_order && fused < L && fused < kMaxGatherLayers &&
+         layers[fused].table_format == ENGRAM_TABLE_FP8_E8M0)
+    ++fused;
   if (fused > 0) {
     HashGatherParams g{};
     g.h = hp;
@@ -595,14 +611,21 @@ int forward_core(const EngramDims* dims, const EngramHashTables* tables, const E
     const bool on_side = l >= side_from && n_ev < kSideEvents;
     cudaStream_t gst = on_side ? side : st;
     const bool gpdl = !on_side;
-    cudaError_t ce;
+    cudaError_t ce = cudaSuccess;
+    if (table_order) {                         // each layer's rows in table order
+      for (int j = l; j < e && ce == cudaSuccess; ++j)
+        ce = launch_row_order(ids + (int64_t)j * C, (int64_t)L * C, T, C, layers[j].table_rows, hist_of(j),
+                              perm_of(j), gst, gpdl);
+      if (ce != cudaSuccess) return fail_cuda(ce, "engram_forward: table-order launch");
+    }
     if (mx) {
       GatherCodesLayers m{};
       m.n = e - l;
       for (int j = l; j < e; ++j)
         m.l[j - l] = GatherCodesParams{ids + (int64_t)j * C, (int64_t)L * C, T, C, dims->head_dim, layers[j].table,
                                        layers[j].table_scales, layers[j].table_rows,
-                                       operand_gather(j) ? nullptr : rows_of(j), scales_of(j), err_flag};
+                                       operand_gather(j) ? nullptr : rows_of(j), scales_of(j), err_flag,
+                                       table_order ? perm_of(j) : nullptr};
       ce = launch_gather_codes(m, gst, gpdl);
     } else {
       GatherLayers m{};
@@ -610,7 +633,8 @@ int forward_core(const EngramDims* dims, const EngramHashTables* tables, const E
       for (int j = l; j < e; ++j)
         m.l[j - l] = GatherParams{fmt, ids + (int64_t)j * C, (int64_t)L * C, T, C, dims->head_dim, layers[j].table,
                                   layers[j].table_scales, layers[j].table_rows,
-                                  reinterpret_cast<uint16_t*>(rows_of(j)), err_flag};
+                                  reinterpret_cast<uint16_t*>(rows_of(j)), err_flag,
+                                  table_order ? perm_of(j) : nullptr};
       ce = launch_gather(m, gst, gpdl);
     }
     if (ce != cudaSuccess) return fail_cuda(ce, "engram_forward: gather launch");

@@ -55,11 +55,19 @@ __device__ __forceinline__ void flag(int32_t* err, int32_t bit) {
 // launch fits in 31 bits (a 32-bit division by a loop-invariant divisor, whose reciprocal the
 // compiler keeps out of the loop), else int64_t. (The multiply-and-shift of fastdiv.h measured
 // slower here at large T, though faster in the Q2_K and code gathers, which use it.)
+// With a permutation (table-order gathers) the walk's row r is the row perm[r], and the chunk is
+// written at that row's place (out_chunk); otherwise out_chunk = i.
 template <typename I>
-__device__ __forceinline__ void split_chunk(int64_t i, int chunks_per_row, int C, I& t, int& col, int& j) {
+__device__ __forceinline__ void split_chunk(int64_t i, int chunks_per_row, int C, const int32_t* perm, I& t,
+                                            int& col, int& j, int64_t& out_chunk) {
   const I ii = (I)i;
-  const I r = ii / (I)chunks_per_row;
+  I r = ii / (I)chunks_per_row;
   j = (int)(ii - r * (I)chunks_per_row);
+  out_chunk = i;
+  if (perm != nullptr) {
+    r = (I)__ldg(perm + r);
+    out_chunk = (int64_t)r * chunks_per_row + j;
+  }
   t = r / (I)C;
   col = (int)(r - t * (I)C);
 }
@@ -82,16 +90,18 @@ gather_fp8_kernel(const GatherLayers m) {
     uint4 v[kChunksPerThread];
     uint32_t sb[kChunksPerThread];
     bool ok[kChunksPerThread];
+    int64_t oi[kChunksPerThread];               // where each chunk goes
 #pragma unroll
     for (int u = 0; u < kChunksPerThread; ++u) {
       const int64_t i = base + u * stride;
       ok[u] = false;
       v[u] = make_uint4(0, 0, 0, 0);
       sb[u] = 0;
+      oi[u] = i;
       if (i < total) {
         I t;
         int col, j;
-        split_chunk<I>(i, chunks_per_row, p.C, t, col, j);
+        split_chunk<I>(i, chunks_per_row, p.C, p.perm, t, col, j, oi[u]);
         const int64_t id = __ldg(p.ids + (int64_t)t * p.ids_stride_t + col);
         if (id >= 0 && id < p.num_rows) {
           ok[u] = true;
@@ -118,7 +128,7 @@ gather_fp8_kernel(const GatherLayers m) {
         hi.z = dequant_pair(v[u].w, scale);
         hi.w = dequant_pair(v[u].w >> 16, scale);
       }
-      uint4* dst = reinterpret_cast<uint4*>(p.out + (i << 4));   // chunk i -> 16 bf16 at 16*i
+      uint4* dst = reinterpret_cast<uint4*>(p.out + (oi[u] << 4));   // chunk c -> 16 bf16 at 16*c
       dst[0] = lo;
       dst[1] = hi;
     }
@@ -139,14 +149,16 @@ gather_bf16_kernel(const GatherLayers m) {
   for (int64_t base = (int64_t)blockIdx.x * kThreads + threadIdx.x; base < total;
        base += stride * kChunksPerThread) {
     uint4 v[kChunksPerThread];
+    int64_t oi[kChunksPerThread];               // where each chunk goes
 #pragma unroll
     for (int u = 0; u < kChunksPerThread; ++u) {
       const int64_t i = base + u * stride;
       v[u] = make_uint4(0, 0, 0, 0);
+      oi[u] = i;
       if (i < total) {
         I t;
         int col, j;
-        split_chunk<I>(i, chunks_per_row, p.C, t, col, j);
+        split_chunk<I>(i, chunks_per_row, p.C, p.perm, t, col, j, oi[u]);
         const int64_t id = __ldg(p.ids + (int64_t)t * p.ids_stride_t + col);
         if (id >= 0 && id < p.num_rows) {
           v[u] = ld_stream_v4(table + id * p.D + (j << 3));
@@ -158,7 +170,7 @@ gather_bf16_kernel(const GatherLayers m) {
 #pragma unroll
     for (int u = 0; u < kChunksPerThread; ++u) {
       const int64_t i = base + u * stride;
-      if (i < total) reinterpret_cast<uint4*>(p.out)[i] = v[u];
+      if (i < total) reinterpret_cast<uint4*>(p.out)[oi[u]] = v[u];
     }
   }
 }
@@ -188,12 +200,15 @@ gather_q2k_kernel(const GatherLayers m) {
   for (int64_t r0 = warp * kQ2kRowsPerWarp; r0 < rows; r0 += nwarps * kQ2kRowsPerWarp) {
     uint32_t word[kQ2kRowsPerWarp];
     bool ok[kQ2kRowsPerWarp];
+    int64_t orow[kQ2kRowsPerWarp];              // where each row goes (its own place in token order)
 #pragma unroll
     for (int u = 0; u < kQ2kRowsPerWarp; ++u) {
-      const int64_t r = r0 + u;
+      int64_t r = r0 + u;
       ok[u] = false;
       word[u] = 0;
+      orow[u] = r;
       if (r < rows) {
+        if (p.perm != nullptr) orow[u] = r = __ldg(p.perm + r);   // table-order walk
         I t;
         if constexpr (std::is_same<I, uint32_t>::value) t = fast_div((uint32_t)r, m.div_c);
         else t = r / p.C;
@@ -231,7 +246,7 @@ gather_q2k_kernel(const GatherLayers m) {
         o.z = pack_bf16x2(y[4], y[5]);
         o.w = pack_bf16x2(y[6], y[7]);
       }
-      reinterpret_cast<uint4*>(p.out + r * 256)[lane] = o;
+      reinterpret_cast<uint4*>(p.out + orow[u] * 256)[lane] = o;
     }
   }
 }

@@ -139,6 +139,7 @@ struct GatherParams {
   int64_t num_rows;
   uint16_t* out;
   int32_t* err;
+  const int32_t* perm;        // NULL: rows in token order; else row n of the gather is perm[n] (table order)
 };
 // n layers of the same format, T, C and D in one launch (grid y = layer); the launcher fills the
 // division by C (the Q2_K gather's)
@@ -210,6 +211,7 @@ struct GatherCodesParams {
   uint8_t* codes;             // [T, C*D], or NULL: only the scale words (the projection gathers the codes)
   uint8_t* out_scales;        // [T, C*D/32]
   int32_t* err;
+  const int32_t* perm;        // NULL: rows in token order; else row n of the gather is perm[n] (table order)
 };
 struct GatherCodesLayers {
   int32_t n;
@@ -223,6 +225,14 @@ inline cudaError_t launch_gather_codes(const GatherCodesParams& p, cudaStream_t 
   m.l[0] = p;
   return launch_gather_codes(m, stream, pdl);
 }
+// Table-order gathers (engram_set_gather_order): a permutation of one layer's T * C (token, column)
+// rows sorted by table region (id >> shift, kOrderBuckets regions), so that a gather reads the
+// table in address order. hist holds kOrderBuckets words of scratch. Four launches: clear, count,
+// scan, scatter.
+constexpr int kOrderBuckets = 16384;
+cudaError_t launch_row_order(const int32_t* ids, int64_t ids_stride, int64_t T, int32_t C, int64_t num_rows,
+                             uint32_t* hist, int32_t* perm, cudaStream_t stream, bool pdl);
+
 cudaError_t launch_quantize_mxfp8(const uint16_t* w, int64_t N, int32_t K, uint8_t* codes, uint8_t* scales,
                                   cudaStream_t stream);
 

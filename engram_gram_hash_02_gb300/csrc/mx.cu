@@ -87,18 +87,27 @@ gather_fp8_codes_kernel(const GatherCodesLayers m) {
   for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < total; i += (int64_t)gridDim.x * kThreads) {
     // index split: multiply-and-shift by the launch's constants when its indices fit in 31 bits
     // (I = uint32_t), else int64_t divisions
-    int64_t t;
+    // (with a permutation, the walk's row r is the row perm[r], written at that row's place)
+    int64_t t, oi = i;
     int j, col;
     if constexpr (std::is_same<I, uint32_t>::value) {
       const uint32_t ii = (uint32_t)i;
-      const uint32_t r = fast_div(ii, m.div_cpr);
+      uint32_t r = fast_div(ii, m.div_cpr);
       j = (int)(ii - r * (uint32_t)chunks_per_row);
+      if (p.perm != nullptr) {
+        r = (uint32_t)__ldg(p.perm + r);
+        oi = (int64_t)r * chunks_per_row + j;
+      }
       const uint32_t tt = fast_div(r, m.div_c);
       t = tt;
       col = (int)(r - tt * (uint32_t)p.C);
     } else {
-      const int64_t r = i / chunks_per_row;
+      int64_t r = i / chunks_per_row;
       j = (int)(i - r * chunks_per_row);
+      if (p.perm != nullptr) {
+        r = __ldg(p.perm + r);
+        oi = r * chunks_per_row + j;
+      }
       t = r / p.C;
       col = (int)(r - t * p.C);
     }
@@ -108,7 +117,7 @@ gather_fp8_codes_kernel(const GatherCodesLayers m) {
     if (p.codes != nullptr) {                    // NULL: scale words only (the projection gathers the codes)
       uint4 v = make_uint4(0, 0, 0, 0);
       if (ok) v = ld_stream_v4(weight + id * p.D + (j << 4));
-      *reinterpret_cast<uint4*>(p.codes + (i << 4)) = v;
+      *reinterpret_cast<uint4*>(p.codes + (oi << 4)) = v;
     }
     // scale bytes: the row's D/32 bytes, copied by the threads of the first D/32 chunks into the
     // projection's word layout (block b of token t at byte 4 * ((b / 4) * rows4 + t) + b % 4)

@@ -322,6 +322,18 @@ void engram_set_gate_fusion(int32_t mode);
  */
 void engram_set_operand_gather(int32_t on);
 
+/*
+ * Tuning knob for engram_forward (and engram_forward2 / engram_forward_noalloc): the order in which
+ * a layer's gather reads the table ([vLLM] ParallelEngramEmbedding.lookup sorts a lookup's ids
+ * before reading a table in host memory; _engram_lookup_thresholds). 0 (the default): token order,
+ * the leading FP8 layers' rows fetched by the hash launch. 1: table order: per layer, the
+ * (token, column) rows are grouped by table region (at most 16384 regions, by id >> shift) with a
+ * counting pass, a scan and a scatter into a permutation (four more launches per layer, their
+ * scratch in the workspace), then the gather walks the permutation and writes every row at its own
+ * place. The results are bit-identical to token order. Process-wide; not thread-safe against calls.
+ */
+void engram_set_gather_order(int32_t mode);
+
 /* Per-layer resident weights ([Atlas] EngramLayerWeights; [vLLM] Engram parameters). */
 typedef struct EngramLayerWeights {
   int32_t table_format;        /* EngramTableFmt */
